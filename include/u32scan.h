@@ -1,0 +1,121 @@
+/*
+ * u32scan.h -- C ABI of the GB300 (sm_103a) U32 scan library, libu32scan.so.
+ *
+ * Device-wide parallel prefix sums over arrays of 32-bit unsigned integers,
+ * sums wrapping at 2^32, and the primitives built on them: segmented scan and
+ * reduce over head-flagged segments, stream compaction (flags -> inclusive
+ * offsets -> gathered indices -> count) and a stable LSD radix-sort
+ * permutation of U32 keys.
+ *
+ * Conventions for every entry point below:
+ *   - Pointers named as device pointers must point to memory the current
+ *     CUDA device can access (cudaMalloc, torch tensors, managed memory),
+ *     aligned to 4 bytes. 16-byte alignment is not required.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream). Results, totals and counts stay in device memory.
+ *   - The caller owns every buffer. The library allocates no memory and
+ *     keeps no state between calls other than what lives in `ws`.
+ *   - `ws`/`ws_bytes` is caller-provided device workspace of at least
+ *     u32scan_workspace_bytes(op, n) bytes (256-byte aligned). It must be
+ *     zero-filled once before its first use (cudaMemset or
+ *     u32scan_workspace_init); after that the library keeps it consistent
+ *     itself, so it is reused across calls without clearing. A workspace
+ *     serves one call at a time: calls that share one workspace must be
+ *     ordered (the same stream, or events).
+ *   - Return value: U32SCAN_OK, or a negative status. Argument errors are
+ *     found on the host before anything is launched; nothing is written
+ *     then. U32SCAN_ECUDA reports a launch failure (cudaGetLastError).
+ *     A device-side status (a carry wait that ran out of time) is reported
+ *     by u32scan_check().
+ *   - n == 0 is valid: nothing is read, and totals/counts are set to 0.
+ */
+#ifndef U32SCAN_H
+#define U32SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle (cudaStream_t), declared without
+ * including any CUDA header. */
+typedef struct CUstream_st *u32scan_stream_t;
+
+#define U32SCAN_OK 0
+#define U32SCAN_EINVAL (-1)     /* a null pointer with n > 0, misalignment, n too large */
+#define U32SCAN_EWORKSPACE (-2) /* ws null or ws_bytes below u32scan_workspace_bytes */
+#define U32SCAN_ECUDA (-3)      /* a CUDA runtime error (launch, memset, sync) */
+#define U32SCAN_ETIMEOUT (-4)   /* device: a wait for a predecessor tile's carry timed out */
+
+/* Operation codes for u32scan_workspace_bytes. */
+#define U32SCAN_OP_SCAN 1      /* scan_exclusive_u32, scan_inclusive_u32 */
+#define U32SCAN_OP_SEGSCAN 2   /* segscan_inclusive_u32, segreduce_u32 */
+#define U32SCAN_OP_COMPACT 3   /* compact_indices_u32 */
+#define U32SCAN_OP_RADIX 4     /* radix_sort_perm_u32 */
+
+/* Bytes of device workspace an operation needs for n elements (a multiple
+ * of 256, at least 256). Returns 0 for an unknown op. Pure host function. */
+size_t u32scan_workspace_bytes(int op, size_t n);
+
+/* Zero-fill a workspace (cudaMemsetAsync on `stream`). */
+int u32scan_workspace_init(void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/* Wait for `stream`, then read and clear the device-side status that the
+ * calls using `ws` left: U32SCAN_OK, or U32SCAN_ETIMEOUT when a tile gave up
+ * waiting for its predecessor's carry (its results are then wrong).
+ * U32SCAN_ECUDA if the synchronisation or the read fails. */
+int u32scan_check(void *ws, u32scan_stream_t stream);
+
+/* A static string for a status code. */
+const char *u32scan_strerror(int status);
+
+/* Library version, MAJOR * 10000 + MINOR * 100 + PATCH. */
+int u32scan_version(void);
+
+/*
+ * Exclusive scan, in place.
+ * Source: "scan.bend source" (bendlib), section API, `exclusive`: a[j]
+ * becomes a[0] + .. + a[j-1] (a[0] becomes 0) and the call returns the
+ * total a[0] + .. + a[n-1]; header comment: sums wrap at 2^32. Also the
+ * CAIRN "Concurrency" page, section "scan" (`scan + exclusive`, binds the
+ * total).
+ *   data  device, uint32_t[n], read and overwritten with the scan.
+ *   n     element count; any n up to 2^32 - 1.
+ *   total device, one uint32_t written with the wrapped total; may be NULL.
+ * Errors: EINVAL if data is NULL with n > 0, if data or total is not 4-byte
+ * aligned, or n >= 2^32; EWORKSPACE; ECUDA.
+ */
+int scan_exclusive_u32(uint32_t *data, size_t n, uint32_t *total,
+                       void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * Inclusive scan, in place: a[j] becomes a[0] + .. + a[j], wrapping.
+ * Source: "scan.bend source", section API, `inclusive`; CAIRN "scan"
+ * (`scan + out`, out[i] = e(0) + .. + e(i)). Arguments and errors as
+ * scan_exclusive_u32.
+ */
+int scan_inclusive_u32(uint32_t *data, size_t n, uint32_t *total,
+                       void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * Test hook for the bounded carry wait (no counterpart on the pages; the
+ * Relay page names the hazard it guards against: a tile waiting on a
+ * predecessor that never hands its carry on). Runs scan_exclusive_u32,
+ * except that tile `skip_tile` of the launch never publishes its carry,
+ * so the tiles after it wait `limit_ns` nanoseconds, give up, and the next
+ * u32scan_check() on `ws` returns U32SCAN_ETIMEOUT. The results are then
+ * wrong by design; nothing else is affected, and `ws` stays usable.
+ */
+int u32scan_test_scan_skip_publish(uint32_t *data, size_t n, uint32_t *total,
+                                   void *ws, size_t ws_bytes,
+                                   unsigned int skip_tile,
+                                   unsigned long long limit_ns,
+                                   u32scan_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* U32SCAN_H */

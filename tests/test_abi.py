@@ -1,0 +1,92 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/*.h declares, sizes workspaces, and rejects bad arguments on the
+host before any CUDA call."""
+
+import ctypes
+import pathlib
+import re
+
+import pytest
+
+from u32_prefix_scan_gb300 import _native
+
+ROOT = pathlib.Path(__file__).resolve().parents[1]
+
+
+def declared_functions():
+    names = []
+    for h in sorted((ROOT / "include").glob("*.h")):
+        text = re.sub(r"/\*.*?\*/", "", h.read_text(), flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(",
+                             text, flags=re.M):
+            names.append(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from u32_prefix_scan_gb300 import build
+
+    build.build()
+    return _native.lib()
+
+
+def test_header_declares_the_five_primitives_and_more():
+    names = set(declared_functions())
+    for must in ("scan_exclusive_u32", "scan_inclusive_u32", "u32scan_workspace_bytes", "u32scan_check"):
+        assert must in names
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert names
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+        assert name in _native.SIGNATURES, f"{name} has no ctypes signature in the binding"
+
+
+def test_strerror_and_version(lib):
+    for code in (_native.OK, _native.EINVAL, _native.EWORKSPACE, _native.ECUDA, _native.ETIMEOUT):
+        assert _native.strerror(code) and _native.strerror(code) != "unknown status"
+    assert _native.strerror(12345) == "unknown status"
+    assert lib.u32scan_version() >= 100
+
+
+def test_workspace_bytes(lib):
+    wb = lib.u32scan_workspace_bytes
+    assert wb(999, 10) == 0
+    for n in (0, 1, 1000, 1 << 16, (1 << 22) - 1, 1 << 22, 1 << 28, (1 << 32) - 1):
+        b = wb(_native.OP_SCAN, n)
+        assert b >= 256 and b % 256 == 0
+        # at least one carry word per 16384-element tile (the widest shape)
+        assert b >= 256 + 8 * (n // 16384)
+    # one 8-byte carry word per tile at most, plus the 256-byte header
+    assert wb(_native.OP_SCAN, 1 << 28) <= 256 + 8 * ((1 << 28) // 2048 + 2) + 256
+
+
+@pytest.mark.parametrize("name", ["scan_exclusive_u32", "scan_inclusive_u32"])
+def test_scan_rejects_bad_arguments_on_host(lib, name):
+    fn = getattr(lib, name)
+    fake = 0x10000  # never dereferenced: every case below fails a host check first
+    ws_need = lib.u32scan_workspace_bytes(_native.OP_SCAN, 1000)
+    assert fn(None, 10, None, fake, ws_need, None) == _native.EINVAL          # null data
+    assert fn(fake + 2, 10, None, fake, ws_need, None) == _native.EINVAL      # misaligned data
+    assert fn(fake, 10, fake + 1, fake, ws_need, None) == _native.EINVAL      # misaligned total
+    assert fn(fake, 1 << 32, None, fake, 1 << 40, None) == _native.EINVAL     # n too large
+    assert fn(fake, 1000, None, None, ws_need, None) == _native.EWORKSPACE    # no workspace
+    assert fn(fake, 1000, None, fake, ws_need - 256, None) == _native.EWORKSPACE  # too small
+    assert fn(fake, 1000, None, fake + 16, ws_need, None) == _native.EWORKSPACE   # misaligned ws
+    # n == 0 with no total: a no-op that touches nothing
+    assert fn(None, 0, None, None, 0, None) == _native.OK
+
+
+def test_workspace_init_rejects_null(lib):
+    assert lib.u32scan_workspace_init(None, 4096, None) == _native.EWORKSPACE
+    assert lib.u32scan_check(None, None) == _native.EWORKSPACE
+
+
+def test_package_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_native, "SO", tmp_path / "missing.so")
+    monkeypatch.setattr(_native, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _native.lib()

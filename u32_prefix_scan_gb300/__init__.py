@@ -1,0 +1,22 @@
+"""u32_prefix_scan_gb300: U32 prefix scans and the primitives built on them,
+as hand-written CUDA kernels for GB300 (sm_103a) behind a C ABI
+(include/u32scan.h, libu32scan.so), with a thin torch-tensor binding.
+
+The tensor-level functions live in `api` (imported lazily so that the seeded
+input generator in `inputs` can be used without torch or the library).
+"""
+
+_API = {
+    "Workspace",
+    "scan_exclusive_u32",
+    "scan_inclusive_u32",
+    "check",
+}
+
+
+def __getattr__(name):
+    if name in _API:
+        from . import api
+
+        return getattr(api, name)
+    raise AttributeError(name)

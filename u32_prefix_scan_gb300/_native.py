@@ -1,0 +1,73 @@
+"""ctypes view of libu32scan.so: the C ABI declared in include/u32scan.h.
+
+Loading fails loudly when the library has not been built; there is no
+fallback implementation anywhere in this package.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import pathlib
+
+SO = pathlib.Path(__file__).resolve().parent / "libu32scan.so"
+
+OK = 0
+EINVAL = -1
+EWORKSPACE = -2
+ECUDA = -3
+ETIMEOUT = -4
+
+OP_SCAN = 1
+OP_SEGSCAN = 2
+OP_COMPACT = 3
+OP_RADIX = 4
+
+_vp = ctypes.c_void_p
+_sz = ctypes.c_size_t
+_int = ctypes.c_int
+
+# name -> (restype, argtypes)
+SIGNATURES = {
+    "u32scan_workspace_bytes": (_sz, [_int, _sz]),
+    "u32scan_workspace_init": (_int, [_vp, _sz, _vp]),
+    "u32scan_check": (_int, [_vp, _vp]),
+    "u32scan_strerror": (ctypes.c_char_p, [_int]),
+    "u32scan_version": (_int, []),
+    "scan_exclusive_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
+    "scan_inclusive_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
+    "u32scan_test_scan_skip_publish": (_int, [_vp, _sz, _vp, _vp, _sz, ctypes.c_uint, ctypes.c_ulonglong, _vp]),
+}
+
+_lib = None
+
+
+class U32ScanError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {strerror(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library with its signatures declared."""
+    global _lib
+    if _lib is None:
+        if not SO.exists():
+            raise RuntimeError(
+                f"{SO.name} is not built: run `python -c 'import __graft_entry__ as g; g.build()'` "
+                "(needs nvcc); this package has no CPU fallback")
+        handle = ctypes.CDLL(str(SO))
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().u32scan_strerror(status).decode()
+
+
+def check(status: int, what: str) -> None:
+    if status != OK:
+        raise U32ScanError(status, what)

@@ -1,0 +1,132 @@
+"""Torch-tensor front end of libu32scan.so: argument marshalling only.
+
+Every function takes CUDA tensors, checks dtype/device/contiguity, and
+passes raw device pointers, sizes and the current CUDA stream to the C
+entry point of the same name. All computation happens in the library's
+kernels; nothing here touches tensor data.
+
+U32 arrays are accepted as torch.int32 or torch.uint32 tensors (the bits are
+the same; wrapping u32 addition and two's-complement int32 addition agree).
+"""
+
+from __future__ import annotations
+
+import threading
+
+import torch
+
+from . import _native
+
+__all__ = [
+    "Workspace",
+    "scan_exclusive_u32",
+    "scan_inclusive_u32",
+    "check",
+]
+
+_U32_DTYPES = (torch.int32, getattr(torch, "uint32", torch.int32))
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _require_cuda(t: torch.Tensor, name: str, dtypes=_U32_DTYPES) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (this library has no CPU path)")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class Workspace:
+    """Device workspace for the library's carries, reused across calls.
+
+    One zero-filled byte buffer per (device, stream), grown on demand. The
+    library keeps it consistent between calls by itself; calls sharing a
+    workspace must be ordered, which one stream guarantees.
+    """
+
+    _lock = threading.Lock()
+    _cache: dict = {}
+
+    def __init__(self, nbytes: int, device: torch.device):
+        self.buf = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    @property
+    def nbytes(self) -> int:
+        return self.buf.numel()
+
+    @classmethod
+    def get(cls, op: int, n: int, device: torch.device, stream_handle: int) -> "Workspace":
+        need = _native.lib().u32scan_workspace_bytes(op, n)
+        key = (device.index, stream_handle)
+        with cls._lock:
+            ws = cls._cache.get(key)
+            if ws is None or ws.nbytes < need:
+                ws = cls(max(need, 2 * ws.nbytes if ws else need), device)
+                cls._cache[key] = ws
+        return ws
+
+
+def _ws(op: int, n: int, device, stream_handle: int, workspace) -> Workspace:
+    if workspace is not None:
+        return workspace
+    return Workspace.get(op, n, device, stream_handle)
+
+
+def _scalar_out(out, like: torch.Tensor, dtype) -> torch.Tensor:
+    if out is None:
+        return torch.empty(1, dtype=dtype, device=like.device)
+    _require_cuda(out, "out", (dtype,) if dtype not in _U32_DTYPES else _U32_DTYPES)
+    if out.numel() < 1:
+        raise ValueError("out must hold at least one element")
+    return out
+
+
+def _scan(name: str, data: torch.Tensor, total, stream, workspace) -> torch.Tensor:
+    _require_cuda(data, "data")
+    total = _scalar_out(total, data, data.dtype)
+    n = data.numel()
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_SCAN, n, data.device, sh, workspace)
+    fn = getattr(_native.lib(), name)
+    _native.check(fn(data.data_ptr(), n, total.data_ptr(), ws.ptr, ws.nbytes, sh), name)
+    return total
+
+
+def scan_exclusive_u32(data: torch.Tensor, total: torch.Tensor | None = None, *, stream=None,
+                       workspace: Workspace | None = None) -> torch.Tensor:
+    """In place: data[j] <- data[0] + .. + data[j-1] (mod 2^32). Returns the
+    one-element device tensor holding the wrapped total."""
+    return _scan("scan_exclusive_u32", data, total, stream, workspace)
+
+
+def scan_inclusive_u32(data: torch.Tensor, total: torch.Tensor | None = None, *, stream=None,
+                       workspace: Workspace | None = None) -> torch.Tensor:
+    """In place: data[j] <- data[0] + .. + data[j] (mod 2^32). Returns the
+    one-element device tensor holding the wrapped total."""
+    return _scan("scan_inclusive_u32", data, total, stream, workspace)
+
+
+def check(stream=None, workspace: Workspace | None = None, device=None) -> int:
+    """Synchronise the stream and raise if a kernel that used the stream's
+    cached workspace reported a device-side error (a carry-wait timeout)."""
+    sh = _stream_handle(stream)
+    if workspace is None:
+        dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+        workspace = Workspace._cache.get((dev.index, sh))
+        if workspace is None:
+            torch.cuda.synchronize()
+            return _native.OK
+    status = _native.lib().u32scan_check(workspace.ptr, sh)
+    _native.check(status, "u32scan_check")
+    return status

@@ -1,0 +1,54 @@
+// api.cu -- the library-wide entry points: workspace sizing and set-up,
+// device-status readout, error strings, version.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.cuh"
+
+using namespace u32scan;
+
+extern "C" size_t u32scan_workspace_bytes(int op, size_t n) {
+    switch (op) {
+    case U32SCAN_OP_SCAN:
+        return scan_workspace_bytes(n);
+    default:
+        return 0;
+    }
+}
+
+extern "C" int u32scan_workspace_init(void *ws, size_t ws_bytes, u32scan_stream_t stream) {
+    if (ws == nullptr || ws_bytes < kHeaderBytes) return U32SCAN_EWORKSPACE;
+    return cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream) == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
+}
+
+extern "C" int u32scan_check(void *ws, u32scan_stream_t stream) {
+    if (ws == nullptr) return U32SCAN_EWORKSPACE;
+    WsHeader *hdr = static_cast<WsHeader *>(ws);
+    unsigned int status = 0;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return U32SCAN_ECUDA;
+    if (cudaMemcpy(&status, &hdr->status, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return U32SCAN_ECUDA;
+    if (status == 0) return U32SCAN_OK;
+    const unsigned int zero[2] = {0u, 0u};
+    if (cudaMemcpy(&hdr->status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return U32SCAN_ECUDA;
+    return (status & kStatusTimeout) ? U32SCAN_ETIMEOUT : U32SCAN_ECUDA;
+}
+
+extern "C" const char *u32scan_strerror(int status) {
+    switch (status) {
+    case U32SCAN_OK:
+        return "ok";
+    case U32SCAN_EINVAL:
+        return "invalid argument (null pointer, misaligned pointer or n out of range)";
+    case U32SCAN_EWORKSPACE:
+        return "workspace missing, misaligned or smaller than u32scan_workspace_bytes";
+    case U32SCAN_ECUDA:
+        return "CUDA runtime error";
+    case U32SCAN_ETIMEOUT:
+        return "a tile timed out waiting for its predecessor's carry; results are invalid";
+    default:
+        return "unknown status";
+    }
+}
+
+extern "C" int u32scan_version(void) { return 100; }

@@ -1,0 +1,185 @@
+// internal.cuh -- device-side building blocks shared by the library's kernels.
+//
+// Single-pass tile carry ("decoupled look-back"): every tile of a kernel
+// publishes, in one 64-bit word of the workspace, first its own aggregate
+// and later its inclusive prefix (the sum of everything up to and including
+// it). A tile finds its exclusive prefix by reading its predecessors' words
+// 32 at a time, newest first, adding aggregates until it meets an inclusive
+// prefix. This replaces the three-pass block-sums / base-scan / rescan scheme
+// of the scan.bend page and the turn-passing relay of cubecl's Relay: the
+// data is read once and written once (8 bytes per element for a scan).
+//
+// Forward progress: a tile's index comes from an atomic counter, not from
+// blockIdx, so every predecessor of a running tile has already started
+// (the hazard the Relay page names: a waiting block holds its place on the
+// device). Every wait is bounded by a time limit read from %globaltimer;
+// on expiry the tile records U32SCAN_ETIMEOUT in the workspace status word,
+// stops waiting and finishes, so a kernel never hangs the GPU.
+//
+// Workspace: [header (256 B)] [tile words, 8 B each].
+// Descriptors carry a tag derived from a per-workspace call counter
+// ("epoch"), so words left by earlier calls read as "not ready" and the
+// workspace needs zeroing only once, before its first use. The block that
+// draws the last tile index resets the tile counter and advances the epoch
+// for the next call; every other block has read the epoch before its own
+// draw, and the draw is an acq_rel RMW, so none can see the new epoch.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "u32scan.h"
+
+namespace u32scan {
+
+struct WsHeader {
+    unsigned int counter;   // next tile index to hand out
+    unsigned int epoch;     // call generation
+    unsigned int status;    // device-side error bits (kStatus*)
+    unsigned int detail;    // first tile that timed out, + 1 (0 = none)
+    unsigned int pad[60];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+constexpr size_t kHeaderBytes = 256;
+constexpr unsigned int kStatusTimeout = 1u;
+constexpr unsigned long long kDefaultLimitNs = 1000000000ull;  // 1 s
+constexpr unsigned int kMaxSpinIters = 1u << 24;
+
+// Tile word layout: bits 0..31 value, bit 32 P (inclusive prefix, else
+// aggregate), bit 33 H (segmented: a head lies in the summed range),
+// bits 34..63 tag (never 0 for a published word).
+constexpr unsigned long long kFlagP = 1ull << 32;
+constexpr unsigned long long kFlagH = 1ull << 33;
+constexpr unsigned long long kTagMask = ~((1ull << 34) - 1ull);
+
+__host__ __device__ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__device__ __forceinline__ unsigned long long tag_of(unsigned int epoch) {
+    return (unsigned long long)((epoch & 0x1FFFFFFFu) + 1u) << 34;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int ld_relaxed_u32(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u32(unsigned int *p, unsigned int v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int atom_add_acq_rel(unsigned int *p, unsigned int v) {
+    unsigned int r;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(r) : "l"(p), "r"(v) : "memory");
+    return r;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Draw this block's tile index (thread 0 only). Returns the index and the
+// epoch of this call; the block drawing index n_tiles - 1 re-arms the header.
+__device__ __forceinline__ unsigned int draw_tile(WsHeader *hdr, unsigned int n_tiles,
+                                                  unsigned int *epoch_out) {
+    unsigned int e = ld_relaxed_u32(&hdr->epoch);
+    unsigned int t = atom_add_acq_rel(&hdr->counter, 1u);
+    if (t == n_tiles - 1u) {
+        st_relaxed_u32(&hdr->counter, 0u);
+        st_relaxed_u32(&hdr->epoch, e + 1u);
+    }
+    *epoch_out = e;
+    return t;
+}
+
+__device__ __forceinline__ void report_timeout(WsHeader *hdr, unsigned int tile) {
+    atomicOr(&hdr->status, kStatusTimeout);
+    atomicCAS(&hdr->detail, 0u, tile + 1u);
+}
+
+// Inclusive warp scan (wrapping u32 sums).
+__device__ __forceinline__ unsigned int warp_inclusive_sum(unsigned int x, int lane) {
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        unsigned int y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+    }
+    return x;
+}
+
+// Wait until every lane's word (read by `load`) carries `tag`, bounded by
+// limit_ns. Lanes whose word is still not ready when time runs out get an
+// inclusive-prefix word of value 0, which ends the walk; the timeout is
+// recorded in the header. Warp-uniform control flow.
+template <typename Load>
+__device__ __forceinline__ unsigned long long wait_ready(Load load, unsigned long long tag, WsHeader *hdr,
+                                                         unsigned int tile, unsigned long long limit_ns,
+                                                         int lane) {
+    unsigned long long d = load();
+    if (__all_sync(0xffffffffu, (d & kTagMask) == tag)) return d;
+    const unsigned long long t0 = __shfl_sync(0xffffffffu, globaltimer(), 0);
+    unsigned int backoff = 32;
+    for (unsigned int iter = 0;; ++iter) {
+        __nanosleep(backoff);
+        if (backoff < 512) backoff <<= 1;
+        d = load();
+        const bool ok = (d & kTagMask) == tag;
+        if (__all_sync(0xffffffffu, ok)) return d;
+        const unsigned long long now = __shfl_sync(0xffffffffu, globaltimer(), 0);
+        // Second bound, on the iteration count, in case the timer stalls.
+        if (now - t0 > limit_ns || iter >= kMaxSpinIters) {
+            if (lane == 0) report_timeout(hdr, tile);
+            return ok ? d : (tag | kFlagP);
+        }
+    }
+}
+
+// Exclusive prefix of tile t under wrapping addition. All 32 lanes of one
+// warp call it with the same arguments. Publishes the tile's aggregate at
+// once and its inclusive prefix at the end (unless `publish` is false,
+// which only a test hook uses). Returns the sum of tiles 0 .. t-1.
+__device__ __forceinline__ unsigned int lookback_sum(unsigned long long *desc, unsigned int t, unsigned int agg,
+                                                     unsigned long long tag, WsHeader *hdr,
+                                                     unsigned long long limit_ns, bool publish, int lane) {
+    if (t == 0) {
+        if (publish && lane == 0) st_relaxed(desc, tag | kFlagP | agg);
+        return 0u;
+    }
+    if (publish && lane == 0) st_relaxed(desc + t, tag | agg);
+    unsigned int prefix = 0;
+    long long pos = (long long)t - 1;
+    while (true) {
+        const long long idx = pos - lane;
+        const unsigned long long d = wait_ready(
+            [&]() { return idx >= 0 ? ld_relaxed(desc + idx) : (tag | kFlagP); }, tag, hdr, t, limit_ns, lane);
+        const unsigned int pmask = __ballot_sync(0xffffffffu, (d & kFlagP) != 0);
+        unsigned int v = (unsigned int)d;
+        if (pmask) {
+            const int k = __ffs(pmask) - 1;  // nearest predecessor holding an inclusive prefix
+            prefix += __reduce_add_sync(0xffffffffu, lane <= k ? v : 0u);
+            break;
+        }
+        prefix += __reduce_add_sync(0xffffffffu, v);
+        pos -= 32;
+    }
+    if (publish && lane == 0) st_relaxed(desc + t, tag | kFlagP | (unsigned int)(prefix + agg));
+    return prefix;
+}
+
+// Host-side workspace sizing of each operation (defined beside its kernels).
+size_t scan_workspace_bytes(unsigned long long n);
+
+}  // namespace u32scan

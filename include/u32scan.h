@@ -14,7 +14,8 @@
  *   - Every call is asynchronous on `stream` (NULL = the legacy default
  *     stream). Results, totals and counts stay in device memory.
  *   - The caller owns every buffer. The library allocates no memory and
- *     keeps no state between calls other than what lives in `ws`.
+ *     keeps no state between calls other than what lives in `ws` (and, for
+ *     scan_exclusive_u32_noalloc, in that entry point's own static array).
  *   - `ws`/`ws_bytes` is caller-provided device workspace of at least
  *     u32scan_workspace_bytes(op, n) bytes (256-byte aligned). It must be
  *     zero-filled once before its first use (cudaMemset or
@@ -98,6 +99,30 @@ int scan_exclusive_u32(uint32_t *data, size_t n, uint32_t *total,
  */
 int scan_inclusive_u32(uint32_t *data, size_t n, uint32_t *total,
                        void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * Exclusive scan that allocates nothing and needs no workspace argument.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory (for instance code inside an allocator's
+ * own callbacks, or a runtime that only lends out buffers it owns), so
+ * they cannot provide the workspace scan_exclusive_u32 needs.
+ *   data, n, total, stream: as scan_exclusive_u32; n at most 2^31.
+ * Scratch: a fixed device array inside this library (about 4 MiB, held on
+ * every GPU that loads the library until the process exits). The first
+ * call on each device looks up that array's device address
+ * (cudaGetSymbolAddress) with the device current; make that first call
+ * before any stream capture. Each call enqueues a 4-byte cudaMemsetAsync on
+ * `stream` (re-arming the array's tile counter) and then the scan kernel;
+ * it calls no cudaMalloc or cudaFree.
+ * All calls share the one array: calls that overlap on the GPU (different
+ * streams, or different host threads without ordering) race and give wrong
+ * results. Order them, e.g. on one stream.
+ * Errors: EINVAL for n > 2^31 (the scratch limit) and as scan_exclusive_u32;
+ * ECUDA if the set-up or a launch fails. A carry-wait timeout is recorded
+ * in the internal array only and is not reported by this entry point.
+ */
+int scan_exclusive_u32_noalloc(uint32_t *data, size_t n, uint32_t *total,
+                               u32scan_stream_t stream);
 
 /*
  * Test hook for the bounded carry wait (no counterpart on the pages; the

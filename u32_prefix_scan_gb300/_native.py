@@ -35,6 +35,7 @@ SIGNATURES = {
     "u32scan_version": (_int, []),
     "scan_exclusive_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
     "scan_inclusive_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
+    "scan_exclusive_u32_noalloc": (_int, [_vp, _sz, _vp, _vp]),
     "u32scan_test_scan_skip_publish": (_int, [_vp, _sz, _vp, _vp, _sz, ctypes.c_uint, ctypes.c_ulonglong, _vp]),
 }
 

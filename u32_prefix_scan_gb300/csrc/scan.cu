@@ -21,6 +21,7 @@
 // [head, head + n) uses 16-byte loads and stores, the (at most two) others
 // use guarded scalar accesses.
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "internal.cuh"
@@ -197,4 +198,65 @@ extern "C" int u32scan_test_scan_skip_publish(uint32_t *data, size_t n, uint32_t
                                               unsigned int skip_tile, unsigned long long limit_ns,
                                               u32scan_stream_t stream) {
     return scan_launch<false>(data, n, total, ws, ws_bytes, (cudaStream_t)stream, skip_tile, limit_ns);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free exclusive scan.
+//
+// Some callers cannot allocate device memory at all: code running where
+// cudaMalloc is forbidden or unavailable (inside a custom allocator's own
+// callbacks, a real-time path with a no-allocation rule, an embedding
+// runtime that hands out only the buffers it owns). For them the carry
+// workspace lives in a fixed file-scope device array, sized for n up to
+// kStaticMaxN. Every GPU that loads this library holds the array (about
+// 4 MiB) until the process exits.
+//
+// In host code the array's name is only a host-side stand-in, so its device
+// address is looked up once per device, with that device current, through
+// cudaGetSymbolAddress. That lookup happens on the first call on each device;
+// make that first call before any stream capture begins.
+// ---------------------------------------------------------------------------
+namespace u32scan {
+
+constexpr unsigned long long kStaticMaxN = 1ull << 31;
+// Header plus one carry word per tile for tiles as small as 4096 elements.
+constexpr size_t kStaticScratchBytes = (kHeaderBytes + 8 * ((kStaticMaxN + 3) / 4096 + 2) + 255) / 256 * 256;
+
+static __device__ __align__(256) unsigned char g_scan_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_static_mu;
+static void *g_static_addr[kMaxDevices];
+
+static int static_scratch(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return U32SCAN_ECUDA;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_scan_static_scratch) != cudaSuccess || p == nullptr) return U32SCAN_ECUDA;
+        g_static_addr[dev] = p;
+    }
+    *out = g_static_addr[dev];
+    return U32SCAN_OK;
+}
+
+}  // namespace u32scan
+
+extern "C" int scan_exclusive_u32_noalloc(uint32_t *data, size_t n, uint32_t *total, u32scan_stream_t stream) {
+    if (n > kStaticMaxN) return U32SCAN_EINVAL;
+    if (n == 0)
+        return scan_launch<false>(data, 0, total, nullptr, 0, (cudaStream_t)stream, 0xffffffffu, kDefaultLimitNs);
+    void *ws = nullptr;
+    const int rc = static_scratch(&ws);
+    if (rc != U32SCAN_OK) return rc;
+    if (scan_workspace_bytes(n) > kStaticScratchBytes) return U32SCAN_EINVAL;
+    // The array keeps the previous call's contents. Carry words are tagged
+    // with a call counter, so stale ones are never taken for current ones;
+    // only the tile counter must read zero when a launch starts. Each launch
+    // leaves it at zero, and it is cleared here as well, in case an earlier
+    // launch on this array never completed.
+    if (cudaMemsetAsync(ws, 0, sizeof(unsigned int), (cudaStream_t)stream) != cudaSuccess) return U32SCAN_ECUDA;
+    return scan_launch<false>(data, n, total, ws, kStaticScratchBytes, (cudaStream_t)stream, 0xffffffffu,
+                              kDefaultLimitNs);
 }

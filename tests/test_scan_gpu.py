@@ -141,17 +141,18 @@ def test_closed_forms_at_full_size(u):
     assert torch.equal(got, want)
 
 
-def test_timeout_is_reported_and_workspace_recovers(u):
+@pytest.mark.parametrize("n,skip", [(2048 * 8, 2), ((1 << 22) + 4096 * 3 + 5, 3)],
+                         ids=["one-tile-kernel", "persistent-kernel"])
+def test_timeout_is_reported_and_workspace_recovers(u, n, skip):
     from u32_prefix_scan_gb300 import _native
 
     lib = _native.lib()
-    n = 2048 * 8
     a = inputs.scan_values(n, 11)
     d = to_dev(a)
     total = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = u.Workspace(lib.u32scan_workspace_bytes(_native.OP_SCAN, n), torch.device("cuda"))
     stream = torch.cuda.current_stream().cuda_stream
-    rc = lib.u32scan_test_scan_skip_publish(d.data_ptr(), n, total.data_ptr(), ws.ptr, ws.nbytes, 2,
+    rc = lib.u32scan_test_scan_skip_publish(d.data_ptr(), n, total.data_ptr(), ws.ptr, ws.nbytes, skip,
                                             20_000_000, stream)
     assert rc == _native.OK
     assert lib.u32scan_check(ws.ptr, stream) == _native.ETIMEOUT

@@ -179,6 +179,215 @@ __device__ __forceinline__ unsigned int lookback_sum(unsigned long long *desc, u
     return prefix;
 }
 
+// ---------------------------------------------------------------------------
+// Wide look-back: each lane reads K carry words per round trip, so one round
+// covers 32 * K predecessors (nearest first: word j of lane l is the tile
+// 32 * j + l + 1 places back). All K loads are issued before any is used.
+// ---------------------------------------------------------------------------
+template <int K>
+__device__ __forceinline__ unsigned int lookback_sum_wide(unsigned long long *desc, unsigned int t, unsigned int agg,
+                                                          unsigned long long tag, WsHeader *hdr,
+                                                          unsigned long long limit_ns, bool publish, int lane) {
+    if (t == 0) {
+        if (publish && lane == 0) st_relaxed(desc, tag | kFlagP | agg);
+        return 0u;
+    }
+    if (publish && lane == 0) st_relaxed(desc + t, tag | agg);
+    unsigned int prefix = 0;
+    long long pos = (long long)t - 1;
+    while (true) {
+        unsigned long long d[K];
+        bool ok = true;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const long long idx = pos - 32 * j - lane;
+            d[j] = idx >= 0 ? ld_relaxed(desc + idx) : (tag | kFlagP);
+        }
+#pragma unroll
+        for (int j = 0; j < K; ++j) ok = ok && ((d[j] & kTagMask) == tag);
+        if (!__all_sync(0xffffffffu, ok)) {
+            const unsigned long long t0 = __shfl_sync(0xffffffffu, globaltimer(), 0);
+            for (unsigned int iter = 0;; ++iter) {
+                if (iter >= 8) __nanosleep(64);
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    const long long idx = pos - 32 * j - lane;
+                    if ((d[j] & kTagMask) != tag && idx >= 0) d[j] = ld_relaxed(desc + idx);
+                }
+                ok = true;
+#pragma unroll
+                for (int j = 0; j < K; ++j) ok = ok && ((d[j] & kTagMask) == tag);
+                if (__all_sync(0xffffffffu, ok)) break;
+                const unsigned long long now = __shfl_sync(0xffffffffu, globaltimer(), 0);
+                if (now - t0 > limit_ns || iter >= kMaxSpinIters) {
+                    if (lane == 0) report_timeout(hdr, t);
+#pragma unroll
+                    for (int j = 0; j < K; ++j)
+                        if ((d[j] & kTagMask) != tag) d[j] = tag | kFlagP;
+                    break;
+                }
+            }
+        }
+        bool found = false;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            if (!found) {
+                const unsigned int pmask = __ballot_sync(0xffffffffu, (d[j] & kFlagP) != 0);
+                const int k = pmask ? __ffs(pmask) - 1 : 31;
+                prefix += __reduce_add_sync(0xffffffffu, lane <= k ? (unsigned int)d[j] : 0u);
+                found = pmask != 0;
+            }
+        }
+        if (found) break;
+        pos -= 32 * K;
+    }
+    if (publish && lane == 0) st_relaxed(desc + t, tag | kFlagP | (unsigned int)(prefix + agg));
+    return prefix;
+}
+
+// Split form of the wide look-back for software-pipelined blocks, which
+// publish a tile's aggregate as soon as it is known and walk its look-back
+// one tile later: publish_aggregate, then lookback_prefix_wide, then
+// publish_inclusive. Tile 0's aggregate is its inclusive prefix at once.
+__device__ __forceinline__ void publish_aggregate(unsigned long long *desc, unsigned int t, unsigned int agg,
+                                                  unsigned long long tag) {
+    st_relaxed(desc + t, tag | (t == 0 ? kFlagP : 0ull) | agg);
+}
+
+__device__ __forceinline__ void publish_inclusive(unsigned long long *desc, unsigned int t, unsigned int incl,
+                                                  unsigned long long tag) {
+    st_relaxed(desc + t, tag | kFlagP | incl);
+}
+
+// Sum of tiles 0 .. t-1 (all 32 lanes call it). Stops at the nearest word
+// holding an inclusive prefix; a round needs readiness only up to there, so
+// slow far-away words are never waited for.
+template <int K>
+__device__ __forceinline__ unsigned int lookback_prefix_wide(const unsigned long long *desc, unsigned int t,
+                                                             unsigned long long tag, WsHeader *hdr,
+                                                             unsigned long long limit_ns, int lane) {
+    if (t == 0) return 0u;
+    unsigned int prefix = 0;
+    long long pos = (long long)t - 1;
+    while (true) {
+        unsigned long long d[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const long long idx = pos - 32 * j - lane;
+            d[j] = idx >= 0 ? ld_relaxed(desc + idx) : (tag | kFlagP);
+        }
+        unsigned long long t0 = 0;
+        for (unsigned int iter = 0;; ++iter) {
+            // Distance order: word j of lane l is 32 * j + l + 1 tiles back.
+            // Find the first word (in that order) that is either not ready
+            // or an inclusive prefix.
+            int stop_j = K, stop_lane = 0;
+            bool stop_ready = true;
+#pragma unroll
+            for (int j = K - 1; j >= 0; --j) {
+                const bool ready = (d[j] & kTagMask) == tag;
+                const unsigned int m = __ballot_sync(0xffffffffu, !ready || (d[j] & kFlagP));
+                if (m) {
+                    stop_j = j;
+                    stop_lane = __ffs(m) - 1;
+                    stop_ready = (__shfl_sync(0xffffffffu, ready ? 1u : 0u, stop_lane) != 0);
+                }
+            }
+            if (stop_j == K) {  // whole window ready, no inclusive prefix: add it all, move back
+                unsigned int sum = 0;
+#pragma unroll
+                for (int j = 0; j < K; ++j) sum += (unsigned int)d[j];
+                prefix += __reduce_add_sync(0xffffffffu, sum);
+                break;
+            }
+            if (stop_ready) {  // an inclusive prefix with everything nearer ready: done
+                unsigned int sum = 0;
+#pragma unroll
+                for (int j = 0; j < K; ++j)
+                    if (j < stop_j || (j == stop_j && lane <= stop_lane)) sum += (unsigned int)d[j];
+                prefix += __reduce_add_sync(0xffffffffu, sum);
+                return prefix;
+            }
+            // A nearer word is not ready yet: reload the words not ready.
+            if (iter == 0) t0 = __shfl_sync(0xffffffffu, globaltimer(), 0);
+            if (iter >= 8) __nanosleep(32);
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const long long idx = pos - 32 * j - lane;
+                if (idx >= 0 && (d[j] & kTagMask) != tag) d[j] = ld_relaxed(desc + idx);
+            }
+            const unsigned long long now = __shfl_sync(0xffffffffu, globaltimer(), 0);
+            if (iter > 0 && (now - t0 > limit_ns || iter >= kMaxSpinIters)) {
+                if (lane == 0) report_timeout(hdr, t);
+#pragma unroll
+                for (int j = 0; j < K; ++j)
+                    if ((d[j] & kTagMask) != tag) d[j] = tag | kFlagP;
+            }
+        }
+        pos -= 32 * K;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory staging with the Tensor Memory Accelerator's bulk copy
+// (cp.async.bulk, 1-D: 16-byte aligned addresses, size a multiple of 16)
+// completing on an mbarrier.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned int smem_u32(const void *p) {
+    return static_cast<unsigned int>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(unsigned int bar, unsigned int count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier shared-memory accesses (and, after a block
+// barrier, those of the block) before later async-proxy (bulk copy) ones.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned int bar, unsigned int bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned int bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned int bar, unsigned int parity) {
+    unsigned int done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    return done != 0;
+}
+
+// Wait for phase `parity` of the barrier to complete, bounded by limit_ns
+// (and an iteration cap). Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned int bar, unsigned int parity,
+                                                  unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (unsigned int iter = 0; iter < kMaxSpinIters; ++iter) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > limit_ns) return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(unsigned int dst_smem, const void *src, unsigned int bytes,
+                                          unsigned int bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst_smem),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // Host-side workspace sizing of each operation (defined beside its kernels).
 size_t scan_workspace_bytes(unsigned long long n);
 

@@ -26,6 +26,26 @@
 
 #include "internal.cuh"
 
+// Persistent launch shape (threads, u32x4 loads per thread per tile, ring
+// stages, look-back words per lane, minimum resident blocks per SM); the
+// defaults were chosen by measurement on GB300 and can be overridden at
+// build time for tuning sweeps.
+#ifndef U32SCAN_P_THREADS
+#define U32SCAN_P_THREADS 512
+#endif
+#ifndef U32SCAN_P_V
+#define U32SCAN_P_V 8
+#endif
+#ifndef U32SCAN_P_STAGES
+#define U32SCAN_P_STAGES 2
+#endif
+#ifndef U32SCAN_P_LOOK
+#define U32SCAN_P_LOOK 2
+#endif
+#ifndef U32SCAN_P_MINB
+#define U32SCAN_P_MINB 1
+#endif
+
 namespace u32scan {
 
 template <int THREADS, int V, bool INCLUSIVE>
@@ -137,21 +157,284 @@ scan_u32_kernel(uint32_t *__restrict__ data, unsigned long long n, uint32_t *tot
     }
 }
 
-// Launch shapes, chosen by n: long arrays take wide tiles (few carries to
-// chain), short ones narrow tiles (enough blocks to fill the GPU).
+// Persistent form for long arrays. Each block loops over tiles drawn from
+// the tile counter, keeping S tiles in flight: tile loads are 1-D bulk
+// copies (TMA) into an S-deep ring of shared-memory stages, each completing
+// on its own mbarrier, so global loads keep streaming while the block waits
+// on a predecessor's carry.
+//
+// The block is software-pipelined by one tile: in each round it scans the
+// next tile locally and publishes that tile's aggregate, then walks the
+// look-back of the current tile (whose aggregate went out a round earlier),
+// adds the prefix and stores it. Aggregates thus appear one round before any
+// tile needs them, and a look-back never waits on a neighbour that is
+// merely behind in its own queue.
+//
+// Tiles are drawn in globally increasing order and each block processes its
+// draws in order, so every predecessor of a waiting tile is held by a running
+// block that publishes it (forward progress). Each block draws exactly S
+// indices past the last tile; the draw of n_tiles + S * gridDim.x - 1 is the
+// last of the launch and re-arms the header.
+template <int V, bool INCLUSIVE>
+__device__ __forceinline__ unsigned int warp_scan_rounds(uint4 (&x)[V], int lane) {
+    unsigned int carry = 0;
+#pragma unroll
+    for (int r = 0; r < V; ++r) {
+        const unsigned int sum = x[r].x + x[r].y + x[r].z + x[r].w;
+        const unsigned int inc = warp_inclusive_sum(sum, lane);
+        const unsigned int ex = carry + (inc - sum);
+        if (INCLUSIVE) {
+            x[r].x += ex;
+            x[r].y += x[r].x;
+            x[r].z += x[r].y;
+            x[r].w += x[r].z;
+        } else {
+            const unsigned int a = x[r].x, b = x[r].y, c = x[r].z;
+            x[r].x = ex;
+            x[r].y = ex + a;
+            x[r].z = x[r].y + b;
+            x[r].w = x[r].z + c;
+        }
+        carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    return carry;
+}
+
+template <int THREADS, int V, int S, int K, bool INCLUSIVE>
+__global__ void __launch_bounds__(THREADS, U32SCAN_P_MINB)
+scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t *total, WsHeader *hdr,
+                    unsigned long long *desc, unsigned int n_tiles, unsigned int head, unsigned int skip_tile,
+                    unsigned long long limit_ns) {
+    constexpr int WARPS = THREADS / 32;
+    constexpr unsigned int TILE = THREADS * V * 4;
+    constexpr unsigned int TILE_BYTES = TILE * 4;
+    static_assert(WARPS <= 32, "one warp scans the warp totals");
+    static_assert(S >= 2, "the pipeline reads one stage ahead");
+    extern __shared__ __align__(128) uint4 stage_buf[];  // S stages of TILE elements
+    __shared__ __align__(8) unsigned long long bar[S];
+    __shared__ unsigned int s_tile[S];
+    __shared__ unsigned int s_wt[2][WARPS];  // warp totals of the current / next tile
+    __shared__ unsigned int s_base[WARPS];   // per-warp prefix of the current tile
+    __shared__ unsigned int s_epoch;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const unsigned int last_draw = n_tiles + (unsigned int)S * gridDim.x - 1u;
+    uint32_t *vbase = reinterpret_cast<uint32_t *>(reinterpret_cast<uintptr_t>(data) - 4ull * head);
+    // The producer (lane 0 of the last warp) draws tiles and starts their
+    // copies, so its atomic round trip stays off warp 0's look-back path.
+    const bool producer = threadIdx.x == THREADS - 32;
+    unsigned int latest_parity = 0;  // producer: bit st = phase parity of stage st's latest draw
+
+    auto tile_full = [&](unsigned int id) {
+        const unsigned long long v0 = (unsigned long long)id * TILE;
+        return v0 >= head && v0 + TILE <= head + n;
+    };
+    auto issue = [&](int st) {  // producer only
+        const unsigned int id = atom_add_acq_rel(&hdr->counter, 1u);
+        if (id == last_draw) {
+            st_relaxed_u32(&hdr->counter, 0u);
+            st_relaxed_u32(&hdr->epoch, s_epoch + 1u);
+        }
+        s_tile[st] = id;
+        const unsigned int b = smem_u32(&bar[st]);
+        if (id < n_tiles && tile_full(id)) {
+            mbar_arrive_expect_tx(b, TILE_BYTES);
+            bulk_load(smem_u32(stage_buf + st * (TILE / 4)), vbase + (unsigned long long)id * TILE, TILE_BYTES, b);
+        } else {
+            mbar_arrive(b);  // nothing to copy: a partial tile reads global memory, a past-the-end draw stops
+        }
+    };
+    const unsigned int li0 = (unsigned int)warp * (128 * V) + 4u * (unsigned int)lane;
+    volatile unsigned int *vs_tile = s_tile;
+
+    // Read draw number u (stage u % S) into x and scan it per warp; the warp
+    // totals go to s_wt[u & 1]. Returns the tile index, n_tiles if the draw
+    // is past the end, or n_tiles + 1 if its copy timed out.
+    auto read_tile = [&](unsigned int u, uint4 (&x)[V]) -> unsigned int {
+        const int st = (int)(u % S);
+        if (!mbar_wait_bounded(smem_u32(&bar[st]), (u / S) & 1u, limit_ns)) {
+            report_timeout(hdr, 0xfffffffeu);
+            return n_tiles + 1u;
+        }
+        const unsigned int t = vs_tile[st];
+        if (t >= n_tiles) return n_tiles;
+        const unsigned long long tile_v0 = (unsigned long long)t * TILE;
+        if (tile_full(t)) {
+            const uint4 *sb = stage_buf + st * (TILE / 4) + (li0 >> 2);
+#pragma unroll
+            for (int r = 0; r < V; ++r) x[r] = sb[32 * r];
+        } else {
+            const unsigned int lo = tile_v0 < head ? (unsigned int)(head - tile_v0) : 0u;
+            const unsigned long long left = head + n - tile_v0;
+            const unsigned int hi = left < TILE ? (unsigned int)left : TILE;
+            const uint32_t *tb = vbase + tile_v0;
+#pragma unroll
+            for (int r = 0; r < V; ++r) {
+                unsigned int e[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const unsigned int li = li0 + 128 * r + c;
+                    e[c] = (li >= lo && li < hi) ? tb[li] : 0u;
+                }
+                x[r] = make_uint4(e[0], e[1], e[2], e[3]);
+            }
+        }
+        const unsigned int wtot = warp_scan_rounds<V, INCLUSIVE>(x, lane);
+        if (lane == 0) s_wt[u & 1][warp] = wtot;
+        return t;
+    };
+    auto store_tile = [&](unsigned int t, const uint4 (&x)[V], unsigned int base) {
+        const unsigned long long tile_v0 = (unsigned long long)t * TILE;
+        uint32_t *tb = vbase + tile_v0;
+        if (tile_full(t)) {
+#pragma unroll
+            for (int r = 0; r < V; ++r) {
+                const uint4 y = make_uint4(x[r].x + base, x[r].y + base, x[r].z + base, x[r].w + base);
+                __stcs(reinterpret_cast<uint4 *>(tb + li0 + 128 * r), y);
+            }
+        } else {
+            const unsigned int lo = tile_v0 < head ? (unsigned int)(head - tile_v0) : 0u;
+            const unsigned long long left = head + n - tile_v0;
+            const unsigned int hi = left < TILE ? (unsigned int)left : TILE;
+#pragma unroll
+            for (int r = 0; r < V; ++r) {
+                const unsigned int e[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const unsigned int li = li0 + 128 * r + c;
+                    if (li >= lo && li < hi) tb[li] = e[c] + base;
+                }
+            }
+        }
+    };
+    // Warp 0: block aggregate of the tile whose warp totals are in s_wt[slot];
+    // returns it, and leaves in wex this lane's exclusive warp offset.
+    auto block_aggregate = [&](int slot, unsigned int &wex) -> unsigned int {
+        const unsigned int wt = lane < WARPS ? s_wt[slot][lane] : 0u;
+        const unsigned int winc = warp_inclusive_sum(wt, lane);
+        wex = winc - wt;
+        return __shfl_sync(0xffffffffu, winc, 31);
+    };
+
+    if (producer) {
+#pragma unroll
+        for (int st = 0; st < S; ++st) mbar_init(smem_u32(&bar[st]), 1u);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        s_epoch = ld_relaxed_u32(&hdr->epoch);
+#pragma unroll
+        for (int st = 0; st < S; ++st) issue(st);
+    }
+    __syncthreads();
+    const unsigned long long tag = tag_of(s_epoch);
+
+    // Prologue: read draw 0.
+    uint4 xc[V], xn[V];
+    unsigned int tc = read_tile(0, xc);
+    unsigned int agg_c = 0, wex_c = 0;
+    if (!__syncthreads_or(tc >= n_tiles)) {
+        if (producer) {
+            fence_proxy_async_smem();
+            issue(0);
+            latest_parity ^= 1u;
+        }
+        if (warp == 0) {
+            agg_c = block_aggregate(0, wex_c);
+            if (lane == 0 && tc != skip_tile) publish_aggregate(desc, tc, agg_c, tag);
+        }
+        for (unsigned int u = 1;; ++u) {
+            // Look ahead: read draw u and publish its aggregate.
+            const unsigned int tn = read_tile(u, xn);
+            const bool more = !__syncthreads_or(tn >= n_tiles);  // barrier A
+            unsigned int agg_n = 0, wex_n = 0;
+            if (more && producer) {
+                fence_proxy_async_smem();
+                const int st = (int)(u % S);
+                issue(st);
+                latest_parity ^= 1u << st;
+            }
+            if (warp == 0) {
+                if (more) {
+                    agg_n = block_aggregate((int)(u & 1), wex_n);
+                    if (lane == 0 && tn != skip_tile) publish_aggregate(desc, tn, agg_n, tag);
+                }
+                // Finish the current tile: its look-back, inclusive prefix, bases.
+                const unsigned int prefix = lookback_prefix_wide<K>(desc, tc, tag, hdr, limit_ns, lane);
+                if (lane == 0 && tc != 0 && tc != skip_tile) publish_inclusive(desc, tc, prefix + agg_c, tag);
+                if (lane < WARPS) s_base[lane] = prefix + wex_c;
+                if (tc == n_tiles - 1u && lane == 0 && total != nullptr) *total = prefix + agg_c;
+            }
+            __syncthreads();  // barrier B: bases of the current tile are visible
+            store_tile(tc, xc, s_base[warp]);
+            if (!more) break;
+#pragma unroll
+            for (int r = 0; r < V; ++r) xc[r] = xn[r];
+            tc = tn;
+            agg_c = agg_n;
+            wex_c = wex_n;
+        }
+    }
+    // Leave no bulk copy in flight into this block's shared memory: wait
+    // (bounded) for the latest phase of every stage. On the normal path the
+    // outstanding draws are all past the end and have completed already.
+    if (producer) {
+#pragma unroll
+        for (int st = 0; st < S; ++st)
+            (void)mbar_wait_bounded(smem_u32(&bar[st]), (latest_parity >> st) & 1u, limit_ns);
+    }
+}
+
+// Launch shapes, chosen by n: long arrays use the persistent kernel, short
+// ones the one-tile-per-block kernel (narrow tiles, enough blocks).
+constexpr int kPThreads = U32SCAN_P_THREADS, kPV = U32SCAN_P_V, kPStages = U32SCAN_P_STAGES,
+              kPLook = U32SCAN_P_LOOK;
+constexpr unsigned long long kPTile = (unsigned long long)kPThreads * kPV * 4;
+constexpr size_t kPSmem = (size_t)kPStages * kPTile * 4;
+constexpr unsigned long long kPersistentMinN = 1ull << 22;
+
 struct ScanShape {
+    bool persistent;
     int threads, v;
     unsigned long long tile() const { return (unsigned long long)threads * v * 4; }
 };
 
 static ScanShape scan_shape(unsigned long long n) {
-    if (n >= (1ull << 22)) return {512, 8};
-    return {256, 2};
+    if (n >= kPersistentMinN) return {true, kPThreads, kPV};
+    return {false, 256, 2};
 }
 
 size_t scan_workspace_bytes(unsigned long long n) {
     const unsigned long long tiles = (n + 3 + scan_shape(n).tile() - 1) / scan_shape(n).tile();
     return round_up(kHeaderBytes + 8 * tiles, 256);
+}
+
+// Per-device launch facts for the persistent kernels, looked up once.
+struct DeviceFacts {
+    int sms = 0;
+    int blocks_per_sm[2] = {0, 0};
+};
+static std::mutex g_facts_mu;
+static DeviceFacts g_facts[64];
+
+template <bool INCLUSIVE>
+static int persistent_grid(int *grid_out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return U32SCAN_ECUDA;
+    std::lock_guard<std::mutex> lock(g_facts_mu);
+    DeviceFacts &f = g_facts[dev];
+    if (f.sms == 0 && cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return U32SCAN_ECUDA;
+    int &bps = f.blocks_per_sm[INCLUSIVE ? 1 : 0];
+    if (bps == 0) {
+        auto kern = scan_u32_persistent<kPThreads, kPV, kPStages, kPLook, INCLUSIVE>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem) != cudaSuccess)
+            return U32SCAN_ECUDA;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, kPThreads, kPSmem) != cudaSuccess || bps < 1)
+            return U32SCAN_ECUDA;
+    }
+    *grid_out = f.sms * bps;
+    return U32SCAN_OK;
 }
 
 template <bool INCLUSIVE>
@@ -171,12 +454,17 @@ static int scan_launch(uint32_t *data, unsigned long long n, uint32_t *total, vo
     const unsigned int n_tiles = (unsigned int)((n + head + sh.tile() - 1) / sh.tile());
     WsHeader *hdr = static_cast<WsHeader *>(ws);
     unsigned long long *desc = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
-    if (sh.threads == 512)
-        scan_u32_kernel<512, 8, INCLUSIVE><<<n_tiles, 512, 0, stream>>>(data, n, total, hdr, desc, n_tiles, head,
-                                                                        skip_tile, limit_ns);
-    else
+    if (sh.persistent) {
+        int grid = 0;
+        const int rc = persistent_grid<INCLUSIVE>(&grid);
+        if (rc != U32SCAN_OK) return rc;
+        if ((unsigned int)grid > n_tiles) grid = (int)n_tiles;
+        scan_u32_persistent<kPThreads, kPV, kPStages, kPLook, INCLUSIVE><<<grid, kPThreads, kPSmem, stream>>>(
+            data, n, total, hdr, desc, n_tiles, head, skip_tile, limit_ns);
+    } else {
         scan_u32_kernel<256, 2, INCLUSIVE><<<n_tiles, 256, 0, stream>>>(data, n, total, hdr, desc, n_tiles, head,
                                                                         skip_tile, limit_ns);
+    }
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }
 

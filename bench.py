@@ -331,7 +331,7 @@ def run_ours(args, rank, local_rank, world):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": traffic, "algorithmic_bytes_per_launch": BYTES_PER_ELEM * N,
-                     "kernel": "scan_u32_persistent<512,8,2,2,exclusive>"},
+                     "kernel": "scan_u32_persistent<512,8,2,1,exclusive>"},
         "e2e": {"value": world * N / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": 4 * N, "d2h_bytes_per_step": 4 * N + 4},
         "clocks": clocks,

@@ -259,23 +259,32 @@ __device__ __forceinline__ void publish_inclusive(unsigned long long *desc, unsi
     st_relaxed(desc + t, tag | kFlagP | incl);
 }
 
-// Sum of tiles 0 .. t-1 (all 32 lanes call it). Stops at the nearest word
-// holding an inclusive prefix; a round needs readiness only up to there, so
-// slow far-away words are never waited for.
+// First look-back window of tile t: word j of lane l is the carry word of
+// the tile 32 * j + l + 1 places back (a virtual inclusive 0 before tile 0).
+// Loading it early lets its L2 round trip overlap other work.
+template <int K>
+__device__ __forceinline__ void lookback_window(const unsigned long long *desc, long long pos,
+                                                unsigned long long tag, int lane, unsigned long long (&d)[K]) {
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        const long long idx = pos - 32 * j - lane;
+        d[j] = idx >= 0 ? ld_relaxed(desc + idx) : (tag | kFlagP);
+    }
+}
+
+// Sum of tiles 0 .. t-1 (all 32 lanes call it), starting from a first
+// window `d` already loaded by lookback_window(desc, t - 1, ...). Stops at
+// the nearest word holding an inclusive prefix; a round needs readiness only
+// up to there, so slow far-away words are never waited for.
 template <int K>
 __device__ __forceinline__ unsigned int lookback_prefix_wide(const unsigned long long *desc, unsigned int t,
                                                              unsigned long long tag, WsHeader *hdr,
-                                                             unsigned long long limit_ns, int lane) {
+                                                             unsigned long long limit_ns, int lane,
+                                                             unsigned long long (&d)[K]) {
     if (t == 0) return 0u;
     unsigned int prefix = 0;
     long long pos = (long long)t - 1;
     while (true) {
-        unsigned long long d[K];
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            const long long idx = pos - 32 * j - lane;
-            d[j] = idx >= 0 ? ld_relaxed(desc + idx) : (tag | kFlagP);
-        }
         unsigned long long t0 = 0;
         for (unsigned int iter = 0;; ++iter) {
             // Distance order: word j of lane l is 32 * j + l + 1 tiles back.
@@ -325,6 +334,7 @@ __device__ __forceinline__ unsigned int lookback_prefix_wide(const unsigned long
             }
         }
         pos -= 32 * K;
+        lookback_window<K>(desc, pos, tag, lane, d);
     }
 }
 

@@ -40,7 +40,7 @@
 #define U32SCAN_P_STAGES 2
 #endif
 #ifndef U32SCAN_P_LOOK
-#define U32SCAN_P_LOOK 2
+#define U32SCAN_P_LOOK 1
 #endif
 #ifndef U32SCAN_P_MINB
 #define U32SCAN_P_MINB 1
@@ -360,7 +360,9 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
                     if (lane == 0 && tn != skip_tile) publish_aggregate(desc, tn, agg_n, tag);
                 }
                 // Finish the current tile: its look-back, inclusive prefix, bases.
-                const unsigned int prefix = lookback_prefix_wide<K>(desc, tc, tag, hdr, limit_ns, lane);
+                unsigned long long win[K];
+                lookback_window<K>(desc, (long long)tc - 1, tag, lane, win);
+                const unsigned int prefix = lookback_prefix_wide<K>(desc, tc, tag, hdr, limit_ns, lane, win);
                 if (lane == 0 && tc != 0 && tc != skip_tile) publish_inclusive(desc, tc, prefix + agg_c, tag);
                 if (lane < WARPS) s_base[lane] = prefix + wex_c;
                 if (tc == n_tiles - 1u && lane == 0 && total != nullptr) *total = prefix + agg_c;

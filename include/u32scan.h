@@ -101,6 +101,43 @@ int scan_inclusive_u32(uint32_t *data, size_t n, uint32_t *total,
                        void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /*
+ * Segmented inclusive scan, in place, optionally with per-segment sums.
+ * Source: "Futhark.Pass.ExtractKernels.Segmented" (regularSegmentedScan;
+ * regularSegmentedRedomap for the per-segment reduce, "a single value per
+ * segment"). A non-zero head_flags[j] opens a segment at j; index 0 always
+ * opens one. data[j] becomes data[h] + .. + data[j] (mod 2^32), h the last
+ * head at or before j.
+ *   data         device, uint32_t[n], read and overwritten.
+ *   head_flags   device, int32_t[n], read only.
+ *   n            element count, below 2^32.
+ *   seg_sums     device, uint32_t[seg_capacity] or NULL: seg_sums[k] gets
+ *                the wrapped sum of segment k (segments in index order);
+ *                segments k >= seg_capacity are not written.
+ *   seg_capacity slots in seg_sums (ignored when seg_sums is NULL).
+ *   nseg         device, one uint32_t or NULL: the number of segments
+ *                (0 when n == 0), even when it exceeds seg_capacity.
+ *   ws, ws_bytes u32scan_workspace_bytes(U32SCAN_OP_SEGSCAN, n) bytes.
+ * data and head_flags need 4-byte alignment; when their addresses differ
+ * mod 16 the kernel falls back to scalar loads (correct, slower).
+ * Errors: EINVAL (null data/flags with n > 0, misaligned pointers,
+ * n >= 2^32), EWORKSPACE, ECUDA.
+ */
+int segscan_inclusive_u32(uint32_t *data, const int32_t *head_flags, size_t n,
+                          uint32_t *seg_sums, size_t seg_capacity, uint32_t *nseg,
+                          void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * Per-segment reduce: the sums and count of segscan_inclusive_u32 without
+ * writing the scan (data is only read). Source as above
+ * (regularSegmentedRedomap). At least one of seg_sums and nseg must be
+ * non-NULL (EINVAL otherwise); other arguments and errors as
+ * segscan_inclusive_u32.
+ */
+int segreduce_u32(const uint32_t *data, const int32_t *head_flags, size_t n,
+                  uint32_t *seg_sums, size_t seg_capacity, uint32_t *nseg,
+                  void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
  * Exclusive scan that allocates nothing and needs no workspace argument.
  * The pages have no counterpart: this entry point exists for callers that
  * cannot allocate device memory (for instance code inside an allocator's

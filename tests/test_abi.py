@@ -90,3 +90,20 @@ def test_package_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_native, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         _native.lib()
+
+
+@pytest.mark.parametrize("name", ["segscan_inclusive_u32", "segreduce_u32"])
+def test_segmented_rejects_bad_arguments_on_host(lib, name):
+    fn = getattr(lib, name)
+    fake = 0x10000
+    need = lib.u32scan_workspace_bytes(_native.OP_SEGSCAN, 1000)
+    assert need >= 256 + 16 * (1000 // 8192)
+    assert fn(None, fake, 10, fake, 10, fake, fake, need, None) == _native.EINVAL      # null data
+    assert fn(fake, None, 10, fake, 10, fake, fake, need, None) == _native.EINVAL      # null flags
+    assert fn(fake, fake + 2, 10, fake, 10, fake, fake, need, None) == _native.EINVAL  # misaligned flags
+    assert fn(fake, fake, 10, fake + 1, 10, fake, fake, need, None) == _native.EINVAL  # misaligned sums
+    assert fn(fake, fake, 1 << 32, fake, 10, fake, fake, 1 << 40, None) == _native.EINVAL
+    assert fn(fake, fake, 1000, fake, 10, fake, None, need, None) == _native.EWORKSPACE
+    assert fn(fake, fake, 1000, fake, 10, fake, fake, need - 256, None) == _native.EWORKSPACE
+    assert fn(None, None, 0, None, 0, None, None, 0, None) == (_native.EINVAL if name == "segreduce_u32"
+                                                               else _native.OK)

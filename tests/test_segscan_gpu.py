@@ -1,0 +1,162 @@
+"""GPU parity of the segmented scan and per-segment reduce against the CPU
+oracle, through the C ABI: bit-exact scans, sums and counts over head
+patterns from one segment to all heads, geometric and length-4 segments,
+ragged tails, misaligned and differently aligned streams, a capacity below
+the segment count, repeated calls on one workspace, and both benchmark
+workloads at full size (n = 2^26)."""
+
+import numpy as np
+import pytest
+
+import oracle
+from u32_prefix_scan_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def u():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from u32_prefix_scan_gb300 import build
+
+    build.build()
+    import u32_prefix_scan_gb300 as u
+
+    return u
+
+
+def dev(a: np.ndarray, offset: int = 0):
+    buf = torch.empty(a.size + offset + 4, dtype=torch.int32, device="cuda")
+    view = buf[offset: offset + a.size]
+    view.copy_(torch.from_numpy(np.ascontiguousarray(a).view(np.int32)))
+    return view
+
+
+def host(t) -> np.ndarray:
+    return t.cpu().numpy().view(np.uint32)
+
+
+def heads(kind: str, n: int, seed: int = 3) -> np.ndarray:
+    if kind == "geometric":
+        return inputs.segment_heads_geometric(n, seed)
+    if kind == "geometric16":
+        return inputs.segment_heads_geometric(n, seed, log2_mean=4)
+    if kind == "regular4":
+        return inputs.segment_heads_regular(n, 4)
+    if kind == "regular7":
+        return inputs.segment_heads_regular(n, 7)
+    if kind == "all":
+        return np.ones(n, np.int32)
+    if kind == "none":
+        return np.zeros(n, np.int32)
+    if kind == "half":
+        f = (inputs.splitmix_u32(seed, 1, n) < np.uint32(1 << 31)).astype(np.int32)
+        f[f != 0] = np.where(np.arange(int(f.sum())) % 3 == 0, -5, 9)  # any non-zero value is a head
+        return f
+    raise ValueError(kind)
+
+
+def check_segscan(u, a, f, offset_a=0, offset_f=0, cap=None):
+    n = a.size
+    d, fl = dev(a, offset_a), dev(f, offset_f)
+    want_sums, want_nseg = oracle.segreduce(a, f)
+    cap = max(n, 1) if cap is None else cap
+    sums = torch.full((max(cap, 1),), -1, dtype=torch.int32, device="cuda")
+    nseg = u.segscan_inclusive_u32(d, fl, sums[:cap] if cap else None)
+    u.check()
+    assert np.array_equal(host(d), oracle.segscan_inclusive(a, f))
+    assert int(host(nseg)[0]) == want_nseg
+    k = min(cap, want_nseg)
+    assert np.array_equal(host(sums)[:k], want_sums[:k])
+    assert np.all(host(sums)[k:cap] == 0xFFFFFFFF)  # nothing written past the segments / capacity
+
+
+SIZES = [1, 2, 5, 4096 + 3, 8192, 8192 + 1, 3 * 8192 + 77, 100003, (1 << 20) + 5]
+
+
+@pytest.mark.parametrize("kind", ["geometric", "geometric16", "regular4", "regular7", "all", "none", "half"])
+@pytest.mark.parametrize("n", SIZES)
+def test_segscan_parity(u, kind, n):
+    check_segscan(u, inputs.scan_values(n, 3), heads(kind, n))
+
+
+@pytest.mark.parametrize("offsets", [(1, 1), (2, 2), (3, 3), (1, 2), (0, 3), (3, 0)])
+@pytest.mark.parametrize("n", [7, 8192 * 3 + 5, (1 << 18) + 3])
+def test_segscan_misaligned(u, offsets, n):
+    check_segscan(u, inputs.scan_values(n, 5), heads("half", n, 5), *offsets)
+
+
+def test_segscan_capacity_below_count(u):
+    n = 100003
+    check_segscan(u, inputs.scan_values(n, 3), heads("geometric16", n), cap=1000)
+
+
+@pytest.mark.parametrize("kind", ["geometric", "regular4", "half", "none"])
+@pytest.mark.parametrize("n", [1, 8192 + 1, 100003, (1 << 20) + 5])
+def test_segreduce_parity(u, kind, n):
+    a, f = inputs.scan_values(n, 3), heads(kind, n)
+    d, fl = dev(a), dev(f)
+    sums, nseg = u.segreduce_u32(d, fl)
+    u.check()
+    want_sums, want_nseg = oracle.segreduce(a, f)
+    assert int(host(nseg)[0]) == want_nseg
+    assert np.array_equal(host(sums)[:want_nseg], want_sums)
+    assert np.array_equal(host(d), a)  # the reduce leaves data as it was
+
+
+def test_segreduce_count_only_and_empty(u):
+    from u32_prefix_scan_gb300 import _native
+
+    lib = _native.lib()
+    n = 50000
+    a, f = inputs.scan_values(n, 3), heads("geometric16", n)
+    d, fl = dev(a), dev(f)
+    nseg = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = u.Workspace(lib.u32scan_workspace_bytes(_native.OP_SEGSCAN, n), torch.device("cuda"))
+    s = torch.cuda.current_stream().cuda_stream
+    assert lib.segreduce_u32(d.data_ptr(), fl.data_ptr(), n, None, 0, nseg.data_ptr(), ws.ptr, ws.nbytes,
+                             s) == _native.OK
+    assert lib.u32scan_check(ws.ptr, s) == _native.OK
+    assert int(nseg.item()) == oracle.segreduce(a, f)[1]
+    nseg.fill_(7)
+    assert lib.segscan_inclusive_u32(d.data_ptr(), fl.data_ptr(), 0, None, 0, nseg.data_ptr(), ws.ptr,
+                                     ws.nbytes, s) == _native.OK
+    torch.cuda.synchronize()
+    assert int(nseg.item()) == 0
+
+
+def test_repeated_calls_share_one_workspace(u):
+    ws = u.Workspace(1 << 20, torch.device("cuda"))
+    rng = np.random.default_rng(4)
+    for k in range(24):
+        n = int(rng.choice([1, 777, 8192 * 3, 100003, (1 << 20) + 5]))
+        a = inputs.splitmix_u32(9, 0, n, start=k * 1000)
+        f = heads(["geometric16", "regular4", "half"][k % 3], n, 9 + k)
+        d, fl = dev(a), dev(f)
+        if k % 2:
+            sums, nseg = u.segreduce_u32(d, fl, workspace=ws)
+            u.check(workspace=ws)
+            want, cnt = oracle.segreduce(a, f)
+            assert int(host(nseg)[0]) == cnt and np.array_equal(host(sums)[:cnt], want), k
+        else:
+            u.segscan_inclusive_u32(d, fl, workspace=ws)
+            u.check(workspace=ws)
+            assert np.array_equal(host(d), oracle.segscan_inclusive(a, f)), k
+
+
+@pytest.mark.parametrize("kind", ["geometric", "regular4"])
+def test_workload_2_26_full_parity(u, kind):
+    # The segmented benchmark configurations: n = 2^26, values u32(3, 0, i),
+    # heads Bernoulli(2^-10) (mean length 1024) or every 4th index.
+    n = 1 << 26
+    a = inputs.scan_values(n, 3)
+    f = heads(kind, n)
+    check_segscan(u, a, f)
+    d, fl = dev(a), dev(f)
+    sums, nseg = u.segreduce_u32(d, fl)
+    u.check()
+    want_sums, want_nseg = oracle.segreduce(a, f)
+    assert int(host(nseg)[0]) == want_nseg
+    assert np.array_equal(host(sums)[:want_nseg], want_sums)

@@ -10,6 +10,8 @@ _API = {
     "Workspace",
     "scan_exclusive_u32",
     "scan_inclusive_u32",
+    "segscan_inclusive_u32",
+    "segreduce_u32",
     "check",
 }
 

@@ -21,6 +21,8 @@ __all__ = [
     "Workspace",
     "scan_exclusive_u32",
     "scan_inclusive_u32",
+    "segscan_inclusive_u32",
+    "segreduce_u32",
     "check",
 ]
 
@@ -115,6 +117,53 @@ def scan_inclusive_u32(data: torch.Tensor, total: torch.Tensor | None = None, *,
     """In place: data[j] <- data[0] + .. + data[j] (mod 2^32). Returns the
     one-element device tensor holding the wrapped total."""
     return _scan("scan_inclusive_u32", data, total, stream, workspace)
+
+
+def _seg_args(data, head_flags, seg_sums, nseg):
+    _require_cuda(data, "data")
+    _require_cuda(head_flags, "head_flags", (torch.int32,))
+    if head_flags.numel() != data.numel():
+        raise ValueError("data and head_flags differ in length")
+    if seg_sums is not None:
+        _require_cuda(seg_sums, "seg_sums")
+    nseg = _scalar_out(nseg, data, data.dtype)
+    return nseg
+
+
+def segscan_inclusive_u32(data: torch.Tensor, head_flags: torch.Tensor, seg_sums: torch.Tensor | None = None,
+                          nseg: torch.Tensor | None = None, *, stream=None,
+                          workspace: Workspace | None = None) -> torch.Tensor:
+    """In place: data[j] <- sum of data over j's segment up to j (mod 2^32);
+    a non-zero head flag opens a segment, index 0 always does. If seg_sums
+    is given, seg_sums[k] <- segment k's sum (for k < seg_sums.numel()).
+    Returns the one-element device tensor holding the segment count."""
+    nseg = _seg_args(data, head_flags, seg_sums, nseg)
+    n = data.numel()
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_SEGSCAN, n, data.device, sh, workspace)
+    _native.check(_native.lib().segscan_inclusive_u32(
+        data.data_ptr(), head_flags.data_ptr(), n, seg_sums.data_ptr() if seg_sums is not None else None,
+        seg_sums.numel() if seg_sums is not None else 0, nseg.data_ptr(), ws.ptr, ws.nbytes, sh),
+        "segscan_inclusive_u32")
+    return nseg
+
+
+def segreduce_u32(data: torch.Tensor, head_flags: torch.Tensor, seg_sums: torch.Tensor | None = None,
+                  nseg: torch.Tensor | None = None, *, stream=None, workspace: Workspace | None = None):
+    """Per-segment wrapped sums without writing the scan. seg_sums defaults
+    to a fresh tensor of n elements (enough for any flag pattern). Returns
+    (seg_sums, nseg): the first nseg entries of seg_sums are the sums."""
+    if seg_sums is None:
+        _require_cuda(data, "data")
+        seg_sums = torch.empty(max(data.numel(), 1), dtype=data.dtype, device=data.device)
+    nseg = _seg_args(data, head_flags, seg_sums, nseg)
+    n = data.numel()
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_SEGSCAN, n, data.device, sh, workspace)
+    _native.check(_native.lib().segreduce_u32(
+        data.data_ptr(), head_flags.data_ptr(), n, seg_sums.data_ptr(), seg_sums.numel(), nseg.data_ptr(),
+        ws.ptr, ws.nbytes, sh), "segreduce_u32")
+    return seg_sums, nseg
 
 
 def check(stream=None, workspace: Workspace | None = None, device=None) -> int:

@@ -11,6 +11,8 @@ extern "C" size_t u32scan_workspace_bytes(int op, size_t n) {
     switch (op) {
     case U32SCAN_OP_SCAN:
         return scan_workspace_bytes(n);
+    case U32SCAN_OP_SEGSCAN:
+        return segscan_workspace_bytes(n);
     default:
         return 0;
     }

@@ -339,6 +339,98 @@ __device__ __forceinline__ unsigned int lookback_prefix_wide(const unsigned long
 }
 
 // ---------------------------------------------------------------------------
+// Segmented scans carry two words per tile (at desc2 + 2 * tile):
+//   word A  the segmented carry: value = sum since the last head in the
+//           summed range; kFlagH when that range holds a head (the value is
+//           then complete on its own); kFlagP when it is the final value at
+//           the tile's end;
+//   word B  the running head count (plain sum), kFlagP when final.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned int lanemask_le(int lane) { return 0xffffffffu >> (31 - lane); }
+__device__ __forceinline__ unsigned int lanemask_lt(int lane) { return (1u << lane) - 1u; }
+
+// Segmented inclusive scan across the lanes of a warp. Lane l holds the
+// segmented sum of its own run (`t`: the sum since its last head, or of the
+// whole run when `has_head` is false); `carry` is the segmented value before
+// lane 0. Returns the segmented value at the end of lane l's run. With P the
+// plain inclusive scan of t and L the last lane at or before l holding a
+// head, that value is P[l] - P[L-1] (or carry + P[l] when there is no L).
+__device__ __forceinline__ unsigned int warp_segmented_inclusive(unsigned int t, bool has_head, unsigned int carry,
+                                                                 int lane) {
+    const unsigned int P = warp_inclusive_sum(t, lane);
+    const unsigned int m = __ballot_sync(0xffffffffu, has_head) & lanemask_le(lane);
+    const int L = 31 - __clz(m | 1u);  // (m | 1) keeps the index valid; unused when m == 0
+    const unsigned int before_L = __shfl_sync(0xffffffffu, P - t, L);
+    return m ? P - before_L : carry + P;
+}
+
+struct SegPrefix {
+    unsigned int seg;  // segmented value just before the tile
+    unsigned int cnt;  // heads before the tile
+};
+
+// Both look-backs of tile t (all 32 lanes call it), 32 words per round trip
+// each; word A stops at the nearest word with a head or a final value, word
+// B at the nearest final count.
+__device__ __forceinline__ SegPrefix lookback_seg(const unsigned long long *desc2, unsigned int t,
+                                                  unsigned long long tag, WsHeader *hdr,
+                                                  unsigned long long limit_ns, int lane) {
+    SegPrefix pre{0u, 0u};
+    if (t == 0) return pre;
+    long long pos_a = (long long)t - 1, pos_b = pos_a;
+    bool done_a = false, done_b = false;
+    unsigned long long wa = 0, wb = 0;
+    bool need_a = true, need_b = true;  // the window at pos_a / pos_b must be (re)loaded
+    unsigned long long t0 = 0;
+    for (unsigned int iter = 0;; ++iter) {
+        const long long ia = pos_a - lane, ib = pos_b - lane;
+        if (!done_a && need_a) wa = ia >= 0 ? ld_relaxed(desc2 + 2 * ia) : (tag | kFlagP);
+        if (!done_b && need_b) wb = ib >= 0 ? ld_relaxed(desc2 + 2 * ib + 1) : (tag | kFlagP);
+        bool waiting = false;
+        if (!done_a) {
+            const bool ready = (wa & kTagMask) == tag;
+            const unsigned int m = __ballot_sync(0xffffffffu, !ready || (wa & (kFlagP | kFlagH)));
+            const int k = m ? __ffs(m) - 1 : 31;
+            const bool k_ready = __shfl_sync(0xffffffffu, ready ? 1u : 0u, k) != 0;
+            if (k_ready) {
+                pre.seg += __reduce_add_sync(0xffffffffu, lane <= k ? (unsigned int)wa : 0u);
+                if (m) done_a = true; else pos_a -= 32;
+                need_a = true;
+            } else {
+                waiting = true;
+                need_a = !ready;  // reload only the words not ready yet
+            }
+        }
+        if (!done_b) {
+            const bool ready = (wb & kTagMask) == tag;
+            const unsigned int m = __ballot_sync(0xffffffffu, !ready || (wb & kFlagP));
+            const int k = m ? __ffs(m) - 1 : 31;
+            const bool k_ready = __shfl_sync(0xffffffffu, ready ? 1u : 0u, k) != 0;
+            if (k_ready) {
+                pre.cnt += __reduce_add_sync(0xffffffffu, lane <= k ? (unsigned int)wb : 0u);
+                if (m) done_b = true; else pos_b -= 32;
+                need_b = true;
+            } else {
+                waiting = true;
+                need_b = !ready;
+            }
+        }
+        if (done_a && done_b) return pre;
+        if (waiting) {
+            if (t0 == 0) t0 = __shfl_sync(0xffffffffu, globaltimer(), 0) | 1ull;
+            if (iter >= 8) __nanosleep(32);
+            const unsigned long long now = __shfl_sync(0xffffffffu, globaltimer(), 0);
+            if (now - t0 > limit_ns || iter >= kMaxSpinIters) {
+                if (lane == 0) report_timeout(hdr, t);
+                if (!done_a && (wa & kTagMask) != tag) wa = tag | kFlagP;
+                if (!done_b && (wb & kTagMask) != tag) wb = tag | kFlagP;
+                need_a = need_b = false;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Shared-memory staging with the Tensor Memory Accelerator's bulk copy
 // (cp.async.bulk, 1-D: 16-byte aligned addresses, size a multiple of 16)
 // completing on an mbarrier.
@@ -400,5 +492,6 @@ __device__ __forceinline__ void bulk_load(unsigned int dst_smem, const void *src
 
 // Host-side workspace sizing of each operation (defined beside its kernels).
 size_t scan_workspace_bytes(unsigned long long n);
+size_t segscan_workspace_bytes(unsigned long long n);
 
 }  // namespace u32scan

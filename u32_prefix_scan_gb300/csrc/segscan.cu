@@ -1,0 +1,421 @@
+// segscan.cu -- segmented inclusive U32 scan and per-segment reduce.
+//
+// Source: "Futhark.Pass.ExtractKernels.Segmented": regularSegmentedScan
+// names the segmented scan; regularSegmentedRedomap reduces every segment
+// "until there is only a single value per segment". Segments are marked by
+// head flags: a non-zero int32 flag at j opens a segment at j, and index 0
+// always opens one. The scan gives out[j] = a[h] + .. + a[j] (mod 2^32), h
+// the last head at or before j; the reduce gives one wrapped sum per
+// segment, in segment order, and the segment count.
+//
+// The page's two strategies (one group per segment for long segments,
+// several segments per group for short ones, chosen at run time) are prior
+// art: here one single-pass kernel serves every segment-length mix, because
+// the segmented operator (head, sum) is associative and carries across
+// tiles like a plain sum. A tile's carry stops at the nearest earlier tile
+// that holds a head.
+//
+// Kernel: persistent, one block per SM, the same one-tile software pipeline
+// as the plain scan (scan.cu): two 1-D bulk copies per tile (values and head
+// flags) into a ring of shared-memory stages; each round reads and scans
+// the next tile and publishes its aggregate, then walks the current tile's
+// look-back, adds the carry and stores. Per tile the look-back carries two
+// words (internal.cuh): the segmented value and the running head count; the
+// head count gives every segment end its index into the sums.
+//
+// Layout inside a tile (as in scan.cu): warp w owns the w-th run of 128 * V
+// elements; lane l holds, for r = 0 .. V-1, the four elements at 128 * r +
+// 4 * l of that run. Head flags become one bit per element (bit 4 * r + c).
+#include <cstdint>
+#include <mutex>
+#include <cuda_runtime.h>
+
+#include "internal.cuh"
+
+namespace u32scan {
+
+constexpr unsigned int kNoHead = 0xffffffffu;
+
+template <int THREADS, int V, int S, bool WRITE_SCAN, bool WANT_SUMS>
+__global__ void __launch_bounds__(THREADS, 1)
+segscan_u32_persistent(uint32_t *__restrict__ data, const int32_t *__restrict__ flags, unsigned long long n,
+                       uint32_t *seg_sums, unsigned long long seg_cap, uint32_t *nseg, WsHeader *hdr,
+                       unsigned long long *desc2, unsigned int n_tiles, unsigned int head, int streams_aligned,
+                       unsigned int skip_tile, unsigned long long limit_ns) {
+    constexpr int WARPS = THREADS / 32;
+    constexpr unsigned int CHUNK = 128 * V;  // elements per warp
+    constexpr unsigned int TILE = THREADS * V * 4;
+    constexpr unsigned int TILE_BYTES = TILE * 4;  // per stream
+    static_assert(WARPS <= 32 && 4 * V <= 32, "one lane per warp; head bits fit in a word");
+    extern __shared__ __align__(128) uint4 stage_buf[];  // S stages of [values | flags], TILE each
+    __shared__ __align__(8) unsigned long long bar[S];
+    __shared__ unsigned int s_tile[S];
+    __shared__ unsigned int s_wval[2][WARPS], s_wcnt[2][WARPS], s_whas[2][WARPS];
+    // Head bit of each warp's first element, read after barrier B by the
+    // previous warp; three slots, so a warp already reading the next tile
+    // never overwrites the slot of a tile still being stored.
+    __shared__ unsigned int s_wfirst[3][WARPS];
+    __shared__ unsigned int s_bval[WARPS], s_bcnt[WARPS], s_nexthead;
+    __shared__ unsigned int s_epoch;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const unsigned int last_draw = n_tiles + (unsigned int)S * gridDim.x - 1u;
+    uint32_t *vdata = reinterpret_cast<uint32_t *>(reinterpret_cast<uintptr_t>(data) - 4ull * head);
+    const int32_t *vflags = reinterpret_cast<const int32_t *>(reinterpret_cast<uintptr_t>(flags) - 4ull * head);
+    const bool producer = threadIdx.x == THREADS - 32;
+    unsigned int latest_parity = 0;
+
+    auto tile_full = [&](unsigned int id) {
+        const unsigned long long v0 = (unsigned long long)id * TILE;
+        return streams_aligned && v0 >= head && v0 + TILE <= head + n;
+    };
+    auto tile_range = [&](unsigned int id, unsigned int &lo, unsigned int &hi) {
+        const unsigned long long v0 = (unsigned long long)id * TILE;
+        lo = v0 < head ? (unsigned int)(head - v0) : 0u;
+        const unsigned long long left = head + n - v0;
+        hi = left < TILE ? (unsigned int)left : TILE;
+    };
+    auto issue = [&](int st) {  // producer only
+        const unsigned int id = atom_add_acq_rel(&hdr->counter, 1u);
+        if (id == last_draw) {
+            st_relaxed_u32(&hdr->counter, 0u);
+            st_relaxed_u32(&hdr->epoch, s_epoch + 1u);
+        }
+        s_tile[st] = id;
+        const unsigned int b = smem_u32(&bar[st]);
+        if (id < n_tiles && tile_full(id)) {
+            const unsigned long long v0 = (unsigned long long)id * TILE;
+            mbar_arrive_expect_tx(b, 2 * TILE_BYTES);
+            bulk_load(smem_u32(stage_buf + st * (TILE / 2)), vdata + v0, TILE_BYTES, b);
+            bulk_load(smem_u32(stage_buf + st * (TILE / 2) + TILE / 4), vflags + v0, TILE_BYTES, b);
+        } else {
+            mbar_arrive(b);  // nothing to copy: a partial tile reads global memory, a past-the-end draw stops
+        }
+    };
+
+    if (producer) {
+#pragma unroll
+        for (int st = 0; st < S; ++st) mbar_init(smem_u32(&bar[st]), 1u);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        s_epoch = ld_relaxed_u32(&hdr->epoch);
+#pragma unroll
+        for (int st = 0; st < S; ++st) issue(st);
+    }
+    __syncthreads();
+    const unsigned long long tag = tag_of(s_epoch);
+    const unsigned int li0 = (unsigned int)warp * CHUNK + 4u * (unsigned int)lane;
+    volatile unsigned int *vs_tile = s_tile;
+
+    // Read draw u into registers (values x, head bits hb), scan it within
+    // each warp and leave the warp aggregates in slot u & 1. Returns the
+    // tile, or n_tiles and above past the end / on a timeout.
+    auto read_tile = [&](unsigned int u, uint4 (&x)[V], unsigned int &hb, unsigned int &pfirst) -> unsigned int {
+        const int st = (int)(u % S);
+        if (!mbar_wait_bounded(smem_u32(&bar[st]), (u / S) & 1u, limit_ns)) {
+            report_timeout(hdr, 0xfffffffeu);
+            return n_tiles + 1u;
+        }
+        const unsigned int t = vs_tile[st];
+        if (t >= n_tiles) return n_tiles;
+        const unsigned long long tile_v0 = (unsigned long long)t * TILE;
+        hb = 0;
+        if (tile_full(t)) {
+            const uint4 *sv = stage_buf + st * (TILE / 2) + (li0 >> 2);
+            const int4 *sf = reinterpret_cast<const int4 *>(stage_buf + st * (TILE / 2) + TILE / 4) + (li0 >> 2);
+#pragma unroll
+            for (int r = 0; r < V; ++r) {
+                x[r] = sv[32 * r];
+                const int4 f = sf[32 * r];
+                hb |= ((f.x != 0) | ((f.y != 0) << 1) | ((f.z != 0) << 2) | ((f.w != 0) << 3)) << (4 * r);
+            }
+        } else {
+            unsigned int lo, hi;
+            tile_range(t, lo, hi);
+            const uint32_t *tv = vdata + tile_v0;
+            const int32_t *tf = vflags + tile_v0;
+#pragma unroll
+            for (int r = 0; r < V; ++r) {
+                unsigned int e[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const unsigned int li = li0 + 128 * r + c;
+                    const bool in = li >= lo && li < hi;
+                    e[c] = in ? tv[li] : 0u;
+                    if (in && tf[li] != 0) hb |= 1u << (4 * r + c);
+                }
+                x[r] = make_uint4(e[0], e[1], e[2], e[3]);
+            }
+        }
+        // index 0 of the array always opens a segment
+        if (tile_v0 <= head && head < tile_v0 + TILE) {
+            const unsigned int li = (unsigned int)(head - tile_v0);
+            // element li belongs to warp li / CHUNK, lane (li % 128) / 4, round (li % CHUNK) / 128, c = li % 4
+            if (li / CHUNK == (unsigned int)warp && ((li % 128u) >> 2) == (unsigned int)lane)
+                hb |= 1u << (4 * ((li % CHUNK) / 128u) + (li & 3u));
+        }
+        // Per-round segmented scan within the warp, carry from round to round.
+        unsigned int carry = 0;
+        pfirst = kNoHead;
+#pragma unroll
+        for (int r = 0; r < V; ++r) {
+            const unsigned int b = (hb >> (4 * r)) & 0xfu;
+            const unsigned int e0 = x[r].x;
+            const unsigned int e1 = (b & 2u) ? x[r].y : e0 + x[r].y;
+            const unsigned int e2 = (b & 4u) ? x[r].z : e1 + x[r].z;
+            const unsigned int e3 = (b & 8u) ? x[r].w : e2 + x[r].w;
+            const unsigned int sl = warp_segmented_inclusive(e3, b != 0u, carry, lane);
+            unsigned int cin = __shfl_up_sync(0xffffffffu, sl, 1);
+            if (lane == 0) cin = carry;
+            x[r].x = (b & 1u) ? e0 : cin + e0;
+            x[r].y = (b & 3u) ? e1 : cin + e1;
+            x[r].z = (b & 7u) ? e2 : cin + e2;
+            x[r].w = (b & 15u) ? e3 : cin + e3;
+            carry = __shfl_sync(0xffffffffu, sl, 31);
+            const unsigned int hm = __ballot_sync(0xffffffffu, b != 0u);
+            if (pfirst == kNoHead && hm) {
+                const int lf = __ffs(hm) - 1;
+                const unsigned int bf = __shfl_sync(0xffffffffu, b, lf);
+                pfirst = 128u * r + 4u * lf + (unsigned int)(__ffs(bf) - 1);
+            }
+        }
+        const unsigned int wcnt = __reduce_add_sync(0xffffffffu, (unsigned int)__popc(hb));
+        if (lane == 0) {
+            const int slot = (int)(u & 1u);
+            s_wval[slot][warp] = carry;
+            s_wcnt[slot][warp] = wcnt;
+            s_whas[slot][warp] = pfirst != kNoHead;
+            s_wfirst[u % 3][warp] = hb & 1u;
+        }
+        return t;
+    };
+
+    // Store the current tile (first-head slot cs): add each warp's carry-in to the
+    // elements before its first head, write the scan, and write each
+    // segment's sum at the segment's last element.
+    auto store_tile = [&](unsigned int t, int cs, const uint4 (&x)[V], unsigned int hb, unsigned int pfirst) {
+        const unsigned long long tile_v0 = (unsigned long long)t * TILE;
+        const unsigned int cin = s_bval[warp];
+        const bool full = tile_full(t);
+        unsigned int lo = 0, hi = TILE;
+        if (!full) tile_range(t, lo, hi);
+        uint32_t *tv = vdata + tile_v0;
+        unsigned int hbase = 0, next_first = 0;
+        if (WANT_SUMS) {
+            hbase = s_bcnt[warp];
+            next_first = warp + 1 < WARPS ? s_wfirst[cs][warp + 1] : s_nexthead;
+        }
+        // tile-local index of the array's last element (TILE when outside)
+        const unsigned long long last_v = head + n - 1 - tile_v0;
+        const unsigned int last_li = last_v < TILE ? (unsigned int)last_v : TILE;
+#pragma unroll
+        for (int r = 0; r < V; ++r) {
+            const unsigned int p0 = 128u * r + 4u * lane;
+            const unsigned int y[4] = {x[r].x + (p0 + 0 < pfirst ? cin : 0u), x[r].y + (p0 + 1 < pfirst ? cin : 0u),
+                                       x[r].z + (p0 + 2 < pfirst ? cin : 0u), x[r].w + (p0 + 3 < pfirst ? cin : 0u)};
+            if (WRITE_SCAN) {
+                if (full) {
+                    __stcs(reinterpret_cast<uint4 *>(tv + li0 + 128 * r), make_uint4(y[0], y[1], y[2], y[3]));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const unsigned int li = li0 + 128 * r + c;
+                        if (li >= lo && li < hi) tv[li] = y[c];
+                    }
+                }
+            }
+            if (WANT_SUMS) {
+                const unsigned int b = (hb >> (4 * r)) & 0xfu;
+                // head bit of the element after this lane's last one
+                const unsigned int down = __shfl_down_sync(0xffffffffu, b & 1u, 1);
+                unsigned int wrap = next_first;
+                if (r + 1 < V) wrap = __shfl_sync(0xffffffffu, (hb >> (4 * (r + 1))) & 1u, 0);
+                const unsigned int after = lane < 31 ? down : wrap;
+                const unsigned int next_bits = (b >> 1) | (after << 3);  // bit c: element c + 1 is a head
+                const unsigned int pc = (unsigned int)__popc(b);
+                const unsigned int incl = warp_inclusive_sum(pc, lane);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const unsigned int li = li0 + 128 * r + c;
+                    const bool end = li >= lo && li < hi && (((next_bits >> c) & 1u) || li == last_li);
+                    if (end) {
+                        const unsigned long long k =
+                            (unsigned long long)hbase + (incl - pc) + (unsigned int)__popc(b & ((2u << c) - 1u)) - 1u;
+                        if (k < seg_cap) seg_sums[k] = y[c];
+                    }
+                }
+                hbase += __shfl_sync(0xffffffffu, incl, 31);
+            }
+        }
+    };
+
+    uint4 xc[V], xn[V];
+    unsigned int hbc = 0, hbn = 0, pfc = kNoHead, pfn = kNoHead;
+    unsigned int tc = read_tile(0, xc, hbc, pfc);
+    // warp 0 keeps, per lane w < WARPS, what the look-back needs for the
+    // current tile: the tile aggregate and warp w's exclusive offsets
+    unsigned int agg_val = 0, agg_cnt = 0, wex_val = 0, wex_cnt = 0;
+    bool agg_head = false, head_before = false;
+    auto block_aggregate = [&](int slot, unsigned int t, unsigned int &a_val, bool &a_head, unsigned int &a_cnt,
+                               unsigned int &x_val, bool &h_before, unsigned int &x_cnt) {
+        const unsigned int wv = lane < WARPS ? s_wval[slot][lane] : 0u;
+        const unsigned int wc = lane < WARPS ? s_wcnt[slot][lane] : 0u;
+        const bool wh = lane < WARPS ? s_whas[slot][lane] != 0 : false;
+        const unsigned int sw = warp_segmented_inclusive(wv, wh, 0u, lane);
+        const unsigned int hm = __ballot_sync(0xffffffffu, wh);
+        a_val = __shfl_sync(0xffffffffu, sw, 31);
+        a_head = hm != 0;
+        const unsigned int cw = warp_inclusive_sum(wc, lane);
+        a_cnt = __shfl_sync(0xffffffffu, cw, 31);
+        x_val = __shfl_up_sync(0xffffffffu, sw, 1);
+        if (lane == 0) x_val = 0;
+        h_before = (hm & lanemask_lt(lane)) != 0;
+        x_cnt = cw - wc;
+        if (lane == 0 && t != skip_tile) {
+            // a tile holding a head knows its segmented carry at once
+            st_relaxed(desc2 + 2ull * t, tag | (a_head || t == 0 ? (kFlagH | kFlagP) : 0ull) | a_val);
+            st_relaxed(desc2 + 2ull * t + 1, tag | (t == 0 ? kFlagP : 0ull) | a_cnt);
+        }
+    };
+
+    if (!__syncthreads_or(tc >= n_tiles)) {
+        if (producer) {
+            fence_proxy_async_smem();
+            issue(0);
+            latest_parity ^= 1u;
+        }
+        if (warp == 0) block_aggregate(0, tc, agg_val, agg_head, agg_cnt, wex_val, head_before, wex_cnt);
+        for (unsigned int u = 1;; ++u) {
+            const unsigned int tn = read_tile(u, xn, hbn, pfn);
+            const bool more = !__syncthreads_or(tn >= n_tiles);  // barrier A
+            unsigned int n_val = 0, n_cnt = 0, n_xval = 0, n_xcnt = 0;
+            bool n_head = false, n_before = false;
+            if (more && producer) {
+                fence_proxy_async_smem();
+                const int st = (int)(u % S);
+                issue(st);
+                latest_parity ^= 1u << st;
+            }
+            if (warp == 0) {
+                if (more) block_aggregate((int)(u & 1u), tn, n_val, n_head, n_cnt, n_xval, n_before, n_xcnt);
+                const SegPrefix pre = lookback_seg(desc2, tc, tag, hdr, limit_ns, lane);
+                if (lane == 0 && tc != 0 && tc != skip_tile) {
+                    if (!agg_head) st_relaxed(desc2 + 2ull * tc, tag | kFlagP | (unsigned int)(pre.seg + agg_val));
+                    st_relaxed(desc2 + 2ull * tc + 1, tag | kFlagP | (unsigned int)(pre.cnt + agg_cnt));
+                }
+                if (lane < WARPS) {
+                    s_bval[lane] = head_before ? wex_val : pre.seg + wex_val;
+                    s_bcnt[lane] = pre.cnt + wex_cnt;
+                }
+                if (lane == 0) {
+                    if (tc == n_tiles - 1u && nseg != nullptr) *nseg = pre.cnt + agg_cnt;
+                    if (WANT_SUMS) {
+                        // head flag of the element just after the tile
+                        const unsigned long long after = (unsigned long long)(tc + 1) * TILE;
+                        s_nexthead = after < head + n && vflags[after] != 0 ? 1u : 0u;
+                    }
+                }
+            }
+            __syncthreads();  // barrier B: carries of the current tile are visible
+            store_tile(tc, (int)((u - 1) % 3), xc, hbc, pfc);
+            if (!more) break;
+#pragma unroll
+            for (int r = 0; r < V; ++r) xc[r] = xn[r];
+            hbc = hbn;
+            pfc = pfn;
+            tc = tn;
+            agg_val = n_val;
+            agg_head = n_head;
+            agg_cnt = n_cnt;
+            wex_val = n_xval;
+            head_before = n_before;
+            wex_cnt = n_xcnt;
+        }
+    }
+    // Leave no bulk copy in flight into this block's shared memory.
+    if (producer) {
+#pragma unroll
+        for (int st = 0; st < S; ++st)
+            (void)mbar_wait_bounded(smem_u32(&bar[st]), (latest_parity >> st) & 1u, limit_ns);
+    }
+}
+
+constexpr int kSThreads = 512, kSV = 4, kSStages = 3;
+constexpr unsigned long long kSTile = (unsigned long long)kSThreads * kSV * 4;
+constexpr size_t kSSmem = (size_t)kSStages * kSTile * 8;
+
+size_t segscan_workspace_bytes(unsigned long long n) {
+    const unsigned long long tiles = (n + 3 + kSTile - 1) / kSTile;
+    return round_up(kHeaderBytes + 16 * tiles, 256);
+}
+
+static std::mutex g_seg_mu;
+static int g_seg_sms[64];
+static bool g_seg_attr[64][4];
+
+template <bool WRITE_SCAN, bool WANT_SUMS>
+static int segscan_launch(uint32_t *data, const int32_t *flags, unsigned long long n, uint32_t *seg_sums,
+                          unsigned long long seg_cap, uint32_t *nseg, void *ws, size_t ws_bytes, cudaStream_t stream,
+                          unsigned int skip_tile, unsigned long long limit_ns) {
+    if (n >= (1ull << 32)) return U32SCAN_EINVAL;
+    if (n > 0 && (data == nullptr || flags == nullptr)) return U32SCAN_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(data) & 3) || (reinterpret_cast<uintptr_t>(flags) & 3) ||
+        (reinterpret_cast<uintptr_t>(seg_sums) & 3) || (reinterpret_cast<uintptr_t>(nseg) & 3))
+        return U32SCAN_EINVAL;
+    if (n == 0) {
+        if (nseg && cudaMemsetAsync(nseg, 0, sizeof(uint32_t), stream) != cudaSuccess) return U32SCAN_ECUDA;
+        return U32SCAN_OK;
+    }
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < segscan_workspace_bytes(n))
+        return U32SCAN_EWORKSPACE;
+    const unsigned int head = (unsigned int)((reinterpret_cast<uintptr_t>(data) & 15) >> 2);
+    const int aligned = ((reinterpret_cast<uintptr_t>(data) ^ reinterpret_cast<uintptr_t>(flags)) & 15) == 0;
+    const unsigned int n_tiles = (unsigned int)((n + head + kSTile - 1) / kSTile);
+    auto kern = segscan_u32_persistent<kSThreads, kSV, kSStages, WRITE_SCAN, WANT_SUMS>;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return U32SCAN_ECUDA;
+    int sms;
+    {
+        std::lock_guard<std::mutex> lock(g_seg_mu);
+        if (g_seg_sms[dev] == 0 &&
+            cudaDeviceGetAttribute(&g_seg_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return U32SCAN_ECUDA;
+        const int which = (WRITE_SCAN ? 2 : 0) + (WANT_SUMS ? 1 : 0);
+        if (!g_seg_attr[dev][which]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSSmem) != cudaSuccess)
+                return U32SCAN_ECUDA;
+            g_seg_attr[dev][which] = true;
+        }
+        sms = g_seg_sms[dev];
+    }
+    const unsigned int grid = n_tiles < (unsigned int)sms ? n_tiles : (unsigned int)sms;
+    WsHeader *hdr = static_cast<WsHeader *>(ws);
+    unsigned long long *desc2 = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
+    kern<<<grid, kSThreads, kSSmem, stream>>>(data, flags, n, seg_sums, seg_cap, nseg, hdr, desc2, n_tiles, head,
+                                             aligned, skip_tile, limit_ns);
+    return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
+}
+
+}  // namespace u32scan
+
+using namespace u32scan;
+
+extern "C" int segscan_inclusive_u32(uint32_t *data, const int32_t *head_flags, size_t n, uint32_t *seg_sums,
+                                     size_t seg_capacity, uint32_t *nseg, void *ws, size_t ws_bytes,
+                                     u32scan_stream_t stream) {
+    if (seg_sums != nullptr)
+        return segscan_launch<true, true>(data, head_flags, n, seg_sums, seg_capacity, nseg, ws, ws_bytes,
+                                          (cudaStream_t)stream, 0xffffffffu, kDefaultLimitNs);
+    return segscan_launch<true, false>(data, head_flags, n, nullptr, 0, nseg, ws, ws_bytes, (cudaStream_t)stream,
+                                       0xffffffffu, kDefaultLimitNs);
+}
+
+extern "C" int segreduce_u32(const uint32_t *data, const int32_t *head_flags, size_t n, uint32_t *seg_sums,
+                             size_t seg_capacity, uint32_t *nseg, void *ws, size_t ws_bytes,
+                             u32scan_stream_t stream) {
+    if (seg_sums == nullptr && nseg == nullptr) return U32SCAN_EINVAL;
+    return segscan_launch<false, true>(const_cast<uint32_t *>(data), head_flags, n, seg_sums,
+                                       seg_sums ? seg_capacity : 0, nseg, ws, ws_bytes, (cudaStream_t)stream,
+                                       0xffffffffu, kDefaultLimitNs);
+}

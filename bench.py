@@ -1,30 +1,41 @@
 #!/usr/bin/env python3
-"""Benchmark: U32 exclusive scan, in place, n = 2^28, on one GB300.
+"""Benchmark of the U32 scan primitives on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--op OP] [--heads geometric|regular4]
 
-One step is one call of scan_exclusive_u32 on a resident 1 GiB array of
-uniform u32 (seed 2), in place, with its total; the same buffer is rescanned
-every step (identical traffic; the 1 GiB input is far larger than the
-129 MB L2, so no flush is needed between steps). Rank 0 prints one JSON line.
+Default (--op scan_exclusive): one step is one call of scan_exclusive_u32 on
+a resident 1 GiB array (n = 2^28 uniform u32, seed 2), in place, with its
+total; the same buffer is rescanned every step (identical traffic; the input
+is far larger than the 129 MB L2, so no flush is needed between steps).
+Other ops time the other primitives on their own workloads:
 
-value      elements scanned per second over all ranks (Gelem/s), device-timed
+  scan_inclusive  scan_inclusive_u32, n = 2^28, seed 2
+  segscan         segscan_inclusive_u32 in place, n = 2^26, values seed 3,
+                  heads --heads (Bernoulli 2^-10 or every 4th index)
+  segscan_sums    the same, also writing every segment's sum and the count
+  segreduce       segreduce_u32: sums and count only
+
+Rank 0 prints one JSON line.
+
+value      elements processed per second over all ranks (Gelem/s), timed
            with CUDA events on the launching stream, max over ranks.
-roofline   the scan kernel's algorithmic bytes (4 read + 4 written per
-           element) over its measured time, against the measured HBM copy
-           peak in MEASURED_PEAKS.json (fallback 6800 GB/s when absent).
-e2e        the same metric through the same C-ABI call, with a pinned host
-           input copied in and the result and total copied out every step.
+roofline   algorithmic bytes of one launch over its measured time, against
+           the measured HBM copy peak in MEASURED_PEAKS.json (fallback
+           6800 GB/s when absent).
+e2e        the same metric through the same C-ABI call, with pinned host
+           inputs copied in and the outputs copied out every step.
 cpu_baseline  the CPU oracle (one thread, as it stands) on a bounded sample.
 
 --impl reference times that oracle alone on the host cores (rank 0 only).
-Under torchrun each rank scans its own array on its own GPU (independent
-replicas: weak scaling, no data-path collective).
+Under torchrun each rank runs its own replica of the workload on its own GPU
+(independent replicas: weak scaling, no data-path collective).
 """
 
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -39,17 +50,213 @@ ROOT = pathlib.Path(__file__).resolve().parent
 if str(ROOT) not in sys.path:
     sys.path.insert(0, str(ROOT))
 
-N = 1 << 28
-SEED = 2
-BYTES_PER_ELEM = 8  # one 4-byte read and one 4-byte write per element
-METRIC = "U32 exclusive scan Gelem/s and HBM GB/s (fraction of peak) at n=2^28, 1 GB300"
 UNIT = "Gelem/s"
 FALLBACK_HBM_GBS = 6800.0
-WORKLOAD = "u32 exclusive scan in place + total, n=2^28, uniform u32 seed 2"
-KERNEL_SOURCES = ["u32_prefix_scan_gb300/csrc/scan.cu", "u32_prefix_scan_gb300/csrc/internal.cuh"]
-TRAFFIC_FILE = ROOT / "profiles" / "scan_exclusive_u32_n2p28.traffic.json"
 REF_SAMPLE = 1 << 24  # elements per reference-arm step
 
+
+# ------------------------------------------------------------------ ops ----
+
+class Op:
+    """One benchmarked primitive on its workload."""
+
+    name = ""
+    metric = ""
+    kernel = ""
+    kernel_sources: list = []
+    log2n = 28
+
+    def __init__(self, args):
+        self.args = args
+        self.n = 1 << (args.log2n if args.log2n is not None else self.log2n)
+
+    @property
+    def traffic_file(self):
+        return ROOT / "profiles" / f"{self.name}_n2p{self.log2n}.traffic.json"
+
+    def workload(self) -> str:
+        raise NotImplementedError
+
+    def algorithmic_bytes(self) -> int:
+        raise NotImplementedError
+
+
+class ScanOp(Op):
+    log2n = 28
+    kernel_sources = ["u32_prefix_scan_gb300/csrc/scan.cu", "u32_prefix_scan_gb300/csrc/internal.cuh"]
+
+    def __init__(self, args, inclusive: bool):
+        super().__init__(args)
+        self.inclusive = inclusive
+        self.name = "scan_inclusive_u32" if inclusive else "scan_exclusive_u32"
+        form = "inclusive" if inclusive else "exclusive"
+        self.metric = f"U32 {form} scan Gelem/s and HBM GB/s (fraction of peak) at n=2^28, 1 GB300"
+        self.kernel = f"scan_u32_persistent<512,8,2,1,{form}>"
+
+    def workload(self):
+        form = "inclusive" if self.inclusive else "exclusive"
+        return f"u32 {form} scan in place + total, n=2^{self.n.bit_length() - 1}, uniform u32 seed 2"
+
+    def algorithmic_bytes(self):
+        return 8 * self.n  # read 4 + write 4 per element
+
+    def host_inputs(self):
+        from u32_prefix_scan_gb300 import inputs
+
+        return {"data": inputs.scan_values(self.n, 2)}
+
+    def setup(self, dev, host):
+        import numpy as np
+        import torch
+
+        import u32_prefix_scan_gb300 as u
+        from u32_prefix_scan_gb300 import _native
+
+        self.u = u
+        self.fn = u.scan_inclusive_u32 if self.inclusive else u.scan_exclusive_u32
+        self.data = torch.from_numpy(host["data"].view(np.int32)).to(dev)
+        self.total = torch.empty(1, dtype=torch.int32, device=dev)
+        self.ws = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_SCAN, self.n), dev)
+        self.pinned_in = {"data": torch.from_numpy(host["data"].view(np.int32)).pin_memory()}
+        self.pinned_out = {"data": torch.empty(self.n, dtype=torch.int32).pin_memory(),
+                           "total": torch.empty(1, dtype=torch.int32).pin_memory()}
+
+    def step(self):
+        self.fn(self.data, self.total, workspace=self.ws)
+
+    def e2e_step(self):
+        self.data.copy_(self.pinned_in["data"], non_blocking=True)
+        self.step()
+        self.pinned_out["data"].copy_(self.data, non_blocking=True)
+        self.pinned_out["total"].copy_(self.total, non_blocking=True)
+        return 4 * self.n, 4 * self.n + 4
+
+    def check_e2e(self, host):
+        # consecutive differences of the copied-back scan give the input
+        import numpy as np
+
+        k = min(self.n, 1 << 20)
+        got = self.pinned_out["data"][:k].numpy().view(np.uint32)
+        a = host["data"][:k]
+        if self.inclusive:
+            return got[0] == a[0] and np.array_equal(got[1:] - got[:-1], a[1:])
+        return got[0] == 0 and np.array_equal(got[1:] - got[:-1], a[:-1])
+
+    def oracle_step(self, lib, arrays):
+        f = lib.oracle_scan_inclusive_u32 if self.inclusive else lib.oracle_scan_exclusive_u32
+        f(arrays["data"].ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)), arrays["data"].size)
+
+
+class SegOp(Op):
+    log2n = 26
+    kernel_sources = ["u32_prefix_scan_gb300/csrc/segscan.cu", "u32_prefix_scan_gb300/csrc/internal.cuh"]
+
+    def __init__(self, args, mode: str):
+        super().__init__(args)
+        self.mode = mode  # segscan | segscan_sums | segreduce
+        self.heads = args.heads
+        self.name = f"{mode}_{self.heads}"
+        what = {"segscan": "segmented inclusive scan", "segscan_sums": "segmented inclusive scan + segment sums",
+                "segreduce": "per-segment reduce"}[mode]
+        lengths = "geometric lengths mean 1024" if self.heads == "geometric" else "2^24 segments of length 4"
+        self.metric = f"U32 {what} Gelem/s and HBM GB/s (fraction of peak) at n=2^26 ({lengths}), 1 GB300"
+        kind = {"segscan": "true,false", "segscan_sums": "true,true", "segreduce": "false,true"}[mode]
+        self.kernel = f"segscan_u32_persistent<512,7,2,{kind}>"
+        self.nseg = None
+
+    def workload(self):
+        lengths = "Bernoulli(2^-10) heads" if self.heads == "geometric" else "a head every 4th index"
+        return (f"u32 {self.mode} n=2^{self.n.bit_length() - 1}, values uniform u32 seed 3, int32 head "
+                f"flags: {lengths}")
+
+    def algorithmic_bytes(self):
+        n, nseg = self.n, self.nseg
+        if self.mode == "segscan":
+            return 12 * n  # values 4 + flags 4 read, values 4 written
+        if self.mode == "segscan_sums":
+            return 12 * n + 4 * nseg + 4
+        return 8 * n + 4 * nseg + 4  # segreduce: values + flags read, one sum per segment
+
+    def host_inputs(self):
+        import numpy as np
+
+        from u32_prefix_scan_gb300 import inputs
+
+        f = (inputs.segment_heads_geometric(self.n, 3) if self.heads == "geometric"
+             else inputs.segment_heads_regular(self.n, 4))
+        self.nseg = int(np.count_nonzero(f))
+        return {"data": inputs.scan_values(self.n, 3), "flags": f}
+
+    def setup(self, dev, host):
+        import numpy as np
+        import torch
+
+        import u32_prefix_scan_gb300 as u
+        from u32_prefix_scan_gb300 import _native
+
+        self.u = u
+        self.data = torch.from_numpy(host["data"].view(np.int32)).to(dev)
+        self.flags = torch.from_numpy(host["flags"]).to(dev)
+        self.sums = torch.empty(self.nseg, dtype=torch.int32, device=dev) if self.mode != "segscan" else None
+        self.count = torch.empty(1, dtype=torch.int32, device=dev)
+        self.ws = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_SEGSCAN, self.n), dev)
+        self.pinned_in = {"data": torch.from_numpy(host["data"].view(np.int32)).pin_memory(),
+                          "flags": torch.from_numpy(host["flags"]).pin_memory()}
+        self.pinned_out = {"count": torch.empty(1, dtype=torch.int32).pin_memory()}
+        if self.mode != "segreduce":
+            self.pinned_out["data"] = torch.empty(self.n, dtype=torch.int32).pin_memory()
+        if self.sums is not None:
+            self.pinned_out["sums"] = torch.empty(self.nseg, dtype=torch.int32).pin_memory()
+
+    def step(self):
+        if self.mode == "segreduce":
+            self.u.segreduce_u32(self.data, self.flags, self.sums, self.count, workspace=self.ws)
+        else:
+            self.u.segscan_inclusive_u32(self.data, self.flags, self.sums, self.count, workspace=self.ws)
+
+    def e2e_step(self):
+        self.data.copy_(self.pinned_in["data"], non_blocking=True)
+        self.flags.copy_(self.pinned_in["flags"], non_blocking=True)
+        self.step()
+        d2h = 4
+        self.pinned_out["count"].copy_(self.count, non_blocking=True)
+        if "data" in self.pinned_out:
+            self.pinned_out["data"].copy_(self.data, non_blocking=True)
+            d2h += 4 * self.n
+        if "sums" in self.pinned_out:
+            self.pinned_out["sums"].copy_(self.sums, non_blocking=True)
+            d2h += 4 * self.nseg
+        return 8 * self.n, d2h
+
+    def check_e2e(self, host):
+        return int(self.pinned_out["count"][0]) == self.nseg
+
+    def oracle_step(self, lib, arrays):
+        u32p, i32p = ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_int32)
+        a, f = arrays["data"], arrays["flags"]
+        if self.mode == "segscan":
+            lib.oracle_segscan_inclusive_u32(a.ctypes.data_as(u32p), f.ctypes.data_as(i32p), a.size)
+            return
+        if "sums" not in arrays:
+            import numpy as np
+
+            arrays["sums"] = np.zeros(max(a.size, 1), dtype=np.uint32)
+        lib.oracle_segreduce_u32(a.ctypes.data_as(u32p), f.ctypes.data_as(i32p), a.size,
+                                 arrays["sums"].ctypes.data_as(u32p))
+        if self.mode == "segscan_sums":
+            lib.oracle_segscan_inclusive_u32(a.ctypes.data_as(u32p), f.ctypes.data_as(i32p), a.size)
+
+
+OPS = ["scan_exclusive", "scan_inclusive", "segscan", "segscan_sums", "segreduce"]
+
+
+def make_op(args) -> Op:
+    if args.op in ("scan_exclusive", "scan_inclusive"):
+        return ScanOp(args, args.op == "scan_inclusive")
+    return SegOp(args, args.op)
+
+
+# -------------------------------------------------------------- helpers ----
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -57,11 +264,13 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--op", choices=OPS, default="scan_exclusive")
+    p.add_argument("--heads", choices=["geometric", "regular4"], default="geometric")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--log2n", type=int, default=28,
-                   help="array size 2^log2n (28 is the benchmark; smaller sizes are for profiler captures)")
+    p.add_argument("--log2n", type=int, default=None,
+                   help="array size 2^log2n instead of the workload's (for profiler captures)")
     a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -74,9 +283,9 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
-def kernel_source_hash() -> str:
+def source_hash(rels) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in rels:
         h.update((ROOT / rel).read_bytes())
     return h.hexdigest()[:16]
 
@@ -90,13 +299,14 @@ def load_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def load_traffic():
-    """ncu DRAM bytes per launch, if captured for the current kernel source."""
+def load_traffic(op: Op):
+    """ncu DRAM bytes per launch, if captured for the current kernel source
+    at this workload size."""
     try:
-        d = json.loads(TRAFFIC_FILE.read_text())
+        d = json.loads(op.traffic_file.read_text())
     except Exception:
         return None
-    if d.get("source_hash") != kernel_source_hash():
+    if d.get("source_hash") != source_hash(op.kernel_sources) or d.get("scaled_to_n") != op.n:
         return None
     return float(d["dram_bytes_per_launch"])
 
@@ -165,33 +375,13 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def time_oracle_scan(host_u32, seconds: float):
-    """The oracle's exclusive scan (one thread), repeated in place over the
-    given array until `seconds` have passed. Returns elements/s and reps."""
-    import ctypes
-
-    import oracle
-
-    lib = oracle._load()
-    ptr = host_u32.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32))
-    n = host_u32.size
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        lib.oracle_scan_exclusive_u32(ptr, n)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            return n * reps / el, reps, el
-
-
 def max_over_ranks(x: float, world: int) -> float:
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64,
-                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -203,62 +393,70 @@ def barrier(world: int):
         dist.barrier()
 
 
-def run_reference(args, rank, world):
+def time_oracle(op: Op, host: dict, seconds: float, sample: int):
+    """The oracle (one thread, as it stands) repeated on the first `sample`
+    elements of the workload until `seconds` pass. Returns elements/s."""
+    import oracle
+
+    lib = oracle._load()
+    arrays = {k: v[:sample].copy() for k, v in host.items()}
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        op.oracle_step(lib, arrays)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return sample * reps / el, reps, el
+
+
+# ----------------------------------------------------------------- arms ----
+
+def run_reference(args, rank):
     """The reference arm: the CPU oracle on the host cores, rank 0 only."""
     if rank != 0:
         return None
-    import numpy as np
-
-    from u32_prefix_scan_gb300 import inputs
-
     import oracle
 
     oracle.build()
-    sample = min(N, REF_SAMPLE)
-    host = inputs.scan_values(sample, SEED)
-    import ctypes
-
+    op = make_op(args)
+    host = op.host_inputs()
+    sample = min(op.n, REF_SAMPLE)
     lib = oracle._load()
-    ptr = host.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32))
+    arrays = {k: v[:sample].copy() for k, v in host.items()}
     for _ in range(args.warmup):
-        lib.oracle_scan_exclusive_u32(ptr, sample)
+        op.oracle_step(lib, arrays)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        lib.oracle_scan_exclusive_u32(ptr, sample)
+        op.oracle_step(lib, arrays)
     el = time.perf_counter() - t0
     value = sample * args.steps / el / 1e9
-    desc = f"oracle_scan_exclusive_u32 on the first 2^{sample.bit_length() - 1} elements of the workload per step"
+    desc = f"{op.name} oracle on the first 2^{sample.bit_length() - 1} elements of the workload per step"
     return {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": op.metric, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "n": N, "seed": SEED, "sample_per_step": sample},
+        "config": {"workload": op.workload(), "n": op.n, "op": args.op, "sample_per_step": sample},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
 def run_ours(args, rank, local_rank, world):
-    import numpy as np
     import torch
 
-    import u32_prefix_scan_gb300 as u
-    from u32_prefix_scan_gb300 import _native, inputs
     from u32_prefix_scan_gb300 import build as native_build
 
     native_build.build()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.current_stream()
-
-    host = inputs.scan_values(N, SEED)
-    data = torch.from_numpy(host.view(np.int32)).to(dev)
-    total = torch.empty(1, dtype=torch.int32, device=dev)
-    ws = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_SCAN, N), dev)
+    op = make_op(args)
+    host = op.host_inputs()
+    op.setup(dev, host)
 
     for _ in range(args.warmup):
-        u.scan_exclusive_u32(data, total, workspace=ws)
-    u.check(workspace=ws)
+        op.step()
+    op.u.check(workspace=op.ws)
 
     sampler = ClockSampler(torch.cuda.current_device()).start()
     time.sleep(0.15)
@@ -268,52 +466,42 @@ def run_ours(args, rank, local_rank, world):
     w0 = time.time()
     start.record(stream)
     for _ in range(args.steps):
-        u.scan_exclusive_u32(data, total, workspace=ws)
+        op.step()
     end.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
     barrier(world)
     sampler.window(w0, w1)
     clocks = sampler.stop()
-    u.check(workspace=ws)
+    op.u.check(workspace=op.ws)
     ms = start.elapsed_time(end) / args.steps
     ms_max = max_over_ranks(ms, world)
 
-    # end to end through the C ABI: pinned host in -> scan -> host out
-    h_in = torch.from_numpy(host.view(np.int32)).pin_memory()
-    h_out = torch.empty(N, dtype=torch.int32).pin_memory()
-    h_tot = torch.empty(1, dtype=torch.int32).pin_memory()
-    for _ in range(2):
-        data.copy_(h_in, non_blocking=True)
-        u.scan_exclusive_u32(data, total, workspace=ws)
-        h_out.copy_(data, non_blocking=True)
-        h_tot.copy_(total, non_blocking=True)
-    torch.cuda.synchronize()
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_start.record(stream)
-    for _ in range(args.e2e_steps):
-        data.copy_(h_in, non_blocking=True)
-        u.scan_exclusive_u32(data, total, workspace=ws)
-        h_out.copy_(data, non_blocking=True)
-        h_tot.copy_(total, non_blocking=True)
-    e_end.record(stream)
-    torch.cuda.synchronize()
-    u.check(workspace=ws)
-    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.e2e_steps, world)
-
-    # sanity property of the copied-back result (exclusive scan of host):
-    # out[0] = 0 and out[j+1] - out[j] = in[j] (mod 2^32) on a prefix
-    k = 1 << 20
-    got = h_out[:k].numpy().view(np.uint32)
-    if got[0] != 0 or not np.array_equal(got[1:] - got[:-1], host[: k - 1]):
-        raise SystemExit("bench: e2e result is not the exclusive scan of its input")
+    # end to end through the C ABI: pinned host inputs in, outputs back out
+    h2d = d2h = 0
+    e2e_ms = None
+    if args.e2e_steps:
+        for _ in range(2):
+            op.e2e_step()
+        torch.cuda.synchronize()
+        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_start.record(stream)
+        for _ in range(args.e2e_steps):
+            h2d, d2h = op.e2e_step()
+        e_end.record(stream)
+        torch.cuda.synchronize()
+        op.u.check(workspace=op.ws)
+        e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.e2e_steps, world)
+        if not op.check_e2e(host):
+            raise SystemExit("bench: e2e result fails its property check")
 
     peak, peak_kind = load_peak()
-    achieved = BYTES_PER_ELEM * N / (ms * 1e-3) / 1e9
-    traffic = load_traffic()
+    nbytes = op.algorithmic_bytes()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    full = op.n == 1 << op.log2n
     result = {
-        "metric": METRIC,
-        "value": world * N / (ms_max * 1e-3) / 1e9,
+        "metric": op.metric,
+        "value": world * op.n / (ms_max * 1e-3) / 1e9,
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
@@ -324,36 +512,32 @@ def run_ours(args, rank, local_rank, world):
         "vs_baseline": None,
         "dtype": "u32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD if N == 1 << 28 else f"profiling case n=2^{args.log2n}", "n": N,
-                   "seed": SEED, "per_rank": "one independent array per GPU",
-                   "l2": "input 1 GiB > 129 MB L2; no flush between steps"},
+        "config": {"workload": op.workload() if full else f"profiling case: {op.workload()}", "n": op.n,
+                   "op": args.op, "per_rank": "one independent replica per GPU",
+                   "l2": "inputs larger than the 129 MB L2; no flush between steps"},
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": traffic, "algorithmic_bytes_per_launch": BYTES_PER_ELEM * N,
-                     "kernel": "scan_u32_persistent<512,8,2,1,exclusive>"},
-        "e2e": {"value": world * N / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
-                "h2d_bytes_per_step": 4 * N, "d2h_bytes_per_step": 4 * N + 4},
+                     "traffic": load_traffic(op), "algorithmic_bytes_per_launch": nbytes, "kernel": op.kernel},
+        "e2e": {"value": world * op.n / (e2e_ms * 1e-3) / 1e9 if e2e_ms else None, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks,
         "gpu_launches": args.steps,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        sample = host.copy()
-        v, reps, el = time_oracle_scan(sample, args.cpu_seconds)
+        v, reps, el = time_oracle(op, host, args.cpu_seconds, op.n)
         result["cpu_baseline"] = {"value": v / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                  "sample": f"oracle_scan_exclusive_u32 over the full 2^28 workload, "
-                                            f"in place, {reps} repetitions in {el:.1f} s"}
+                                  "sample": f"{op.name} oracle over the full workload "
+                                            f"(n=2^{op.n.bit_length() - 1}), {reps} repetitions in {el:.1f} s"}
     return result
 
 
 def main(argv=None):
-    global N
     args = parse_args(argv)
-    N = 1 << args.log2n
     rank, local_rank, world = dist_env()
     if args.impl == "reference":
         # rank 0 alone times the oracle; other ranks exit without work
-        out = run_reference(args, rank, world)
+        out = run_reference(args, rank)
         if out is not None:
             print(json.dumps(out), flush=True)
         return

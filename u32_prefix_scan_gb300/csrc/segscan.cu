@@ -341,7 +341,15 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const int32_t *__restrict__ 
     }
 }
 
-constexpr int kSThreads = 512, kSV = 4, kSStages = 3;
+// Launch shape (512 threads, u32x4 per lane per tile, ring stages); chosen
+// by measurement on GB300, overridable at build time for tuning sweeps.
+#ifndef U32SCAN_S_V
+#define U32SCAN_S_V 7
+#endif
+#ifndef U32SCAN_S_STAGES
+#define U32SCAN_S_STAGES 2
+#endif
+constexpr int kSThreads = 512, kSV = U32SCAN_S_V, kSStages = U32SCAN_S_STAGES;
 constexpr unsigned long long kSTile = (unsigned long long)kSThreads * kSV * 4;
 constexpr size_t kSSmem = (size_t)kSStages * kSTile * 8;
 

@@ -15,6 +15,8 @@ Other ops time the other primitives on their own workloads:
                   heads --heads (Bernoulli 2^-10 or every 4th index)
   segscan_sums    the same, also writing every segment's sum and the count
   segreduce       segreduce_u32: sums and count only
+  compact         compact_indices_u32, n = 2^27 int32 flags, keep
+                  probability --p (0.1 or 0.9), seed 4
 
 Rank 0 prints one JSON line.
 
@@ -247,12 +249,86 @@ class SegOp(Op):
             lib.oracle_segscan_inclusive_u32(a.ctypes.data_as(u32p), f.ctypes.data_as(i32p), a.size)
 
 
-OPS = ["scan_exclusive", "scan_inclusive", "segscan", "segscan_sums", "segreduce"]
+class CompactOp(Op):
+    log2n = 27
+    kernel_sources = ["u32_prefix_scan_gb300/csrc/compact.cu", "u32_prefix_scan_gb300/csrc/internal.cuh"]
+
+    def __init__(self, args):
+        super().__init__(args)
+        self.p = args.p
+        self.name = f"compact_p{self.p}"
+        self.metric = (f"stream compaction Gelem/s and HBM GB/s (fraction of peak) at n=2^27, "
+                       f"Bernoulli p={self.p} int32 flags, 1 GB300")
+        self.kernel = "compact_persistent<512,8,2>"
+
+    def workload(self):
+        return (f"compaction of n=2^{self.n.bit_length() - 1} int32 flags, Bernoulli p={self.p} (seed 4): "
+                f"inclusive offsets, kept indices with -1 tail, count")
+
+    def algorithmic_bytes(self):
+        return 12 * self.n + 4  # flags read; offsets and one index slot written per element; the count
+
+    def host_inputs(self):
+        from u32_prefix_scan_gb300 import inputs
+
+        return {"flags": inputs.compact_flags(self.n, 4, self.p)}
+
+    def setup(self, dev, host):
+        import torch
+
+        import u32_prefix_scan_gb300 as u
+        from u32_prefix_scan_gb300 import _native
+
+        self.u = u
+        self.flags = torch.from_numpy(host["flags"]).to(dev)
+        self.offsets = torch.empty(self.n, dtype=torch.int32, device=dev)
+        self.indices = torch.empty(self.n, dtype=torch.int32, device=dev)
+        self.count = torch.empty(1, dtype=torch.int32, device=dev)
+        self.ws = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_COMPACT, self.n), dev)
+        self.pinned_in = {"flags": torch.from_numpy(host["flags"]).pin_memory()}
+        self.pinned_out = {k: torch.empty(self.n, dtype=torch.int32).pin_memory() for k in ("offsets", "indices")}
+        self.pinned_out["count"] = torch.empty(1, dtype=torch.int32).pin_memory()
+
+    def step(self):
+        self.u.compact_indices_u32(self.flags, self.offsets, self.indices, self.count, workspace=self.ws)
+
+    def e2e_step(self):
+        self.flags.copy_(self.pinned_in["flags"], non_blocking=True)
+        self.step()
+        self.pinned_out["offsets"].copy_(self.offsets, non_blocking=True)
+        self.pinned_out["indices"].copy_(self.indices, non_blocking=True)
+        self.pinned_out["count"].copy_(self.count, non_blocking=True)
+        return 4 * self.n, 8 * self.n + 4
+
+    def check_e2e(self, host):
+        import numpy as np
+
+        c = int(self.pinned_out["count"][0])
+        return (c == int(np.count_nonzero(host["flags"])) and int(self.pinned_out["offsets"][-1]) == c
+                and (c == self.n or int(self.pinned_out["indices"][c]) == -1))
+
+    def oracle_step(self, lib, arrays):
+        import numpy as np
+
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        f = arrays["flags"]
+        for k in ("offsets", "indices"):
+            if k not in arrays:
+                arrays[k] = np.empty(f.size, dtype=np.int32)
+        if "count" not in arrays:
+            arrays["count"] = np.zeros(1, dtype=np.int32)
+        lib.oracle_compact_indices(f.ctypes.data_as(i32p), f.size, arrays["offsets"].ctypes.data_as(i32p),
+                                   arrays["indices"].ctypes.data_as(i32p), arrays["count"].ctypes.data_as(i32p))
+
+
+OPS = ["scan_exclusive", "scan_inclusive", "segscan", "segscan_sums", "segreduce", "compact"]
 
 
 def make_op(args) -> Op:
     if args.op in ("scan_exclusive", "scan_inclusive"):
         return ScanOp(args, args.op == "scan_inclusive")
+    if args.op == "compact":
+        return CompactOp(args)
     return SegOp(args, args.op)
 
 
@@ -266,6 +342,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--op", choices=OPS, default="scan_exclusive")
     p.add_argument("--heads", choices=["geometric", "regular4"], default="geometric")
+    p.add_argument("--p", type=float, choices=[0.1, 0.9], default=0.1, help="compaction keep probability")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -138,6 +138,30 @@ int segreduce_u32(const uint32_t *data, const int32_t *head_flags, size_t n,
                   void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /*
+ * Stream compaction: flags -> inclusive offsets -> gathered indices -> count.
+ * Source: the "parallel" package reference (entelechy docs), graph
+ * `compact`: compact_offsets (inclusive prefix sum, a kept element at i
+ * belongs at offsets[i] - 1), compact_gather (each kept index written where
+ * its rank says), compact_blank (an unfilled slot holds -1), compact_total
+ * (the count as a row of one). A non-zero flag keeps its element.
+ *   flags    device, int32_t[n], read only.
+ *   n        element count, below 2^31.
+ *   offsets  device, int32_t[n] or NULL: offsets[i] = number of non-zero
+ *            flags in flags[0..i].
+ *   indices  device, int32_t[n]: the kept indices in increasing order at the
+ *            front, -1 in every slot after them. Every slot is written.
+ *   count    device, one int32_t or NULL: the number of kept elements.
+ *   ws, ws_bytes  u32scan_workspace_bytes(U32SCAN_OP_COMPACT, n) bytes.
+ * All pointers need 4-byte alignment; offsets is written with 16-byte
+ * stores when it has flags' alignment mod 16, else with 4-byte stores.
+ * Errors: EINVAL (null flags or indices with n > 0, misaligned pointers,
+ * n >= 2^31), EWORKSPACE, ECUDA.
+ */
+int compact_indices_u32(const int32_t *flags, size_t n, int32_t *offsets,
+                        int32_t *indices, int32_t *count,
+                        void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
  * Exclusive scan that allocates nothing and needs no workspace argument.
  * The pages have no counterpart: this entry point exists for callers that
  * cannot allocate device memory (for instance code inside an allocator's

@@ -107,3 +107,18 @@ def test_segmented_rejects_bad_arguments_on_host(lib, name):
     assert fn(fake, fake, 1000, fake, 10, fake, fake, need - 256, None) == _native.EWORKSPACE
     assert fn(None, None, 0, None, 0, None, None, 0, None) == (_native.EINVAL if name == "segreduce_u32"
                                                                else _native.OK)
+
+
+def test_compact_rejects_bad_arguments_on_host(lib):
+    fn = lib.compact_indices_u32
+    fake = 0x10000
+    need = lib.u32scan_workspace_bytes(_native.OP_COMPACT, 1000)
+    assert need >= 256 + 8 * (1000 // 16384)
+    assert fn(None, 10, fake, fake, fake, fake, need, None) == _native.EINVAL       # null flags
+    assert fn(fake, 10, fake, None, fake, fake, need, None) == _native.EINVAL       # null indices
+    assert fn(fake + 1, 10, fake, fake, fake, fake, need, None) == _native.EINVAL   # misaligned flags
+    assert fn(fake, 10, fake + 2, fake, fake, fake, need, None) == _native.EINVAL   # misaligned offsets
+    assert fn(fake, 1 << 31, fake, fake, fake, fake, 1 << 40, None) == _native.EINVAL  # n too large for int32
+    assert fn(fake, 1000, fake, fake, fake, None, need, None) == _native.EWORKSPACE
+    assert fn(fake, 1000, fake, fake, fake, fake, need - 256, None) == _native.EWORKSPACE
+    assert fn(None, 0, None, None, None, None, 0, None) == _native.OK

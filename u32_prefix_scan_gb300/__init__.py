@@ -12,6 +12,7 @@ _API = {
     "scan_inclusive_u32",
     "segscan_inclusive_u32",
     "segreduce_u32",
+    "compact_indices_u32",
     "check",
 }
 

@@ -38,6 +38,7 @@ SIGNATURES = {
     "scan_exclusive_u32_noalloc": (_int, [_vp, _sz, _vp, _vp]),
     "segscan_inclusive_u32": (_int, [_vp, _vp, _sz, _vp, _sz, _vp, _vp, _sz, _vp]),
     "segreduce_u32": (_int, [_vp, _vp, _sz, _vp, _sz, _vp, _vp, _sz, _vp]),
+    "compact_indices_u32": (_int, [_vp, _sz, _vp, _vp, _vp, _vp, _sz, _vp]),
     "u32scan_test_scan_skip_publish": (_int, [_vp, _sz, _vp, _vp, _sz, ctypes.c_uint, ctypes.c_ulonglong, _vp]),
 }
 

@@ -23,6 +23,7 @@ __all__ = [
     "scan_inclusive_u32",
     "segscan_inclusive_u32",
     "segreduce_u32",
+    "compact_indices_u32",
     "check",
 ]
 
@@ -164,6 +165,35 @@ def segreduce_u32(data: torch.Tensor, head_flags: torch.Tensor, seg_sums: torch.
         data.data_ptr(), head_flags.data_ptr(), n, seg_sums.data_ptr(), seg_sums.numel(), nseg.data_ptr(),
         ws.ptr, ws.nbytes, sh), "segreduce_u32")
     return seg_sums, nseg
+
+
+def compact_indices_u32(flags: torch.Tensor, offsets: torch.Tensor | None = None,
+                        indices: torch.Tensor | None = None, count: torch.Tensor | None = None, *,
+                        want_offsets: bool = True, stream=None, workspace: Workspace | None = None):
+    """Stream compaction of int32 flags (non-zero keeps an element).
+    Returns (offsets, indices, count): inclusive offsets (None when
+    want_offsets is False and none were given), the kept indices at the
+    front of `indices` with -1 after them, and the one-element count."""
+    _require_cuda(flags, "flags", (torch.int32,))
+    n = flags.numel()
+    if offsets is None and want_offsets:
+        offsets = torch.empty(n, dtype=torch.int32, device=flags.device)
+    if offsets is not None:
+        _require_cuda(offsets, "offsets", (torch.int32,))
+        if offsets.numel() != n:
+            raise ValueError("offsets must have n elements")
+    if indices is None:
+        indices = torch.empty(n, dtype=torch.int32, device=flags.device)
+    _require_cuda(indices, "indices", (torch.int32,))
+    if indices.numel() != n:
+        raise ValueError("indices must have n elements")
+    count = _scalar_out(count, flags, torch.int32)
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_COMPACT, n, flags.device, sh, workspace)
+    _native.check(_native.lib().compact_indices_u32(
+        flags.data_ptr(), n, offsets.data_ptr() if offsets is not None else None, indices.data_ptr(),
+        count.data_ptr(), ws.ptr, ws.nbytes, sh), "compact_indices_u32")
+    return offsets, indices, count
 
 
 def check(stream=None, workspace: Workspace | None = None, device=None) -> int:

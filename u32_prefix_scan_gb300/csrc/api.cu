@@ -13,6 +13,8 @@ extern "C" size_t u32scan_workspace_bytes(int op, size_t n) {
         return scan_workspace_bytes(n);
     case U32SCAN_OP_SEGSCAN:
         return segscan_workspace_bytes(n);
+    case U32SCAN_OP_COMPACT:
+        return compact_workspace_bytes(n);
     default:
         return 0;
     }

@@ -493,5 +493,6 @@ __device__ __forceinline__ void bulk_load(unsigned int dst_smem, const void *src
 // Host-side workspace sizing of each operation (defined beside its kernels).
 size_t scan_workspace_bytes(unsigned long long n);
 size_t segscan_workspace_bytes(unsigned long long n);
+size_t compact_workspace_bytes(unsigned long long n);
 
 }  // namespace u32scan

@@ -17,6 +17,8 @@ Other ops time the other primitives on their own workloads:
   segreduce       segreduce_u32: sums and count only
   compact         compact_indices_u32, n = 2^27 int32 flags, keep
                   probability --p (0.1 or 0.9), seed 4
+  radix           radix_sort_perm_u32, n = 2^25 keys seed 5, uniform u32
+                  or (--ties) in [0, 256)
 
 Rank 0 prints one JSON line.
 
@@ -321,7 +323,81 @@ class CompactOp(Op):
                                    arrays["indices"].ctypes.data_as(i32p), arrays["count"].ctypes.data_as(i32p))
 
 
-OPS = ["scan_exclusive", "scan_inclusive", "segscan", "segscan_sums", "segreduce", "compact"]
+class RadixOp(Op):
+    log2n = 25
+    kernel_sources = ["u32_prefix_scan_gb300/csrc/radix.cu", "u32_prefix_scan_gb300/csrc/scan.cu",
+                      "u32_prefix_scan_gb300/csrc/internal.cuh"]
+
+    def __init__(self, args):
+        super().__init__(args)
+        self.ties = args.ties
+        self.name = "radix_sort_perm_u32" + ("_ties" if self.ties else "")
+        keys = "keys in [0,256)" if self.ties else "uniform u32 keys"
+        self.metric = f"stable LSD radix-sort permutation Gelem/s at n=2^25 ({keys}), 1 GB300"
+        self.kernel = "radix_downsweep_kernel + radix_upsweep_kernel (per active 8-bit digit)"
+
+    def workload(self):
+        keys = "u32(5,0,i) >> 24, in [0,256)" if self.ties else "u32(5,0,i), uniform"
+        return f"stable radix-sort permutation of n=2^{self.n.bit_length() - 1} u32 keys {keys} -> int32 perm"
+
+    def passes(self):
+        return 1 if self.ties else 4  # digits not constant over the keys
+
+    def algorithmic_bytes(self):
+        # this design's bytes: a 4-byte histogram read, then per active digit
+        # an upsweep read of the keys (4) and a downsweep that reads keys (4)
+        # and indices (4, not on the first pass) and writes keys (4, not on
+        # the last pass) and indices (4)
+        m, n = self.passes(), self.n
+        per = [4 + 4 + (4 if j else 0) + (4 if j < m - 1 else 0) + 4 for j in range(m)]
+        return n * (4 + 4 * m + sum(per) - 4 * m)
+
+    def host_inputs(self):
+        from u32_prefix_scan_gb300 import inputs
+
+        return {"keys": inputs.radix_keys(self.n, 5, ties=self.ties)}
+
+    def setup(self, dev, host):
+        import numpy as np
+        import torch
+
+        import u32_prefix_scan_gb300 as u
+        from u32_prefix_scan_gb300 import _native
+
+        self.u = u
+        self.keys = torch.from_numpy(host["keys"].view(np.int32)).to(dev)
+        self.perm = torch.empty(self.n, dtype=torch.int32, device=dev)
+        self.ws = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_RADIX, self.n), dev)
+        self.pinned_in = {"keys": torch.from_numpy(host["keys"].view(np.int32)).pin_memory()}
+        self.pinned_out = {"perm": torch.empty(self.n, dtype=torch.int32).pin_memory()}
+
+    def step(self):
+        self.u.radix_sort_perm_u32(self.keys, self.perm, workspace=self.ws)
+
+    def e2e_step(self):
+        self.keys.copy_(self.pinned_in["keys"], non_blocking=True)
+        self.step()
+        self.pinned_out["perm"].copy_(self.perm, non_blocking=True)
+        return 4 * self.n, 4 * self.n
+
+    def check_e2e(self, host):
+        import numpy as np
+
+        p = self.pinned_out["perm"].numpy()
+        s = host["keys"][p]
+        return bool(np.all(s[1:] >= s[:-1]))
+
+    def oracle_step(self, lib, arrays):
+        import numpy as np
+
+        k = arrays["keys"]
+        if "perm" not in arrays:
+            arrays["perm"] = np.empty(k.size, dtype=np.int32)
+        lib.oracle_sort_perm_u32(k.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)), k.size,
+                                 arrays["perm"].ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+
+
+OPS = ["scan_exclusive", "scan_inclusive", "segscan", "segscan_sums", "segreduce", "compact", "radix"]
 
 
 def make_op(args) -> Op:
@@ -329,6 +405,8 @@ def make_op(args) -> Op:
         return ScanOp(args, args.op == "scan_inclusive")
     if args.op == "compact":
         return CompactOp(args)
+    if args.op == "radix":
+        return RadixOp(args)
     return SegOp(args, args.op)
 
 
@@ -343,6 +421,7 @@ def parse_args(argv=None):
     p.add_argument("--op", choices=OPS, default="scan_exclusive")
     p.add_argument("--heads", choices=["geometric", "regular4"], default="geometric")
     p.add_argument("--p", type=float, choices=[0.1, 0.9], default=0.1, help="compaction keep probability")
+    p.add_argument("--ties", action="store_true", help="radix: keys in [0, 256) instead of uniform u32")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -162,6 +162,27 @@ int compact_indices_u32(const int32_t *flags, size_t n, int32_t *offsets,
                         void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /*
+ * Stable LSD radix-sort permutation of U32 keys.
+ * Source: the "parallel" package reference (entelechy docs), graph `sort`
+ * (the permutation that orders the keys, least significant bit first;
+ * sort_zeros / sort_place: a stable pass per bit), and the CAIRN
+ * "Concurrency" page, section "scan" (std.sort.radix_sort places each
+ * digit with an exclusive scan, so it is stable).
+ *   keys   device, uint32_t[n], read only; all 32 bits, unsigned order.
+ *   n      element count, below 2^31.
+ *   perm   device, int32_t[n]: keys[perm[0]] <= keys[perm[1]] <= ..., equal
+ *          keys in increasing index order (the unique stable permutation).
+ *   ws, ws_bytes  u32scan_workspace_bytes(U32SCAN_OP_RADIX, n) bytes (about
+ *          12 * n bytes: two key buffers and one index buffer).
+ * Digits that are equal for every key are skipped; which passes run is
+ * decided on the device, so the call is asynchronous like the others.
+ * Errors: EINVAL (null keys or perm with n > 0, misaligned pointers,
+ * n >= 2^31), EWORKSPACE, ECUDA.
+ */
+int radix_sort_perm_u32(const uint32_t *keys, size_t n, int32_t *perm,
+                        void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
  * Exclusive scan that allocates nothing and needs no workspace argument.
  * The pages have no counterpart: this entry point exists for callers that
  * cannot allocate device memory (for instance code inside an allocator's

@@ -122,3 +122,17 @@ def test_compact_rejects_bad_arguments_on_host(lib):
     assert fn(fake, 1000, fake, fake, fake, None, need, None) == _native.EWORKSPACE
     assert fn(fake, 1000, fake, fake, fake, fake, need - 256, None) == _native.EWORKSPACE
     assert fn(None, 0, None, None, None, None, 0, None) == _native.OK
+
+
+def test_radix_rejects_bad_arguments_on_host(lib):
+    fn = lib.radix_sort_perm_u32
+    fake = 0x10000
+    need = lib.u32scan_workspace_bytes(_native.OP_RADIX, 1000)
+    assert need >= 3 * 4 * 1000  # two key buffers and one index buffer
+    assert fn(None, 10, fake, fake, need, None) == _native.EINVAL
+    assert fn(fake, 10, None, fake, need, None) == _native.EINVAL
+    assert fn(fake + 2, 10, fake, fake, need, None) == _native.EINVAL
+    assert fn(fake, 1 << 31, fake, fake, 1 << 40, None) == _native.EINVAL
+    assert fn(fake, 1000, fake, None, need, None) == _native.EWORKSPACE
+    assert fn(fake, 1000, fake, fake, need - 256, None) == _native.EWORKSPACE
+    assert fn(None, 0, None, None, 0, None) == _native.OK

@@ -24,6 +24,7 @@ __all__ = [
     "segscan_inclusive_u32",
     "segreduce_u32",
     "compact_indices_u32",
+    "radix_sort_perm_u32",
     "check",
 ]
 
@@ -194,6 +195,24 @@ def compact_indices_u32(flags: torch.Tensor, offsets: torch.Tensor | None = None
         flags.data_ptr(), n, offsets.data_ptr() if offsets is not None else None, indices.data_ptr(),
         count.data_ptr(), ws.ptr, ws.nbytes, sh), "compact_indices_u32")
     return offsets, indices, count
+
+
+def radix_sort_perm_u32(keys: torch.Tensor, perm: torch.Tensor | None = None, *, stream=None,
+                        workspace: Workspace | None = None) -> torch.Tensor:
+    """The stable sorting permutation of u32 keys (int32 or uint32 tensor,
+    unsigned order): keys[perm] is non-decreasing, ties by index."""
+    _require_cuda(keys, "keys")
+    n = keys.numel()
+    if perm is None:
+        perm = torch.empty(n, dtype=torch.int32, device=keys.device)
+    _require_cuda(perm, "perm", (torch.int32,))
+    if perm.numel() != n:
+        raise ValueError("perm must have n elements")
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_RADIX, n, keys.device, sh, workspace)
+    _native.check(_native.lib().radix_sort_perm_u32(keys.data_ptr(), n, perm.data_ptr(), ws.ptr, ws.nbytes, sh),
+                  "radix_sort_perm_u32")
+    return perm
 
 
 def check(stream=None, workspace: Workspace | None = None, device=None) -> int:

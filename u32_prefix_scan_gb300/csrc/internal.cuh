@@ -494,5 +494,10 @@ __device__ __forceinline__ void bulk_load(unsigned int dst_smem, const void *src
 size_t scan_workspace_bytes(unsigned long long n);
 size_t segscan_workspace_bytes(unsigned long long n);
 size_t compact_workspace_bytes(unsigned long long n);
+size_t radix_workspace_bytes(unsigned long long n);
+
+// In-library launch of the exclusive scan (no total), for operations built
+// on it.
+int scan_exclusive_launch(uint32_t *data, unsigned long long n, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 }  // namespace u32scan

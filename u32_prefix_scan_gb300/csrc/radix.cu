@@ -1,0 +1,279 @@
+// radix.cu -- stable LSD radix-sort permutation of U32 keys.
+//
+// Source: the "parallel" package reference (entelechy docs), graph `sort`:
+// the permutation that orders the keys, least significant bit first; per
+// bit, sort_zeros counts the zeros at or before each place and sort_place
+// sends a zero to its rank among the zeros and a one behind all the zeros at
+// its rank among the ones ("the rank is the whole of what a stable radix
+// pass needs"). The CAIRN "Concurrency" page, section "scan", builds its
+// radix sort on an exclusive scan per digit the same way.
+//
+// Here a pass handles an 8-bit digit instead of one bit: a stable pass over
+// a digit is the composition of the eight stable one-bit passes over its
+// bits, so the result is the same unique stable permutation with 4 passes
+// instead of 32. Per digit pass:
+//   upsweep    each 8192-key tile counts its keys per digit value (warp
+//              match-any ranking into per-warp counters in shared memory) and
+//              writes the 256 counts into a digit-major table;
+//   scan       one exclusive scan of that table (the library's own scan
+//              kernel) gives every (digit value, tile) its first output slot:
+//              all smaller digit values first, then earlier tiles;
+//   downsweep  each tile ranks its keys stably within the tile and scatters
+//              (key, index) pairs to their slots.
+// A histogram of all four digits, taken first, finds digits that are equal
+// for every key; their passes are skipped (exact: such a pass moves
+// nothing). Which passes run, and which buffers they read and write, is
+// decided on the device, so the call stays asynchronous. The last pass
+// writes only indices, into `perm`.
+#include <cstdint>
+#include <mutex>
+#include <cuda_runtime.h>
+
+#include "internal.cuh"
+
+namespace u32scan {
+
+constexpr int kRThreads = 512;
+constexpr int kRKeys = 16;  // keys per thread per tile
+constexpr unsigned int kRTile = kRThreads * kRKeys;
+constexpr int kRWarps = kRThreads / 32;
+
+// One pass's role, decided on the device from the histograms.
+struct RadixPlan {
+    int active;  // this digit differs between keys
+    int j;       // index of this pass among the active ones
+    int m;       // number of active passes
+    int pad;
+};
+
+// Workspace layout for n keys (all regions 256-byte aligned). It starts
+// with the table scan's own workspace, whose 256-byte header (tile counter,
+// call epoch, device status) is the header every operation keeps at offset
+// 0, so u32scan_check reads the status of this call and the workspace stays
+// valid for any operation afterwards.
+struct RadixLayout {
+    size_t scan_ws, hist, plan, table, k1, k2, i1, total;
+    unsigned int n_tiles;
+    explicit RadixLayout(unsigned long long n) {
+        n_tiles = (unsigned int)((n + kRTile - 1) / kRTile);
+        const unsigned long long cells = 256ull * n_tiles;
+        size_t o = 0;
+        scan_ws = o;
+        o += scan_workspace_bytes(cells);
+        hist = o;
+        o += round_up(4 * 256 * 4, 256);
+        plan = o;
+        o += round_up(4 * sizeof(RadixPlan), 256);
+        table = o;
+        o += round_up(4 * cells, 256);
+        k1 = o;
+        o += round_up(4 * n, 256);
+        k2 = o;
+        o += round_up(4 * n, 256);
+        i1 = o;
+        o += round_up(4 * n, 256);
+        total = o;
+    }
+};
+
+__global__ void radix_histogram_kernel(const uint32_t *__restrict__ keys, unsigned long long n,
+                                       unsigned int *__restrict__ hist) {
+    __shared__ unsigned int s_h[4][256];
+    for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) (&s_h[0][0])[i] = 0;
+    __syncthreads();
+    for (unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (unsigned long long)gridDim.x * blockDim.x) {
+        const uint32_t k = keys[i];
+        atomicAdd(&s_h[0][k & 255u], 1u);
+        atomicAdd(&s_h[1][(k >> 8) & 255u], 1u);
+        atomicAdd(&s_h[2][(k >> 16) & 255u], 1u);
+        atomicAdd(&s_h[3][k >> 24], 1u);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) {
+        const unsigned int c = (&s_h[0][0])[i];
+        if (c) atomicAdd(hist + i, c);
+    }
+}
+
+// One warp: a digit is constant when one value holds all n keys.
+__global__ void radix_plan_kernel(const unsigned int *__restrict__ hist, unsigned long long n, RadixPlan *plan) {
+    const int lane = threadIdx.x & 31;
+    int active[4];
+    int m = 0;
+    for (int p = 0; p < 4; ++p) {
+        bool whole = false;
+        for (int b = lane; b < 256; b += 32) whole = whole || hist[256 * p + b] == n;
+        active[p] = __any_sync(0xffffffffu, whole) ? 0 : 1;
+        m += active[p];
+    }
+    if (lane == 0) {
+        int j = 0;
+        for (int p = 0; p < 4; ++p) {
+            plan[p].active = active[p];
+            plan[p].j = j;
+            plan[p].m = m;
+            j += active[p];
+        }
+    }
+}
+
+// Buffers of one pass (see the header comment of this file).
+struct PassBuffers {
+    const uint32_t *in_keys;
+    const int32_t *in_idx;  // null: the identity (first pass)
+    uint32_t *out_keys;     // null: last pass, keys are not needed any more
+    int32_t *out_idx;
+};
+
+__device__ __forceinline__ PassBuffers pass_buffers(const RadixPlan &pl, const uint32_t *keys, uint32_t *k1,
+                                                    uint32_t *k2, int32_t *i1, int32_t *perm) {
+    PassBuffers b;
+    const int j = pl.j, m = pl.m;
+    auto idx_of = [&](int q) -> int32_t * { return q == m - 1 ? perm : (((m - 1 - q) & 1) ? i1 : perm); };
+    b.in_keys = j == 0 ? keys : ((j - 1) & 1 ? k2 : k1);
+    b.in_idx = j == 0 ? nullptr : idx_of(j - 1);
+    b.out_keys = j == m - 1 ? nullptr : (j & 1 ? k2 : k1);
+    b.out_idx = idx_of(j);
+    return b;
+}
+
+// Load this thread's keys of tile t (warp-striped: round r of warp w covers
+// 32 consecutive keys) and rank them stably within the tile: after the call
+// wrank[r] is the key's rank among the keys of its digit value in this warp
+// (in tile order) and s_cnt[w][d] the warp's count of digit value d.
+// Invalid slots past n get digit 0xffff and take no part.
+__device__ __forceinline__ void radix_rank_tile(const uint32_t *__restrict__ in_keys, unsigned long long n,
+                                                unsigned int t, int shift, uint32_t (&k)[kRKeys],
+                                                unsigned int (&d)[kRKeys], unsigned int (&wrank)[kRKeys],
+                                                unsigned int (*s_cnt)[256], int lane, int warp) {
+    const unsigned long long base = (unsigned long long)t * kRTile + (unsigned long long)warp * (32 * kRKeys);
+    for (int i = lane; i < 256; i += 32) s_cnt[warp][i] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < kRKeys; ++r) {
+        const unsigned long long e = base + 32 * r + lane;
+        k[r] = e < n ? in_keys[e] : 0u;
+        d[r] = e < n ? (k[r] >> shift) & 255u : 0xffffu;
+    }
+#pragma unroll
+    for (int r = 0; r < kRKeys; ++r) {
+        const unsigned int same = __match_any_sync(0xffffffffu, d[r]);
+        const unsigned int below = (unsigned int)__popc(same & lanemask_lt(lane));
+        unsigned int old = 0;
+        if (d[r] < 256u) old = s_cnt[warp][d[r]];
+        wrank[r] = old + below;
+        __syncwarp();
+        if (d[r] < 256u && below == 0) s_cnt[warp][d[r]] = old + (unsigned int)__popc(same);
+        __syncwarp();
+    }
+}
+
+__global__ void __launch_bounds__(kRThreads, 1)
+radix_upsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
+                     int32_t *i1, int32_t *perm, unsigned long long n, unsigned int n_tiles,
+                     unsigned int *__restrict__ table) {
+    const RadixPlan pl = plan[p];
+    if (!pl.active) return;
+    __shared__ unsigned int s_cnt[kRWarps][256];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm);
+    uint32_t k[kRKeys];
+    unsigned int d[kRKeys], wrank[kRKeys];
+    radix_rank_tile(b.in_keys, n, blockIdx.x, 8 * p, k, d, wrank, s_cnt, lane, warp);
+    __syncthreads();
+    for (int v = threadIdx.x; v < 256; v += kRThreads) {
+        unsigned int c = 0;
+#pragma unroll
+        for (int w = 0; w < kRWarps; ++w) c += s_cnt[w][v];
+        table[(unsigned long long)v * n_tiles + blockIdx.x] = c;
+    }
+}
+
+__global__ void __launch_bounds__(kRThreads, 1)
+radix_downsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
+                       int32_t *i1, int32_t *perm, unsigned long long n, unsigned int n_tiles,
+                       const unsigned int *__restrict__ slots) {
+    const RadixPlan pl = plan[p];
+    if (!pl.active) return;
+    __shared__ unsigned int s_cnt[kRWarps][256];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned int t = blockIdx.x;
+    const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm);
+    uint32_t k[kRKeys];
+    unsigned int d[kRKeys], wrank[kRKeys];
+    radix_rank_tile(b.in_keys, n, t, 8 * p, k, d, wrank, s_cnt, lane, warp);
+    __syncthreads();
+    // s_cnt[w][v] <- first output slot of warp w's keys of digit value v
+    for (int v = threadIdx.x; v < 256; v += kRThreads) {
+        unsigned int run = slots[(unsigned long long)v * n_tiles + t];
+#pragma unroll
+        for (int w = 0; w < kRWarps; ++w) {
+            const unsigned int c = s_cnt[w][v];
+            s_cnt[w][v] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    const unsigned long long base = (unsigned long long)t * kRTile + (unsigned long long)warp * (32 * kRKeys);
+#pragma unroll
+    for (int r = 0; r < kRKeys; ++r) {
+        if (d[r] < 256u) {
+            const unsigned long long e = base + 32 * r + lane;
+            const unsigned int slot = s_cnt[warp][d[r]] + wrank[r];
+            const int32_t idx = b.in_idx ? b.in_idx[e] : (int32_t)e;
+            if (b.out_keys) b.out_keys[slot] = k[r];
+            b.out_idx[slot] = idx;
+        }
+    }
+}
+
+// All digits constant (every key equal): the permutation is the identity.
+__global__ void radix_identity_kernel(const RadixPlan *__restrict__ plan, int32_t *perm, unsigned long long n) {
+    if (plan[0].m != 0) return;
+    for (unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (unsigned long long)gridDim.x * blockDim.x)
+        perm[i] = (int32_t)i;
+}
+
+size_t radix_workspace_bytes(unsigned long long n) { return RadixLayout(n).total; }
+
+static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *perm, void *ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+    if (n >= (1ull << 31)) return U32SCAN_EINVAL;
+    if (n > 0 && (keys == nullptr || perm == nullptr)) return U32SCAN_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(keys) & 3) || (reinterpret_cast<uintptr_t>(perm) & 3)) return U32SCAN_EINVAL;
+    if (n == 0) return U32SCAN_OK;
+    const RadixLayout L(n);
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < L.total) return U32SCAN_EWORKSPACE;
+    char *w = static_cast<char *>(ws);
+    unsigned int *hist = reinterpret_cast<unsigned int *>(w + L.hist);
+    RadixPlan *plan = reinterpret_cast<RadixPlan *>(w + L.plan);
+    unsigned int *table = reinterpret_cast<unsigned int *>(w + L.table);
+    uint32_t *k1 = reinterpret_cast<uint32_t *>(w + L.k1);
+    uint32_t *k2 = reinterpret_cast<uint32_t *>(w + L.k2);
+    int32_t *i1 = reinterpret_cast<int32_t *>(w + L.i1);
+    if (cudaMemsetAsync(hist, 0, 4 * 256 * 4, stream) != cudaSuccess) return U32SCAN_ECUDA;
+    radix_histogram_kernel<<<1024, 512, 0, stream>>>(keys, n, hist);
+    radix_plan_kernel<<<1, 32, 0, stream>>>(hist, n, plan);
+    const unsigned long long cells = 256ull * L.n_tiles;
+    for (int p = 0; p < 4; ++p) {
+        radix_upsweep_kernel<<<L.n_tiles, kRThreads, 0, stream>>>(plan, p, keys, k1, k2, i1, perm, n, L.n_tiles,
+                                                                   table);
+        const int rc = scan_exclusive_launch(table, cells, w + L.scan_ws, scan_workspace_bytes(cells), stream);
+        if (rc != U32SCAN_OK) return rc;
+        radix_downsweep_kernel<<<L.n_tiles, kRThreads, 0, stream>>>(plan, p, keys, k1, k2, i1, perm, n, L.n_tiles,
+                                                                     table);
+    }
+    radix_identity_kernel<<<1024, 256, 0, stream>>>(plan, perm, n);
+    return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
+}
+
+}  // namespace u32scan
+
+using namespace u32scan;
+
+extern "C" int radix_sort_perm_u32(const uint32_t *keys, size_t n, int32_t *perm, void *ws, size_t ws_bytes,
+                                   u32scan_stream_t stream) {
+    return radix_launch(keys, n, perm, ws, ws_bytes, (cudaStream_t)stream);
+}

@@ -76,19 +76,46 @@ struct RadixLayout {
     }
 };
 
+// Counts of all four digits over all keys (one read), for the plan.
 __global__ void radix_histogram_kernel(const uint32_t *__restrict__ keys, unsigned long long n,
                                        unsigned int *__restrict__ hist) {
     __shared__ unsigned int s_h[4][256];
     for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) (&s_h[0][0])[i] = 0;
     __syncthreads();
-    for (unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (unsigned long long)gridDim.x * blockDim.x) {
-        const uint32_t k = keys[i];
+    auto add = [&](uint32_t k) {
         atomicAdd(&s_h[0][k & 255u], 1u);
         atomicAdd(&s_h[1][(k >> 8) & 255u], 1u);
         atomicAdd(&s_h[2][(k >> 16) & 255u], 1u);
         atomicAdd(&s_h[3][k >> 24], 1u);
+    };
+    // scalar head up to 16-byte alignment, 16-byte body, scalar tail
+    const unsigned long long head = ((16 - (reinterpret_cast<uintptr_t>(keys) & 15)) & 15) / 4;
+    const unsigned long long h = head < n ? head : n;
+    const unsigned long long nv = (n - h) / 4;
+    const unsigned long long gtid = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const unsigned long long gstride = (unsigned long long)gridDim.x * blockDim.x;
+    if (gtid < h) add(keys[gtid]);
+    const uint4 *kv = reinterpret_cast<const uint4 *>(keys + h);
+    for (unsigned long long i = gtid; i < nv; i += gstride) {
+        const uint4 q = kv[i];
+        // a quad whose four keys agree on a digit (common when the digit is
+        // constant over the keys) takes one atomic for it instead of four
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const unsigned int s = 8 * p;
+            const unsigned int a = (q.x >> s) & 255u, b = (q.y >> s) & 255u, c = (q.z >> s) & 255u,
+                               d = (q.w >> s) & 255u;
+            if (a == b && b == c && c == d) {
+                atomicAdd(&s_h[p][a], 4u);
+            } else {
+                atomicAdd(&s_h[p][a], 1u);
+                atomicAdd(&s_h[p][b], 1u);
+                atomicAdd(&s_h[p][c], 1u);
+                atomicAdd(&s_h[p][d], 1u);
+            }
+        }
     }
+    for (unsigned long long i = h + 4 * nv + gtid; i < n; i += gstride) add(keys[i]);
     __syncthreads();
     for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) {
         const unsigned int c = (&s_h[0][0])[i];
@@ -141,35 +168,52 @@ __device__ __forceinline__ PassBuffers pass_buffers(const RadixPlan &pl, const u
 // Load this thread's keys of tile t (warp-striped: round r of warp w covers
 // 32 consecutive keys) and rank them stably within the tile: after the call
 // wrank[r] is the key's rank among the keys of its digit value in this warp
-// (in tile order) and s_cnt[w][d] the warp's count of digit value d.
-// Invalid slots past n get digit 0xffff and take no part.
-__device__ __forceinline__ void radix_rank_tile(const uint32_t *__restrict__ in_keys, unsigned long long n,
-                                                unsigned int t, int shift, uint32_t (&k)[kRKeys],
-                                                unsigned int (&d)[kRKeys], unsigned int (&wrank)[kRKeys],
-                                                unsigned int (*s_cnt)[256], int lane, int warp) {
+// (in tile order) and s_cnt[w][v] the warp's count of digit value v. Bit r
+// of the returned mask says whether key r lies inside the array.
+__device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restrict__ in_keys, unsigned long long n,
+                                                        unsigned int t, int shift, uint32_t (&k)[kRKeys],
+                                                        unsigned int (&wrank)[kRKeys], unsigned int (*s_cnt)[256],
+                                                        int lane, int warp) {
     const unsigned long long base = (unsigned long long)t * kRTile + (unsigned long long)warp * (32 * kRKeys);
     for (int i = lane; i < 256; i += 32) s_cnt[warp][i] = 0;
     __syncwarp();
+    unsigned int valid_bits = 0;
 #pragma unroll
     for (int r = 0; r < kRKeys; ++r) {
         const unsigned long long e = base + 32 * r + lane;
         k[r] = e < n ? in_keys[e] : 0u;
-        d[r] = e < n ? (k[r] >> shift) & 255u : 0xffffu;
+        valid_bits |= (e < n ? 1u : 0u) << r;
     }
 #pragma unroll
     for (int r = 0; r < kRKeys; ++r) {
-        const unsigned int same = __match_any_sync(0xffffffffu, d[r]);
+        // lanes holding the same digit value: the AND over the digit's eight
+        // bits of the ballot (bit set) or its complement (bit clear), and
+        // the same for validity
+        const bool valid = (valid_bits >> r) & 1u;
+        const unsigned int dr = (k[r] >> shift) & 255u;
+        const unsigned int vb = __ballot_sync(0xffffffffu, valid);
+        unsigned int same = valid ? vb : ~vb;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const bool bit = (dr >> b) & 1u;
+            const unsigned int bb = __ballot_sync(0xffffffffu, bit);
+            same &= bit ? bb : ~bb;
+        }
         const unsigned int below = (unsigned int)__popc(same & lanemask_lt(lane));
         unsigned int old = 0;
-        if (d[r] < 256u) old = s_cnt[warp][d[r]];
+        if (valid) old = s_cnt[warp][dr];
         wrank[r] = old + below;
         __syncwarp();
-        if (d[r] < 256u && below == 0) s_cnt[warp][d[r]] = old + (unsigned int)__popc(same);
+        if (valid && below == 0) s_cnt[warp][dr] = old + (unsigned int)__popc(same);
         __syncwarp();
     }
+    return valid_bits;
 }
 
-__global__ void __launch_bounds__(kRThreads, 1)
+// Upsweep of one pass: the tile's count of each digit value, written into
+// the digit-major table. Counting needs no ranks, so each warp adds its keys
+// into its own row of shared-memory counters with atomics.
+__global__ void __launch_bounds__(kRThreads, 2)
 radix_upsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
                      int32_t *i1, int32_t *perm, unsigned long long n, unsigned int n_tiles,
                      unsigned int *__restrict__ table) {
@@ -178,9 +222,19 @@ radix_upsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *
     __shared__ unsigned int s_cnt[kRWarps][256];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm);
+    for (int i = lane; i < 256; i += 32) s_cnt[warp][i] = 0;
+    __syncwarp();
+    const unsigned long long base = (unsigned long long)blockIdx.x * kRTile + (unsigned long long)warp * (32 * kRKeys);
     uint32_t k[kRKeys];
-    unsigned int d[kRKeys], wrank[kRKeys];
-    radix_rank_tile(b.in_keys, n, blockIdx.x, 8 * p, k, d, wrank, s_cnt, lane, warp);
+#pragma unroll
+    for (int r = 0; r < kRKeys; ++r) {
+        const unsigned long long e = base + 32 * r + lane;
+        k[r] = e < n ? b.in_keys[e] : 0u;
+    }
+    const int shift = 8 * p;
+#pragma unroll
+    for (int r = 0; r < kRKeys; ++r)
+        if (base + 32 * r + lane < n) atomicAdd(&s_cnt[warp][(k[r] >> shift) & 255u], 1u);
     __syncthreads();
     for (int v = threadIdx.x; v < 256; v += kRThreads) {
         unsigned int c = 0;
@@ -190,43 +244,77 @@ radix_upsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *
     }
 }
 
-__global__ void __launch_bounds__(kRThreads, 1)
+// Downsweep of one pass: rank the tile, order it by digit value in shared
+// memory (stable), then write each digit value's run of (key, index) pairs
+// to its slots with consecutive threads on consecutive slots.
+__global__ void __launch_bounds__(kRThreads, 2)
 radix_downsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
                        int32_t *i1, int32_t *perm, unsigned long long n, unsigned int n_tiles,
                        const unsigned int *__restrict__ slots) {
     const RadixPlan pl = plan[p];
     if (!pl.active) return;
-    __shared__ unsigned int s_cnt[kRWarps][256];
+    extern __shared__ __align__(16) unsigned int r_smem[];
+    unsigned int(*s_cnt)[256] = reinterpret_cast<unsigned int(*)[256]>(r_smem);  // [kRWarps][256]
+    unsigned int *s_tileoff = r_smem + kRWarps * 256;                           // [256] digit start in tile
+    unsigned int *s_glob = s_tileoff + 256;                                     // [256] digit's first slot
+    unsigned int *s_keys = s_glob + 256;                                        // [kRTile]
+    int32_t *s_idx = reinterpret_cast<int32_t *>(s_keys + kRTile);              // [kRTile]
+    __shared__ unsigned int s_part[kRThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned int t = blockIdx.x;
     const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm);
     uint32_t k[kRKeys];
-    unsigned int d[kRKeys], wrank[kRKeys];
-    radix_rank_tile(b.in_keys, n, t, 8 * p, k, d, wrank, s_cnt, lane, warp);
+    unsigned int wrank[kRKeys];
+    const unsigned int valid_bits = radix_rank_tile(b.in_keys, n, t, 8 * p, k, wrank, s_cnt, lane, warp);
     __syncthreads();
-    // s_cnt[w][v] <- first output slot of warp w's keys of digit value v
-    for (int v = threadIdx.x; v < 256; v += kRThreads) {
-        unsigned int run = slots[(unsigned long long)v * n_tiles + t];
+    // Per digit value v (threads 0..255): warp offsets within the value's
+    // run in this tile, and the run's length; then the runs' starts.
+    unsigned int tot = 0;
+    if (threadIdx.x < 256) {
+        const int v = threadIdx.x;
 #pragma unroll
         for (int w = 0; w < kRWarps; ++w) {
             const unsigned int c = s_cnt[w][v];
-            s_cnt[w][v] = run;
-            run += c;
+            s_cnt[w][v] = tot;
+            tot += c;
         }
+        s_glob[v] = slots[(unsigned long long)v * n_tiles + t];
+    }
+    // exclusive scan of the 256 run lengths over threads 0..255
+    const unsigned int inc = warp_inclusive_sum(tot, lane);
+    if (lane == 31 && threadIdx.x < 256) s_part[warp] = inc;
+    __syncthreads();
+    if (threadIdx.x < 256) {
+        unsigned int before = 0;
+        for (int w = 0; w < warp; ++w) before += s_part[w];
+        s_tileoff[threadIdx.x] = before + inc - tot;
     }
     __syncthreads();
     const unsigned long long base = (unsigned long long)t * kRTile + (unsigned long long)warp * (32 * kRKeys);
 #pragma unroll
     for (int r = 0; r < kRKeys; ++r) {
-        if (d[r] < 256u) {
+        if ((valid_bits >> r) & 1u) {
             const unsigned long long e = base + 32 * r + lane;
-            const unsigned int slot = s_cnt[warp][d[r]] + wrank[r];
-            const int32_t idx = b.in_idx ? b.in_idx[e] : (int32_t)e;
-            if (b.out_keys) b.out_keys[slot] = k[r];
-            b.out_idx[slot] = idx;
+            const unsigned int v = (k[r] >> (8 * p)) & 255u;
+            const unsigned int pos = s_tileoff[v] + s_cnt[warp][v] + wrank[r];
+            s_keys[pos] = k[r];
+            s_idx[pos] = b.in_idx ? b.in_idx[e] : (int32_t)e;
         }
     }
+    __syncthreads();
+    const unsigned long long tile0 = (unsigned long long)t * kRTile;
+    const unsigned int count = n - tile0 < kRTile ? (unsigned int)(n - tile0) : kRTile;
+    const int shift = 8 * p;
+    for (unsigned int i = threadIdx.x; i < count; i += kRThreads) {
+        const unsigned int key = s_keys[i];
+        const unsigned int v = (key >> shift) & 255u;
+        const unsigned int slot = s_glob[v] + (i - s_tileoff[v]);
+        if (b.out_keys) b.out_keys[slot] = key;
+        b.out_idx[slot] = s_idx[i];
+    }
 }
+
+constexpr size_t kRDownSmem = (size_t)(kRWarps * 256 + 512 + 2 * kRTile) * 4;
 
 // All digits constant (every key equal): the permutation is the identity.
 __global__ void radix_identity_kernel(const RadixPlan *__restrict__ plan, int32_t *perm, unsigned long long n) {
@@ -253,6 +341,19 @@ static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *per
     uint32_t *k1 = reinterpret_cast<uint32_t *>(w + L.k1);
     uint32_t *k2 = reinterpret_cast<uint32_t *>(w + L.k2);
     int32_t *i1 = reinterpret_cast<int32_t *>(w + L.i1);
+    {
+        static std::mutex mu;
+        static bool attr_set[64];
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return U32SCAN_ECUDA;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(radix_downsweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kRDownSmem) != cudaSuccess)
+                return U32SCAN_ECUDA;
+            attr_set[dev] = true;
+        }
+    }
     if (cudaMemsetAsync(hist, 0, 4 * 256 * 4, stream) != cudaSuccess) return U32SCAN_ECUDA;
     radix_histogram_kernel<<<1024, 512, 0, stream>>>(keys, n, hist);
     radix_plan_kernel<<<1, 32, 0, stream>>>(hist, n, plan);
@@ -262,8 +363,8 @@ static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *per
                                                                    table);
         const int rc = scan_exclusive_launch(table, cells, w + L.scan_ws, scan_workspace_bytes(cells), stream);
         if (rc != U32SCAN_OK) return rc;
-        radix_downsweep_kernel<<<L.n_tiles, kRThreads, 0, stream>>>(plan, p, keys, k1, k2, i1, perm, n, L.n_tiles,
-                                                                     table);
+        radix_downsweep_kernel<<<L.n_tiles, kRThreads, kRDownSmem, stream>>>(plan, p, keys, k1, k2, i1, perm, n,
+                                                                              L.n_tiles, table);
     }
     radix_identity_kernel<<<1024, 256, 0, stream>>>(plan, perm, n);
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;

@@ -1,0 +1,83 @@
+"""bench.py's host logic on the CPU: arguments, per-op algorithmic bytes, the
+traffic record check, and the multi-rank path (two gloo ranks: barrier and
+max over ranks; the reference arm runs on rank 0 only)."""
+
+import json
+import os
+import socket
+
+import pytest
+
+import bench
+
+
+def free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_defaults_and_validation():
+    a = bench.parse_args([])
+    assert a.op == "scan_exclusive" and a.gpus == 1 and a.warmup >= 3 and a.impl == "ours"
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--warmup", "2"])
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--steps", "0"])
+
+
+def test_algorithmic_bytes_per_op():
+    n28, n26, n27, n25 = 1 << 28, 1 << 26, 1 << 27, 1 << 25
+    assert bench.make_op(bench.parse_args([])).algorithmic_bytes() == 8 * n28
+    assert bench.make_op(bench.parse_args(["--op", "scan_inclusive"])).algorithmic_bytes() == 8 * n28
+    seg = bench.make_op(bench.parse_args(["--op", "segscan"]))
+    seg.nseg = 5
+    assert seg.algorithmic_bytes() == 12 * n26
+    red = bench.make_op(bench.parse_args(["--op", "segreduce", "--heads", "regular4"]))
+    red.nseg = n26 // 4
+    assert red.algorithmic_bytes() == 8 * n26 + 4 * (n26 // 4) + 4
+    assert bench.make_op(bench.parse_args(["--op", "compact"])).algorithmic_bytes() == 12 * n27 + 4
+    assert bench.make_op(bench.parse_args(["--op", "radix"])).algorithmic_bytes() == 76 * n25
+    assert bench.make_op(bench.parse_args(["--op", "radix", "--ties"])).algorithmic_bytes() == 16 * n25
+    assert bench.make_op(bench.parse_args(["--log2n", "20"])).n == 1 << 20
+
+
+def test_traffic_record_must_match_source_and_size(tmp_path, monkeypatch):
+    op = bench.make_op(bench.parse_args([]))
+    f = tmp_path / "t.json"
+    monkeypatch.setattr(type(op), "traffic_file", property(lambda self: f))
+    assert bench.load_traffic(op) is None  # no record
+    rec = {"source_hash": bench.source_hash(op.kernel_sources), "scaled_to_n": op.n, "dram_bytes_per_launch": 123.0}
+    f.write_text(json.dumps(rec))
+    assert bench.load_traffic(op) == 123.0
+    f.write_text(json.dumps({**rec, "source_hash": "stale"}))
+    assert bench.load_traffic(op) is None  # the kernel changed since the capture
+    f.write_text(json.dumps({**rec, "scaled_to_n": op.n // 2}))
+    assert bench.load_traffic(op) is None
+
+
+def _rank_main(rank, world, port, out_dir):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier(world)
+        got = bench.max_over_ranks(1.5 + rank, world)
+        ref = bench.run_reference(bench.parse_args(["--impl", "reference", "--steps", "1", "--warmup", "3",
+                                                    "--log2n", "12"]), rank)
+        with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as fh:
+            json.dump({"max": got, "ref": None if ref is None else ref["impl"]}, fh)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_barrier_max_and_reference_on_rank0(tmp_path):
+    import torch.multiprocessing as mp
+
+    world = 2
+    mp.spawn(_rank_main, args=(world, free_port(), str(tmp_path)), nprocs=world, join=True)
+    r0 = json.loads((tmp_path / "rank0.json").read_text())
+    r1 = json.loads((tmp_path / "rank1.json").read_text())
+    assert r0["max"] == r1["max"] == 2.5  # the slowest rank's time
+    assert r0["ref"] == "reference" and r1["ref"] is None

@@ -95,7 +95,7 @@ class ScanOp(Op):
         self.name = "scan_inclusive_u32" if inclusive else "scan_exclusive_u32"
         form = "inclusive" if inclusive else "exclusive"
         self.metric = f"U32 {form} scan Gelem/s and HBM GB/s (fraction of peak) at n=2^28, 1 GB300"
-        self.kernel = f"scan_u32_persistent<512,8,2,1,{form}>"
+        self.kernel = f"scan_u32_persistent<512,8,2,1,{form}> (bulk-copy stores)"
 
     def workload(self):
         form = "inclusive" if self.inclusive else "exclusive"

@@ -490,6 +490,20 @@ __device__ __forceinline__ void bulk_load(unsigned int dst_smem, const void *src
         : "memory");
 }
 
+// Shared memory -> global 1-D bulk copy (16-byte aligned, size a multiple of
+// 16), tracked as a bulk-async group of the issuing thread.
+__device__ __forceinline__ void bulk_store(void *dst, unsigned int src_smem, unsigned int bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until this thread's bulk stores have read their shared-memory source.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Wait until this thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Host-side workspace sizing of each operation (defined beside its kernels).
 size_t scan_workspace_bytes(unsigned long long n);
 size_t segscan_workspace_bytes(unsigned long long n);

@@ -42,6 +42,11 @@
 #ifndef U32SCAN_P_LOOK
 #define U32SCAN_P_LOOK 1
 #endif
+// 1: a full tile's results are written to a shared-memory buffer and stored
+// by one 1-D bulk copy (TMA); 0: 16-byte streaming stores from registers.
+#ifndef U32SCAN_P_BULKSTORE
+#define U32SCAN_P_BULKSTORE 1
+#endif
 #ifndef U32SCAN_P_MINB
 #define U32SCAN_P_MINB 1
 #endif
@@ -210,7 +215,7 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
     constexpr unsigned int TILE_BYTES = TILE * 4;
     static_assert(WARPS <= 32, "one warp scans the warp totals");
     static_assert(S >= 2, "the pipeline reads one stage ahead");
-    extern __shared__ __align__(128) uint4 stage_buf[];  // S stages of TILE elements
+    extern __shared__ __align__(128) uint4 stage_buf[];  // S stages of TILE elements (+ the output buffer)
     __shared__ __align__(8) unsigned long long bar[S];
     __shared__ unsigned int s_tile[S];
     __shared__ unsigned int s_wt[2][WARPS];  // warp totals of the current / next tile
@@ -284,14 +289,29 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
         if (lane == 0) s_wt[u & 1][warp] = wtot;
         return t;
     };
+    // Store the current tile. With bulk stores, a full tile goes through the
+    // output buffer after the S stages: every thread writes its part, a
+    // barrier, then thread 0 starts one 1-D bulk copy of the whole tile (its
+    // previous copy has finished reading the buffer: thread 0 waited for
+    // that before barrier B). tile_full(t) is the same for every thread.
     auto store_tile = [&](unsigned int t, const uint4 (&x)[V], unsigned int base) {
         const unsigned long long tile_v0 = (unsigned long long)t * TILE;
         uint32_t *tb = vbase + tile_v0;
         if (tile_full(t)) {
+            if (U32SCAN_P_BULKSTORE) {
+                uint4 *ob = stage_buf + S * (TILE / 4);
 #pragma unroll
-            for (int r = 0; r < V; ++r) {
-                const uint4 y = make_uint4(x[r].x + base, x[r].y + base, x[r].z + base, x[r].w + base);
-                __stcs(reinterpret_cast<uint4 *>(tb + li0 + 128 * r), y);
+                for (int r = 0; r < V; ++r)
+                    ob[(li0 >> 2) + 32 * r] = make_uint4(x[r].x + base, x[r].y + base, x[r].z + base, x[r].w + base);
+                fence_proxy_async_smem();
+                __syncthreads();  // barrier C: the output buffer is complete
+                if (threadIdx.x == 0) bulk_store(tb, smem_u32(ob), TILE_BYTES);
+            } else {
+#pragma unroll
+                for (int r = 0; r < V; ++r) {
+                    const uint4 y = make_uint4(x[r].x + base, x[r].y + base, x[r].z + base, x[r].w + base);
+                    __stcs(reinterpret_cast<uint4 *>(tb + li0 + 128 * r), y);
+                }
             }
         } else {
             const unsigned int lo = tile_v0 < head ? (unsigned int)(head - tile_v0) : 0u;
@@ -367,6 +387,7 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
                 if (lane < WARPS) s_base[lane] = prefix + wex_c;
                 if (tc == n_tiles - 1u && lane == 0 && total != nullptr) *total = prefix + agg_c;
             }
+            if (U32SCAN_P_BULKSTORE && threadIdx.x == 0) bulk_wait_read();  // output buffer free again
             __syncthreads();  // barrier B: bases of the current tile are visible
             store_tile(tc, xc, s_base[warp]);
             if (!more) break;
@@ -377,14 +398,16 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
             wex_c = wex_n;
         }
     }
-    // Leave no bulk copy in flight into this block's shared memory: wait
-    // (bounded) for the latest phase of every stage. On the normal path the
-    // outstanding draws are all past the end and have completed already.
+    // Leave no bulk copy in flight into or out of this block's shared
+    // memory: wait (bounded) for the latest phase of every stage (on the
+    // normal path the outstanding draws are past the end and completed
+    // already), and for thread 0's bulk stores.
     if (producer) {
 #pragma unroll
         for (int st = 0; st < S; ++st)
             (void)mbar_wait_bounded(smem_u32(&bar[st]), (latest_parity >> st) & 1u, limit_ns);
     }
+    if (U32SCAN_P_BULKSTORE && threadIdx.x == 0) bulk_wait_all();
 }
 
 // Launch shapes, chosen by n: long arrays use the persistent kernel, short
@@ -392,7 +415,7 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
 constexpr int kPThreads = U32SCAN_P_THREADS, kPV = U32SCAN_P_V, kPStages = U32SCAN_P_STAGES,
               kPLook = U32SCAN_P_LOOK;
 constexpr unsigned long long kPTile = (unsigned long long)kPThreads * kPV * 4;
-constexpr size_t kPSmem = (size_t)kPStages * kPTile * 4;
+constexpr size_t kPSmem = (size_t)(kPStages + (U32SCAN_P_BULKSTORE ? 1 : 0)) * kPTile * 4;
 constexpr unsigned long long kPersistentMinN = 1ull << 22;
 
 struct ScanShape {

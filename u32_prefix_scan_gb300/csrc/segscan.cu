@@ -233,19 +233,23 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const int32_t *__restrict__ 
                 if (r + 1 < V) wrap = __shfl_sync(0xffffffffu, (hb >> (4 * (r + 1))) & 1u, 0);
                 const unsigned int after = lane < 31 ? down : wrap;
                 const unsigned int next_bits = (b >> 1) | (after << 3);  // bit c: element c + 1 is a head
+                const bool last_here = last_li - (li0 + 128 * r) < 4u;  // the array's last element is one of mine
                 const unsigned int pc = (unsigned int)__popc(b);
-                const unsigned int incl = warp_inclusive_sum(pc, lane);
+                // Most rounds of long segments hold no segment end: skip them.
+                if (__any_sync(0xffffffffu, next_bits != 0u || last_here)) {
+                    const unsigned int incl = warp_inclusive_sum(pc, lane);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const unsigned int li = li0 + 128 * r + c;
-                    const bool end = li >= lo && li < hi && (((next_bits >> c) & 1u) || li == last_li);
-                    if (end) {
-                        const unsigned long long k =
-                            (unsigned long long)hbase + (incl - pc) + (unsigned int)__popc(b & ((2u << c) - 1u)) - 1u;
-                        if (k < seg_cap) seg_sums[k] = y[c];
+                    for (int c = 0; c < 4; ++c) {
+                        const unsigned int li = li0 + 128 * r + c;
+                        const bool end = li >= lo && li < hi && (((next_bits >> c) & 1u) || li == last_li);
+                        if (end) {
+                            const unsigned long long k = (unsigned long long)hbase + (incl - pc) +
+                                                         (unsigned int)__popc(b & ((2u << c) - 1u)) - 1u;
+                            if (k < seg_cap) seg_sums[k] = y[c];
+                        }
                     }
                 }
-                hbase += __shfl_sync(0xffffffffu, incl, 31);
+                hbase += __reduce_add_sync(0xffffffffu, pc);
             }
         }
     };

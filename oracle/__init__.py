@@ -52,6 +52,8 @@ def _configure(lib):
     lib.oracle_scan_exclusive_u32.restype = ctypes.c_uint32
     lib.oracle_scan_inclusive_u32.argtypes = [_u32p, _u64]
     lib.oracle_scan_inclusive_u32.restype = ctypes.c_uint32
+    lib.oracle_scan_op_u32.argtypes = [ctypes.c_int, ctypes.c_int, _u32p, _u64]
+    lib.oracle_scan_op_u32.restype = ctypes.c_uint32
     lib.oracle_scan_blocked_u32.argtypes = [ctypes.c_int, ctypes.c_uint, _u32p, _u64, _u32p]
     lib.oracle_scan_blocked_u32.restype = ctypes.c_uint32
     lib.oracle_segscan_inclusive_u32.argtypes = [_u32p, _i32p, _u64]
@@ -102,6 +104,17 @@ def scan_inclusive(a):
     """(scanned copy, total): out[j] = a[0] + .. + a[j] mod 2^32."""
     out = _u32(a)
     total = _load().oracle_scan_inclusive_u32(_p(out, _u32p), out.size)
+    return out, int(total)
+
+
+SCAN_OPS = {"add": 0, "mul": 1, "and": 2, "or": 3, "xor": 4, "min": 5, "max": 6}
+
+
+def scan_op(a, op: str, inclusive: bool):
+    """(scanned copy, fold) under one of the CAIRN integer operators on
+    uint32: add, mul (both wrapping), and, or, xor, min, max."""
+    out = _u32(a)
+    total = _load().oracle_scan_op_u32(SCAN_OPS[op], int(bool(inclusive)), _p(out, _u32p), out.size)
     return out, int(total)
 
 

@@ -120,6 +120,54 @@ uint32_t oracle_scan_blocked_u32(int inclusive, unsigned b, uint32_t *a,
 }
 
 /* ------------------------------------------------------------------------
+ * Scans under the other operators of the CAIRN "Concurrency" page, section
+ * "reduce and compact" (the operators of reduce, which scan shares per
+ * section "scan"): add_wrap, mul_wrap, &, |, ^, min and max on integers,
+ * here on uint32. Each is associative and commutative, with identity 0, 1,
+ * all ones, 0, 0, all ones and 0. Exclusive: a[j] = e . a[0] . .. . a[j-1]
+ * (e the identity); inclusive: through a[j]; returns the fold of all n.
+ * op: 0 add, 1 mul, 2 and, 3 or, 4 xor, 5 min, 6 max.
+ * ---------------------------------------------------------------------- */
+
+static uint32_t oracle_apply(int op, uint32_t x, uint32_t y)
+{
+    switch (op) {
+    case 0: return x + y;
+    case 1: return x * y;
+    case 2: return x & y;
+    case 3: return x | y;
+    case 4: return x ^ y;
+    case 5: return x < y ? x : y;
+    default: return x > y ? x : y;
+    }
+}
+
+static uint32_t oracle_identity(int op)
+{
+    switch (op) {
+    case 1: return 1u;
+    case 2: case 5: return 0xffffffffu;
+    default: return 0u;
+    }
+}
+
+uint32_t oracle_scan_op_u32(int op, int inclusive, uint32_t *a, uint64_t n)
+{
+    uint32_t s = oracle_identity(op);
+    for (uint64_t j = 0; j < n; ++j) {
+        uint32_t x = a[j];
+        if (inclusive) {
+            s = oracle_apply(op, s, x);
+            a[j] = s;
+        } else {
+            a[j] = s;
+            s = oracle_apply(op, s, x);
+        }
+    }
+    return s;
+}
+
+/* ------------------------------------------------------------------------
  * Segmented scan and reduce.  [Futhark] regularSegmentedScan names the
  * segmented scan; regularSegmentedRedomap reduces "until there is only a
  * single value per segment". Segments are marked by head flags: a non-zero

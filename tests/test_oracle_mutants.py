@@ -37,6 +37,8 @@ MUTANTS = [
      ["compact_numpy"]),
     ("sort_skips_bit0", "for (unsigned bit = 0; bit < bits; ++bit)",
      "for (unsigned bit = 1; bit < bits; ++bit)", ["lsd", "radix_brute"]),
+    ("min_identity_zero", "case 2: case 5: return 0xffffffffu;", "case 2: return 0xffffffffu;",
+     ["opscan_min"]),
     ("sort_ties_descending", "return (a->idx > b->idx) - (a->idx < b->idx);",
      "return (a->idx < b->idx) - (a->idx > b->idx);", ["sort_numpy", "radix_brute"]),
 ]
@@ -55,6 +57,7 @@ PINS = {
     "lsd": lambda o: pins.test_per_bit_lsd_equals_stable_sort(o, True),
     "radix_brute": lambda o: pins.test_radix_brute_force_tiny(o),
     "sort_numpy": lambda o: pins.test_sort_perm_against_numpy_stable_argsort(o, True),
+    "opscan_min": lambda o: pins.test_operator_scans_against_numpy_accumulate(o, "min"),
 }
 
 

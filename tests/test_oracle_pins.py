@@ -286,3 +286,64 @@ def test_radix_properties(oracle_mod):
     assert np.all(s[1:] >= s[:-1])
     same = s[1:] == s[:-1]
     assert np.all(perm[1:][same] > perm[:-1][same])
+
+
+# ------------------------------------------------------- operator scans ----
+
+NP_ACCUM = {"add": np.add, "mul": np.multiply, "and": np.bitwise_and, "or": np.bitwise_or,
+            "xor": np.bitwise_xor, "min": np.minimum, "max": np.maximum}
+IDENTITY = {"add": 0, "mul": 1, "and": M32 - 1, "or": 0, "xor": 0, "min": M32 - 1, "max": 0}
+
+
+def test_golden_cairn_scan_max(oracle_mod):
+    g = read_golden("cairn_scan_max.txt")
+    a = [int(x) for x in g["input"].split()]
+    out, _ = oracle_mod.scan_op(a, "max", inclusive=True)
+    for pair in g["expect_at"].split():
+        j, v = pair.split(":")
+        assert int(out[int(j)]) == int(v)
+
+
+def test_golden_cairn_reduce_max(oracle_mod):
+    g = read_golden("cairn_reduce_max.txt")
+    a = np.arange(int(g["n"])) % 7
+    for inclusive in (False, True):
+        assert oracle_mod.scan_op(a, "max", inclusive)[1] == int(g["total"])
+
+
+@pytest.mark.parametrize("op", sorted(NP_ACCUM))
+def test_operator_scans_against_numpy_accumulate(oracle_mod, op):
+    a = inputs.scan_values(100003, 1)
+    if op == "mul":
+        a = a | np.uint32(1)  # odd factors keep the wrapped product from collapsing to 0
+    want_inc = NP_ACCUM[op].accumulate(a, dtype=np.uint32)
+    want_ex = np.concatenate([[np.uint32(IDENTITY[op])], want_inc[:-1]]).astype(np.uint32)
+    inc, tinc = oracle_mod.scan_op(a, op, True)
+    ex, tex = oracle_mod.scan_op(a, op, False)
+    assert np.array_equal(inc, want_inc) and np.array_equal(ex, want_ex)
+    assert tinc == tex == int(want_inc[-1])
+    e, te = oracle_mod.scan_op(np.zeros(0, np.uint32), op, False)
+    assert e.size == 0 and te == IDENTITY[op]
+
+
+def test_add_operator_is_the_plain_scan(oracle_mod):
+    a = inputs.scan_values(5000, 2)
+    assert np.array_equal(oracle_mod.scan_op(a, "add", False)[0], oracle_mod.scan_exclusive(a)[0])
+    assert np.array_equal(oracle_mod.scan_op(a, "add", True)[0], oracle_mod.scan_inclusive(a)[0])
+
+
+def test_operator_scans_brute_force(oracle_mod):
+    import functools
+    import operator
+
+    fns = {"add": lambda x, y: (x + y) % M32, "mul": lambda x, y: (x * y) % M32, "and": operator.and_,
+           "or": operator.or_, "xor": operator.xor, "min": min, "max": max}
+    rng = np.random.default_rng(5)
+    for op, f in fns.items():
+        for n in range(0, 12):
+            a = [int(x) for x in rng.integers(0, M32, size=n, dtype=np.uint64)]
+            inc, _ = oracle_mod.scan_op(a, op, True)
+            ex, _ = oracle_mod.scan_op(a, op, False)
+            for j in range(n):
+                assert int(inc[j]) == functools.reduce(f, a[: j + 1], IDENTITY[op])
+                assert int(ex[j]) == functools.reduce(f, a[:j], IDENTITY[op])

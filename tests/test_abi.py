@@ -136,3 +136,13 @@ def test_radix_rejects_bad_arguments_on_host(lib):
     assert fn(fake, 1000, fake, None, need, None) == _native.EWORKSPACE
     assert fn(fake, 1000, fake, fake, need - 256, None) == _native.EWORKSPACE
     assert fn(None, 0, None, None, 0, None) == _native.OK
+
+
+def test_scan_op_rejects_bad_arguments_on_host(lib):
+    fake = 0x10000
+    need = lib.u32scan_workspace_bytes(_native.OP_SCAN, 1000)
+    for bad_op in (-1, 7, 99):
+        assert lib.scan_u32_op(bad_op, 0, fake, 1000, None, fake, need, None) == _native.EINVAL
+    assert lib.scan_u32_op(6, 1, None, 10, None, fake, need, None) == _native.EINVAL
+    assert lib.scan_u32_op(1, 0, fake, 1000, None, None, need, None) == _native.EWORKSPACE
+    assert lib.scan_u32_op(5, 0, None, 0, None, None, 0, None) == _native.OK

@@ -10,6 +10,7 @@ _API = {
     "Workspace",
     "scan_exclusive_u32",
     "scan_inclusive_u32",
+    "scan_u32_op",
     "segscan_inclusive_u32",
     "segreduce_u32",
     "compact_indices_u32",

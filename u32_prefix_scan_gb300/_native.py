@@ -17,6 +17,8 @@ EWORKSPACE = -2
 ECUDA = -3
 ETIMEOUT = -4
 
+SCAN_OPS = {"add": 0, "mul": 1, "and": 2, "or": 3, "xor": 4, "min": 5, "max": 6}
+
 OP_SCAN = 1
 OP_SEGSCAN = 2
 OP_COMPACT = 3
@@ -36,6 +38,7 @@ SIGNATURES = {
     "scan_exclusive_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
     "scan_inclusive_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
     "scan_exclusive_u32_noalloc": (_int, [_vp, _sz, _vp, _vp]),
+    "scan_u32_op": (_int, [_int, _int, _vp, _sz, _vp, _vp, _sz, _vp]),
     "segscan_inclusive_u32": (_int, [_vp, _vp, _sz, _vp, _sz, _vp, _vp, _sz, _vp]),
     "segreduce_u32": (_int, [_vp, _vp, _sz, _vp, _sz, _vp, _vp, _sz, _vp]),
     "compact_indices_u32": (_int, [_vp, _sz, _vp, _vp, _vp, _vp, _sz, _vp]),

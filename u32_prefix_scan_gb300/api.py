@@ -21,6 +21,7 @@ __all__ = [
     "Workspace",
     "scan_exclusive_u32",
     "scan_inclusive_u32",
+    "scan_u32_op",
     "segscan_inclusive_u32",
     "segreduce_u32",
     "compact_indices_u32",
@@ -119,6 +120,23 @@ def scan_inclusive_u32(data: torch.Tensor, total: torch.Tensor | None = None, *,
     """In place: data[j] <- data[0] + .. + data[j] (mod 2^32). Returns the
     one-element device tensor holding the wrapped total."""
     return _scan("scan_inclusive_u32", data, total, stream, workspace)
+
+
+def scan_u32_op(data: torch.Tensor, op: str, inclusive: bool = False, total: torch.Tensor | None = None, *,
+                stream=None, workspace: Workspace | None = None) -> torch.Tensor:
+    """In place scan under op in {add, mul, and, or, xor, min, max} (u32;
+    add and mul wrap). Returns the one-element device tensor holding the
+    fold of all elements."""
+    if op not in _native.SCAN_OPS:
+        raise ValueError(f"op must be one of {sorted(_native.SCAN_OPS)}")
+    _require_cuda(data, "data")
+    total = _scalar_out(total, data, data.dtype)
+    n = data.numel()
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_SCAN, n, data.device, sh, workspace)
+    _native.check(_native.lib().scan_u32_op(_native.SCAN_OPS[op], int(bool(inclusive)), data.data_ptr(), n,
+                                            total.data_ptr(), ws.ptr, ws.nbytes, sh), "scan_u32_op")
+    return total
 
 
 def _seg_args(data, head_flags, seg_sums, nseg):

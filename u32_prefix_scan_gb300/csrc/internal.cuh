@@ -120,130 +120,61 @@ __device__ __forceinline__ unsigned int warp_inclusive_sum(unsigned int x, int l
     return x;
 }
 
-// Wait until every lane's word (read by `load`) carries `tag`, bounded by
-// limit_ns. Lanes whose word is still not ready when time runs out get an
-// inclusive-prefix word of value 0, which ends the walk; the timeout is
-// recorded in the header. Warp-uniform control flow.
-template <typename Load>
-__device__ __forceinline__ unsigned long long wait_ready(Load load, unsigned long long tag, WsHeader *hdr,
-                                                         unsigned int tile, unsigned long long limit_ns,
-                                                         int lane) {
-    unsigned long long d = load();
-    if (__all_sync(0xffffffffu, (d & kTagMask) == tag)) return d;
-    const unsigned long long t0 = __shfl_sync(0xffffffffu, globaltimer(), 0);
-    unsigned int backoff = 32;
-    for (unsigned int iter = 0;; ++iter) {
-        __nanosleep(backoff);
-        if (backoff < 512) backoff <<= 1;
-        d = load();
-        const bool ok = (d & kTagMask) == tag;
-        if (__all_sync(0xffffffffu, ok)) return d;
-        const unsigned long long now = __shfl_sync(0xffffffffu, globaltimer(), 0);
-        // Second bound, on the iteration count, in case the timer stalls.
-        if (now - t0 > limit_ns || iter >= kMaxSpinIters) {
-            if (lane == 0) report_timeout(hdr, tile);
-            return ok ? d : (tag | kFlagP);
-        }
-    }
-}
-
-// Exclusive prefix of tile t under wrapping addition. All 32 lanes of one
-// warp call it with the same arguments. Publishes the tile's aggregate at
-// once and its inclusive prefix at the end (unless `publish` is false,
-// which only a test hook uses). Returns the sum of tiles 0 .. t-1.
-__device__ __forceinline__ unsigned int lookback_sum(unsigned long long *desc, unsigned int t, unsigned int agg,
-                                                     unsigned long long tag, WsHeader *hdr,
-                                                     unsigned long long limit_ns, bool publish, int lane) {
-    if (t == 0) {
-        if (publish && lane == 0) st_relaxed(desc, tag | kFlagP | agg);
-        return 0u;
-    }
-    if (publish && lane == 0) st_relaxed(desc + t, tag | agg);
-    unsigned int prefix = 0;
-    long long pos = (long long)t - 1;
-    while (true) {
-        const long long idx = pos - lane;
-        const unsigned long long d = wait_ready(
-            [&]() { return idx >= 0 ? ld_relaxed(desc + idx) : (tag | kFlagP); }, tag, hdr, t, limit_ns, lane);
-        const unsigned int pmask = __ballot_sync(0xffffffffu, (d & kFlagP) != 0);
-        unsigned int v = (unsigned int)d;
-        if (pmask) {
-            const int k = __ffs(pmask) - 1;  // nearest predecessor holding an inclusive prefix
-            prefix += __reduce_add_sync(0xffffffffu, lane <= k ? v : 0u);
-            break;
-        }
-        prefix += __reduce_add_sync(0xffffffffu, v);
-        pos -= 32;
-    }
-    if (publish && lane == 0) st_relaxed(desc + t, tag | kFlagP | (unsigned int)(prefix + agg));
-    return prefix;
-}
-
 // ---------------------------------------------------------------------------
-// Wide look-back: each lane reads K carry words per round trip, so one round
-// covers 32 * K predecessors (nearest first: word j of lane l is the tile
-// 32 * j + l + 1 places back). All K loads are issued before any is used.
+// The scans' operators: the integer operators of the CAIRN "Concurrency"
+// page's reduce and scan (add_wrap, mul_wrap, &, |, ^, min, max), on u32.
+// Each is associative and commutative, so a look-back may combine words in
+// any order.
 // ---------------------------------------------------------------------------
-template <int K>
-__device__ __forceinline__ unsigned int lookback_sum_wide(unsigned long long *desc, unsigned int t, unsigned int agg,
-                                                          unsigned long long tag, WsHeader *hdr,
-                                                          unsigned long long limit_ns, bool publish, int lane) {
-    if (t == 0) {
-        if (publish && lane == 0) st_relaxed(desc, tag | kFlagP | agg);
-        return 0u;
+enum MonoidCode { kAdd = 0, kMul = 1, kAnd = 2, kOr = 3, kXor = 4, kMin = 5, kMax = 6 };
+
+template <int OP>
+struct Monoid {
+    static __device__ __forceinline__ unsigned int identity() {
+        return OP == kMul ? 1u : (OP == kAnd || OP == kMin) ? 0xffffffffu : 0u;
     }
-    if (publish && lane == 0) st_relaxed(desc + t, tag | agg);
-    unsigned int prefix = 0;
-    long long pos = (long long)t - 1;
-    while (true) {
-        unsigned long long d[K];
-        bool ok = true;
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            const long long idx = pos - 32 * j - lane;
-            d[j] = idx >= 0 ? ld_relaxed(desc + idx) : (tag | kFlagP);
+    static __device__ __forceinline__ unsigned int apply(unsigned int a, unsigned int b) {
+        switch (OP) {
+        case kAdd: return a + b;
+        case kMul: return a * b;
+        case kAnd: return a & b;
+        case kOr: return a | b;
+        case kXor: return a ^ b;
+        case kMin: return a < b ? a : b;
+        default: return a > b ? a : b;
         }
-#pragma unroll
-        for (int j = 0; j < K; ++j) ok = ok && ((d[j] & kTagMask) == tag);
-        if (!__all_sync(0xffffffffu, ok)) {
-            const unsigned long long t0 = __shfl_sync(0xffffffffu, globaltimer(), 0);
-            for (unsigned int iter = 0;; ++iter) {
-                if (iter >= 8) __nanosleep(64);
-#pragma unroll
-                for (int j = 0; j < K; ++j) {
-                    const long long idx = pos - 32 * j - lane;
-                    if ((d[j] & kTagMask) != tag && idx >= 0) d[j] = ld_relaxed(desc + idx);
-                }
-                ok = true;
-#pragma unroll
-                for (int j = 0; j < K; ++j) ok = ok && ((d[j] & kTagMask) == tag);
-                if (__all_sync(0xffffffffu, ok)) break;
-                const unsigned long long now = __shfl_sync(0xffffffffu, globaltimer(), 0);
-                if (now - t0 > limit_ns || iter >= kMaxSpinIters) {
-                    if (lane == 0) report_timeout(hdr, t);
-#pragma unroll
-                    for (int j = 0; j < K; ++j)
-                        if ((d[j] & kTagMask) != tag) d[j] = tag | kFlagP;
-                    break;
-                }
-            }
-        }
-        bool found = false;
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            if (!found) {
-                const unsigned int pmask = __ballot_sync(0xffffffffu, (d[j] & kFlagP) != 0);
-                const int k = pmask ? __ffs(pmask) - 1 : 31;
-                prefix += __reduce_add_sync(0xffffffffu, lane <= k ? (unsigned int)d[j] : 0u);
-                found = pmask != 0;
-            }
-        }
-        if (found) break;
-        pos -= 32 * K;
     }
-    if (publish && lane == 0) st_relaxed(desc + t, tag | kFlagP | (unsigned int)(prefix + agg));
-    return prefix;
-}
+    // Fold of the 32 lanes' values (all lanes get it).
+    static __device__ __forceinline__ unsigned int warp_fold(unsigned int v) {
+        switch (OP) {
+        case kAdd: return __reduce_add_sync(0xffffffffu, v);
+        case kAnd: return __reduce_and_sync(0xffffffffu, v);
+        case kOr: return __reduce_or_sync(0xffffffffu, v);
+        case kXor: return __reduce_xor_sync(0xffffffffu, v);
+        case kMin: return __reduce_min_sync(0xffffffffu, v);
+        case kMax: return __reduce_max_sync(0xffffffffu, v);
+        default:
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) v = apply(v, __shfl_xor_sync(0xffffffffu, v, d));
+            return v;
+        }
+    }
+    // Inclusive scan across the lanes of a warp.
+    static __device__ __forceinline__ unsigned int warp_inclusive(unsigned int x, int lane) {
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const unsigned int y = __shfl_up_sync(0xffffffffu, x, d);
+            if (lane >= d) x = apply(y, x);
+        }
+        return x;
+    }
+    // The lane's exclusive value given its inclusive one and its own input.
+    static __device__ __forceinline__ unsigned int warp_exclusive(unsigned int inc, unsigned int own, int lane) {
+        if (OP == kAdd) return inc - own;
+        const unsigned int prev = __shfl_up_sync(0xffffffffu, inc, 1);
+        return lane == 0 ? identity() : prev;
+    }
+};
 
 // Split form of the wide look-back for software-pipelined blocks, which
 // publish a tile's aggregate as soon as it is known and walk its look-back
@@ -260,29 +191,31 @@ __device__ __forceinline__ void publish_inclusive(unsigned long long *desc, unsi
 }
 
 // First look-back window of tile t: word j of lane l is the carry word of
-// the tile 32 * j + l + 1 places back (a virtual inclusive 0 before tile 0).
+// the tile 32 * j + l + 1 places back (a virtual inclusive prefix holding
+// the operator's identity before tile 0).
 // Loading it early lets its L2 round trip overlap other work.
-template <int K>
+template <int K, int OP = kAdd>
 __device__ __forceinline__ void lookback_window(const unsigned long long *desc, long long pos,
                                                 unsigned long long tag, int lane, unsigned long long (&d)[K]) {
 #pragma unroll
     for (int j = 0; j < K; ++j) {
         const long long idx = pos - 32 * j - lane;
-        d[j] = idx >= 0 ? ld_relaxed(desc + idx) : (tag | kFlagP);
+        d[j] = idx >= 0 ? ld_relaxed(desc + idx) : (tag | kFlagP | Monoid<OP>::identity());
     }
 }
 
-// Sum of tiles 0 .. t-1 (all 32 lanes call it), starting from a first
-// window `d` already loaded by lookback_window(desc, t - 1, ...). Stops at
-// the nearest word holding an inclusive prefix; a round needs readiness only
-// up to there, so slow far-away words are never waited for.
-template <int K>
+// Fold (under OP) of tiles 0 .. t-1 (all 32 lanes call it), starting from a
+// first window `d` already loaded by lookback_window(desc, t - 1, ...).
+// Stops at the nearest word holding an inclusive prefix; a round needs
+// readiness only up to there, so slow far-away words are never waited for.
+template <int K, int OP = kAdd>
 __device__ __forceinline__ unsigned int lookback_prefix_wide(const unsigned long long *desc, unsigned int t,
                                                              unsigned long long tag, WsHeader *hdr,
                                                              unsigned long long limit_ns, int lane,
                                                              unsigned long long (&d)[K]) {
-    if (t == 0) return 0u;
-    unsigned int prefix = 0;
+    using M = Monoid<OP>;
+    if (t == 0) return M::identity();
+    unsigned int prefix = M::identity();
     long long pos = (long long)t - 1;
     while (true) {
         unsigned long long t0 = 0;
@@ -302,19 +235,19 @@ __device__ __forceinline__ unsigned int lookback_prefix_wide(const unsigned long
                     stop_ready = (__shfl_sync(0xffffffffu, ready ? 1u : 0u, stop_lane) != 0);
                 }
             }
-            if (stop_j == K) {  // whole window ready, no inclusive prefix: add it all, move back
-                unsigned int sum = 0;
+            if (stop_j == K) {  // whole window ready, no inclusive prefix: fold it all, move back
+                unsigned int sum = M::identity();
 #pragma unroll
-                for (int j = 0; j < K; ++j) sum += (unsigned int)d[j];
-                prefix += __reduce_add_sync(0xffffffffu, sum);
+                for (int j = 0; j < K; ++j) sum = M::apply(sum, (unsigned int)d[j]);
+                prefix = M::apply(prefix, M::warp_fold(sum));
                 break;
             }
             if (stop_ready) {  // an inclusive prefix with everything nearer ready: done
-                unsigned int sum = 0;
+                unsigned int sum = M::identity();
 #pragma unroll
                 for (int j = 0; j < K; ++j)
-                    if (j < stop_j || (j == stop_j && lane <= stop_lane)) sum += (unsigned int)d[j];
-                prefix += __reduce_add_sync(0xffffffffu, sum);
+                    if (j < stop_j || (j == stop_j && lane <= stop_lane)) sum = M::apply(sum, (unsigned int)d[j]);
+                prefix = M::apply(prefix, M::warp_fold(sum));
                 return prefix;
             }
             // A nearer word is not ready yet: reload the words not ready.
@@ -330,11 +263,11 @@ __device__ __forceinline__ unsigned int lookback_prefix_wide(const unsigned long
                 if (lane == 0) report_timeout(hdr, t);
 #pragma unroll
                 for (int j = 0; j < K; ++j)
-                    if ((d[j] & kTagMask) != tag) d[j] = tag | kFlagP;
+                    if ((d[j] & kTagMask) != tag) d[j] = tag | kFlagP | M::identity();
             }
         }
         pos -= 32 * K;
-        lookback_window<K>(desc, pos, tag, lane, d);
+        lookback_window<K, OP>(desc, pos, tag, lane, d);
     }
 }
 

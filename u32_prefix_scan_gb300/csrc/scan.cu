@@ -53,11 +53,41 @@
 
 namespace u32scan {
 
-template <int THREADS, int V, bool INCLUSIVE>
+// Per-round warp scan of a tile held in registers (layout above), under OP:
+// x becomes the scan relative to the warp's start; returns the warp's fold.
+template <int V, bool INCLUSIVE, int OP>
+__device__ __forceinline__ unsigned int warp_scan_rounds(uint4 (&x)[V], int lane) {
+    using M = Monoid<OP>;
+    unsigned int carry = M::identity();
+#pragma unroll
+    for (int r = 0; r < V; ++r) {
+        const unsigned int sum = M::apply(M::apply(x[r].x, x[r].y), M::apply(x[r].z, x[r].w));
+        const unsigned int inc = M::warp_inclusive(sum, lane);
+        const unsigned int ex = M::apply(carry, M::warp_exclusive(inc, sum, lane));
+        if (INCLUSIVE) {
+            x[r].x = M::apply(ex, x[r].x);
+            x[r].y = M::apply(x[r].x, x[r].y);
+            x[r].z = M::apply(x[r].y, x[r].z);
+            x[r].w = M::apply(x[r].z, x[r].w);
+        } else {
+            const unsigned int a = x[r].x, b = x[r].y, c = x[r].z;
+            x[r].x = ex;
+            x[r].y = M::apply(ex, a);
+            x[r].z = M::apply(x[r].y, b);
+            x[r].w = M::apply(x[r].z, c);
+        }
+        carry = M::apply(carry, __shfl_sync(0xffffffffu, inc, 31));
+    }
+    return carry;
+}
+
+// One tile per block, for short arrays: enough blocks to fill the GPU.
+template <int THREADS, int V, bool INCLUSIVE, int OP>
 __global__ void __launch_bounds__(THREADS, (THREADS >= 512 ? 2 : 4))
 scan_u32_kernel(uint32_t *__restrict__ data, unsigned long long n, uint32_t *total, WsHeader *hdr,
                 unsigned long long *desc, unsigned int n_tiles, unsigned int head, unsigned int skip_tile,
                 unsigned long long limit_ns) {
+    using M = Monoid<OP>;
     constexpr int WARPS = THREADS / 32;
     constexpr unsigned long long TILE = (unsigned long long)THREADS * V * 4;
     static_assert(WARPS <= 32, "one warp scans the warp totals");
@@ -98,53 +128,38 @@ scan_u32_kernel(uint32_t *__restrict__ data, unsigned long long n, uint32_t *tot
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const unsigned int li = li0 + 128 * r + c;
-                e[c] = (li >= lo && li < hi) ? tbase[li] : 0u;
+                e[c] = (li >= lo && li < hi) ? tbase[li] : M::identity();
             }
             x[r] = make_uint4(e[0], e[1], e[2], e[3]);
         }
     }
-
-    // Warp-level scan, r-major; x becomes the scan relative to the warp start.
-    unsigned int carry = 0;
-#pragma unroll
-    for (int r = 0; r < V; ++r) {
-        const unsigned int s = x[r].x + x[r].y + x[r].z + x[r].w;
-        const unsigned int inc = warp_inclusive_sum(s, lane);
-        const unsigned int ex = carry + (inc - s);
-        if (INCLUSIVE) {
-            x[r].x += ex;
-            x[r].y += x[r].x;
-            x[r].z += x[r].y;
-            x[r].w += x[r].z;
-        } else {
-            const unsigned int a = x[r].x, b = x[r].y, c = x[r].z;
-            x[r].x = ex;
-            x[r].y = ex + a;
-            x[r].z = x[r].y + b;
-            x[r].w = x[r].z + c;
-        }
-        carry += __shfl_sync(0xffffffffu, inc, 31);
-    }
-    if (lane == 0) s_warp[warp] = carry;
+    const unsigned int wtot = warp_scan_rounds<V, INCLUSIVE, OP>(x, lane);
+    if (lane == 0) s_warp[warp] = wtot;
     __syncthreads();
 
     if (warp == 0) {
-        const unsigned int wt = lane < WARPS ? s_warp[lane] : 0u;
-        const unsigned int winc = warp_inclusive_sum(wt, lane);
+        const unsigned int wt = lane < WARPS ? s_warp[lane] : M::identity();
+        const unsigned int winc = M::warp_inclusive(wt, lane);
         const unsigned int agg = __shfl_sync(0xffffffffu, winc, 31);
-        const unsigned int prefix = lookback_sum(desc, t, agg, tag, hdr, limit_ns, t != skip_tile, lane);
-        if (lane < WARPS) s_warp[lane] = prefix + (winc - wt);
-        if (t == n_tiles - 1u && lane == 0 && total != nullptr) *total = prefix + agg;
+        const unsigned int wex = M::warp_exclusive(winc, wt, lane);
+        const bool publish = t != skip_tile;
+        if (lane == 0 && publish) publish_aggregate(desc, t, agg, tag);
+        unsigned long long win[1];
+        lookback_window<1, OP>(desc, (long long)t - 1, tag, lane, win);
+        const unsigned int prefix = lookback_prefix_wide<1, OP>(desc, t, tag, hdr, limit_ns, lane, win);
+        if (lane == 0 && publish && t != 0) publish_inclusive(desc, t, M::apply(prefix, agg), tag);
+        if (lane < WARPS) s_warp[lane] = M::apply(prefix, wex);
+        if (t == n_tiles - 1u && lane == 0 && total != nullptr) *total = M::apply(prefix, agg);
     }
     __syncthreads();
 
     const unsigned int base = s_warp[warp];
 #pragma unroll
     for (int r = 0; r < V; ++r) {
-        x[r].x += base;
-        x[r].y += base;
-        x[r].z += base;
-        x[r].w += base;
+        x[r].x = M::apply(base, x[r].x);
+        x[r].y = M::apply(base, x[r].y);
+        x[r].z = M::apply(base, x[r].z);
+        x[r].w = M::apply(base, x[r].w);
     }
     if (full) {
 #pragma unroll
@@ -180,36 +195,12 @@ scan_u32_kernel(uint32_t *__restrict__ data, unsigned long long n, uint32_t *tot
 // block that publishes it (forward progress). Each block draws exactly S
 // indices past the last tile; the draw of n_tiles + S * gridDim.x - 1 is the
 // last of the launch and re-arms the header.
-template <int V, bool INCLUSIVE>
-__device__ __forceinline__ unsigned int warp_scan_rounds(uint4 (&x)[V], int lane) {
-    unsigned int carry = 0;
-#pragma unroll
-    for (int r = 0; r < V; ++r) {
-        const unsigned int sum = x[r].x + x[r].y + x[r].z + x[r].w;
-        const unsigned int inc = warp_inclusive_sum(sum, lane);
-        const unsigned int ex = carry + (inc - sum);
-        if (INCLUSIVE) {
-            x[r].x += ex;
-            x[r].y += x[r].x;
-            x[r].z += x[r].y;
-            x[r].w += x[r].z;
-        } else {
-            const unsigned int a = x[r].x, b = x[r].y, c = x[r].z;
-            x[r].x = ex;
-            x[r].y = ex + a;
-            x[r].z = x[r].y + b;
-            x[r].w = x[r].z + c;
-        }
-        carry += __shfl_sync(0xffffffffu, inc, 31);
-    }
-    return carry;
-}
-
-template <int THREADS, int V, int S, int K, bool INCLUSIVE>
+template <int THREADS, int V, int S, int K, bool INCLUSIVE, int OP>
 __global__ void __launch_bounds__(THREADS, U32SCAN_P_MINB)
 scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t *total, WsHeader *hdr,
                     unsigned long long *desc, unsigned int n_tiles, unsigned int head, unsigned int skip_tile,
                     unsigned long long limit_ns) {
+    using M = Monoid<OP>;
     constexpr int WARPS = THREADS / 32;
     constexpr unsigned int TILE = THREADS * V * 4;
     constexpr unsigned int TILE_BYTES = TILE * 4;
@@ -280,12 +271,12 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const unsigned int li = li0 + 128 * r + c;
-                    e[c] = (li >= lo && li < hi) ? tb[li] : 0u;
+                    e[c] = (li >= lo && li < hi) ? tb[li] : M::identity();
                 }
                 x[r] = make_uint4(e[0], e[1], e[2], e[3]);
             }
         }
-        const unsigned int wtot = warp_scan_rounds<V, INCLUSIVE>(x, lane);
+        const unsigned int wtot = warp_scan_rounds<V, INCLUSIVE, OP>(x, lane);
         if (lane == 0) s_wt[u & 1][warp] = wtot;
         return t;
     };
@@ -302,14 +293,14 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
                 uint4 *ob = stage_buf + S * (TILE / 4);
 #pragma unroll
                 for (int r = 0; r < V; ++r)
-                    ob[(li0 >> 2) + 32 * r] = make_uint4(x[r].x + base, x[r].y + base, x[r].z + base, x[r].w + base);
+                    ob[(li0 >> 2) + 32 * r] = make_uint4(M::apply(base, x[r].x), M::apply(base, x[r].y), M::apply(base, x[r].z), M::apply(base, x[r].w));
                 fence_proxy_async_smem();
                 __syncthreads();  // barrier C: the output buffer is complete
                 if (threadIdx.x == 0) bulk_store(tb, smem_u32(ob), TILE_BYTES);
             } else {
 #pragma unroll
                 for (int r = 0; r < V; ++r) {
-                    const uint4 y = make_uint4(x[r].x + base, x[r].y + base, x[r].z + base, x[r].w + base);
+                    const uint4 y = make_uint4(M::apply(base, x[r].x), M::apply(base, x[r].y), M::apply(base, x[r].z), M::apply(base, x[r].w));
                     __stcs(reinterpret_cast<uint4 *>(tb + li0 + 128 * r), y);
                 }
             }
@@ -323,7 +314,7 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const unsigned int li = li0 + 128 * r + c;
-                    if (li >= lo && li < hi) tb[li] = e[c] + base;
+                    if (li >= lo && li < hi) tb[li] = M::apply(base, e[c]);
                 }
             }
         }
@@ -331,9 +322,9 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
     // Warp 0: block aggregate of the tile whose warp totals are in s_wt[slot];
     // returns it, and leaves in wex this lane's exclusive warp offset.
     auto block_aggregate = [&](int slot, unsigned int &wex) -> unsigned int {
-        const unsigned int wt = lane < WARPS ? s_wt[slot][lane] : 0u;
-        const unsigned int winc = warp_inclusive_sum(wt, lane);
-        wex = winc - wt;
+        const unsigned int wt = lane < WARPS ? s_wt[slot][lane] : M::identity();
+        const unsigned int winc = M::warp_inclusive(wt, lane);
+        wex = M::warp_exclusive(winc, wt, lane);
         return __shfl_sync(0xffffffffu, winc, 31);
     };
 
@@ -381,11 +372,12 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
                 }
                 // Finish the current tile: its look-back, inclusive prefix, bases.
                 unsigned long long win[K];
-                lookback_window<K>(desc, (long long)tc - 1, tag, lane, win);
-                const unsigned int prefix = lookback_prefix_wide<K>(desc, tc, tag, hdr, limit_ns, lane, win);
-                if (lane == 0 && tc != 0 && tc != skip_tile) publish_inclusive(desc, tc, prefix + agg_c, tag);
-                if (lane < WARPS) s_base[lane] = prefix + wex_c;
-                if (tc == n_tiles - 1u && lane == 0 && total != nullptr) *total = prefix + agg_c;
+                lookback_window<K, OP>(desc, (long long)tc - 1, tag, lane, win);
+                const unsigned int prefix = lookback_prefix_wide<K, OP>(desc, tc, tag, hdr, limit_ns, lane, win);
+                if (lane == 0 && tc != 0 && tc != skip_tile)
+                    publish_inclusive(desc, tc, M::apply(prefix, agg_c), tag);
+                if (lane < WARPS) s_base[lane] = M::apply(prefix, wex_c);
+                if (tc == n_tiles - 1u && lane == 0 && total != nullptr) *total = M::apply(prefix, agg_c);
             }
             if (U32SCAN_P_BULKSTORE && threadIdx.x == 0) bulk_wait_read();  // output buffer free again
             __syncthreads();  // barrier B: bases of the current tile are visible
@@ -434,15 +426,17 @@ size_t scan_workspace_bytes(unsigned long long n) {
     return round_up(kHeaderBytes + 8 * tiles, 256);
 }
 
+static const unsigned int kOne = 1u;  // the multiply identity, copied to `total` when n == 0
+
 // Per-device launch facts for the persistent kernels, looked up once.
 struct DeviceFacts {
     int sms = 0;
-    int blocks_per_sm[2] = {0, 0};
+    int blocks_per_sm[2][7] = {};
 };
 static std::mutex g_facts_mu;
 static DeviceFacts g_facts[64];
 
-template <bool INCLUSIVE>
+template <bool INCLUSIVE, int OP>
 static int persistent_grid(int *grid_out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return U32SCAN_ECUDA;
@@ -450,9 +444,9 @@ static int persistent_grid(int *grid_out) {
     DeviceFacts &f = g_facts[dev];
     if (f.sms == 0 && cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return U32SCAN_ECUDA;
-    int &bps = f.blocks_per_sm[INCLUSIVE ? 1 : 0];
+    int &bps = f.blocks_per_sm[INCLUSIVE ? 1 : 0][OP];
     if (bps == 0) {
-        auto kern = scan_u32_persistent<kPThreads, kPV, kPStages, kPLook, INCLUSIVE>;
+        auto kern = scan_u32_persistent<kPThreads, kPV, kPStages, kPLook, INCLUSIVE, OP>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem) != cudaSuccess)
             return U32SCAN_ECUDA;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, kPThreads, kPSmem) != cudaSuccess || bps < 1)
@@ -462,14 +456,19 @@ static int persistent_grid(int *grid_out) {
     return U32SCAN_OK;
 }
 
-template <bool INCLUSIVE>
+template <bool INCLUSIVE, int OP = kAdd>
 static int scan_launch(uint32_t *data, unsigned long long n, uint32_t *total, void *ws, size_t ws_bytes,
                        cudaStream_t stream, unsigned int skip_tile, unsigned long long limit_ns) {
     if ((n > 0 && data == nullptr) || n >= (1ull << 32)) return U32SCAN_EINVAL;
     if ((reinterpret_cast<uintptr_t>(data) & 3) || (reinterpret_cast<uintptr_t>(total) & 3))
         return U32SCAN_EINVAL;
     if (n == 0) {
-        if (total && cudaMemsetAsync(total, 0, sizeof(uint32_t), stream) != cudaSuccess) return U32SCAN_ECUDA;
+        if (total) {  // the fold of nothing is the operator's identity
+            const unsigned int id = OP == kMul ? 1u : (OP == kAnd || OP == kMin) ? 0xffffffffu : 0u;
+            if (cudaMemsetAsync(total, id ? 0xff : 0, sizeof(uint32_t), stream) != cudaSuccess) return U32SCAN_ECUDA;
+            if (id == 1u && cudaMemcpyAsync(total, &kOne, sizeof(uint32_t), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+                return U32SCAN_ECUDA;
+        }
         return U32SCAN_OK;
     }
     if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < scan_workspace_bytes(n))
@@ -481,13 +480,13 @@ static int scan_launch(uint32_t *data, unsigned long long n, uint32_t *total, vo
     unsigned long long *desc = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
     if (sh.persistent) {
         int grid = 0;
-        const int rc = persistent_grid<INCLUSIVE>(&grid);
+        const int rc = persistent_grid<INCLUSIVE, OP>(&grid);
         if (rc != U32SCAN_OK) return rc;
         if ((unsigned int)grid > n_tiles) grid = (int)n_tiles;
-        scan_u32_persistent<kPThreads, kPV, kPStages, kPLook, INCLUSIVE><<<grid, kPThreads, kPSmem, stream>>>(
+        scan_u32_persistent<kPThreads, kPV, kPStages, kPLook, INCLUSIVE, OP><<<grid, kPThreads, kPSmem, stream>>>(
             data, n, total, hdr, desc, n_tiles, head, skip_tile, limit_ns);
     } else {
-        scan_u32_kernel<256, 2, INCLUSIVE><<<n_tiles, 256, 0, stream>>>(data, n, total, hdr, desc, n_tiles, head,
+        scan_u32_kernel<256, 2, INCLUSIVE, OP><<<n_tiles, 256, 0, stream>>>(data, n, total, hdr, desc, n_tiles, head,
                                                                         skip_tile, limit_ns);
     }
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
@@ -511,6 +510,29 @@ extern "C" int scan_exclusive_u32(uint32_t *data, size_t n, uint32_t *total, voi
 extern "C" int scan_inclusive_u32(uint32_t *data, size_t n, uint32_t *total, void *ws, size_t ws_bytes,
                                   u32scan_stream_t stream) {
     return scan_launch<true>(data, n, total, ws, ws_bytes, (cudaStream_t)stream, 0xffffffffu, kDefaultLimitNs);
+}
+
+extern "C" int scan_u32_op(int op, int inclusive, uint32_t *data, size_t n, uint32_t *total, void *ws,
+                           size_t ws_bytes, u32scan_stream_t stream) {
+    const cudaStream_t s = (cudaStream_t)stream;
+    const unsigned int k = 0xffffffffu;
+    const unsigned long long lim = kDefaultLimitNs;
+#define U32SCAN_OP_CASE(CODE)                                                                 \
+    case CODE:                                                                               \
+        return inclusive ? scan_launch<true, CODE>(data, n, total, ws, ws_bytes, s, k, lim)  \
+                         : scan_launch<false, CODE>(data, n, total, ws, ws_bytes, s, k, lim);
+    switch (op) {
+        U32SCAN_OP_CASE(kAdd)
+        U32SCAN_OP_CASE(kMul)
+        U32SCAN_OP_CASE(kAnd)
+        U32SCAN_OP_CASE(kOr)
+        U32SCAN_OP_CASE(kXor)
+        U32SCAN_OP_CASE(kMin)
+        U32SCAN_OP_CASE(kMax)
+    default:
+        return U32SCAN_EINVAL;
+    }
+#undef U32SCAN_OP_CASE
 }
 
 extern "C" int u32scan_test_scan_skip_publish(uint32_t *data, size_t n, uint32_t *total, void *ws, size_t ws_bytes,

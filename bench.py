@@ -20,7 +20,8 @@ Other ops time the other primitives on their own workloads:
   compact         compact_indices_u32, n = 2^27 int32 flags, keep
                   probability --p (0.1 or 0.9), seed 4
   radix           radix_sort_perm_u32, n = 2^25 keys seed 5, uniform u32
-                  or (--ties) in [0, 256)
+                  or (--ties) in [0, 256); --sort pairs|keys times
+                  radix_sort_u32 writing sorted keys (+ perm unless keys)
 
 Rank 0 prints one JSON line.
 
@@ -343,17 +344,23 @@ class RadixOp(Op):
     kernel_sources = ["u32_prefix_scan_gb300/csrc/radix.cu", "u32_prefix_scan_gb300/csrc/scan.cu",
                       "u32_prefix_scan_gb300/csrc/internal.cuh"]
 
+    OUTPUTS = {"perm": "int32 perm", "pairs": "sorted keys + int32 perm", "keys": "sorted keys"}
+
     def __init__(self, args):
         super().__init__(args)
         self.ties = args.ties
-        self.name = "radix_sort_perm_u32" + ("_ties" if self.ties else "")
+        self.mode = args.sort
+        entry = "radix_sort_perm_u32" if self.mode == "perm" else "radix_sort_u32"
+        self.name = entry + ("" if self.mode == "perm" else "_" + self.mode) + ("_ties" if self.ties else "")
         keys = "keys in [0,256)" if self.ties else "uniform u32 keys"
-        self.metric = f"stable LSD radix-sort permutation Gelem/s at n=2^25 ({keys}), 1 GB300"
+        what = {"perm": "radix-sort permutation", "pairs": "radix sort (keys + permutation)",
+                "keys": "radix sort (keys only)"}[self.mode]
+        self.metric = f"stable LSD {what} Gelem/s at n=2^25 ({keys}), 1 GB300"
         self.kernel = "radix_downsweep_kernel + radix_upsweep_kernel (per active 8-bit digit)"
 
     def workload(self):
         keys = "u32(5,0,i) >> 24, in [0,256)" if self.ties else "u32(5,0,i), uniform"
-        return f"stable radix-sort permutation of n=2^{self.n.bit_length() - 1} u32 keys {keys} -> int32 perm"
+        return f"stable radix sort of n=2^{self.n.bit_length() - 1} u32 keys {keys} -> {self.OUTPUTS[self.mode]}"
 
     def passes(self):
         return 1 if self.ties else 4  # digits not constant over the keys
@@ -361,11 +368,19 @@ class RadixOp(Op):
     def algorithmic_bytes(self):
         # this design's bytes: a 4-byte histogram read, then per active digit
         # an upsweep read of the keys (4) and a downsweep that reads keys (4)
-        # and indices (4, not on the first pass) and writes keys (4, not on
-        # the last pass) and indices (4)
+        # and, when indices are produced, reads them (4, not on the first
+        # pass) and writes them (4); keys are written (4) on every pass but
+        # the last of the permutation-only sort
         m, n = self.passes(), self.n
-        per = [4 + 4 + (4 if j else 0) + (4 if j < m - 1 else 0) + 4 for j in range(m)]
-        return n * (4 + 4 * m + sum(per) - 4 * m)
+        idx = self.mode != "keys"
+        total = 4
+        for j in range(m):
+            total += 8
+            if idx:
+                total += (4 if j else 0) + 4
+            if j < m - 1 or self.mode != "perm":
+                total += 4
+        return n * total
 
     def host_inputs(self):
         from u32_prefix_scan_gb300 import inputs
@@ -381,26 +396,39 @@ class RadixOp(Op):
 
         self.u = u
         self.keys = torch.from_numpy(host["keys"].view(np.int32)).to(dev)
-        self.perm = torch.empty(self.n, dtype=torch.int32, device=dev)
+        self.perm = None if self.mode == "keys" else torch.empty(self.n, dtype=torch.int32, device=dev)
+        self.keys_out = None if self.mode == "perm" else torch.empty(self.n, dtype=torch.int32, device=dev)
         self.ws = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_RADIX, self.n), dev)
         self.pinned_in = {"keys": torch.from_numpy(host["keys"].view(np.int32)).pin_memory()}
-        self.pinned_out = {"perm": torch.empty(self.n, dtype=torch.int32).pin_memory()}
+        self.pinned_out = {}
+        if self.perm is not None:
+            self.pinned_out["perm"] = torch.empty(self.n, dtype=torch.int32).pin_memory()
+        if self.keys_out is not None:
+            self.pinned_out["keys_out"] = torch.empty(self.n, dtype=torch.int32).pin_memory()
 
     def step(self):
-        self.u.radix_sort_perm_u32(self.keys, self.perm, workspace=self.ws)
+        if self.mode == "perm":
+            self.u.radix_sort_perm_u32(self.keys, self.perm, workspace=self.ws)
+        else:
+            self.u.radix_sort_u32(self.keys, self.keys_out, self.perm, workspace=self.ws)
 
     def e2e_step(self):
         self.keys.copy_(self.pinned_in["keys"], non_blocking=True)
         self.step()
-        self.pinned_out["perm"].copy_(self.perm, non_blocking=True)
-        return 4 * self.n, 4 * self.n
+        for name, t in self.pinned_out.items():
+            t.copy_(getattr(self, name), non_blocking=True)
+        return 4 * self.n, 4 * self.n * len(self.pinned_out)
 
     def check_e2e(self, host):
         import numpy as np
 
-        p = self.pinned_out["perm"].numpy()
-        s = host["keys"][p]
-        return bool(np.all(s[1:] >= s[:-1]))
+        ok = True
+        if "perm" in self.pinned_out:
+            s = host["keys"][self.pinned_out["perm"].numpy()]
+            ok &= bool(np.all(s[1:] >= s[:-1]))
+        if "keys_out" in self.pinned_out:
+            ok &= bool(np.array_equal(self.pinned_out["keys_out"].numpy().view(np.uint32), np.sort(host["keys"])))
+        return ok
 
     def oracle_step(self, lib, arrays):
         import numpy as np
@@ -410,6 +438,8 @@ class RadixOp(Op):
             arrays["perm"] = np.empty(k.size, dtype=np.int32)
         lib.oracle_sort_perm_u32(k.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)), k.size,
                                  arrays["perm"].ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+        if self.mode != "perm":
+            arrays["keys_out"] = k[arrays["perm"]]
 
 
 OPS = ["scan_exclusive", "scan_inclusive", "scan_op", "segscan", "segscan_sums", "segreduce", "compact", "radix"]
@@ -439,6 +469,8 @@ def parse_args(argv=None):
     p.add_argument("--heads", choices=["geometric", "regular4"], default="geometric")
     p.add_argument("--p", type=float, choices=[0.1, 0.9], default=0.1, help="compaction keep probability")
     p.add_argument("--ties", action="store_true", help="radix: keys in [0, 256) instead of uniform u32")
+    p.add_argument("--sort", choices=["perm", "pairs", "keys"], default="perm",
+                   help="radix outputs: the permutation, sorted keys and the permutation, or sorted keys only")
     p.add_argument("--monoid", choices=["add", "mul", "and", "or", "xor", "min", "max"], default="max",
                    help="scan_op: the operator")
     p.add_argument("--inclusive", action="store_true", help="scan_op: inclusive instead of exclusive")

@@ -212,6 +212,23 @@ int radix_sort_perm_u32(const uint32_t *keys, size_t n, int32_t *perm,
                         void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /*
+ * Stable LSD radix sort of U32 keys, with the sorted keys as output: the
+ * permutation passes of radix_sort_perm_u32, whose last pass also writes
+ * the keys. Same source passages.
+ *   keys      device, uint32_t[n], read only.
+ *   keys_out  device, uint32_t[n]: the keys in non-decreasing order; must not
+ *             overlap keys.
+ *   perm      device, int32_t[n] or NULL: the stable permutation as in
+ *             radix_sort_perm_u32 (keys_out[i] = keys[perm[i]]). NULL sorts
+ *             the keys alone and moves no indices.
+ *   ws, ws_bytes  u32scan_workspace_bytes(U32SCAN_OP_RADIX, n) bytes.
+ * Errors: EINVAL (null keys or keys_out with n > 0, misaligned pointers,
+ * overlapping keys and keys_out, n >= 2^31), EWORKSPACE, ECUDA.
+ */
+int radix_sort_u32(const uint32_t *keys, size_t n, uint32_t *keys_out, int32_t *perm,
+                   void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
  * Exclusive scan that allocates nothing and needs no workspace argument.
  * The pages have no counterpart: this entry point exists for callers that
  * cannot allocate device memory (for instance code inside an allocator's

@@ -146,3 +146,15 @@ def test_scan_op_rejects_bad_arguments_on_host(lib):
     assert lib.scan_u32_op(6, 1, None, 10, None, fake, need, None) == _native.EINVAL
     assert lib.scan_u32_op(1, 0, fake, 1000, None, None, need, None) == _native.EWORKSPACE
     assert lib.scan_u32_op(5, 0, None, 0, None, None, 0, None) == _native.OK
+
+
+def test_radix_sort_rejects_bad_arguments_on_host(lib):
+    fn = lib.radix_sort_u32
+    fake = 0x100000
+    need = lib.u32scan_workspace_bytes(_native.OP_RADIX, 1000)
+    assert fn(fake, 10, None, fake, fake, need, None) == _native.EINVAL               # no keys_out
+    assert fn(fake, 1000, fake + 400, None, fake, need, None) == _native.EINVAL       # overlapping output
+    assert fn(fake, 1000, fake - 400, None, fake, need, None) == _native.EINVAL       # overlapping output
+    assert fn(fake, 1000, fake + 4000, fake + 8001, fake, need, None) == _native.EINVAL  # misaligned perm
+    assert fn(fake, 1000, fake + 4000, None, None, need, None) == _native.EWORKSPACE
+    assert lib.radix_sort_perm_u32(fake, 10, None, fake, need, None) == _native.EINVAL

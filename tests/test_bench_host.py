@@ -39,6 +39,9 @@ def test_algorithmic_bytes_per_op():
     assert bench.make_op(bench.parse_args(["--op", "compact"])).algorithmic_bytes() == 12 * n27 + 4
     assert bench.make_op(bench.parse_args(["--op", "radix"])).algorithmic_bytes() == 76 * n25
     assert bench.make_op(bench.parse_args(["--op", "radix", "--ties"])).algorithmic_bytes() == 16 * n25
+    assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "pairs"])).algorithmic_bytes() == 80 * n25
+    assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "keys"])).algorithmic_bytes() == 52 * n25
+    assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "keys", "--ties"])).algorithmic_bytes() == 16 * n25
     assert bench.make_op(bench.parse_args(["--log2n", "20"])).n == 1 << 20
 
 

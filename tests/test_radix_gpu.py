@@ -98,3 +98,35 @@ def test_repeated_calls_share_one_workspace(u):
 def test_workload_2_25_full_parity(u, kind):
     # The radix benchmark: n = 2^25 keys u32(5, 0, i), and the [0, 256) variant.
     check_perm(u, keys_for(kind, 1 << 25))
+
+
+@pytest.mark.parametrize("kind", ["uniform", "ties256", "equal", "top_digit", "two_values", "reversed"])
+@pytest.mark.parametrize("n", [1, 8193, 100003, (1 << 20) + 5])
+def test_sort_keys_and_permutation(u, kind, n):
+    keys = keys_for(kind, n)
+    d = torch.from_numpy(keys.view(np.int32).copy()).cuda()
+    out, perm = u.radix_sort_u32(d)
+    u.check()
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), np.sort(keys))
+    assert np.array_equal(perm.cpu().numpy(), oracle.sort_perm(keys))
+    assert np.array_equal(d.cpu().numpy().view(np.uint32), keys)
+
+
+@pytest.mark.parametrize("kind", ["uniform", "ties256", "equal"])
+def test_sort_keys_only(u, kind):
+    keys = keys_for(kind, 300007)
+    d = torch.from_numpy(keys.view(np.int32).copy()).cuda()
+    out, perm = u.radix_sort_u32(d, want_perm=False)
+    u.check()
+    assert perm is None
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), np.sort(keys))
+
+
+@pytest.mark.parametrize("ties", [False, True])
+def test_sort_keys_full_size(u, ties):
+    keys = inputs.radix_keys(1 << 25, 5, ties=ties)
+    d = torch.from_numpy(keys.view(np.int32).copy()).cuda()
+    out, perm = u.radix_sort_u32(d)
+    u.check()
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), np.sort(keys))
+    assert np.array_equal(perm.cpu().numpy(), oracle.sort_perm(keys))

@@ -15,6 +15,7 @@ _API = {
     "segreduce_u32",
     "compact_indices_u32",
     "radix_sort_perm_u32",
+    "radix_sort_u32",
     "check",
 }
 

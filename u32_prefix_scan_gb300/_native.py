@@ -43,6 +43,7 @@ SIGNATURES = {
     "segreduce_u32": (_int, [_vp, _vp, _sz, _vp, _sz, _vp, _vp, _sz, _vp]),
     "compact_indices_u32": (_int, [_vp, _sz, _vp, _vp, _vp, _vp, _sz, _vp]),
     "radix_sort_perm_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
+    "radix_sort_u32": (_int, [_vp, _sz, _vp, _vp, _vp, _sz, _vp]),
     "u32scan_test_scan_skip_publish": (_int, [_vp, _sz, _vp, _vp, _sz, ctypes.c_uint, ctypes.c_ulonglong, _vp]),
 }
 

@@ -26,6 +26,7 @@ __all__ = [
     "segreduce_u32",
     "compact_indices_u32",
     "radix_sort_perm_u32",
+    "radix_sort_u32",
     "check",
 ]
 
@@ -231,6 +232,32 @@ def radix_sort_perm_u32(keys: torch.Tensor, perm: torch.Tensor | None = None, *,
     _native.check(_native.lib().radix_sort_perm_u32(keys.data_ptr(), n, perm.data_ptr(), ws.ptr, ws.nbytes, sh),
                   "radix_sort_perm_u32")
     return perm
+
+
+def radix_sort_u32(keys: torch.Tensor, keys_out: torch.Tensor | None = None, perm: torch.Tensor | None = None,
+                   *, want_perm: bool = True, stream=None, workspace: Workspace | None = None):
+    """Stable radix sort of u32 keys (unsigned order). Returns (keys_out,
+    perm): the sorted keys and, unless want_perm is False and no perm was
+    given, the stable permutation (keys_out = keys[perm])."""
+    _require_cuda(keys, "keys")
+    n = keys.numel()
+    if keys_out is None:
+        keys_out = torch.empty_like(keys)
+    _require_cuda(keys_out, "keys_out")
+    if keys_out.numel() != n:
+        raise ValueError("keys_out must have n elements")
+    if perm is None and want_perm:
+        perm = torch.empty(n, dtype=torch.int32, device=keys.device)
+    if perm is not None:
+        _require_cuda(perm, "perm", (torch.int32,))
+        if perm.numel() != n:
+            raise ValueError("perm must have n elements")
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_RADIX, n, keys.device, sh, workspace)
+    _native.check(_native.lib().radix_sort_u32(keys.data_ptr(), n, keys_out.data_ptr(),
+                                               perm.data_ptr() if perm is not None else None, ws.ptr, ws.nbytes, sh),
+                  "radix_sort_u32")
+    return keys_out, perm
 
 
 def check(stream=None, workspace: Workspace | None = None, device=None) -> int:

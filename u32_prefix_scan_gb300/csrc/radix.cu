@@ -24,7 +24,8 @@
 // for every key; their passes are skipped (exact: such a pass moves
 // nothing). Which passes run, and which buffers they read and write, is
 // decided on the device, so the call stays asynchronous. The last pass
-// writes only indices, into `perm`.
+// writes the indices into `perm` and, for radix_sort_u32, the sorted keys
+// into `keys_out`; a keys-only sort moves no indices at all.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -145,22 +146,38 @@ __global__ void radix_plan_kernel(const unsigned int *__restrict__ hist, unsigne
     }
 }
 
-// Buffers of one pass (see the header comment of this file).
+// Buffers of one pass. Pass j of m active ones reads what pass j - 1 wrote
+// (pass 0 reads the caller's keys and the identity permutation) and the
+// last pass writes the results: indices into `perm` and, when sorted keys
+// are wanted, keys into `keys_out`. Earlier passes alternate between a
+// scratch buffer and the result buffer itself, counted back from the last
+// pass so that it never reads the buffer it writes. Without keys_out the
+// second key buffer is workspace (k2) and the last pass writes no keys;
+// without perm no indices are moved at all.
 struct PassBuffers {
     const uint32_t *in_keys;
-    const int32_t *in_idx;  // null: the identity (first pass)
-    uint32_t *out_keys;     // null: last pass, keys are not needed any more
-    int32_t *out_idx;
+    const int32_t *in_idx;  // null: the identity (first pass) or no indices
+    uint32_t *out_keys;     // null: last pass of a permutation-only call
+    int32_t *out_idx;       // null: keys-only sort
 };
 
 __device__ __forceinline__ PassBuffers pass_buffers(const RadixPlan &pl, const uint32_t *keys, uint32_t *k1,
-                                                    uint32_t *k2, int32_t *i1, int32_t *perm) {
+                                                    uint32_t *k2, int32_t *i1, int32_t *perm,
+                                                    uint32_t *keys_out) {
     PassBuffers b;
     const int j = pl.j, m = pl.m;
-    auto idx_of = [&](int q) -> int32_t * { return q == m - 1 ? perm : (((m - 1 - q) & 1) ? i1 : perm); };
-    b.in_keys = j == 0 ? keys : ((j - 1) & 1 ? k2 : k1);
+    uint32_t *klast = keys_out ? keys_out : k2;
+    auto keys_of = [&](int q) -> uint32_t * {
+        if (q == m - 1) return keys_out;  // null for a permutation-only call
+        return ((m - 1 - q) & 1) ? k1 : klast;
+    };
+    auto idx_of = [&](int q) -> int32_t * {
+        if (perm == nullptr) return nullptr;
+        return q == m - 1 ? perm : (((m - 1 - q) & 1) ? i1 : perm);
+    };
+    b.in_keys = j == 0 ? keys : keys_of(j - 1);
     b.in_idx = j == 0 ? nullptr : idx_of(j - 1);
-    b.out_keys = j == m - 1 ? nullptr : (j & 1 ? k2 : k1);
+    b.out_keys = keys_of(j);
     b.out_idx = idx_of(j);
     return b;
 }
@@ -215,13 +232,13 @@ __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restri
 // into its own row of shared-memory counters with atomics.
 __global__ void __launch_bounds__(kRThreads, 2)
 radix_upsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
-                     int32_t *i1, int32_t *perm, unsigned long long n, unsigned int n_tiles,
+                     int32_t *i1, int32_t *perm, uint32_t *keys_out, unsigned long long n, unsigned int n_tiles,
                      unsigned int *__restrict__ table) {
     const RadixPlan pl = plan[p];
     if (!pl.active) return;
     __shared__ unsigned int s_cnt[kRWarps][256];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm);
+    const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm, keys_out);
     for (int i = lane; i < 256; i += 32) s_cnt[warp][i] = 0;
     __syncwarp();
     const unsigned long long base = (unsigned long long)blockIdx.x * kRTile + (unsigned long long)warp * (32 * kRKeys);
@@ -249,7 +266,7 @@ radix_upsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *
 // to its slots with consecutive threads on consecutive slots.
 __global__ void __launch_bounds__(kRThreads, 2)
 radix_downsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
-                       int32_t *i1, int32_t *perm, unsigned long long n, unsigned int n_tiles,
+                       int32_t *i1, int32_t *perm, uint32_t *keys_out, unsigned long long n, unsigned int n_tiles,
                        const unsigned int *__restrict__ slots) {
     const RadixPlan pl = plan[p];
     if (!pl.active) return;
@@ -262,7 +279,7 @@ radix_downsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t
     __shared__ unsigned int s_part[kRThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned int t = blockIdx.x;
-    const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm);
+    const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm, keys_out);
     uint32_t k[kRKeys];
     unsigned int wrank[kRKeys];
     const unsigned int valid_bits = radix_rank_tile(b.in_keys, n, t, 8 * p, k, wrank, s_cnt, lane, warp);
@@ -298,7 +315,7 @@ radix_downsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t
             const unsigned int v = (k[r] >> (8 * p)) & 255u;
             const unsigned int pos = s_tileoff[v] + s_cnt[warp][v] + wrank[r];
             s_keys[pos] = k[r];
-            s_idx[pos] = b.in_idx ? b.in_idx[e] : (int32_t)e;
+            if (b.out_idx) s_idx[pos] = b.in_idx ? b.in_idx[e] : (int32_t)e;
         }
     }
     __syncthreads();
@@ -310,27 +327,36 @@ radix_downsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t
         const unsigned int v = (key >> shift) & 255u;
         const unsigned int slot = s_glob[v] + (i - s_tileoff[v]);
         if (b.out_keys) b.out_keys[slot] = key;
-        b.out_idx[slot] = s_idx[i];
+        if (b.out_idx) b.out_idx[slot] = s_idx[i];
     }
 }
 
 constexpr size_t kRDownSmem = (size_t)(kRWarps * 256 + 512 + 2 * kRTile) * 4;
 
 // All digits constant (every key equal): the permutation is the identity.
-__global__ void radix_identity_kernel(const RadixPlan *__restrict__ plan, int32_t *perm, unsigned long long n) {
+__global__ void radix_identity_kernel(const RadixPlan *__restrict__ plan, const uint32_t *keys, int32_t *perm,
+                                      uint32_t *keys_out, unsigned long long n) {
     if (plan[0].m != 0) return;
     for (unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (unsigned long long)gridDim.x * blockDim.x)
-        perm[i] = (int32_t)i;
+         i += (unsigned long long)gridDim.x * blockDim.x) {
+        if (perm) perm[i] = (int32_t)i;
+        if (keys_out) keys_out[i] = keys[i];
+    }
 }
 
 size_t radix_workspace_bytes(unsigned long long n) { return RadixLayout(n).total; }
 
-static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *perm, void *ws, size_t ws_bytes,
-                        cudaStream_t stream) {
+static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *perm, uint32_t *keys_out, void *ws,
+                        size_t ws_bytes, cudaStream_t stream) {
     if (n >= (1ull << 31)) return U32SCAN_EINVAL;
-    if (n > 0 && (keys == nullptr || perm == nullptr)) return U32SCAN_EINVAL;
-    if ((reinterpret_cast<uintptr_t>(keys) & 3) || (reinterpret_cast<uintptr_t>(perm) & 3)) return U32SCAN_EINVAL;
+    if (n > 0 && (keys == nullptr || (perm == nullptr && keys_out == nullptr))) return U32SCAN_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(keys) & 3) || (reinterpret_cast<uintptr_t>(perm) & 3) ||
+        (reinterpret_cast<uintptr_t>(keys_out) & 3))
+        return U32SCAN_EINVAL;
+    if (keys_out != nullptr && n > 0 &&
+        reinterpret_cast<const char *>(keys_out) < reinterpret_cast<const char *>(keys + n) &&
+        reinterpret_cast<const char *>(keys) < reinterpret_cast<const char *>(keys_out + n))
+        return U32SCAN_EINVAL;  // the sorted keys may not overlap the input
     if (n == 0) return U32SCAN_OK;
     const RadixLayout L(n);
     if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < L.total) return U32SCAN_EWORKSPACE;
@@ -359,14 +385,14 @@ static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *per
     radix_plan_kernel<<<1, 32, 0, stream>>>(hist, n, plan);
     const unsigned long long cells = 256ull * L.n_tiles;
     for (int p = 0; p < 4; ++p) {
-        radix_upsweep_kernel<<<L.n_tiles, kRThreads, 0, stream>>>(plan, p, keys, k1, k2, i1, perm, n, L.n_tiles,
-                                                                   table);
+        radix_upsweep_kernel<<<L.n_tiles, kRThreads, 0, stream>>>(plan, p, keys, k1, k2, i1, perm, keys_out, n,
+                                                                   L.n_tiles, table);
         const int rc = scan_exclusive_launch(table, cells, w + L.scan_ws, scan_workspace_bytes(cells), stream);
         if (rc != U32SCAN_OK) return rc;
-        radix_downsweep_kernel<<<L.n_tiles, kRThreads, kRDownSmem, stream>>>(plan, p, keys, k1, k2, i1, perm, n,
-                                                                              L.n_tiles, table);
+        radix_downsweep_kernel<<<L.n_tiles, kRThreads, kRDownSmem, stream>>>(plan, p, keys, k1, k2, i1, perm,
+                                                                              keys_out, n, L.n_tiles, table);
     }
-    radix_identity_kernel<<<1024, 256, 0, stream>>>(plan, perm, n);
+    radix_identity_kernel<<<1024, 256, 0, stream>>>(plan, keys, perm, keys_out, n);
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }
 
@@ -376,5 +402,12 @@ using namespace u32scan;
 
 extern "C" int radix_sort_perm_u32(const uint32_t *keys, size_t n, int32_t *perm, void *ws, size_t ws_bytes,
                                    u32scan_stream_t stream) {
-    return radix_launch(keys, n, perm, ws, ws_bytes, (cudaStream_t)stream);
+    if (n > 0 && perm == nullptr) return U32SCAN_EINVAL;
+    return radix_launch(keys, n, perm, nullptr, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" int radix_sort_u32(const uint32_t *keys, size_t n, uint32_t *keys_out, int32_t *perm, void *ws,
+                              size_t ws_bytes, u32scan_stream_t stream) {
+    if (n > 0 && keys_out == nullptr) return U32SCAN_EINVAL;
+    return radix_launch(keys, n, perm, keys_out, ws, ws_bytes, (cudaStream_t)stream);
 }

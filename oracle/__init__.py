@@ -66,6 +66,10 @@ def _configure(lib):
     lib.oracle_radix_perm_bits.restype = None
     lib.oracle_sort_perm_u32.argtypes = [_u32p, _u64, _i32p]
     lib.oracle_sort_perm_u32.restype = ctypes.c_int
+    lib.oracle_runs_layout_u32.argtypes = [_u32p, _u64, _u32p]
+    lib.oracle_runs_layout_u32.restype = ctypes.c_uint32
+    lib.oracle_runs_fill_owner.argtypes = [_u32p, _u32p, _u64, _i32p, _u64]
+    lib.oracle_runs_fill_owner.restype = None
     return lib
 
 
@@ -189,3 +193,25 @@ def sort_perm(keys):
     if _load().oracle_sort_perm_u32(_p(k, _u32p), n, _p(perm, _i32p)) != 0:
         raise MemoryError("oracle_sort_perm_u32 could not allocate")
     return perm
+
+
+def runs_layout(counts):
+    """(ends, entries): ends the inclusive scan of the counts (mod 2^32),
+    entries = max(total, 1)."""
+    c = _u32(counts)
+    ends = np.empty(c.size, dtype=np.uint32)
+    entries = _load().oracle_runs_layout_u32(_p(c, _u32p), c.size, _p(ends, _u32p))
+    return ends, int(entries)
+
+
+def runs_owner(counts):
+    """(ends, entries, owner row): the runs layout, then its `entries` slots
+    filled by the scatter over the owners with each owner's index, so that
+    slot e holds owner(e, ends); -1 where no run reaches."""
+    c = _u32(counts)
+    if c.size >= (1 << 31):
+        raise ValueError("n must be below 2^31")
+    ends, entries = runs_layout(c)
+    slots = np.empty(entries, dtype=np.int32)
+    _load().oracle_runs_fill_owner(_p(c, _u32p), _p(ends, _u32p), c.size, _p(slots, _i32p), entries)
+    return ends, entries, slots

@@ -21,13 +21,16 @@
  *   [entelechy]  "parallel" package reference (entelechy docs): kernels
  *                compact_blank / compact_offsets / compact_total /
  *                compact_gather, sort_identity / sort_blank / sort_zeros /
- *                sort_place / sort_next_bit, graphs compact and sort.
+ *                sort_place / sort_next_bit, runs_ends / runs_entries /
+ *                runs_slots, graphs compact, sort and runs, function owner.
  *
  * Readings taken where the pages are silent (all restated in the design
  * notes): any n is scanned in full (not only 2^floor(log2 n) entries);
  * n = 0 gives total 0; index 0 always opens a segment; a head flag or a
  * compaction flag is "set" when non-zero; compaction fills unused index
- * slots with -1; sort keys are unsigned 32-bit and all 32 bits are sorted.
+ * slots with -1; sort keys are unsigned 32-bit and all 32 bits are sorted;
+ * run counts are unsigned 32-bit; owner(e, ends) is the owner whose run
+ * holds entry e, -1 for the one slot of a layout with no entries.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -338,4 +341,56 @@ int oracle_sort_perm_u32(const uint32_t *keys, uint64_t n, int32_t *perm)
         perm[i] = p[i].idx;
     free(p);
     return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Runs.  [entelechy] graph "runs": from each owner's count of entries,
+ * where every owner's run ends, how many entries there are, and the row of
+ * slots they are laid in. Its three kernels, in their order:
+ *   runs_ends    -- an inclusive prefix sum of the counts, so owner i's run
+ *                   covers ends[i] - counts[i] up to, not including, ends[i];
+ *   runs_entries -- how many entries the runs hold, at least one so that
+ *                   the row is never empty: max(total, 1);
+ *   runs_slots   -- the row of `entries` slots, every one -1.
+ * Counts and ends are uint32 (ends wrap like the scan; a meaningful layout
+ * keeps the total below 2^31). Returns entries; ends may be counts.
+ * ---------------------------------------------------------------------- */
+
+uint32_t oracle_runs_layout_u32(const uint32_t *counts, uint64_t n, uint32_t *ends)
+{
+    /* runs_ends */
+    uint32_t run = 0;
+    for (uint64_t i = 0; i < n; ++i) {
+        run += counts[i];
+        ends[i] = run;
+    }
+    /* runs_entries */
+    return run > 0 ? run : 1u;
+}
+
+/*
+ * The graph's description fills the slots (after runs_slots made them -1)
+ * with a scatter over the owners that walks each owner's count, putting its
+ * entry of rank r at ends[i] - counts[i] + r, with max. Here the value put
+ * is the owner's index i, so slot e ends up holding the owner of entry e:
+ * owner(e, ends). A slot no run reaches keeps its -1. `slots` holds
+ * `entries` values; a write outside them is dropped.
+ */
+void oracle_runs_fill_owner(const uint32_t *counts, const uint32_t *ends, uint64_t n,
+                            int32_t *slots, uint64_t entries)
+{
+    /* runs_slots */
+    for (uint64_t e = 0; e < entries; ++e)
+        slots[e] = -1;
+    /* the scatter over the owners */
+    for (uint64_t i = 0; i < n; ++i) {
+        uint64_t start = (uint64_t)ends[i] - (uint64_t)counts[i];
+        for (uint64_t r = 0; r < counts[i]; ++r) {
+            uint64_t e = start + r;
+            if (e >= entries)
+                break; /* dropped, and so is the rest of this run */
+            if ((int32_t)i > slots[e])
+                slots[e] = (int32_t)i;
+        }
+    }
 }

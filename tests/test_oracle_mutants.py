@@ -41,6 +41,11 @@ MUTANTS = [
      ["opscan_min"]),
     ("sort_ties_descending", "return (a->idx > b->idx) - (a->idx < b->idx);",
      "return (a->idx < b->idx) - (a->idx > b->idx);", ["sort_numpy", "radix_brute"]),
+    ("runs_ends_exclusive", "run += counts[i];\n        ends[i] = run;", "ends[i] = run;\n        run += counts[i];",
+     ["runs_closed", "runs_numpy"]),
+    ("runs_entries_may_be_zero", "return run > 0 ? run : 1u;", "return run;", ["runs_degenerate"]),
+    ("runs_fill_starts_one_late", "(uint64_t)ends[i] - (uint64_t)counts[i];",
+     "(uint64_t)ends[i] - (uint64_t)counts[i] + 1;", ["runs_closed", "runs_brute"]),
 ]
 
 PINS = {
@@ -58,6 +63,10 @@ PINS = {
     "radix_brute": lambda o: pins.test_radix_brute_force_tiny(o),
     "sort_numpy": lambda o: pins.test_sort_perm_against_numpy_stable_argsort(o, True),
     "opscan_min": lambda o: pins.test_operator_scans_against_numpy_accumulate(o, "min"),
+    "runs_closed": lambda o: pins.test_runs_equal_counts_closed_form(o, 3),
+    "runs_numpy": lambda o: pins.test_runs_against_numpy(o, True),
+    "runs_degenerate": lambda o: pins.test_runs_degenerate(o),
+    "runs_brute": lambda o: pins.test_runs_brute_force(o),
 }
 
 

@@ -347,3 +347,48 @@ def test_operator_scans_brute_force(oracle_mod):
             for j in range(n):
                 assert int(inc[j]) == functools.reduce(f, a[: j + 1], IDENTITY[op])
                 assert int(ex[j]) == functools.reduce(f, a[:j], IDENTITY[op])
+
+
+# ----------------------------------------------------------------- runs ----
+
+@pytest.mark.parametrize("c", [1, 3, 8])
+def test_runs_equal_counts_closed_form(oracle_mod, c):
+    n = 1000
+    ends, entries, owner = oracle_mod.runs_owner(np.full(n, c, dtype=np.uint32))
+    assert np.array_equal(ends, c * np.arange(1, n + 1, dtype=np.uint32))
+    assert entries == c * n
+    assert np.array_equal(owner, np.arange(c * n, dtype=np.int32) // c)
+
+
+@pytest.mark.parametrize("skewed", [False, True])
+def test_runs_against_numpy(oracle_mod, skewed):
+    counts = inputs.run_counts(100003, 6, skewed=skewed)
+    ends, entries, owner = oracle_mod.runs_owner(counts)
+    want_ends = np.cumsum(counts, dtype=np.uint64).astype(np.uint32)
+    assert np.array_equal(ends, want_ends)
+    total = int(want_ends[-1])
+    assert entries == max(total, 1)
+    e = np.arange(total, dtype=np.int64)
+    assert np.array_equal(owner, np.searchsorted(want_ends, e, side="right").astype(np.int32))
+    # every entry lies inside its owner's run, and no owner is empty
+    assert np.all(want_ends[owner] - counts[owner] <= e) and np.all(e < want_ends[owner])
+
+
+def test_runs_degenerate(oracle_mod):
+    for counts in ([], [0], [0, 0, 0]):
+        ends, entries, owner = oracle_mod.runs_owner(np.array(counts, dtype=np.uint32))
+        assert entries == 1 and owner.tolist() == [-1] and ends.tolist() == [0] * len(counts)
+    assert oracle_mod.runs_owner([5])[2].tolist() == [0] * 5
+    assert oracle_mod.runs_owner([0, 0, 2, 0, 1, 0])[2].tolist() == [2, 2, 4]
+    ends, _ = oracle_mod.runs_layout([M32 - 1, 1])  # ends wrap like the scan
+    assert ends.tolist() == [M32 - 1, 0]
+
+
+def test_runs_brute_force(oracle_mod):
+    for n in range(0, 5):
+        for counts in itertools.product(range(3), repeat=n):
+            ends, entries, owner = oracle_mod.runs_owner(list(counts))
+            walk = [i for i, c in enumerate(counts) for _ in range(c)]
+            assert owner.tolist() == (walk or [-1])
+            assert entries == max(len(walk), 1)
+            assert ends.tolist() == [sum(counts[: i + 1]) for i in range(n)]

@@ -26,6 +26,10 @@ Workloads (one per configuration of the benchmark suite):
                index 0 always a head, or every 4th index (length-4 segments)
 * compaction:  int32 flags, 1 where u32(4, 1, i) < T, T = round(p * 2^32)
 * radix:       keys u32(5, 0, i); tie-heavy variant u32 >> 24 in [0, 256)
+* runs:        per-owner counts from u32(6, 0, i) = d: uniform d >> 29 in
+               [0, 8) (mean 3.5, one owner in eight empty), or skewed: d >> 26
+               in [0, 64) when d & 15 == 0, else 0 (one owner in sixteen
+               holds a run, mean count 1.97)
 """
 
 from __future__ import annotations
@@ -42,6 +46,7 @@ __all__ = [
     "segment_heads_regular",
     "compact_flags",
     "radix_keys",
+    "run_counts",
     "COMPACT_THRESHOLD",
 ]
 
@@ -125,3 +130,12 @@ def radix_keys(n: int, seed: int, ties: bool = False) -> np.ndarray:
     if ties:
         k >>= np.uint32(24)
     return k
+
+
+def run_counts(n: int, seed: int, skewed: bool = False) -> np.ndarray:
+    """uint32 per-owner entry counts: uniform in [0, 8), or (skewed) mostly
+    empty with one owner in sixteen holding up to 63 entries."""
+    d = splitmix_u32(seed, 0, n)
+    if not skewed:
+        return d >> np.uint32(29)
+    return np.where((d & np.uint32(15)) == 0, d >> np.uint32(26), np.uint32(0)).astype(np.uint32)

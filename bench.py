@@ -22,6 +22,9 @@ Other ops time the other primitives on their own workloads:
   radix           radix_sort_perm_u32, n = 2^25 keys seed 5, uniform u32
                   or (--ties) in [0, 256); --sort pairs|keys times
                   radix_sort_u32 writing sorted keys (+ perm unless keys)
+  runs            runs_layout_u32 + runs_owner_u32, n = 2^25 owners, counts
+                  u32(6,0,i) >> 29 in [0, 8) or (--skewed) one owner in 16
+                  holding up to 63 entries
 
 Rank 0 prints one JSON line.
 
@@ -72,6 +75,7 @@ class Op:
     kernel = ""
     kernel_sources: list = []
     log2n = 28
+    launches_per_step = 1  # this library's kernels launched by one step
 
     def __init__(self, args):
         self.args = args
@@ -341,6 +345,7 @@ class CompactOp(Op):
 
 class RadixOp(Op):
     log2n = 25
+    launches_per_step = 15  # histogram, plan, 4 x (upsweep, table scan, downsweep), final copy
     kernel_sources = ["u32_prefix_scan_gb300/csrc/radix.cu", "u32_prefix_scan_gb300/csrc/scan.cu",
                       "u32_prefix_scan_gb300/csrc/internal.cuh"]
 
@@ -442,7 +447,113 @@ class RadixOp(Op):
             arrays["keys_out"] = k[arrays["perm"]]
 
 
-OPS = ["scan_exclusive", "scan_inclusive", "scan_op", "segscan", "segscan_sums", "segreduce", "compact", "radix"]
+class RunsOp(Op):
+    """The runs layout (in place) and the owner row. The layout replaces the
+    counts by their ends, so every step first restores the counts with a
+    device-to-device copy (part of the step's time, not of the kernels')."""
+
+    log2n = 25
+    launches_per_step = 3  # layout: scan + entries/slots fill; owner
+    kernel_sources = ["u32_prefix_scan_gb300/csrc/runs.cu"]
+
+    def __init__(self, args):
+        super().__init__(args)
+        self.skewed = args.skewed
+        self.name = "runs_owner_u32" + ("_skewed" if self.skewed else "")
+        mix = "skewed counts, 1/16 of owners in [0,64)" if self.skewed else "counts uniform in [0,8)"
+        self.metric = f"runs layout + owner row Gelem/s (owners) at n=2^25 owners ({mix}), 1 GB300"
+        self.kernel = "runs_owner_kernel<256,8> (merge path of ends with entry indices)"
+        self.entries = None
+
+    def workload(self):
+        mix = "u32(6,0,i): d & 15 == 0 ? d >> 26 : 0" if self.skewed else "u32(6,0,i) >> 29"
+        e = "" if self.entries is None else f", {self.entries} entries"
+        return (f"runs of n=2^{self.n.bit_length() - 1} owners, counts {mix}{e}: ends in place + entries + "
+                f"-1 slots, then owner(e) for every entry (counts restored by a device copy each step)")
+
+    def algorithmic_bytes(self):
+        # the owner kernel: ends read (4 per owner), owner row written (4 per entry)
+        return 4 * self.n + 4 * self.entries
+
+    def host_inputs(self):
+        from u32_prefix_scan_gb300 import inputs
+
+        c = inputs.run_counts(self.n, 6, skewed=self.skewed)
+        self.entries = max(int(c.sum(dtype="u8")), 1)
+        return {"counts": c}
+
+    def setup(self, dev, host):
+        import numpy as np
+        import torch
+
+        import u32_prefix_scan_gb300 as u
+        from u32_prefix_scan_gb300 import _native
+
+        self.u = u
+        self.pristine = torch.from_numpy(host["counts"].view(np.int32)).to(dev)
+        self.ends = torch.empty_like(self.pristine)
+        self.entries_d = torch.empty(1, dtype=torch.int32, device=dev)
+        self.slots = torch.empty(self.entries, dtype=torch.int32, device=dev)
+        self.owner = torch.empty(self.entries, dtype=torch.int32, device=dev)
+        self.ws = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_RUNS, self.n), dev)
+        self.pinned_in = {"counts": torch.from_numpy(host["counts"].view(np.int32)).pin_memory()}
+        self.pinned_out = {"ends": torch.empty(self.n, dtype=torch.int32).pin_memory(),
+                           "entries": torch.empty(1, dtype=torch.int32).pin_memory(),
+                           "owner": torch.empty(self.entries, dtype=torch.int32).pin_memory()}
+
+    def _layout(self):
+        self.u.runs_layout_u32(self.ends, self.entries_d, self.slots, workspace=self.ws)
+
+    def _owner(self):
+        self.u.runs_owner_u32(self.ends, self.owner, capacity=self.entries)
+
+    def step(self):
+        self.ends.copy_(self.pristine)
+        self._layout()
+        self._owner()
+
+    def step_marked(self, before, after):
+        self.ends.copy_(self.pristine)
+        self._layout()
+        before.record()
+        self._owner()
+        after.record()
+
+    def e2e_step(self):
+        self.ends.copy_(self.pinned_in["counts"], non_blocking=True)
+        self._layout()
+        self._owner()
+        for name, t in (("ends", self.ends), ("entries", self.entries_d), ("owner", self.owner)):
+            self.pinned_out[name].copy_(t, non_blocking=True)
+        return 4 * self.n, 4 * self.n + 4 + 4 * self.entries
+
+    def check_e2e(self, host):
+        import numpy as np
+
+        ends = self.pinned_out["ends"].numpy().view(np.uint32)
+        if not np.array_equal(ends, np.cumsum(host["counts"], dtype=np.uint64).astype(np.uint32)):
+            return False
+        if int(self.pinned_out["entries"][0]) != self.entries:
+            return False
+        k = min(self.entries, 1 << 20)
+        want = np.searchsorted(ends, np.arange(k, dtype=np.int64), side="right")
+        return bool(np.array_equal(self.pinned_out["owner"][:k].numpy(), want))
+
+    def oracle_step(self, lib, arrays):
+        import numpy as np
+
+        c = arrays["counts"]
+        if "ends" not in arrays:
+            arrays["ends"] = np.empty(c.size, dtype=np.uint32)
+            arrays["slots"] = np.empty(max(int(c.sum(dtype="u8")), 1), dtype=np.int32)
+        u32p, i32p = ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_int32)
+        entries = lib.oracle_runs_layout_u32(c.ctypes.data_as(u32p), c.size, arrays["ends"].ctypes.data_as(u32p))
+        lib.oracle_runs_fill_owner(c.ctypes.data_as(u32p), arrays["ends"].ctypes.data_as(u32p), c.size,
+                                   arrays["slots"].ctypes.data_as(i32p), entries)
+
+
+OPS = ["scan_exclusive", "scan_inclusive", "scan_op", "segscan", "segscan_sums", "segreduce", "compact", "radix",
+       "runs"]
 
 
 def make_op(args) -> Op:
@@ -454,6 +565,8 @@ def make_op(args) -> Op:
         return CompactOp(args)
     if args.op == "radix":
         return RadixOp(args)
+    if args.op == "runs":
+        return RunsOp(args)
     return SegOp(args, args.op)
 
 
@@ -471,6 +584,7 @@ def parse_args(argv=None):
     p.add_argument("--ties", action="store_true", help="radix: keys in [0, 256) instead of uniform u32")
     p.add_argument("--sort", choices=["perm", "pairs", "keys"], default="perm",
                    help="radix outputs: the permutation, sorted keys and the permutation, or sorted keys only")
+    p.add_argument("--skewed", action="store_true", help="runs: the skewed count mix instead of uniform [0, 8)")
     p.add_argument("--monoid", choices=["add", "mul", "and", "or", "xor", "min", "max"], default="max",
                    help="scan_op: the operator")
     p.add_argument("--inclusive", action="store_true", help="scan_op: inclusive instead of exclusive")
@@ -671,10 +785,18 @@ def run_ours(args, rank, local_rank, world):
     barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # an op whose step runs several calls brackets its dominant kernel with
+    # events on the launching stream; the roofline uses that kernel's time
+    marked = hasattr(op, "step_marked")
+    marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps if marked else 0)]
     w0 = time.time()
     start.record(stream)
-    for _ in range(args.steps):
-        op.step()
+    for k in range(args.steps):
+        if marked:
+            op.step_marked(*marks[k])
+        else:
+            op.step()
     end.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
@@ -684,6 +806,7 @@ def run_ours(args, rank, local_rank, world):
     op.u.check(workspace=op.ws)
     ms = start.elapsed_time(end) / args.steps
     ms_max = max_over_ranks(ms, world)
+    kernel_ms = sum(a.elapsed_time(b) for a, b in marks) / args.steps if marked else ms
 
     # end to end through the C ABI: pinned host inputs in, outputs back out
     h2d = d2h = 0
@@ -705,7 +828,7 @@ def run_ours(args, rank, local_rank, world):
 
     peak, peak_kind = load_peak()
     nbytes = op.algorithmic_bytes()
-    achieved = nbytes / (ms * 1e-3) / 1e9
+    achieved = nbytes / (kernel_ms * 1e-3) / 1e9
     full = op.n == 1 << op.log2n
     result = {
         "metric": op.metric,
@@ -726,11 +849,12 @@ def run_ours(args, rank, local_rank, world):
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": load_traffic(op), "algorithmic_bytes_per_launch": nbytes, "kernel": op.kernel},
+                     "traffic": load_traffic(op), "algorithmic_bytes_per_launch": nbytes, "kernel": op.kernel,
+                     "kernel_ms": kernel_ms},
         "e2e": {"value": world * op.n / (e2e_ms * 1e-3) / 1e9 if e2e_ms else None, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * op.launches_per_step,
     }
     if rank == 0 and not args.no_cpu_baseline:
         v, reps, el = time_oracle(op, host, args.cpu_seconds, op.n)

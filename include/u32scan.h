@@ -65,7 +65,8 @@ typedef struct CUstream_st *u32scan_stream_t;
 #define U32SCAN_OP_SCAN 1      /* scan_exclusive_u32, scan_inclusive_u32 */
 #define U32SCAN_OP_SEGSCAN 2   /* segscan_inclusive_u32, segreduce_u32 */
 #define U32SCAN_OP_COMPACT 3   /* compact_indices_u32 */
-#define U32SCAN_OP_RADIX 4     /* radix_sort_perm_u32 */
+#define U32SCAN_OP_RADIX 4     /* radix_sort_perm_u32, radix_sort_u32 */
+#define U32SCAN_OP_RUNS 5      /* runs_layout_u32 (runs_owner_u32 needs none) */
 
 /* Bytes of device workspace an operation needs for n elements (a multiple
  * of 256, at least 256). Returns 0 for an unknown op. Pure host function. */
@@ -227,6 +228,45 @@ int radix_sort_perm_u32(const uint32_t *keys, size_t n, int32_t *perm,
  */
 int radix_sort_u32(const uint32_t *keys, size_t n, uint32_t *keys_out, int32_t *perm,
                    void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * Runs layout. Source: the "parallel" package reference (entelechy docs),
+ * graph `runs` and its kernels runs_ends (the inclusive prefix sum of the
+ * counts: owner i's run covers ends[i] - counts[i] up to ends[i]),
+ * runs_entries (how many entries, at least one) and runs_slots (the row of
+ * `entries` slots, every one -1).
+ *   counts    device, uint32_t[n]: entries per owner; replaced in place by
+ *             ends (sums wrap at 2^32; a meaningful layout keeps the total
+ *             below 2^31).
+ *   entries   device, uint32_t[1]: max(total, 1).
+ *   slots     device, int32_t[slot_capacity] or NULL: slots[e] = -1 for e in
+ *             [0, min(entries, slot_capacity)); the rest untouched.
+ *   ws, ws_bytes  u32scan_workspace_bytes(U32SCAN_OP_RUNS, n) bytes.
+ * Errors: EINVAL (null counts with n > 0, null entries, misaligned pointers,
+ * n >= 2^31, slot_capacity >= 2^32, entries or slots overlapping counts or
+ * each other), EWORKSPACE, ECUDA; a look-back timeout as the scan's.
+ */
+int runs_layout_u32(uint32_t *counts, size_t n, uint32_t *entries, int32_t *slots, size_t slot_capacity,
+                    void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * owner(e, ends) for every entry of a runs layout. Source: as runs_layout_u32,
+ * function `owner(e: Int, ends: Rows<Int>) -> Int`; the page gives no text for
+ * it, and the owner of entry e is read as the owner whose run holds e: the
+ * least i with e < ends[i].
+ *   ends      device, uint32_t[n], non-decreasing (runs_layout_u32's output).
+ *   owner     device, int32_t[capacity]: owner[e] for e in [0, min(entries,
+ *             capacity)), entries = max(ends[n-1], 1); the one slot of a
+ *             layout with no entries (n = 0 or total 0) is -1. The rest is
+ *             untouched. The row equals the layout's slots after the graph's
+ *             fill scatter with each owner's index as the value.
+ * No workspace. Errors: EINVAL (null ends with n > 0, null owner with
+ * capacity > 0, misaligned pointers, n >= 2^31, capacity >= 2^32, owner
+ * overlapping ends), ECUDA. Ends that are not non-decreasing give an
+ * unspecified row, but every access stays inside ends[0, n) and
+ * owner[0, capacity).
+ */
+int runs_owner_u32(const uint32_t *ends, size_t n, int32_t *owner, size_t capacity, u32scan_stream_t stream);
 
 /*
  * Exclusive scan that allocates nothing and needs no workspace argument.

@@ -158,3 +158,27 @@ def test_radix_sort_rejects_bad_arguments_on_host(lib):
     assert fn(fake, 1000, fake + 4000, fake + 8001, fake, need, None) == _native.EINVAL  # misaligned perm
     assert fn(fake, 1000, fake + 4000, None, None, need, None) == _native.EWORKSPACE
     assert lib.radix_sort_perm_u32(fake, 10, None, fake, need, None) == _native.EINVAL
+
+
+def test_runs_rejects_bad_arguments_on_host(lib):
+    fake = 0x100000
+    need = lib.u32scan_workspace_bytes(_native.OP_RUNS, 1000)
+    assert need == lib.u32scan_workspace_bytes(_native.OP_SCAN, 1000)
+    lay = lib.runs_layout_u32
+    assert lay(fake, 1000, None, None, 0, fake, need, None) == _native.EINVAL            # no entries
+    assert lay(None, 10, fake, None, 0, fake, need, None) == _native.EINVAL              # no counts
+    assert lay(fake, 1000, fake + 400, None, 0, fake, need, None) == _native.EINVAL      # entries inside counts
+    assert lay(fake, 1000, fake + 8000, fake + 3996, 8, fake, need, None) == _native.EINVAL  # slots over counts
+    assert lay(fake, 1000, fake + 8000, fake + 7996, 8, fake, need, None) == _native.EINVAL  # slots over entries
+    assert lay(fake, 1000, fake + 8002, None, 0, fake, need, None) == _native.EINVAL     # misaligned entries
+    assert lay(fake, 1 << 31, fake - 8, None, 0, fake, need, None) == _native.EINVAL     # n too large
+    assert lay(fake, 1000, fake + 8000, fake + 9000, 1 << 32, fake, need, None) == _native.EINVAL
+    assert lay(fake, 1000, fake + 8000, None, 0, None, need, None) == _native.EWORKSPACE
+    own = lib.runs_owner_u32
+    assert own(None, 10, fake, 4, None) == _native.EINVAL                                # no ends
+    assert own(fake, 10, None, 4, None) == _native.EINVAL                                # no owner row
+    assert own(fake, 1000, fake + 3996, 4, None) == _native.EINVAL                       # owner over ends
+    assert own(fake, 1000, fake + 4002, 4, None) == _native.EINVAL                       # misaligned owner
+    assert own(fake, 1 << 31, fake + (1 << 33), 4, None) == _native.EINVAL
+    assert own(fake, 10, fake + 4000, 1 << 32, None) == _native.EINVAL
+    assert own(fake, 10, None, 0, None) == _native.OK                                    # nothing to write

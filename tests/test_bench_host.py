@@ -42,6 +42,9 @@ def test_algorithmic_bytes_per_op():
     assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "pairs"])).algorithmic_bytes() == 80 * n25
     assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "keys"])).algorithmic_bytes() == 52 * n25
     assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "keys", "--ties"])).algorithmic_bytes() == 16 * n25
+    runs = bench.make_op(bench.parse_args(["--op", "runs", "--log2n", "12"]))
+    c = runs.host_inputs()["counts"]
+    assert runs.entries == int(c.sum()) and runs.algorithmic_bytes() == 4 * (1 << 12) + 4 * runs.entries
     assert bench.make_op(bench.parse_args(["--log2n", "20"])).n == 1 << 20
 
 

@@ -16,6 +16,8 @@ _API = {
     "compact_indices_u32",
     "radix_sort_perm_u32",
     "radix_sort_u32",
+    "runs_layout_u32",
+    "runs_owner_u32",
     "check",
 }
 

@@ -23,6 +23,7 @@ OP_SCAN = 1
 OP_SEGSCAN = 2
 OP_COMPACT = 3
 OP_RADIX = 4
+OP_RUNS = 5
 
 _vp = ctypes.c_void_p
 _sz = ctypes.c_size_t
@@ -44,6 +45,8 @@ SIGNATURES = {
     "compact_indices_u32": (_int, [_vp, _sz, _vp, _vp, _vp, _vp, _sz, _vp]),
     "radix_sort_perm_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
     "radix_sort_u32": (_int, [_vp, _sz, _vp, _vp, _vp, _sz, _vp]),
+    "runs_layout_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp, _sz, _vp]),
+    "runs_owner_u32": (_int, [_vp, _sz, _vp, _sz, _vp]),
     "u32scan_test_scan_skip_publish": (_int, [_vp, _sz, _vp, _vp, _sz, ctypes.c_uint, ctypes.c_ulonglong, _vp]),
 }
 

@@ -27,6 +27,8 @@ __all__ = [
     "compact_indices_u32",
     "radix_sort_perm_u32",
     "radix_sort_u32",
+    "runs_layout_u32",
+    "runs_owner_u32",
     "check",
 ]
 
@@ -258,6 +260,45 @@ def radix_sort_u32(keys: torch.Tensor, keys_out: torch.Tensor | None = None, per
                                                perm.data_ptr() if perm is not None else None, ws.ptr, ws.nbytes, sh),
                   "radix_sort_u32")
     return keys_out, perm
+
+
+def runs_layout_u32(counts: torch.Tensor, entries: torch.Tensor | None = None, slots: torch.Tensor | None = None,
+                    *, stream=None, workspace: Workspace | None = None) -> torch.Tensor:
+    """In place: counts[i] <- ends[i] = counts[0] + .. + counts[i] (mod
+    2^32). Returns the one-element device tensor entries = max(total, 1);
+    when given, slots[0 : min(entries, slots.numel())] is set to -1."""
+    _require_cuda(counts, "counts")
+    entries = _scalar_out(entries, counts, counts.dtype)
+    if slots is not None:
+        _require_cuda(slots, "slots", (torch.int32,))
+    n = counts.numel()
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_RUNS, n, counts.device, sh, workspace)
+    _native.check(_native.lib().runs_layout_u32(counts.data_ptr(), n, entries.data_ptr(),
+                                                slots.data_ptr() if slots is not None else None,
+                                                slots.numel() if slots is not None else 0, ws.ptr, ws.nbytes, sh),
+                  "runs_layout_u32")
+    return entries
+
+
+def runs_owner_u32(ends: torch.Tensor, owner: torch.Tensor | None = None, capacity: int | None = None, *,
+                   stream=None) -> torch.Tensor:
+    """owner[e] = the owner whose run holds entry e (the least i with
+    e < ends[i]) for e in [0, min(entries, capacity)); -1 for the one slot of
+    an empty layout. With no `owner` tensor, one of `capacity` elements is
+    made (capacity defaults to entries, read back from the device)."""
+    _require_cuda(ends, "ends")
+    n = ends.numel()
+    if owner is None:
+        if capacity is None:
+            total = int(ends[-1].item()) & 0xFFFFFFFF if n else 0
+            capacity = max(total, 1)
+        owner = torch.empty(capacity, dtype=torch.int32, device=ends.device)
+    _require_cuda(owner, "owner", (torch.int32,))
+    cap = owner.numel() if capacity is None else min(int(capacity), owner.numel())
+    sh = _stream_handle(stream)
+    _native.check(_native.lib().runs_owner_u32(ends.data_ptr(), n, owner.data_ptr(), cap, sh), "runs_owner_u32")
+    return owner
 
 
 def check(stream=None, workspace: Workspace | None = None, device=None) -> int:

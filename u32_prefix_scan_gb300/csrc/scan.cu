@@ -498,6 +498,12 @@ int scan_exclusive_launch(uint32_t *data, unsigned long long n, void *ws, size_t
     return scan_launch<false>(data, n, nullptr, ws, ws_bytes, stream, 0xffffffffu, kDefaultLimitNs);
 }
 
+// The inclusive form with its total, for the runs layout.
+int scan_inclusive_launch(uint32_t *data, unsigned long long n, uint32_t *total, void *ws, size_t ws_bytes,
+                          cudaStream_t stream) {
+    return scan_launch<true>(data, n, total, ws, ws_bytes, stream, 0xffffffffu, kDefaultLimitNs);
+}
+
 }  // namespace u32scan
 
 using namespace u32scan;

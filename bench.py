@@ -179,27 +179,30 @@ class SegOp(Op):
         super().__init__(args)
         self.mode = mode  # segscan | segscan_sums | segreduce
         self.heads = args.heads
-        self.name = f"{mode}_{self.heads}"
+        self.fbytes = 1 if args.u8heads else 4  # bytes per head flag
+        self.name = f"{mode}_{self.heads}" + ("_u8heads" if args.u8heads else "")
         what = {"segscan": "segmented inclusive scan", "segscan_sums": "segmented inclusive scan + segment sums",
                 "segreduce": "per-segment reduce"}[mode]
         lengths = "geometric lengths mean 1024" if self.heads == "geometric" else "2^24 segments of length 4"
-        self.metric = f"U32 {what} Gelem/s and HBM GB/s (fraction of peak) at n=2^26 ({lengths}), 1 GB300"
+        fl = ", u8 head flags" if args.u8heads else ""
+        self.metric = f"U32 {what} Gelem/s and HBM GB/s (fraction of peak) at n=2^26 ({lengths}{fl}), 1 GB300"
         kind = {"segscan": "true,false", "segscan_sums": "true,true", "segreduce": "false,true"}[mode]
-        self.kernel = f"segscan_u32_persistent<512,7,2,{kind}>"
+        self.kernel = f"segscan_u32_persistent<512,7,2,{kind},{'uint8' if args.u8heads else 'int32'}>"
         self.nseg = None
 
     def workload(self):
         lengths = "Bernoulli(2^-10) heads" if self.heads == "geometric" else "a head every 4th index"
-        return (f"u32 {self.mode} n=2^{self.n.bit_length() - 1}, values uniform u32 seed 3, int32 head "
+        ftype = "u8" if self.fbytes == 1 else "int32"
+        return (f"u32 {self.mode} n=2^{self.n.bit_length() - 1}, values uniform u32 seed 3, {ftype} head "
                 f"flags: {lengths}")
 
     def algorithmic_bytes(self):
-        n, nseg = self.n, self.nseg
+        n, nseg, fb = self.n, self.nseg, self.fbytes
         if self.mode == "segscan":
-            return 12 * n  # values 4 + flags 4 read, values 4 written
+            return (8 + fb) * n  # values 4 + flags read, values 4 written
         if self.mode == "segscan_sums":
-            return 12 * n + 4 * nseg + 4
-        return 8 * n + 4 * nseg + 4  # segreduce: values + flags read, one sum per segment
+            return (8 + fb) * n + 4 * nseg + 4
+        return (4 + fb) * n + 4 * nseg + 4  # segreduce: values + flags read, one sum per segment
 
     def host_inputs(self):
         import numpy as np
@@ -209,6 +212,8 @@ class SegOp(Op):
         f = (inputs.segment_heads_geometric(self.n, 3) if self.heads == "geometric"
              else inputs.segment_heads_regular(self.n, 4))
         self.nseg = int(np.count_nonzero(f))
+        if self.fbytes == 1:
+            f = f.astype(np.uint8)
         return {"data": inputs.scan_values(self.n, 3), "flags": f}
 
     def setup(self, dev, host):
@@ -250,13 +255,17 @@ class SegOp(Op):
         if "sums" in self.pinned_out:
             self.pinned_out["sums"].copy_(self.sums, non_blocking=True)
             d2h += 4 * self.nseg
-        return 8 * self.n, d2h
+        return (4 + self.fbytes) * self.n, d2h
 
     def check_e2e(self, host):
         return int(self.pinned_out["count"][0]) == self.nseg
 
     def oracle_step(self, lib, arrays):
         u32p, i32p = ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_int32)
+        if arrays["flags"].itemsize != 4:
+            import numpy as np
+
+            arrays["flags"] = arrays["flags"].astype(np.int32)  # the oracle reads int32 flags
         a, f = arrays["data"], arrays["flags"]
         if self.mode == "segscan":
             lib.oracle_segscan_inclusive_u32(a.ctypes.data_as(u32p), f.ctypes.data_as(i32p), a.size)
@@ -584,6 +593,7 @@ def parse_args(argv=None):
     p.add_argument("--ties", action="store_true", help="radix: keys in [0, 256) instead of uniform u32")
     p.add_argument("--sort", choices=["perm", "pairs", "keys"], default="perm",
                    help="radix outputs: the permutation, sorted keys and the permutation, or sorted keys only")
+    p.add_argument("--u8heads", action="store_true", help="segmented ops: one byte per head flag")
     p.add_argument("--skewed", action="store_true", help="runs: the skewed count mix instead of uniform [0, 8)")
     p.add_argument("--monoid", choices=["add", "mul", "and", "or", "xor", "min", "max"], default="max",
                    help="scan_op: the operator")

@@ -63,7 +63,7 @@ typedef struct CUstream_st *u32scan_stream_t;
 
 /* Operation codes for u32scan_workspace_bytes. */
 #define U32SCAN_OP_SCAN 1      /* scan_exclusive_u32, scan_inclusive_u32 */
-#define U32SCAN_OP_SEGSCAN 2   /* segscan_inclusive_u32, segreduce_u32 */
+#define U32SCAN_OP_SEGSCAN 2   /* segscan_inclusive_u32, segreduce_u32 (and _u8heads) */
 #define U32SCAN_OP_COMPACT 3   /* compact_indices_u32 */
 #define U32SCAN_OP_RADIX 4     /* radix_sort_perm_u32, radix_sort_u32 */
 #define U32SCAN_OP_RUNS 5      /* runs_layout_u32 (runs_owner_u32 needs none) */
@@ -166,6 +166,23 @@ int segscan_inclusive_u32(uint32_t *data, const int32_t *head_flags, size_t n,
 int segreduce_u32(const uint32_t *data, const int32_t *head_flags, size_t n,
                   uint32_t *seg_sums, size_t seg_capacity, uint32_t *nseg,
                   void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * The same two operations with one byte per head flag: a non-zero byte at j
+ * opens a segment at j (the entelechy reading of a flag: non-zero is set).
+ * Arguments, results, workspace (U32SCAN_OP_SEGSCAN) and errors as in
+ * segscan_inclusive_u32 and segreduce_u32, except that head_flags is a
+ * device uint8_t[n] with no alignment requirement. The flags stream by bulk
+ * copy when (head_flags - (data mod 16) / 4) is 16-byte aligned (so for
+ * two buffers of the same 16-byte phase in elements, e.g. fresh
+ * allocations); otherwise by plain loads, with the same results.
+ */
+int segscan_inclusive_u32_u8heads(uint32_t *data, const uint8_t *head_flags, size_t n,
+                                  uint32_t *seg_sums, size_t seg_capacity, uint32_t *nseg,
+                                  void *ws, size_t ws_bytes, u32scan_stream_t stream);
+int segreduce_u32_u8heads(const uint32_t *data, const uint8_t *head_flags, size_t n,
+                          uint32_t *seg_sums, size_t seg_capacity, uint32_t *nseg,
+                          void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /*
  * Stream compaction: flags -> inclusive offsets -> gathered indices -> count.

@@ -182,3 +182,15 @@ def test_runs_rejects_bad_arguments_on_host(lib):
     assert own(fake, 1 << 31, fake + (1 << 33), 4, None) == _native.EINVAL
     assert own(fake, 10, fake + 4000, 1 << 32, None) == _native.EINVAL
     assert own(fake, 10, None, 0, None) == _native.OK                                    # nothing to write
+
+
+def test_u8heads_rejects_bad_arguments_on_host(lib):
+    fake = 0x100000
+    need = lib.u32scan_workspace_bytes(_native.OP_SEGSCAN, 1000)
+    for name in ("segscan_inclusive_u32_u8heads", "segreduce_u32_u8heads"):
+        fn = getattr(lib, name)
+        assert fn(None, fake, 10, fake + 8000, 10, fake + 9000, fake, need, None) == _native.EINVAL
+        assert fn(fake, None, 10, fake + 8000, 10, fake + 9000, fake, need, None) == _native.EINVAL
+        assert fn(fake + 2, fake, 10, fake + 8000, 10, fake + 9000, fake, need, None) == _native.EINVAL
+        assert fn(fake, fake + 4001, 1000, fake + 8000, 10, fake + 9000, None, need, None) == _native.EWORKSPACE
+    assert lib.segreduce_u32_u8heads(fake, fake, 10, None, 0, None, fake, need, None) == _native.EINVAL

@@ -36,6 +36,9 @@ def test_algorithmic_bytes_per_op():
     red = bench.make_op(bench.parse_args(["--op", "segreduce", "--heads", "regular4"]))
     red.nseg = n26 // 4
     assert red.algorithmic_bytes() == 8 * n26 + 4 * (n26 // 4) + 4
+    seg8 = bench.make_op(bench.parse_args(["--op", "segscan", "--u8heads"]))
+    seg8.nseg = 5
+    assert seg8.algorithmic_bytes() == 9 * n26
     assert bench.make_op(bench.parse_args(["--op", "compact"])).algorithmic_bytes() == 12 * n27 + 4
     assert bench.make_op(bench.parse_args(["--op", "radix"])).algorithmic_bytes() == 76 * n25
     assert bench.make_op(bench.parse_args(["--op", "radix", "--ties"])).algorithmic_bytes() == 16 * n25

@@ -144,7 +144,7 @@ def scan_u32_op(data: torch.Tensor, op: str, inclusive: bool = False, total: tor
 
 def _seg_args(data, head_flags, seg_sums, nseg):
     _require_cuda(data, "data")
-    _require_cuda(head_flags, "head_flags", (torch.int32,))
+    _require_cuda(head_flags, "head_flags", (torch.int32, torch.uint8))
     if head_flags.numel() != data.numel():
         raise ValueError("data and head_flags differ in length")
     if seg_sums is not None:
@@ -157,17 +157,17 @@ def segscan_inclusive_u32(data: torch.Tensor, head_flags: torch.Tensor, seg_sums
                           nseg: torch.Tensor | None = None, *, stream=None,
                           workspace: Workspace | None = None) -> torch.Tensor:
     """In place: data[j] <- sum of data over j's segment up to j (mod 2^32);
-    a non-zero head flag opens a segment, index 0 always does. If seg_sums
+    a non-zero head flag (int32 or uint8) opens a segment, index 0 always does. If seg_sums
     is given, seg_sums[k] <- segment k's sum (for k < seg_sums.numel()).
     Returns the one-element device tensor holding the segment count."""
     nseg = _seg_args(data, head_flags, seg_sums, nseg)
     n = data.numel()
     sh = _stream_handle(stream)
     ws = _ws(_native.OP_SEGSCAN, n, data.device, sh, workspace)
-    _native.check(_native.lib().segscan_inclusive_u32(
+    name = "segscan_inclusive_u32" + ("_u8heads" if head_flags.dtype == torch.uint8 else "")
+    _native.check(getattr(_native.lib(), name)(
         data.data_ptr(), head_flags.data_ptr(), n, seg_sums.data_ptr() if seg_sums is not None else None,
-        seg_sums.numel() if seg_sums is not None else 0, nseg.data_ptr(), ws.ptr, ws.nbytes, sh),
-        "segscan_inclusive_u32")
+        seg_sums.numel() if seg_sums is not None else 0, nseg.data_ptr(), ws.ptr, ws.nbytes, sh), name)
     return nseg
 
 
@@ -183,9 +183,10 @@ def segreduce_u32(data: torch.Tensor, head_flags: torch.Tensor, seg_sums: torch.
     n = data.numel()
     sh = _stream_handle(stream)
     ws = _ws(_native.OP_SEGSCAN, n, data.device, sh, workspace)
-    _native.check(_native.lib().segreduce_u32(
+    name = "segreduce_u32" + ("_u8heads" if head_flags.dtype == torch.uint8 else "")
+    _native.check(getattr(_native.lib(), name)(
         data.data_ptr(), head_flags.data_ptr(), n, seg_sums.data_ptr(), seg_sums.numel(), nseg.data_ptr(),
-        ws.ptr, ws.nbytes, sh), "segreduce_u32")
+        ws.ptr, ws.nbytes, sh), name)
     return seg_sums, nseg
 
 

@@ -3,8 +3,10 @@
 // Source: "Futhark.Pass.ExtractKernels.Segmented": regularSegmentedScan
 // names the segmented scan; regularSegmentedRedomap reduces every segment
 // "until there is only a single value per segment". Segments are marked by
-// head flags: a non-zero int32 flag at j opens a segment at j, and index 0
-// always opens one. The scan gives out[j] = a[h] + .. + a[j] (mod 2^32), h
+// head flags: a non-zero flag at j opens a segment at j, and index 0 always
+// opens one. Flags are int32 (segscan_inclusive_u32, segreduce_u32) or one
+// byte each (the _u8heads entry points: 9 bytes per element for the scan
+// instead of 12). The scan gives out[j] = a[h] + .. + a[j] (mod 2^32), h
 // the last head at or before j; the reduce gives one wrapped sum per
 // segment, in segment order, and the segment count.
 //
@@ -25,7 +27,8 @@
 //
 // Layout inside a tile (as in scan.cu): warp w owns the w-th run of 128 * V
 // elements; lane l holds, for r = 0 .. V-1, the four elements at 128 * r +
-// 4 * l of that run. Head flags become one bit per element (bit 4 * r + c).
+// 4 * l of that run. Head flags become one bit per element (bit 4 * r + c);
+// byte flags are read four to a word and tested bytewise.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -36,18 +39,21 @@ namespace u32scan {
 
 constexpr unsigned int kNoHead = 0xffffffffu;
 
-template <int THREADS, int V, int S, bool WRITE_SCAN, bool WANT_SUMS>
+template <int THREADS, int V, int S, bool WRITE_SCAN, bool WANT_SUMS, typename F>
 __global__ void __launch_bounds__(THREADS, 1)
-segscan_u32_persistent(uint32_t *__restrict__ data, const int32_t *__restrict__ flags, unsigned long long n,
+segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags, unsigned long long n,
                        uint32_t *seg_sums, unsigned long long seg_cap, uint32_t *nseg, WsHeader *hdr,
                        unsigned long long *desc2, unsigned int n_tiles, unsigned int head, int streams_aligned,
                        unsigned int skip_tile, unsigned long long limit_ns) {
     constexpr int WARPS = THREADS / 32;
     constexpr unsigned int CHUNK = 128 * V;  // elements per warp
     constexpr unsigned int TILE = THREADS * V * 4;
-    constexpr unsigned int TILE_BYTES = TILE * 4;  // per stream
+    constexpr unsigned int TILE_BYTES = TILE * 4;  // values
+    constexpr unsigned int FLAG_BYTES = TILE * (unsigned int)sizeof(F);
+    constexpr unsigned int STAGE_U4 = (TILE_BYTES + FLAG_BYTES) / 16;
     static_assert(WARPS <= 32 && 4 * V <= 32, "one lane per warp; head bits fit in a word");
-    extern __shared__ __align__(128) uint4 stage_buf[];  // S stages of [values | flags], TILE each
+    static_assert(sizeof(F) == 4 || sizeof(F) == 1, "int32 or byte head flags");
+    extern __shared__ __align__(128) uint4 stage_buf[];  // S stages of [values | flags]
     __shared__ __align__(8) unsigned long long bar[S];
     __shared__ unsigned int s_tile[S];
     __shared__ unsigned int s_wval[2][WARPS], s_wcnt[2][WARPS], s_whas[2][WARPS];
@@ -62,7 +68,7 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const int32_t *__restrict__ 
     const int warp = threadIdx.x >> 5;
     const unsigned int last_draw = n_tiles + (unsigned int)S * gridDim.x - 1u;
     uint32_t *vdata = reinterpret_cast<uint32_t *>(reinterpret_cast<uintptr_t>(data) - 4ull * head);
-    const int32_t *vflags = reinterpret_cast<const int32_t *>(reinterpret_cast<uintptr_t>(flags) - 4ull * head);
+    const F *vflags = reinterpret_cast<const F *>(reinterpret_cast<uintptr_t>(flags) - sizeof(F) * head);
     const bool producer = threadIdx.x == THREADS - 32;
     unsigned int latest_parity = 0;
 
@@ -86,9 +92,9 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const int32_t *__restrict__ 
         const unsigned int b = smem_u32(&bar[st]);
         if (id < n_tiles && tile_full(id)) {
             const unsigned long long v0 = (unsigned long long)id * TILE;
-            mbar_arrive_expect_tx(b, 2 * TILE_BYTES);
-            bulk_load(smem_u32(stage_buf + st * (TILE / 2)), vdata + v0, TILE_BYTES, b);
-            bulk_load(smem_u32(stage_buf + st * (TILE / 2) + TILE / 4), vflags + v0, TILE_BYTES, b);
+            mbar_arrive_expect_tx(b, TILE_BYTES + FLAG_BYTES);
+            bulk_load(smem_u32(stage_buf + st * STAGE_U4), vdata + v0, TILE_BYTES, b);
+            bulk_load(smem_u32(stage_buf + st * STAGE_U4 + TILE / 4), vflags + v0, FLAG_BYTES, b);
         } else {
             mbar_arrive(b);  // nothing to copy: a partial tile reads global memory, a past-the-end draw stops
         }
@@ -122,19 +128,31 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const int32_t *__restrict__ 
         const unsigned long long tile_v0 = (unsigned long long)t * TILE;
         hb = 0;
         if (tile_full(t)) {
-            const uint4 *sv = stage_buf + st * (TILE / 2) + (li0 >> 2);
-            const int4 *sf = reinterpret_cast<const int4 *>(stage_buf + st * (TILE / 2) + TILE / 4) + (li0 >> 2);
+            const uint4 *sv = stage_buf + st * STAGE_U4 + (li0 >> 2);
+            if constexpr (sizeof(F) == 4) {
+                const int4 *sf = reinterpret_cast<const int4 *>(stage_buf + st * STAGE_U4 + TILE / 4) + (li0 >> 2);
 #pragma unroll
-            for (int r = 0; r < V; ++r) {
-                x[r] = sv[32 * r];
-                const int4 f = sf[32 * r];
-                hb |= ((f.x != 0) | ((f.y != 0) << 1) | ((f.z != 0) << 2) | ((f.w != 0) << 3)) << (4 * r);
+                for (int r = 0; r < V; ++r) {
+                    x[r] = sv[32 * r];
+                    const int4 f = sf[32 * r];
+                    hb |= ((f.x != 0) | ((f.y != 0) << 1) | ((f.z != 0) << 2) | ((f.w != 0) << 3)) << (4 * r);
+                }
+            } else {
+                // four byte flags in one word: byte c non-zero -> bit c of a nibble
+                const unsigned int *sf = reinterpret_cast<const unsigned int *>(stage_buf + st * STAGE_U4 + TILE / 4) +
+                                         (li0 >> 2);
+#pragma unroll
+                for (int r = 0; r < V; ++r) {
+                    x[r] = sv[32 * r];
+                    const unsigned int m = __vcmpne4(sf[32 * r], 0u) & 0x08040201u;
+                    hb |= ((m * 0x01010101u) >> 24) << (4 * r);
+                }
             }
         } else {
             unsigned int lo, hi;
             tile_range(t, lo, hi);
             const uint32_t *tv = vdata + tile_v0;
-            const int32_t *tf = vflags + tile_v0;
+            const F *tf = vflags + tile_v0;
 #pragma unroll
             for (int r = 0; r < V; ++r) {
                 unsigned int e[4];
@@ -355,7 +373,8 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const int32_t *__restrict__ 
 #endif
 constexpr int kSThreads = 512, kSV = U32SCAN_S_V, kSStages = U32SCAN_S_STAGES;
 constexpr unsigned long long kSTile = (unsigned long long)kSThreads * kSV * 4;
-constexpr size_t kSSmem = (size_t)kSStages * kSTile * 8;
+template <typename F>
+constexpr size_t seg_smem() { return (size_t)kSStages * kSTile * (4 + sizeof(F)); }
 
 size_t segscan_workspace_bytes(unsigned long long n) {
     const unsigned long long tiles = (n + 3 + kSTile - 1) / kSTile;
@@ -364,15 +383,15 @@ size_t segscan_workspace_bytes(unsigned long long n) {
 
 static std::mutex g_seg_mu;
 static int g_seg_sms[64];
-static bool g_seg_attr[64][4];
+static bool g_seg_attr[64][8];
 
-template <bool WRITE_SCAN, bool WANT_SUMS>
-static int segscan_launch(uint32_t *data, const int32_t *flags, unsigned long long n, uint32_t *seg_sums,
+template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
+static int segscan_launch(uint32_t *data, const F *flags, unsigned long long n, uint32_t *seg_sums,
                           unsigned long long seg_cap, uint32_t *nseg, void *ws, size_t ws_bytes, cudaStream_t stream,
                           unsigned int skip_tile, unsigned long long limit_ns) {
     if (n >= (1ull << 32)) return U32SCAN_EINVAL;
     if (n > 0 && (data == nullptr || flags == nullptr)) return U32SCAN_EINVAL;
-    if ((reinterpret_cast<uintptr_t>(data) & 3) || (reinterpret_cast<uintptr_t>(flags) & 3) ||
+    if ((reinterpret_cast<uintptr_t>(data) & 3) || (reinterpret_cast<uintptr_t>(flags) & (sizeof(F) - 1)) ||
         (reinterpret_cast<uintptr_t>(seg_sums) & 3) || (reinterpret_cast<uintptr_t>(nseg) & 3))
         return U32SCAN_EINVAL;
     if (n == 0) {
@@ -382,9 +401,11 @@ static int segscan_launch(uint32_t *data, const int32_t *flags, unsigned long lo
     if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < segscan_workspace_bytes(n))
         return U32SCAN_EWORKSPACE;
     const unsigned int head = (unsigned int)((reinterpret_cast<uintptr_t>(data) & 15) >> 2);
-    const int aligned = ((reinterpret_cast<uintptr_t>(data) ^ reinterpret_cast<uintptr_t>(flags)) & 15) == 0;
+    // flags stream by bulk copy when they start a tile on a 16-byte boundary too
+    const int aligned = ((reinterpret_cast<uintptr_t>(flags) - sizeof(F) * head) & 15) == 0;
     const unsigned int n_tiles = (unsigned int)((n + head + kSTile - 1) / kSTile);
-    auto kern = segscan_u32_persistent<kSThreads, kSV, kSStages, WRITE_SCAN, WANT_SUMS>;
+    auto kern = segscan_u32_persistent<kSThreads, kSV, kSStages, WRITE_SCAN, WANT_SUMS, F>;
+    constexpr size_t smem = seg_smem<F>();
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return U32SCAN_ECUDA;
     int sms;
@@ -393,9 +414,9 @@ static int segscan_launch(uint32_t *data, const int32_t *flags, unsigned long lo
         if (g_seg_sms[dev] == 0 &&
             cudaDeviceGetAttribute(&g_seg_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return U32SCAN_ECUDA;
-        const int which = (WRITE_SCAN ? 2 : 0) + (WANT_SUMS ? 1 : 0);
+        const int which = (sizeof(F) == 1 ? 4 : 0) + (WRITE_SCAN ? 2 : 0) + (WANT_SUMS ? 1 : 0);
         if (!g_seg_attr[dev][which]) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSSmem) != cudaSuccess)
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
                 return U32SCAN_ECUDA;
             g_seg_attr[dev][which] = true;
         }
@@ -404,7 +425,7 @@ static int segscan_launch(uint32_t *data, const int32_t *flags, unsigned long lo
     const unsigned int grid = n_tiles < (unsigned int)sms ? n_tiles : (unsigned int)sms;
     WsHeader *hdr = static_cast<WsHeader *>(ws);
     unsigned long long *desc2 = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
-    kern<<<grid, kSThreads, kSSmem, stream>>>(data, flags, n, seg_sums, seg_cap, nseg, hdr, desc2, n_tiles, head,
+    kern<<<grid, kSThreads, smem, stream>>>(data, flags, n, seg_sums, seg_cap, nseg, hdr, desc2, n_tiles, head,
                                              aligned, skip_tile, limit_ns);
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }
@@ -426,6 +447,25 @@ extern "C" int segscan_inclusive_u32(uint32_t *data, const int32_t *head_flags, 
 extern "C" int segreduce_u32(const uint32_t *data, const int32_t *head_flags, size_t n, uint32_t *seg_sums,
                              size_t seg_capacity, uint32_t *nseg, void *ws, size_t ws_bytes,
                              u32scan_stream_t stream) {
+    if (seg_sums == nullptr && nseg == nullptr) return U32SCAN_EINVAL;
+    return segscan_launch<false, true>(const_cast<uint32_t *>(data), head_flags, n, seg_sums,
+                                       seg_sums ? seg_capacity : 0, nseg, ws, ws_bytes, (cudaStream_t)stream,
+                                       0xffffffffu, kDefaultLimitNs);
+}
+
+extern "C" int segscan_inclusive_u32_u8heads(uint32_t *data, const uint8_t *head_flags, size_t n, uint32_t *seg_sums,
+                                             size_t seg_capacity, uint32_t *nseg, void *ws, size_t ws_bytes,
+                                             u32scan_stream_t stream) {
+    if (seg_sums != nullptr)
+        return segscan_launch<true, true>(data, head_flags, n, seg_sums, seg_capacity, nseg, ws, ws_bytes,
+                                          (cudaStream_t)stream, 0xffffffffu, kDefaultLimitNs);
+    return segscan_launch<true, false>(data, head_flags, n, nullptr, 0, nseg, ws, ws_bytes, (cudaStream_t)stream,
+                                       0xffffffffu, kDefaultLimitNs);
+}
+
+extern "C" int segreduce_u32_u8heads(const uint32_t *data, const uint8_t *head_flags, size_t n, uint32_t *seg_sums,
+                                     size_t seg_capacity, uint32_t *nseg, void *ws, size_t ws_bytes,
+                                     u32scan_stream_t stream) {
     if (seg_sums == nullptr && nseg == nullptr) return U32SCAN_EINVAL;
     return segscan_launch<false, true>(const_cast<uint32_t *>(data), head_flags, n, seg_sums,
                                        seg_sums ? seg_capacity : 0, nseg, ws, ws_bytes, (cudaStream_t)stream,

@@ -70,6 +70,8 @@ def _configure(lib):
     lib.oracle_runs_layout_u32.restype = ctypes.c_uint32
     lib.oracle_runs_fill_owner.argtypes = [_u32p, _u32p, _u64, _i32p, _u64]
     lib.oracle_runs_fill_owner.restype = None
+    lib.oracle_compact_values_u32.argtypes = [_u32p, _i32p, _u64, _u32p]
+    lib.oracle_compact_values_u32.restype = ctypes.c_uint64
     return lib
 
 
@@ -215,3 +217,19 @@ def runs_owner(counts):
     slots = np.empty(entries, dtype=np.int32)
     _load().oracle_runs_fill_owner(_p(c, _u32p), _p(ends, _u32p), c.size, _p(slots, _i32p), entries)
     return ends, entries, slots
+
+
+def compact_values(values, flags=None, out=None):
+    """(out, count): the kept values in order at the front of a copy of
+    `out` (zeros when not given), the rest of it unchanged. An element is
+    kept when its flag is non-zero, or, with no flags, its value is."""
+    v = _u32(values)
+    o = np.zeros(v.size, dtype=np.uint32) if out is None else _u32(out)
+    if o.size != v.size:
+        raise ValueError("out must have n elements")
+    f = None if flags is None else _i32(flags)
+    if f is not None and f.size != v.size:
+        raise ValueError("values and flags differ in length")
+    used = _load().oracle_compact_values_u32(_p(v, _u32p), None if f is None else _p(f, _i32p), v.size,
+                                            _p(o, _u32p))
+    return o, int(used)

@@ -23,6 +23,8 @@
  *                compact_gather, sort_identity / sort_blank / sort_zeros /
  *                sort_place / sort_next_bit, runs_ends / runs_entries /
  *                runs_slots, graphs compact, sort and runs, function owner.
+ *   [CAIRN compact] "Concurrency" (CAIRN docs), "reduce and compact": the
+ *                `compact out for i in n where p yield e` collector.
  *
  * Readings taken where the pages are silent (all restated in the design
  * notes): any n is scanned in full (not only 2^floor(log2 n) entries);
@@ -393,4 +395,24 @@ void oracle_runs_fill_owner(const uint32_t *counts, const uint32_t *ends, uint64
                 slots[e] = (int32_t)i;
         }
     }
+}
+
+/* ------------------------------------------------------------------------
+ * Compaction of values.  [CAIRN] "reduce and compact": `compact out for i
+ * in n where p yield e` evaluates the test once per input, writes e for
+ * each selected i, in order, to the front of out (capacity n), returns how
+ * many it wrote, and leaves the rest of out unchanged. Here e = values[i]
+ * and the test is flags[i] != 0, or, with no flags, values[i] != 0 (the
+ * page's `where xs[i] > 0` on unsigned values).
+ * ---------------------------------------------------------------------- */
+
+uint64_t oracle_compact_values_u32(const uint32_t *values, const int32_t *flags, uint64_t n, uint32_t *out)
+{
+    uint64_t used = 0;
+    for (uint64_t i = 0; i < n; ++i) {
+        int keep = flags ? flags[i] != 0 : values[i] != 0;
+        if (keep)
+            out[used++] = values[i];
+    }
+    return used;
 }

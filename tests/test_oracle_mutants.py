@@ -46,6 +46,10 @@ MUTANTS = [
     ("runs_entries_may_be_zero", "return run > 0 ? run : 1u;", "return run;", ["runs_degenerate"]),
     ("runs_fill_starts_one_late", "(uint64_t)ends[i] - (uint64_t)counts[i];",
      "(uint64_t)ends[i] - (uint64_t)counts[i] + 1;", ["runs_closed", "runs_brute"]),
+    ("compact_values_positive_flags_only", "int keep = flags ? flags[i] != 0 : values[i] != 0;",
+     "int keep = flags ? flags[i] > 0 : values[i] != 0;", ["cvalues_nonzero"]),
+    ("compact_values_projects_index", "out[used++] = values[i];", "out[used++] = (uint32_t)i;",
+     ["cvalues_numpy", "golden_compact"]),
 ]
 
 PINS = {
@@ -67,6 +71,9 @@ PINS = {
     "runs_numpy": lambda o: pins.test_runs_against_numpy(o, True),
     "runs_degenerate": lambda o: pins.test_runs_degenerate(o),
     "runs_brute": lambda o: pins.test_runs_brute_force(o),
+    "cvalues_nonzero": lambda o: pins.test_compact_values_nonzero_test(o),
+    "cvalues_numpy": lambda o: pins.test_compact_values_against_numpy(o, 0.1),
+    "golden_compact": lambda o: pins.test_golden_cairn_compact(o),
 }
 
 

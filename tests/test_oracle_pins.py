@@ -211,6 +211,8 @@ def test_golden_cairn_compact(oracle_mod):
     assert samples[indices[:count]].tolist() == [int(x) for x in g["front_values"].split()]
     assert indices[count:].tolist() == [-1] * (samples.size - count)
     assert offsets.tolist() == [0, 1, 1, 2]
+    live, used = oracle_mod.compact_values(samples)  # `where xs[i] > 0 yield xs[i]` into a zeroed row
+    assert used == int(g["count"]) and live.tolist() == [int(x) for x in g["live_after"].split()]
 
 
 @pytest.mark.parametrize("p", [0.1, 0.9])
@@ -392,3 +394,37 @@ def test_runs_brute_force(oracle_mod):
             assert owner.tolist() == (walk or [-1])
             assert entries == max(len(walk), 1)
             assert ends.tolist() == [sum(counts[: i + 1]) for i in range(n)]
+
+
+# ------------------------------------------------------ compact values ----
+
+@pytest.mark.parametrize("p", [0.1, 0.9])
+def test_compact_values_against_numpy(oracle_mod, p):
+    n = 100003
+    v = inputs.scan_values(n, 4)
+    f = inputs.compact_flags(n, 4, p)
+    before = inputs.scan_values(n, 9)
+    out, used = oracle_mod.compact_values(v, f, before)
+    keep = v[f != 0]
+    assert used == keep.size == np.count_nonzero(f)
+    assert np.array_equal(out[:used], keep)
+    assert np.array_equal(out[used:], before[used:])  # the rest of out is unchanged
+
+
+def test_compact_values_nonzero_test(oracle_mod):
+    v = np.where(inputs.compact_flags(5000, 4, 0.1) != 0, inputs.scan_values(5000, 4), 0).astype(np.uint32)
+    out, used = oracle_mod.compact_values(v)
+    assert used == np.count_nonzero(v) and np.array_equal(out[:used], v[v != 0]) and not out[used:].any()
+    # flags decide alone: a kept zero value and a dropped non-zero value
+    out, used = oracle_mod.compact_values([0, 5, 6], [1, 0, -2], [9, 9, 9])
+    assert used == 2 and out.tolist() == [0, 6, 9]
+
+
+def test_compact_values_brute_force(oracle_mod):
+    for n in range(0, 7):
+        for bits in range(1 << n):
+            f = [(bits >> i) & 1 for i in range(n)]
+            v = [10 + i for i in range(n)]
+            out, used = oracle_mod.compact_values(v, f, [99] * n)
+            kept = [v[i] for i in range(n) if f[i]]
+            assert used == len(kept) and out.tolist() == kept + [99] * (n - len(kept))

@@ -18,7 +18,8 @@ Other ops time the other primitives on their own workloads:
   segscan_sums    the same, also writing every segment's sum and the count
   segreduce       segreduce_u32: sums and count only
   compact         compact_indices_u32, n = 2^27 int32 flags, keep
-                  probability --p (0.1 or 0.9), seed 4
+                  probability --p (0.1 or 0.9), seed 4; --project values
+                  or nonzero times compact_values_u32 (values u32(4,0,i))
   radix           radix_sort_perm_u32, n = 2^25 keys seed 5, uniform u32
                   or (--ties) in [0, 256); --sort pairs|keys times
                   radix_sort_u32 writing sorted keys (+ perm unless keys)
@@ -352,6 +353,99 @@ class CompactOp(Op):
                                    arrays["indices"].ctypes.data_as(i32p), arrays["count"].ctypes.data_as(i32p))
 
 
+class CompactValuesOp(Op):
+    """compact_values_u32: kept values at the front of out, with int32 flags
+    (Bernoulli p) or, with --project nonzero, the values' own non-zero test."""
+
+    log2n = 27
+    kernel_sources = ["u32_prefix_scan_gb300/csrc/compact_values.cu", "u32_prefix_scan_gb300/csrc/internal.cuh"]
+
+    def __init__(self, args):
+        super().__init__(args)
+        self.p = args.p
+        self.nonzero = args.project == "nonzero"
+        self.name = f"compact_values_{'nonzero' if self.nonzero else 'flags'}_p{self.p}"
+        test = "non-zero values" if self.nonzero else "int32 flags"
+        self.metric = (f"compaction of values Gelem/s and HBM GB/s (fraction of peak) at n=2^27, "
+                       f"kept with probability {self.p} ({test}), 1 GB300")
+        self.kernel = f"compact_values_persistent<512,{7 if self.nonzero else 4},3,{'false' if self.nonzero else 'true'}>"
+        self.kept = None
+
+    def workload(self):
+        if self.nonzero:
+            src = f"values u32(4,0,i) | 1 where u32(4,1,i) < T_p, else 0 (p={self.p})"
+        else:
+            src = f"values u32(4,0,i), int32 flags Bernoulli p={self.p} (seed 4)"
+        return f"compaction of values, n=2^{self.n.bit_length() - 1}: {src} -> kept values at the front + count"
+
+    def algorithmic_bytes(self):
+        # values (and flags) read once; each kept value written once; the count
+        return (4 if self.nonzero else 8) * self.n + 4 * self.kept + 4
+
+    def host_inputs(self):
+        import numpy as np
+
+        from u32_prefix_scan_gb300 import inputs
+
+        f = inputs.compact_flags(self.n, 4, self.p)
+        v = inputs.scan_values(self.n, 4)
+        self.kept = int(np.count_nonzero(f))
+        if self.nonzero:
+            return {"values": np.where(f != 0, v | np.uint32(1), 0).astype(np.uint32)}
+        return {"values": v, "flags": f}
+
+    def setup(self, dev, host):
+        import numpy as np
+        import torch
+
+        import u32_prefix_scan_gb300 as u
+        from u32_prefix_scan_gb300 import _native
+
+        self.u = u
+        self.values = torch.from_numpy(host["values"].view(np.int32)).to(dev)
+        self.flags = None if self.nonzero else torch.from_numpy(host["flags"]).to(dev)
+        self.out = torch.empty(self.n, dtype=torch.int32, device=dev)
+        self.count = torch.empty(1, dtype=torch.int32, device=dev)
+        self.ws = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_COMPACT, self.n), dev)
+        self.pinned_in = {"values": torch.from_numpy(host["values"].view(np.int32)).pin_memory()}
+        if self.flags is not None:
+            self.pinned_in["flags"] = torch.from_numpy(host["flags"]).pin_memory()
+        self.pinned_out = {"out": torch.empty(self.kept, dtype=torch.int32).pin_memory(),
+                           "count": torch.empty(1, dtype=torch.int32).pin_memory()}
+
+    def step(self):
+        self.u.compact_values_u32(self.values, self.flags, self.out, self.count, workspace=self.ws)
+
+    def e2e_step(self):
+        self.values.copy_(self.pinned_in["values"], non_blocking=True)
+        if self.flags is not None:
+            self.flags.copy_(self.pinned_in["flags"], non_blocking=True)
+        self.step()
+        self.pinned_out["out"].copy_(self.out[: self.kept], non_blocking=True)
+        self.pinned_out["count"].copy_(self.count, non_blocking=True)
+        return 4 * self.n * len(self.pinned_in), 4 * self.kept + 4
+
+    def check_e2e(self, host):
+        import numpy as np
+
+        v = host["values"]
+        keep = v != 0 if self.nonzero else host["flags"] != 0
+        k = min(self.kept, 1 << 20)
+        return (int(self.pinned_out["count"][0]) == self.kept
+                and np.array_equal(self.pinned_out["out"][:k].numpy().view(np.uint32), v[keep][:k]))
+
+    def oracle_step(self, lib, arrays):
+        import numpy as np
+
+        u32p, i32p = ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_int32)
+        v = arrays["values"]
+        if "out" not in arrays:
+            arrays["out"] = np.zeros(v.size, dtype=np.uint32)
+        f = arrays.get("flags")
+        lib.oracle_compact_values_u32(v.ctypes.data_as(u32p), None if f is None else f.ctypes.data_as(i32p), v.size,
+                                      arrays["out"].ctypes.data_as(u32p))
+
+
 class RadixOp(Op):
     log2n = 25
     launches_per_step = 15  # histogram, plan, 4 x (upsweep, table scan, downsweep), final copy
@@ -571,7 +665,7 @@ def make_op(args) -> Op:
     if args.op == "scan_op":
         return ScanOp(args, args.inclusive, args.monoid)
     if args.op == "compact":
-        return CompactOp(args)
+        return CompactOp(args) if args.project == "indices" else CompactValuesOp(args)
     if args.op == "radix":
         return RadixOp(args)
     if args.op == "runs":
@@ -593,6 +687,8 @@ def parse_args(argv=None):
     p.add_argument("--ties", action="store_true", help="radix: keys in [0, 256) instead of uniform u32")
     p.add_argument("--sort", choices=["perm", "pairs", "keys"], default="perm",
                    help="radix outputs: the permutation, sorted keys and the permutation, or sorted keys only")
+    p.add_argument("--project", choices=["indices", "values", "nonzero"], default="indices",
+                   help="compact: kept indices (offsets, -1 tail), kept values by flags, or kept non-zero values")
     p.add_argument("--u8heads", action="store_true", help="segmented ops: one byte per head flag")
     p.add_argument("--skewed", action="store_true", help="runs: the skewed count mix instead of uniform [0, 8)")
     p.add_argument("--monoid", choices=["add", "mul", "and", "or", "xor", "min", "max"], default="max",

@@ -64,7 +64,7 @@ typedef struct CUstream_st *u32scan_stream_t;
 /* Operation codes for u32scan_workspace_bytes. */
 #define U32SCAN_OP_SCAN 1      /* scan_exclusive_u32, scan_inclusive_u32 */
 #define U32SCAN_OP_SEGSCAN 2   /* segscan_inclusive_u32, segreduce_u32 (and _u8heads) */
-#define U32SCAN_OP_COMPACT 3   /* compact_indices_u32 */
+#define U32SCAN_OP_COMPACT 3   /* compact_indices_u32, compact_values_u32 */
 #define U32SCAN_OP_RADIX 4     /* radix_sort_perm_u32, radix_sort_u32 */
 #define U32SCAN_OP_RUNS 5      /* runs_layout_u32 (runs_owner_u32 needs none) */
 
@@ -207,6 +207,26 @@ int segreduce_u32_u8heads(const uint32_t *data, const uint8_t *head_flags, size_
 int compact_indices_u32(const int32_t *flags, size_t n, int32_t *offsets,
                         int32_t *indices, int32_t *count,
                         void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * Compaction of values. Source: the CAIRN "Concurrency" page, "reduce and
+ * compact": `compact out for i in n where p yield e` writes e for each
+ * selected i, in order, to the front of out (capacity n), returns how many
+ * it wrote and leaves the rest of out unchanged. Here e = values[i].
+ *   values   device, uint32_t[n], read only.
+ *   flags    device, int32_t[n] or NULL: element i is kept when flags[i] != 0;
+ *            with NULL, when values[i] != 0 (the page's `where xs[i] > 0`).
+ *   out      device, uint32_t[n]: the kept values in order at the front;
+ *            out[count..n) is not written. Must not overlap values or flags.
+ *   count    device, one int32_t or NULL: the number of kept elements.
+ *   ws, ws_bytes  u32scan_workspace_bytes(U32SCAN_OP_COMPACT, n) bytes.
+ * All pointers need 4-byte alignment. Flags stream by bulk copy when they
+ * have values' alignment mod 16, else by plain loads (same results).
+ * Errors: EINVAL (null values or out with n > 0, misaligned pointers,
+ * n >= 2^31, out overlapping values or flags), EWORKSPACE, ECUDA.
+ */
+int compact_values_u32(const uint32_t *values, const int32_t *flags, size_t n, uint32_t *out,
+                       int32_t *count, void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /*
  * Stable LSD radix-sort permutation of U32 keys.

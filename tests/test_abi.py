@@ -194,3 +194,17 @@ def test_u8heads_rejects_bad_arguments_on_host(lib):
         assert fn(fake + 2, fake, 10, fake + 8000, 10, fake + 9000, fake, need, None) == _native.EINVAL
         assert fn(fake, fake + 4001, 1000, fake + 8000, 10, fake + 9000, None, need, None) == _native.EWORKSPACE
     assert lib.segreduce_u32_u8heads(fake, fake, 10, None, 0, None, fake, need, None) == _native.EINVAL
+
+
+def test_compact_values_rejects_bad_arguments_on_host(lib):
+    fn = lib.compact_values_u32
+    fake = 0x100000
+    need = lib.u32scan_workspace_bytes(_native.OP_COMPACT, 1000)
+    assert fn(None, None, 10, fake, None, fake, need, None) == _native.EINVAL              # no values
+    assert fn(fake, None, 10, None, None, fake, need, None) == _native.EINVAL              # no out
+    assert fn(fake, None, 1000, fake + 400, None, fake, need, None) == _native.EINVAL      # out over values
+    assert fn(fake, fake + 8000, 1000, fake + 9000, None, fake, need, None) == _native.EINVAL  # out over flags
+    assert fn(fake + 2, None, 10, fake + 8000, None, fake, need, None) == _native.EINVAL   # misaligned
+    assert fn(fake, None, 1 << 31, fake + (1 << 34), None, fake, need, None) == _native.EINVAL
+    assert fn(fake, None, 1000, fake + 8000, None, None, need, None) == _native.EWORKSPACE
+    assert fn(fake, None, 1000, fake + 8000, None, fake, 256, None) == _native.EWORKSPACE

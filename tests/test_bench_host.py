@@ -45,6 +45,12 @@ def test_algorithmic_bytes_per_op():
     assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "pairs"])).algorithmic_bytes() == 80 * n25
     assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "keys"])).algorithmic_bytes() == 52 * n25
     assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "keys", "--ties"])).algorithmic_bytes() == 16 * n25
+    cv = bench.make_op(bench.parse_args(["--op", "compact", "--project", "values", "--log2n", "12"]))
+    f = cv.host_inputs()["flags"]
+    assert cv.kept == int((f != 0).sum()) and cv.algorithmic_bytes() == 8 * (1 << 12) + 4 * cv.kept + 4
+    cz = bench.make_op(bench.parse_args(["--op", "compact", "--project", "nonzero", "--log2n", "12"]))
+    v = cz.host_inputs()["values"]
+    assert cz.kept == int((v != 0).sum()) and cz.algorithmic_bytes() == 4 * (1 << 12) + 4 * cz.kept + 4
     runs = bench.make_op(bench.parse_args(["--op", "runs", "--log2n", "12"]))
     c = runs.host_inputs()["counts"]
     assert runs.entries == int(c.sum()) and runs.algorithmic_bytes() == 4 * (1 << 12) + 4 * runs.entries

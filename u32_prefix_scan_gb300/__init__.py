@@ -14,6 +14,7 @@ _API = {
     "segscan_inclusive_u32",
     "segreduce_u32",
     "compact_indices_u32",
+    "compact_values_u32",
     "radix_sort_perm_u32",
     "radix_sort_u32",
     "runs_layout_u32",

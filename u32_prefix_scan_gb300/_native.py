@@ -45,6 +45,7 @@ SIGNATURES = {
     "segscan_inclusive_u32_u8heads": (_int, [_vp, _vp, _sz, _vp, _sz, _vp, _vp, _sz, _vp]),
     "segreduce_u32_u8heads": (_int, [_vp, _vp, _sz, _vp, _sz, _vp, _vp, _sz, _vp]),
     "compact_indices_u32": (_int, [_vp, _sz, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "compact_values_u32": (_int, [_vp, _vp, _sz, _vp, _vp, _vp, _sz, _vp]),
     "radix_sort_perm_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
     "radix_sort_u32": (_int, [_vp, _sz, _vp, _vp, _vp, _sz, _vp]),
     "runs_layout_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp, _sz, _vp]),

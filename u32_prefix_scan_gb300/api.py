@@ -25,6 +25,7 @@ __all__ = [
     "segscan_inclusive_u32",
     "segreduce_u32",
     "compact_indices_u32",
+    "compact_values_u32",
     "radix_sort_perm_u32",
     "radix_sort_u32",
     "runs_layout_u32",
@@ -217,6 +218,31 @@ def compact_indices_u32(flags: torch.Tensor, offsets: torch.Tensor | None = None
         flags.data_ptr(), n, offsets.data_ptr() if offsets is not None else None, indices.data_ptr(),
         count.data_ptr(), ws.ptr, ws.nbytes, sh), "compact_indices_u32")
     return offsets, indices, count
+
+
+def compact_values_u32(values: torch.Tensor, flags: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                       count: torch.Tensor | None = None, *, stream=None, workspace: Workspace | None = None):
+    """The kept values, in order, at the front of `out` (the rest of out is
+    left as it was); an element is kept when its flag is non-zero, or, with
+    no flags, when its value is. Returns (out, count)."""
+    _require_cuda(values, "values")
+    n = values.numel()
+    if flags is not None:
+        _require_cuda(flags, "flags", (torch.int32,))
+        if flags.numel() != n:
+            raise ValueError("values and flags differ in length")
+    if out is None:
+        out = torch.empty_like(values)
+    _require_cuda(out, "out")
+    if out.numel() != n:
+        raise ValueError("out must have n elements")
+    count = _scalar_out(count, values, torch.int32)
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_COMPACT, n, values.device, sh, workspace)
+    _native.check(_native.lib().compact_values_u32(values.data_ptr(), flags.data_ptr() if flags is not None else None,
+                                                   n, out.data_ptr(), count.data_ptr(), ws.ptr, ws.nbytes, sh),
+                  "compact_values_u32")
+    return out, count
 
 
 def radix_sort_perm_u32(keys: torch.Tensor, perm: torch.Tensor | None = None, *, stream=None,

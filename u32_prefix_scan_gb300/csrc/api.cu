@@ -13,8 +13,10 @@ extern "C" size_t u32scan_workspace_bytes(int op, size_t n) {
         return scan_workspace_bytes(n);
     case U32SCAN_OP_SEGSCAN:
         return segscan_workspace_bytes(n);
-    case U32SCAN_OP_COMPACT:
-        return compact_workspace_bytes(n);
+    case U32SCAN_OP_COMPACT: {
+        const size_t a = compact_workspace_bytes(n), b = compact_values_workspace_bytes(n);
+        return a > b ? a : b;
+    }
     case U32SCAN_OP_RADIX:
         return radix_workspace_bytes(n);
     case U32SCAN_OP_RUNS:

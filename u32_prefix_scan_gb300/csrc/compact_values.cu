@@ -236,13 +236,26 @@ compact_values_persistent(const uint32_t *__restrict__ values, const int32_t *__
     }
 }
 
-constexpr int kVThreads = 512, kVStages = 3;
-constexpr int kVVFlags = 4, kVVNonzero = 7;  // u32x4 per lane: 224 KB of shared memory either way
+// Launch shape, chosen by measurement on GB300 and overridable at build time
+// for tuning sweeps: ring stages, and u32x4 per lane with and without flags.
+#ifndef U32SCAN_CV_STAGES
+#define U32SCAN_CV_STAGES 3
+#endif
+#ifndef U32SCAN_CV_VF
+#define U32SCAN_CV_VF 4
+#endif
+#ifndef U32SCAN_CV_VN
+#define U32SCAN_CV_VN 7
+#endif
+constexpr int kVThreads = 512, kVStages = U32SCAN_CV_STAGES;
+constexpr int kVVFlags = U32SCAN_CV_VF, kVVNonzero = U32SCAN_CV_VN;
 constexpr unsigned long long vtile(int v) { return (unsigned long long)kVThreads * v * 4; }
 constexpr size_t vsmem(int v, bool flags) { return ((size_t)kVStages * (flags ? 2 : 1) + 1) * vtile(v) * 4; }
+static_assert(vsmem(kVVFlags, true) <= 227 * 1024 && vsmem(kVVNonzero, false) <= 227 * 1024, "shared memory");
 
 size_t compact_values_workspace_bytes(unsigned long long n) {
-    const unsigned long long tiles = (n + 3 + vtile(kVVFlags) - 1) / vtile(kVVFlags);  // the smaller tile
+    constexpr unsigned long long small = vtile(kVVFlags < kVVNonzero ? kVVFlags : kVVNonzero);
+    const unsigned long long tiles = (n + 3 + small - 1) / small;
     return round_up(kHeaderBytes + 8 * tiles, 256);
 }
 

@@ -72,6 +72,8 @@ def _configure(lib):
     lib.oracle_runs_fill_owner.restype = None
     lib.oracle_compact_values_u32.argtypes = [_u32p, _i32p, _u64, _u32p]
     lib.oracle_compact_values_u32.restype = ctypes.c_uint64
+    lib.oracle_scan_op_u64.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_uint64), _u64]
+    lib.oracle_scan_op_u64.restype = ctypes.c_uint64
     return lib
 
 
@@ -233,3 +235,12 @@ def compact_values(values, flags=None, out=None):
     used = _load().oracle_compact_values_u32(_p(v, _u32p), None if f is None else _p(f, _i32p), v.size,
                                             _p(o, _u32p))
     return o, int(used)
+
+
+def scan_op_u64(a, op: str, inclusive: bool):
+    """(scanned copy, fold) of a uint64 row under one of the CAIRN integer
+    operators (add and mul wrap at 2^64)."""
+    out = np.ascontiguousarray(np.asarray(a, dtype=np.uint64)).copy()
+    total = _load().oracle_scan_op_u64(SCAN_OPS[op], int(bool(inclusive)),
+                                       out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), out.size)
+    return out, int(total)

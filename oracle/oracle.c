@@ -416,3 +416,48 @@ uint64_t oracle_compact_values_u32(const uint32_t *values, const int32_t *flags,
     }
     return used;
 }
+
+/* ------------------------------------------------------------------------
+ * The same operators on uint64 rows.  [CAIRN] "reduce and compact": the
+ * page's reductions run over u64 terms (u64(bytes[i]), mul_wrap(...)), and
+ * add_wrap / mul_wrap wrap at 2^64 there. Exclusive and inclusive as in
+ * oracle_scan_op_u32; returns the fold of all n.
+ * ---------------------------------------------------------------------- */
+
+static uint64_t oracle_apply64(int op, uint64_t x, uint64_t y)
+{
+    switch (op) {
+    case 0: return x + y;
+    case 1: return x * y;
+    case 2: return x & y;
+    case 3: return x | y;
+    case 4: return x ^ y;
+    case 5: return x < y ? x : y;
+    default: return x > y ? x : y;
+    }
+}
+
+static uint64_t oracle_identity64(int op)
+{
+    switch (op) {
+    case 1: return 1u;
+    case 2: case 5: return ~(uint64_t)0;
+    default: return 0u;
+    }
+}
+
+uint64_t oracle_scan_op_u64(int op, int inclusive, uint64_t *a, uint64_t n)
+{
+    uint64_t s = oracle_identity64(op);
+    for (uint64_t j = 0; j < n; ++j) {
+        uint64_t x = a[j];
+        if (inclusive) {
+            s = oracle_apply64(op, s, x);
+            a[j] = s;
+        } else {
+            a[j] = s;
+            s = oracle_apply64(op, s, x);
+        }
+    }
+    return s;
+}

@@ -50,6 +50,9 @@ MUTANTS = [
      "int keep = flags ? flags[i] > 0 : values[i] != 0;", ["cvalues_nonzero"]),
     ("compact_values_projects_index", "out[used++] = values[i];", "out[used++] = (uint32_t)i;",
      ["cvalues_numpy", "golden_compact"]),
+    ("u64_add_truncates_to_32_bits", "case 0: return x + y;\n    case 1: return x * y;\n    case 2: return x & y;\n    case 3: return x | y;\n    case 4: return x ^ y;\n    case 5: return x < y ? x : y;\n    default: return x > y ? x : y;\n    }\n}\n\nstatic uint64_t oracle_identity64",
+     "case 0: return (uint32_t)(x + y);\n    case 1: return x * y;\n    case 2: return x & y;\n    case 3: return x | y;\n    case 4: return x ^ y;\n    case 5: return x < y ? x : y;\n    default: return x > y ? x : y;\n    }\n}\n\nstatic uint64_t oracle_identity64",
+     ["u64_wrap", "u64_numpy_add"]),
 ]
 
 PINS = {
@@ -74,6 +77,8 @@ PINS = {
     "cvalues_nonzero": lambda o: pins.test_compact_values_nonzero_test(o),
     "cvalues_numpy": lambda o: pins.test_compact_values_against_numpy(o, 0.1),
     "golden_compact": lambda o: pins.test_golden_cairn_compact(o),
+    "u64_wrap": lambda o: pins.test_u64_add_wraps_at_2_64_not_2_32(o),
+    "u64_numpy_add": lambda o: pins.test_u64_operator_scans_against_numpy_accumulate(o, "add"),
 }
 
 

@@ -428,3 +428,52 @@ def test_compact_values_brute_force(oracle_mod):
             out, used = oracle_mod.compact_values(v, f, [99] * n)
             kept = [v[i] for i in range(n) if f[i]]
             assert used == len(kept) and out.tolist() == kept + [99] * (n - len(kept))
+
+
+# ------------------------------------------------------------ u64 scans ----
+
+M64 = 1 << 64
+IDENTITY64 = {"add": 0, "mul": 1, "and": M64 - 1, "or": 0, "xor": 0, "min": M64 - 1, "max": 0}
+
+
+@pytest.mark.parametrize("op", sorted(NP_ACCUM))
+def test_u64_operator_scans_against_numpy_accumulate(oracle_mod, op):
+    a = inputs.scan_values_u64(50003, 1)
+    if op == "mul":
+        a = a | np.uint64(1)
+    want_inc = NP_ACCUM[op].accumulate(a, dtype=np.uint64)
+    want_ex = np.concatenate([[np.uint64(IDENTITY64[op])], want_inc[:-1]]).astype(np.uint64)
+    inc, tinc = oracle_mod.scan_op_u64(a, op, True)
+    ex, tex = oracle_mod.scan_op_u64(a, op, False)
+    assert np.array_equal(inc, want_inc) and np.array_equal(ex, want_ex)
+    assert tinc == tex == int(want_inc[-1])
+    e, te = oracle_mod.scan_op_u64(np.zeros(0, np.uint64), op, False)
+    assert e.size == 0 and te == IDENTITY64[op]
+
+
+def test_u64_add_wraps_at_2_64_not_2_32(oracle_mod):
+    # iota times 2^40: the sums pass 2^64 within 2^24 + 1 terms
+    n = (1 << 24) + 1000
+    a = np.arange(n, dtype=np.uint64) << np.uint64(40)
+    out, total = oracle_mod.scan_op_u64(a, "add", False)
+    for j in (1, 1 << 12, 1 << 23, (1 << 24) + 999):
+        assert int(out[j]) == ((j * (j - 1) // 2) << 40) % M64
+    assert total == ((n * (n - 1) // 2) << 40) % M64
+
+
+def test_u64_brute_force(oracle_mod):
+    import functools
+    import operator
+
+    fns = {"add": lambda x, y: (x + y) % M64, "mul": lambda x, y: (x * y) % M64, "and": operator.and_,
+           "or": operator.or_, "xor": operator.xor, "min": min, "max": max}
+    rng = np.random.default_rng(6)
+    for op, f in fns.items():
+        for n in range(0, 10):
+            a = [int(x) for x in rng.integers(0, M64, size=n, dtype=np.uint64)]
+            inc, t = oracle_mod.scan_op_u64(a, op, True)
+            ex, _ = oracle_mod.scan_op_u64(a, op, False)
+            want = [functools.reduce(f, a[: j + 1]) for j in range(n)]
+            assert inc.tolist() == want
+            assert ex.tolist() == [IDENTITY64[op]] + want[:-1] if n else ex.tolist() == []
+            assert t == (want[-1] if n else IDENTITY64[op])

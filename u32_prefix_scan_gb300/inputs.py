@@ -26,6 +26,8 @@ Workloads (one per configuration of the benchmark suite):
                index 0 always a head, or every 4th index (length-4 segments)
 * compaction:  int32 flags, 1 where u32(4, 1, i) < T, T = round(p * 2^32)
 * radix:       keys u32(5, 0, i); tie-heavy variant u32 >> 24 in [0, 256)
+* u64 scans:   values u32(seed, 0, 2i) << 32 | u32(seed, 0, 2i + 1), uniform
+               over [0, 2^64)
 * runs:        per-owner counts from u32(6, 0, i) = d: uniform d >> 29 in
                [0, 8) (mean 3.5, one owner in eight empty), or skewed: d >> 26
                in [0, 64) when d & 15 == 0, else 0 (one owner in sixteen
@@ -47,6 +49,7 @@ __all__ = [
     "compact_flags",
     "radix_keys",
     "run_counts",
+    "scan_values_u64",
     "COMPACT_THRESHOLD",
 ]
 
@@ -139,3 +142,9 @@ def run_counts(n: int, seed: int, skewed: bool = False) -> np.ndarray:
     if not skewed:
         return d >> np.uint32(29)
     return np.where((d & np.uint32(15)) == 0, d >> np.uint32(26), np.uint32(0)).astype(np.uint32)
+
+
+def scan_values_u64(n: int, seed: int) -> np.ndarray:
+    """uint64 scan input: two consecutive u32 draws per element (high, low)."""
+    d = splitmix_u32(seed, 0, 2 * n).astype(np.uint64)
+    return (d[0::2] << np.uint64(32)) | d[1::2]

@@ -23,6 +23,8 @@ Other ops time the other primitives on their own workloads:
   radix           radix_sort_perm_u32, n = 2^25 keys seed 5, uniform u32
                   or (--ties) in [0, 256); --sort pairs|keys times
                   radix_sort_u32 writing sorted keys (+ perm unless keys)
+  scan64          scan_u64_op in place, n = 2^27 uint64, --monoid64 (add),
+                  exclusive or --inclusive
   runs            runs_layout_u32 + runs_owner_u32, n = 2^25 owners, counts
                   u32(6,0,i) >> 29 in [0, 8) or (--skewed) one owner in 16
                   holding up to 63 entries
@@ -170,6 +172,78 @@ class ScanOp(Op):
             return
         f = lib.oracle_scan_inclusive_u32 if self.inclusive else lib.oracle_scan_exclusive_u32
         f(ptr, arrays["data"].size)
+
+
+class Scan64Op(Op):
+    """scan_u64_op in place on a 2^27-element (1 GiB) uint64 row."""
+
+    log2n = 27
+    kernel_sources = ["u32_prefix_scan_gb300/csrc/scan64.cu", "u32_prefix_scan_gb300/csrc/internal.cuh"]
+
+    def __init__(self, args):
+        super().__init__(args)
+        self.inclusive = args.inclusive
+        self.monoid = args.monoid64
+        form = "inclusive" if self.inclusive else "exclusive"
+        self.name = f"scan_u64_{self.monoid}_{form}"
+        self.metric = f"U64 {self.monoid} {form} scan Gelem/s and HBM GB/s (fraction of peak) at n=2^27, 1 GB300"
+        self.kernel = f"scan_u64_persistent<512,8,2,{form},{self.monoid}> (bulk-copy stores)"
+
+    def workload(self):
+        form = "inclusive" if self.inclusive else "exclusive"
+        return (f"u64 {self.monoid}-{form} scan in place + fold, n=2^{self.n.bit_length() - 1}, "
+                f"uniform u64 seed 2 (two u32 draws per element)")
+
+    def algorithmic_bytes(self):
+        return 16 * self.n  # read 8 + write 8 per element
+
+    def host_inputs(self):
+        from u32_prefix_scan_gb300 import inputs
+
+        return {"data": inputs.scan_values_u64(self.n, 2)}
+
+    def setup(self, dev, host):
+        import numpy as np
+        import torch
+
+        import u32_prefix_scan_gb300 as u
+        from u32_prefix_scan_gb300 import _native
+
+        self.u = u
+        self.data = torch.from_numpy(host["data"].view(np.int64)).to(dev)
+        self.total = torch.empty(1, dtype=torch.int64, device=dev)
+        self.ws = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_SCAN64, self.n), dev)
+        self.pinned_in = {"data": torch.from_numpy(host["data"].view(np.int64)).pin_memory()}
+        self.pinned_out = {"data": torch.empty(self.n, dtype=torch.int64).pin_memory(),
+                           "total": torch.empty(1, dtype=torch.int64).pin_memory()}
+
+    def step(self):
+        self.u.scan_u64_op(self.data, self.monoid, self.inclusive, self.total, workspace=self.ws)
+
+    def e2e_step(self):
+        self.data.copy_(self.pinned_in["data"], non_blocking=True)
+        self.step()
+        self.pinned_out["data"].copy_(self.data, non_blocking=True)
+        self.pinned_out["total"].copy_(self.total, non_blocking=True)
+        return 8 * self.n, 8 * self.n + 8
+
+    def check_e2e(self, host):
+        import numpy as np
+
+        if self.monoid != "add":
+            return True  # checked bit for bit by the GPU tests
+        k = min(self.n, 1 << 20)
+        got = self.pinned_out["data"][:k].numpy().view(np.uint64)
+        a = host["data"][:k]
+        if self.inclusive:
+            return got[0] == a[0] and np.array_equal(got[1:] - got[:-1], a[1:])
+        return got[0] == 0 and np.array_equal(got[1:] - got[:-1], a[:-1])
+
+    def oracle_step(self, lib, arrays):
+        codes = {"add": 0, "mul": 1, "and": 2, "or": 3, "xor": 4, "min": 5, "max": 6}
+        a = arrays["data"]
+        lib.oracle_scan_op_u64(codes[self.monoid], int(self.inclusive),
+                               a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), a.size)
 
 
 class SegOp(Op):
@@ -655,8 +729,8 @@ class RunsOp(Op):
                                    arrays["slots"].ctypes.data_as(i32p), entries)
 
 
-OPS = ["scan_exclusive", "scan_inclusive", "scan_op", "segscan", "segscan_sums", "segreduce", "compact", "radix",
-       "runs"]
+OPS = ["scan_exclusive", "scan_inclusive", "scan_op", "scan64", "segscan", "segscan_sums", "segreduce", "compact",
+       "radix", "runs"]
 
 
 def make_op(args) -> Op:
@@ -670,6 +744,8 @@ def make_op(args) -> Op:
         return RadixOp(args)
     if args.op == "runs":
         return RunsOp(args)
+    if args.op == "scan64":
+        return Scan64Op(args)
     return SegOp(args, args.op)
 
 
@@ -690,6 +766,8 @@ def parse_args(argv=None):
     p.add_argument("--project", choices=["indices", "values", "nonzero"], default="indices",
                    help="compact: kept indices (offsets, -1 tail), kept values by flags, or kept non-zero values")
     p.add_argument("--u8heads", action="store_true", help="segmented ops: one byte per head flag")
+    p.add_argument("--monoid64", choices=["add", "mul", "and", "or", "xor", "min", "max"], default="add",
+                   help="scan64: the operator")
     p.add_argument("--skewed", action="store_true", help="runs: the skewed count mix instead of uniform [0, 8)")
     p.add_argument("--monoid", choices=["add", "mul", "and", "or", "xor", "min", "max"], default="max",
                    help="scan_op: the operator")

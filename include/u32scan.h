@@ -67,6 +67,7 @@ typedef struct CUstream_st *u32scan_stream_t;
 #define U32SCAN_OP_COMPACT 3   /* compact_indices_u32, compact_values_u32 */
 #define U32SCAN_OP_RADIX 4     /* radix_sort_perm_u32, radix_sort_u32 */
 #define U32SCAN_OP_RUNS 5      /* runs_layout_u32 (runs_owner_u32 needs none) */
+#define U32SCAN_OP_SCAN64 6    /* scan_u64_op */
 
 /* Bytes of device workspace an operation needs for n elements (a multiple
  * of 256, at least 256). Returns 0 for an unknown op. Pure host function. */
@@ -128,6 +129,23 @@ int scan_inclusive_u32(uint32_t *data, size_t n, uint32_t *total,
  * Errors: EINVAL for an unknown op, and as scan_exclusive_u32.
  */
 int scan_u32_op(int op, int inclusive, uint32_t *data, size_t n, uint32_t *total,
+                void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * The same scans on uint64 rows. Source: CAIRN "Concurrency" page, sections
+ * "reduce and compact" (integer operators; its examples reduce u64 terms)
+ * and "scan". add_wrap and mul_wrap wrap at 2^64.
+ *   op, inclusive  as scan_u32_op.
+ *   data     device, uint64_t[n], 8-byte aligned; scanned in place.
+ *   n        element count, below 2^32.
+ *   total    device, one uint64_t (8-byte aligned) or NULL: the fold of all n
+ *            elements (the identity when n == 0).
+ *   ws, ws_bytes  u32scan_workspace_bytes(U32SCAN_OP_SCAN64, n) bytes,
+ *            256-byte aligned, zero-filled once; reusable in stream order.
+ * Errors: EINVAL (unknown op, null data with n > 0, misaligned pointers,
+ * n >= 2^32), EWORKSPACE, ECUDA; a look-back timeout as the u32 scans'.
+ */
+int scan_u64_op(int op, int inclusive, uint64_t *data, size_t n, uint64_t *total,
                 void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /*

@@ -208,3 +208,17 @@ def test_compact_values_rejects_bad_arguments_on_host(lib):
     assert fn(fake, None, 1 << 31, fake + (1 << 34), None, fake, need, None) == _native.EINVAL
     assert fn(fake, None, 1000, fake + 8000, None, None, need, None) == _native.EWORKSPACE
     assert fn(fake, None, 1000, fake + 8000, None, fake, 256, None) == _native.EWORKSPACE
+
+
+def test_scan_u64_rejects_bad_arguments_on_host(lib):
+    fn = lib.scan_u64_op
+    fake = 0x100000
+    need = lib.u32scan_workspace_bytes(_native.OP_SCAN64, 1000)
+    assert need >= 256 + 16 and need % 256 == 0
+    assert fn(7, 0, fake, 1000, None, fake, need, None) == _native.EINVAL        # unknown op
+    assert fn(0, 0, None, 10, None, fake, need, None) == _native.EINVAL          # no data
+    assert fn(0, 0, fake + 4, 10, None, fake, need, None) == _native.EINVAL      # 4-byte aligned only
+    assert fn(0, 1, fake, 10, fake + 12, fake, need, None) == _native.EINVAL     # misaligned total
+    assert fn(0, 0, fake, 1 << 32, None, fake, need, None) == _native.EINVAL
+    assert fn(0, 0, fake, 1000, None, None, need, None) == _native.EWORKSPACE
+    assert fn(0, 0, fake, 1000, None, fake + 8, need, None) == _native.EWORKSPACE  # misaligned workspace

@@ -54,6 +54,7 @@ def test_algorithmic_bytes_per_op():
     runs = bench.make_op(bench.parse_args(["--op", "runs", "--log2n", "12"]))
     c = runs.host_inputs()["counts"]
     assert runs.entries == int(c.sum()) and runs.algorithmic_bytes() == 4 * (1 << 12) + 4 * runs.entries
+    assert bench.make_op(bench.parse_args(["--op", "scan64"])).algorithmic_bytes() == 16 * n27
     assert bench.make_op(bench.parse_args(["--log2n", "20"])).n == 1 << 20
 
 

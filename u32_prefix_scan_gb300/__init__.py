@@ -11,6 +11,7 @@ _API = {
     "scan_exclusive_u32",
     "scan_inclusive_u32",
     "scan_u32_op",
+    "scan_u64_op",
     "segscan_inclusive_u32",
     "segreduce_u32",
     "compact_indices_u32",

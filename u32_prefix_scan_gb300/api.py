@@ -22,6 +22,7 @@ __all__ = [
     "scan_exclusive_u32",
     "scan_inclusive_u32",
     "scan_u32_op",
+    "scan_u64_op",
     "segscan_inclusive_u32",
     "segreduce_u32",
     "compact_indices_u32",
@@ -140,6 +141,26 @@ def scan_u32_op(data: torch.Tensor, op: str, inclusive: bool = False, total: tor
     ws = _ws(_native.OP_SCAN, n, data.device, sh, workspace)
     _native.check(_native.lib().scan_u32_op(_native.SCAN_OPS[op], int(bool(inclusive)), data.data_ptr(), n,
                                             total.data_ptr(), ws.ptr, ws.nbytes, sh), "scan_u32_op")
+    return total
+
+
+def scan_u64_op(data: torch.Tensor, op: str = "add", inclusive: bool = False, total: torch.Tensor | None = None,
+                *, stream=None, workspace: Workspace | None = None) -> torch.Tensor:
+    """In place scan of a 64-bit row (int64 or uint64 bits) under op in
+    {add, mul, and, or, xor, min, max}, unsigned, add and mul wrapping at
+    2^64. Returns the one-element device tensor holding the fold."""
+    if op not in _native.SCAN_OPS:
+        raise ValueError(f"op must be one of {sorted(_native.SCAN_OPS)}")
+    u64 = (torch.int64, getattr(torch, "uint64", torch.int64))
+    _require_cuda(data, "data", u64)
+    if total is None:
+        total = torch.empty(1, dtype=data.dtype, device=data.device)
+    _require_cuda(total, "total", u64)
+    n = data.numel()
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_SCAN64, n, data.device, sh, workspace)
+    _native.check(_native.lib().scan_u64_op(_native.SCAN_OPS[op], int(bool(inclusive)), data.data_ptr(), n,
+                                            total.data_ptr(), ws.ptr, ws.nbytes, sh), "scan_u64_op")
     return total
 
 

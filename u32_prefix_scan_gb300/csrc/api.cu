@@ -21,6 +21,8 @@ extern "C" size_t u32scan_workspace_bytes(int op, size_t n) {
         return radix_workspace_bytes(n);
     case U32SCAN_OP_RUNS:
         return scan_workspace_bytes(n);
+    case U32SCAN_OP_SCAN64:
+        return scan64_workspace_bytes(n);
     default:
         return 0;
     }

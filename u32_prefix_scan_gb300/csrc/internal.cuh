@@ -443,6 +443,7 @@ size_t segscan_workspace_bytes(unsigned long long n);
 size_t compact_workspace_bytes(unsigned long long n);
 size_t radix_workspace_bytes(unsigned long long n);
 size_t compact_values_workspace_bytes(unsigned long long n);
+size_t scan64_workspace_bytes(unsigned long long n);
 
 // In-library launch of the exclusive scan (no total), for operations built
 // on it.

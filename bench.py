@@ -35,7 +35,10 @@ value      elements processed per second over all ranks (Gelem/s), timed
            with CUDA events on the launching stream, max over ranks.
 roofline   algorithmic bytes of one launch over its measured time, against
            the measured HBM copy peak in MEASURED_PEAKS.json (fallback
-           6800 GB/s when absent).
+           6800 GB/s when absent); also against a device copy timed in the
+           same run (copy_gbs_same_run) and the nominal 7900 GB/s. For a
+           step of several calls the dominant kernel is bracketed by its
+           own events (kernel_ms).
 e2e        the same metric through the same C-ABI call, with pinned host
            inputs copied in and the outputs copied out every step.
 cpu_baseline  the CPU oracle (one thread, as it stands) on a bounded sample.
@@ -805,6 +808,45 @@ def load_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
+
+
+def host_cpu() -> str:
+    """The host CPU's model name (context for the CPU baseline)."""
+    try:
+        for line in open("/proc/cpuinfo"):
+            key, _, val = line.partition(":")
+            if key.strip() in ("model name", "CPU part", "Model"):
+                return val.strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.machine()
+
+
+def copy_peak_gbs(dev, nbytes: int = 1 << 30, reps: int = 20) -> float:
+    """Device-to-device copy bandwidth measured now, on this GPU: read +
+    write bytes of `reps` copies of a 1 GiB buffer over their event time."""
+    import torch
+
+    a = torch.empty(nbytes // 4, dtype=torch.int32, device=dev)
+    b = torch.empty_like(a)
+    a.fill_(1)
+    for _ in range(3):
+        b.copy_(a)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        b.copy_(a)
+    e1.record()
+    torch.cuda.synchronize()
+    gbs = 2 * nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del a, b
+    return gbs
+
+
 def load_traffic(op: Op):
     """ncu DRAM bytes per launch, if captured for the current kernel source
     at this workload size."""
@@ -942,7 +984,8 @@ def run_reference(args, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
         "config": {"workload": op.workload(), "n": op.n, "op": args.op, "sample_per_step": sample},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
+                         "host_cpu": host_cpu(), "host_nproc": os.cpu_count()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -1013,6 +1056,7 @@ def run_ours(args, rank, local_rank, world):
     peak, peak_kind = load_peak()
     nbytes = op.algorithmic_bytes()
     achieved = nbytes / (kernel_ms * 1e-3) / 1e9
+    copy_now = copy_peak_gbs(dev)
     full = op.n == 1 << op.log2n
     result = {
         "metric": op.metric,
@@ -1034,7 +1078,8 @@ def run_ours(args, rank, local_rank, world):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": load_traffic(op), "algorithmic_bytes_per_launch": nbytes, "kernel": op.kernel,
-                     "kernel_ms": kernel_ms},
+                     "kernel_ms": kernel_ms, "copy_gbs_same_run": copy_now, "frac_of_same_run_copy": achieved / copy_now,
+                     "nominal_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS},
         "e2e": {"value": world * op.n / (e2e_ms * 1e-3) / 1e9 if e2e_ms else None, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks,
@@ -1043,6 +1088,7 @@ def run_ours(args, rank, local_rank, world):
     if rank == 0 and not args.no_cpu_baseline:
         v, reps, el = time_oracle(op, host, args.cpu_seconds, op.n)
         result["cpu_baseline"] = {"value": v / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                  "host_cpu": host_cpu(), "host_nproc": os.cpu_count(),
                                   "sample": f"{op.name} oracle over the full workload "
                                             f"(n=2^{op.n.bit_length() - 1}), {reps} repetitions in {el:.1f} s"}
     return result

@@ -525,7 +525,7 @@ class CompactValuesOp(Op):
 
 class RadixOp(Op):
     log2n = 25
-    launches_per_step = 15  # histogram, plan, 4 x (upsweep, table scan, downsweep), final copy
+    launches_per_step = 7  # histogram, plan, 4 digit passes (inactive ones return at once), final copy
     kernel_sources = ["u32_prefix_scan_gb300/csrc/radix.cu", "u32_prefix_scan_gb300/csrc/scan.cu",
                       "u32_prefix_scan_gb300/csrc/internal.cuh"]
 
@@ -541,7 +541,7 @@ class RadixOp(Op):
         what = {"perm": "radix-sort permutation", "pairs": "radix sort (keys + permutation)",
                 "keys": "radix sort (keys only)"}[self.mode]
         self.metric = f"stable LSD {what} Gelem/s at n=2^25 ({keys}), 1 GB300"
-        self.kernel = "radix_downsweep_kernel + radix_upsweep_kernel (per active 8-bit digit)"
+        self.kernel = "radix path: histogram + radix_onesweep_kernel per active 8-bit digit"
 
     def workload(self):
         keys = "u32(5,0,i) >> 24, in [0,256)" if self.ties else "u32(5,0,i), uniform"
@@ -552,15 +552,14 @@ class RadixOp(Op):
 
     def algorithmic_bytes(self):
         # this design's bytes: a 4-byte histogram read, then per active digit
-        # an upsweep read of the keys (4) and a downsweep that reads keys (4)
-        # and, when indices are produced, reads them (4, not on the first
-        # pass) and writes them (4); keys are written (4) on every pass but
-        # the last of the permutation-only sort
+        # one pass that reads the keys (4) and, when indices are produced,
+        # reads them (4, not on the first pass) and writes them (4); keys are
+        # written (4) on every pass but the last of the permutation-only sort
         m, n = self.passes(), self.n
         idx = self.mode != "keys"
         total = 4
         for j in range(m):
-            total += 8
+            total += 4
             if idx:
                 total += (4 if j else 0) + 4
             if j < m - 1 or self.mode != "perm":

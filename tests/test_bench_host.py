@@ -40,11 +40,11 @@ def test_algorithmic_bytes_per_op():
     seg8.nseg = 5
     assert seg8.algorithmic_bytes() == 9 * n26
     assert bench.make_op(bench.parse_args(["--op", "compact"])).algorithmic_bytes() == 12 * n27 + 4
-    assert bench.make_op(bench.parse_args(["--op", "radix"])).algorithmic_bytes() == 76 * n25
-    assert bench.make_op(bench.parse_args(["--op", "radix", "--ties"])).algorithmic_bytes() == 16 * n25
-    assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "pairs"])).algorithmic_bytes() == 80 * n25
-    assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "keys"])).algorithmic_bytes() == 52 * n25
-    assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "keys", "--ties"])).algorithmic_bytes() == 16 * n25
+    assert bench.make_op(bench.parse_args(["--op", "radix"])).algorithmic_bytes() == 60 * n25
+    assert bench.make_op(bench.parse_args(["--op", "radix", "--ties"])).algorithmic_bytes() == 12 * n25
+    assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "pairs"])).algorithmic_bytes() == 64 * n25
+    assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "keys"])).algorithmic_bytes() == 36 * n25
+    assert bench.make_op(bench.parse_args(["--op", "radix", "--sort", "keys", "--ties"])).algorithmic_bytes() == 12 * n25
     cv = bench.make_op(bench.parse_args(["--op", "compact", "--project", "values", "--log2n", "12"]))
     f = cv.host_inputs()["flags"]
     assert cv.kept == int((f != 0).sum()) and cv.algorithmic_bytes() == 8 * (1 << 12) + 4 * cv.kept + 4

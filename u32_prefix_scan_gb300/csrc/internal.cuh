@@ -445,9 +445,7 @@ size_t radix_workspace_bytes(unsigned long long n);
 size_t compact_values_workspace_bytes(unsigned long long n);
 size_t scan64_workspace_bytes(unsigned long long n);
 
-// In-library launch of the exclusive scan (no total), for operations built
-// on it.
-int scan_exclusive_launch(uint32_t *data, unsigned long long n, void *ws, size_t ws_bytes, cudaStream_t stream);
+// In-library launch of the inclusive scan with its total (the runs layout).
 int scan_inclusive_launch(uint32_t *data, unsigned long long n, uint32_t *total, void *ws, size_t ws_bytes,
                           cudaStream_t stream);
 

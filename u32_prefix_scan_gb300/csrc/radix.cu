@@ -11,21 +11,23 @@
 // Here a pass handles an 8-bit digit instead of one bit: a stable pass over
 // a digit is the composition of the eight stable one-bit passes over its
 // bits, so the result is the same unique stable permutation with 4 passes
-// instead of 32. Per digit pass:
-//   upsweep    each 8192-key tile counts its keys per digit value (warp
-//              match-any ranking into per-warp counters in shared memory) and
-//              writes the 256 counts into a digit-major table;
-//   scan       one exclusive scan of that table (the library's own scan
-//              kernel) gives every (digit value, tile) its first output slot:
-//              all smaller digit values first, then earlier tiles;
-//   downsweep  each tile ranks its keys stably within the tile and scatters
-//              (key, index) pairs to their slots.
-// A histogram of all four digits, taken first, finds digits that are equal
-// for every key; their passes are skipped (exact: such a pass moves
-// nothing). Which passes run, and which buffers they read and write, is
-// decided on the device, so the call stays asynchronous. The last pass
-// writes the indices into `perm` and, for radix_sort_u32, the sorted keys
-// into `keys_out`; a keys-only sort moves no indices at all.
+// instead of 32. A histogram of all four digits, taken first in one read of
+// the keys, gives every pass its digit bases (keys with a smaller digit
+// value come first) and finds digits that are equal for every key, whose
+// passes are skipped (exact: such a pass moves nothing). Each digit pass is
+// then one kernel over tiles of 8192 keys drawn in order: a tile ranks its
+// keys stably within itself (eight ballots per 32 keys give each key its
+// rank among the warp's keys of its digit value), publishes its 256 digit
+// counts, and finds for every digit value the count of that value in all
+// earlier tiles by a decoupled look-back (thread v walks back over the
+// earlier tiles' words for value v, several a round trip, until one holds an
+// inclusive count), so
+// each key's slot is base + earlier count + rank; the tile is ordered by
+// digit value in shared memory and written out run by run. Which passes run,
+// and which buffers they read and write, is decided on the device, so the
+// call stays asynchronous. The last pass writes the indices into `perm` and,
+// for radix_sort_u32, the sorted keys into `keys_out`; a keys-only sort moves
+// no indices at all.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -38,6 +40,13 @@ constexpr int kRThreads = 512;
 constexpr int kRKeys = 16;  // keys per thread per tile
 constexpr unsigned int kRTile = kRThreads * kRKeys;
 constexpr int kRWarps = kRThreads / 32;
+#ifndef U32SCAN_R_MATCH
+#define U32SCAN_R_MATCH 0  // 1: rank by the match-any instruction instead of eight ballots
+#endif
+#ifndef U32SCAN_R_LOOK
+#define U32SCAN_R_LOOK 8
+#endif
+constexpr int kRLook = U32SCAN_R_LOOK;  // earlier tiles read per look-back round trip
 
 // One pass's role, decided on the device from the histograms.
 struct RadixPlan {
@@ -47,26 +56,24 @@ struct RadixPlan {
     int pad;
 };
 
-// Workspace layout for n keys (all regions 256-byte aligned). It starts
-// with the table scan's own workspace, whose 256-byte header (tile counter,
-// call epoch, device status) is the header every operation keeps at offset
-// 0, so u32scan_check reads the status of this call and the workspace stays
-// valid for any operation afterwards.
+// Workspace layout for n keys (all regions 256-byte aligned): the 256-byte
+// header every operation keeps at offset 0 (tile counter, call epoch,
+// device status), the histograms, the digit bases, the plan, one carry word
+// per (tile, digit value), and the ping-pong buffers.
 struct RadixLayout {
-    size_t scan_ws, hist, plan, table, k1, k2, i1, total;
+    size_t hist, bases, plan, desc, k1, k2, i1, total;
     unsigned int n_tiles;
     explicit RadixLayout(unsigned long long n) {
         n_tiles = (unsigned int)((n + kRTile - 1) / kRTile);
-        const unsigned long long cells = 256ull * n_tiles;
-        size_t o = 0;
-        scan_ws = o;
-        o += scan_workspace_bytes(cells);
+        size_t o = kHeaderBytes;
         hist = o;
+        o += round_up(4 * 256 * 4, 256);
+        bases = o;
         o += round_up(4 * 256 * 4, 256);
         plan = o;
         o += round_up(4 * sizeof(RadixPlan), 256);
-        table = o;
-        o += round_up(4 * cells, 256);
+        desc = o;
+        o += round_up(8ull * 256 * n_tiles, 256);
         k1 = o;
         o += round_up(4 * n, 256);
         k2 = o;
@@ -124,24 +131,39 @@ __global__ void radix_histogram_kernel(const uint32_t *__restrict__ keys, unsign
     }
 }
 
-// One warp: a digit is constant when one value holds all n keys.
-__global__ void radix_plan_kernel(const unsigned int *__restrict__ hist, unsigned long long n, RadixPlan *plan) {
-    const int lane = threadIdx.x & 31;
-    int active[4];
-    int m = 0;
-    for (int p = 0; p < 4; ++p) {
-        bool whole = false;
-        for (int b = lane; b < 256; b += 32) whole = whole || hist[256 * p + b] == n;
-        active[p] = __any_sync(0xffffffffu, whole) ? 0 : 1;
-        m += active[p];
+// Four warps, one per digit: a digit is constant when one value holds all
+// n keys; each pass's base for digit value v is the number of keys whose
+// digit is below v (an exclusive scan of that digit's histogram).
+__global__ void __launch_bounds__(128) radix_plan_kernel(const unsigned int *__restrict__ hist,
+                                                         unsigned long long n, RadixPlan *plan,
+                                                         unsigned int *__restrict__ bases) {
+    __shared__ int s_active[4];
+    const int lane = threadIdx.x & 31, p = threadIdx.x >> 5;
+    // lane l holds digit values 8l .. 8l+7
+    unsigned int c[8], sum = 0;
+    bool whole = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        c[i] = hist[256 * p + 8 * lane + i];
+        sum += c[i];
+        whole = whole || c[i] == n;
     }
-    if (lane == 0) {
-        int j = 0;
-        for (int p = 0; p < 4; ++p) {
-            plan[p].active = active[p];
-            plan[p].j = j;
-            plan[p].m = m;
-            j += active[p];
+    const bool active = !__any_sync(0xffffffffu, whole);
+    unsigned int run = warp_inclusive_sum(sum, lane) - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        bases[256 * p + 8 * lane + i] = run;
+        run += c[i];
+    }
+    if (lane == 0) s_active[p] = active ? 1 : 0;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int j = 0, m = s_active[0] + s_active[1] + s_active[2] + s_active[3];
+        for (int q = 0; q < 4; ++q) {
+            plan[q].active = s_active[q];
+            plan[q].j = j;
+            plan[q].m = m;
+            j += s_active[q];
         }
     }
 }
@@ -208,6 +230,10 @@ __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restri
         // the same for validity
         const bool valid = (valid_bits >> r) & 1u;
         const unsigned int dr = (k[r] >> shift) & 255u;
+#if U32SCAN_R_MATCH
+        // invalid lanes get a label no valid digit has
+        const unsigned int same = __match_any_sync(0xffffffffu, valid ? dr : 256u);
+#else
         const unsigned int vb = __ballot_sync(0xffffffffu, valid);
         unsigned int same = valid ? vb : ~vb;
 #pragma unroll
@@ -216,6 +242,7 @@ __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restri
             const unsigned int bb = __ballot_sync(0xffffffffu, bit);
             same &= bit ? bb : ~bb;
         }
+#endif
         const unsigned int below = (unsigned int)__popc(same & lanemask_lt(lane));
         unsigned int old = 0;
         if (valid) old = s_cnt[warp][dr];
@@ -227,66 +254,48 @@ __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restri
     return valid_bits;
 }
 
-// Upsweep of one pass: the tile's count of each digit value, written into
-// the digit-major table. Counting needs no ranks, so each warp adds its keys
-// into its own row of shared-memory counters with atomics.
+// One digit pass over tile t (drawn in order): rank, carry each digit
+// value's count across tiles by decoupled look-back, order the tile by
+// digit value in shared memory, write each value's run of (key, index)
+// pairs to consecutive slots. Carry word of (tile t, value v) at
+// desc[256 t + v] (tile-major: the 32 values of a warp read 32 consecutive
+// words for each earlier tile): the library's tagged format, value = the
+// tile's count of v (aggregate) or the count of v in tiles 0..t (inclusive,
+// P bit).
 __global__ void __launch_bounds__(kRThreads, 2)
-radix_upsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
-                     int32_t *i1, int32_t *perm, uint32_t *keys_out, unsigned long long n, unsigned int n_tiles,
-                     unsigned int *__restrict__ table) {
-    const RadixPlan pl = plan[p];
-    if (!pl.active) return;
-    __shared__ unsigned int s_cnt[kRWarps][256];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm, keys_out);
-    for (int i = lane; i < 256; i += 32) s_cnt[warp][i] = 0;
-    __syncwarp();
-    const unsigned long long base = (unsigned long long)blockIdx.x * kRTile + (unsigned long long)warp * (32 * kRKeys);
-    uint32_t k[kRKeys];
-#pragma unroll
-    for (int r = 0; r < kRKeys; ++r) {
-        const unsigned long long e = base + 32 * r + lane;
-        k[r] = e < n ? b.in_keys[e] : 0u;
-    }
-    const int shift = 8 * p;
-#pragma unroll
-    for (int r = 0; r < kRKeys; ++r)
-        if (base + 32 * r + lane < n) atomicAdd(&s_cnt[warp][(k[r] >> shift) & 255u], 1u);
-    __syncthreads();
-    for (int v = threadIdx.x; v < 256; v += kRThreads) {
-        unsigned int c = 0;
-#pragma unroll
-        for (int w = 0; w < kRWarps; ++w) c += s_cnt[w][v];
-        table[(unsigned long long)v * n_tiles + blockIdx.x] = c;
-    }
-}
-
-// Downsweep of one pass: rank the tile, order it by digit value in shared
-// memory (stable), then write each digit value's run of (key, index) pairs
-// to its slots with consecutive threads on consecutive slots.
-__global__ void __launch_bounds__(kRThreads, 2)
-radix_downsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
-                       int32_t *i1, int32_t *perm, uint32_t *keys_out, unsigned long long n, unsigned int n_tiles,
-                       const unsigned int *__restrict__ slots) {
+radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
+                      int32_t *i1, int32_t *perm, uint32_t *keys_out, unsigned long long n, unsigned int n_tiles,
+                      const unsigned int *__restrict__ bases, WsHeader *hdr, unsigned long long *desc,
+                      unsigned long long limit_ns) {
     const RadixPlan pl = plan[p];
     if (!pl.active) return;
     extern __shared__ __align__(16) unsigned int r_smem[];
     unsigned int(*s_cnt)[256] = reinterpret_cast<unsigned int(*)[256]>(r_smem);  // [kRWarps][256]
-    unsigned int *s_tileoff = r_smem + kRWarps * 256;                           // [256] digit start in tile
-    unsigned int *s_glob = s_tileoff + 256;                                     // [256] digit's first slot
-    unsigned int *s_keys = s_glob + 256;                                        // [kRTile]
+    unsigned int *s_tileoff = r_smem + kRWarps * 256;                           // [256] value's start in tile
+    unsigned int *s_delta = s_tileoff + 256;                                    // [256] first slot - start
+    unsigned int *s_keys = s_delta + 256;                                       // [kRTile]
     int32_t *s_idx = reinterpret_cast<int32_t *>(s_keys + kRTile);              // [kRTile]
     __shared__ unsigned int s_part[kRThreads / 32];
+    __shared__ unsigned int s_t, s_epoch;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned int t = blockIdx.x;
+    if (threadIdx.x == 0) {
+        unsigned int e;
+        s_t = draw_tile(hdr, n_tiles, &e);
+        s_epoch = e;
+    }
+    __syncthreads();
+    const unsigned int t = s_t;
+    const unsigned long long tag = tag_of(s_epoch);
     const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm, keys_out);
     uint32_t k[kRKeys];
     unsigned int wrank[kRKeys];
-    const unsigned int valid_bits = radix_rank_tile(b.in_keys, n, t, 8 * p, k, wrank, s_cnt, lane, warp);
+    const int shift = 8 * p;
+    const unsigned int valid_bits = radix_rank_tile(b.in_keys, n, t, shift, k, wrank, s_cnt, lane, warp);
     __syncthreads();
     // Per digit value v (threads 0..255): warp offsets within the value's
-    // run in this tile, and the run's length; then the runs' starts.
+    // run in this tile and the run's length, published at once.
     unsigned int tot = 0;
+    unsigned long long *my = nullptr;
     if (threadIdx.x < 256) {
         const int v = threadIdx.x;
 #pragma unroll
@@ -295,43 +304,90 @@ radix_downsweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t
             s_cnt[w][v] = tot;
             tot += c;
         }
-        s_glob[v] = slots[(unsigned long long)v * n_tiles + t];
+        my = desc + 256ull * t + v;
+        st_relaxed(my, tag | (t == 0 ? kFlagP : 0ull) | tot);
     }
-    // exclusive scan of the 256 run lengths over threads 0..255
+    // The runs' starts in the tile: exclusive scan of the 256 run lengths.
     const unsigned int inc = warp_inclusive_sum(tot, lane);
     if (lane == 31 && threadIdx.x < 256) s_part[warp] = inc;
     __syncthreads();
     if (threadIdx.x < 256) {
-        unsigned int before = 0;
-        for (int w = 0; w < warp; ++w) before += s_part[w];
-        s_tileoff[threadIdx.x] = before + inc - tot;
+        unsigned int pre = 0;
+        for (int w = 0; w < warp; ++w) pre += s_part[w];
+        const unsigned int start = pre + inc - tot;
+        s_tileoff[threadIdx.x] = start;
+        // each warp's first position for value v in the tile-ordered buffer
+#pragma unroll
+        for (int w = 0; w < kRWarps; ++w) s_cnt[w][threadIdx.x] += start;
     }
     __syncthreads();
+    // Order the tile by digit value in shared memory (this frees the keys'
+    // registers before the look-back).
     const unsigned long long base = (unsigned long long)t * kRTile + (unsigned long long)warp * (32 * kRKeys);
 #pragma unroll
     for (int r = 0; r < kRKeys; ++r) {
         if ((valid_bits >> r) & 1u) {
             const unsigned long long e = base + 32 * r + lane;
-            const unsigned int v = (k[r] >> (8 * p)) & 255u;
-            const unsigned int pos = s_tileoff[v] + s_cnt[warp][v] + wrank[r];
+            const unsigned int v = (k[r] >> shift) & 255u;
+            const unsigned int pos = s_cnt[warp][v] + wrank[r];
             s_keys[pos] = k[r];
             if (b.out_idx) s_idx[pos] = b.in_idx ? b.in_idx[e] : (int32_t)e;
         }
     }
+    // Look back (threads 0..255, value v): the count of v in all earlier
+    // tiles, W tiles a round trip: load the words of tiles pos-W+1 .. pos
+    // together and add them from pos down to the first inclusive one; a word
+    // not yet published ends the round and is loaded again.
+    if (threadIdx.x < 256) {
+        const int v = threadIdx.x;
+        const unsigned long long *col = desc + v;  // value v's word of tile q at col[256 q]
+        unsigned int before = 0;
+        long long pos = (long long)t - 1;
+        unsigned long long t0 = 0;
+        unsigned int iter = 0;
+        while (pos >= 0) {
+            unsigned long long wd[kRLook];
+#pragma unroll
+            for (int j = 0; j < kRLook; ++j)
+                wd[j] = pos - j >= 0 ? ld_relaxed(col + 256ull * (unsigned long long)(pos - j)) : (tag | kFlagP);
+            bool done = false, stalled = false;
+#pragma unroll
+            for (int j = 0; j < kRLook; ++j) {
+                if (done || stalled) continue;
+                if ((wd[j] & kTagMask) != tag) {
+                    stalled = true;
+                    continue;
+                }
+                before += (unsigned int)wd[j];
+                --pos;
+                if (wd[j] & kFlagP) done = true;
+            }
+            if (done) break;
+            if (!stalled) continue;
+            // a word not published yet: wait, bounded
+            if (iter == 0) t0 = globaltimer();
+            ++iter;
+            if (iter >= 8) __nanosleep(64);
+            if (iter >= kMaxSpinIters || globaltimer() - t0 > limit_ns) {
+                report_timeout(hdr, t);
+                break;
+            }
+        }
+        if (t != 0) st_relaxed(my, tag | kFlagP | (before + tot));
+        s_delta[v] = bases[256 * p + v] + before - s_tileoff[v];
+    }
     __syncthreads();
     const unsigned long long tile0 = (unsigned long long)t * kRTile;
     const unsigned int count = n - tile0 < kRTile ? (unsigned int)(n - tile0) : kRTile;
-    const int shift = 8 * p;
     for (unsigned int i = threadIdx.x; i < count; i += kRThreads) {
         const unsigned int key = s_keys[i];
-        const unsigned int v = (key >> shift) & 255u;
-        const unsigned int slot = s_glob[v] + (i - s_tileoff[v]);
+        const unsigned int slot = s_delta[(key >> shift) & 255u] + i;
         if (b.out_keys) b.out_keys[slot] = key;
         if (b.out_idx) b.out_idx[slot] = s_idx[i];
     }
 }
 
-constexpr size_t kRDownSmem = (size_t)(kRWarps * 256 + 512 + 2 * kRTile) * 4;
+constexpr size_t kRSmem = (size_t)(kRWarps * 256 + 512 + 2 * kRTile) * 4;
 
 // All digits constant (every key equal): the permutation is the identity.
 __global__ void radix_identity_kernel(const RadixPlan *__restrict__ plan, const uint32_t *keys, int32_t *perm,
@@ -361,9 +417,11 @@ static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *per
     const RadixLayout L(n);
     if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < L.total) return U32SCAN_EWORKSPACE;
     char *w = static_cast<char *>(ws);
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(w);
     unsigned int *hist = reinterpret_cast<unsigned int *>(w + L.hist);
+    unsigned int *bases = reinterpret_cast<unsigned int *>(w + L.bases);
     RadixPlan *plan = reinterpret_cast<RadixPlan *>(w + L.plan);
-    unsigned int *table = reinterpret_cast<unsigned int *>(w + L.table);
+    unsigned long long *desc = reinterpret_cast<unsigned long long *>(w + L.desc);
     uint32_t *k1 = reinterpret_cast<uint32_t *>(w + L.k1);
     uint32_t *k2 = reinterpret_cast<uint32_t *>(w + L.k2);
     int32_t *i1 = reinterpret_cast<int32_t *>(w + L.i1);
@@ -374,24 +432,18 @@ static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *per
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return U32SCAN_ECUDA;
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(radix_downsweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kRDownSmem) != cudaSuccess)
+            if (cudaFuncSetAttribute(radix_onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kRSmem) != cudaSuccess)
                 return U32SCAN_ECUDA;
             attr_set[dev] = true;
         }
     }
     if (cudaMemsetAsync(hist, 0, 4 * 256 * 4, stream) != cudaSuccess) return U32SCAN_ECUDA;
     radix_histogram_kernel<<<1024, 512, 0, stream>>>(keys, n, hist);
-    radix_plan_kernel<<<1, 32, 0, stream>>>(hist, n, plan);
-    const unsigned long long cells = 256ull * L.n_tiles;
-    for (int p = 0; p < 4; ++p) {
-        radix_upsweep_kernel<<<L.n_tiles, kRThreads, 0, stream>>>(plan, p, keys, k1, k2, i1, perm, keys_out, n,
-                                                                   L.n_tiles, table);
-        const int rc = scan_exclusive_launch(table, cells, w + L.scan_ws, scan_workspace_bytes(cells), stream);
-        if (rc != U32SCAN_OK) return rc;
-        radix_downsweep_kernel<<<L.n_tiles, kRThreads, kRDownSmem, stream>>>(plan, p, keys, k1, k2, i1, perm,
-                                                                              keys_out, n, L.n_tiles, table);
-    }
+    radix_plan_kernel<<<1, 128, 0, stream>>>(hist, n, plan, bases);
+    for (int p = 0; p < 4; ++p)
+        radix_onesweep_kernel<<<L.n_tiles, kRThreads, kRSmem, stream>>>(plan, p, keys, k1, k2, i1, perm, keys_out, n,
+                                                                         L.n_tiles, bases, hdr, desc, kDefaultLimitNs);
     radix_identity_kernel<<<1024, 256, 0, stream>>>(plan, keys, perm, keys_out, n);
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }

@@ -492,12 +492,6 @@ static int scan_launch(uint32_t *data, unsigned long long n, uint32_t *total, vo
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }
 
-// For the library's own multi-kernel operations (the radix sort scans its
-// table of digit counts with this kernel).
-int scan_exclusive_launch(uint32_t *data, unsigned long long n, void *ws, size_t ws_bytes, cudaStream_t stream) {
-    return scan_launch<false>(data, n, nullptr, ws, ws_bytes, stream, 0xffffffffu, kDefaultLimitNs);
-}
-
 // The inclusive form with its total, for the runs layout.
 int scan_inclusive_launch(uint32_t *data, unsigned long long n, uint32_t *total, void *ws, size_t ws_bytes,
                           cudaStream_t stream) {

@@ -265,7 +265,10 @@ class SegOp(Op):
         fl = ", u8 head flags" if args.u8heads else ""
         self.metric = f"U32 {what} Gelem/s and HBM GB/s (fraction of peak) at n=2^26 ({lengths}{fl}), 1 GB300"
         kind = {"segscan": "true,false", "segscan_sums": "true,true", "segreduce": "false,true"}[mode]
-        self.kernel = f"segscan_u32_persistent<512,7,2,{kind},{'uint8' if args.u8heads else 'int32'}>"
+        # (u32x4 per lane, u32x4 per lane per round) as the library picks them
+        shape = "7,1" if mode != "segreduce" and (mode == "segscan" or not args.u8heads) else (
+            "8,2" if args.u8heads else "6,2")
+        self.kernel = f"segscan_u32_persistent<512,{shape},2,{kind},{'uint8' if args.u8heads else 'int32'}>"
         self.nseg = None
 
     def workload(self):

@@ -25,10 +25,12 @@
 // words (internal.cuh): the segmented value and the running head count; the
 // head count gives every segment end its index into the sums.
 //
-// Layout inside a tile (as in scan.cu): warp w owns the w-th run of 128 * V
-// elements; lane l holds, for r = 0 .. V-1, the four elements at 128 * r +
-// 4 * l of that run. Head flags become one bit per element (bit 4 * r + c);
-// byte flags are read four to a word and tested bytewise.
+// Layout inside a tile: warp w owns the w-th run of 128 * V elements; in
+// round r (of V / Q) lane l holds the E = 4 Q consecutive elements at
+// 32 E r + E l of that run, as Q u32x4. Head flags become one bit per
+// element (bit 4 i + c for component c of the lane's i-th u32x4); byte flags
+// are read four to a word and tested bytewise. Each round costs one warp-wide
+// segmented scan, so more elements a lane a round means fewer per element.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -39,7 +41,15 @@ namespace u32scan {
 
 constexpr unsigned int kNoHead = 0xffffffffu;
 
-template <int THREADS, int V, int S, bool WRITE_SCAN, bool WANT_SUMS, typename F>
+// Component c of a u32x4.
+__device__ __forceinline__ unsigned int comp(const uint4 &v, int c) {
+    return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ void set_comp(uint4 &v, int c, unsigned int a) {
+    if (c == 0) v.x = a; else if (c == 1) v.y = a; else if (c == 2) v.z = a; else v.w = a;
+}
+
+template <int THREADS, int V, int Q, int S, bool WRITE_SCAN, bool WANT_SUMS, typename F>
 __global__ void __launch_bounds__(THREADS, 1)
 segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags, unsigned long long n,
                        uint32_t *seg_sums, unsigned long long seg_cap, uint32_t *nseg, WsHeader *hdr,
@@ -48,6 +58,13 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
     constexpr int WARPS = THREADS / 32;
     constexpr unsigned int CHUNK = 128 * V;  // elements per warp
     constexpr unsigned int TILE = THREADS * V * 4;
+    // A lane takes E = 4 Q consecutive elements a round (Q u32x4), R rounds.
+    constexpr int R = V / Q, E = 4 * Q;
+    constexpr unsigned int kEMask = (1u << E) - 1u;
+    static_assert(V % Q == 0 && E <= 16, "whole rounds of u32x4");
+    // x[i] holds lane-local elements 4i .. 4i + 3: round i / Q, part i % Q;
+    // u4_off(i) is its offset from the lane's first element, in u32x4.
+    auto u4_off = [](int i) -> unsigned int { return 32u * Q * (unsigned int)(i / Q) + (unsigned int)(i % Q); };
     constexpr unsigned int TILE_BYTES = TILE * 4;  // values
     constexpr unsigned int FLAG_BYTES = TILE * (unsigned int)sizeof(F);
     constexpr unsigned int STAGE_U4 = (TILE_BYTES + FLAG_BYTES) / 16;
@@ -111,7 +128,7 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
     }
     __syncthreads();
     const unsigned long long tag = tag_of(s_epoch);
-    const unsigned int li0 = (unsigned int)warp * CHUNK + 4u * (unsigned int)lane;
+    const unsigned int li0 = (unsigned int)warp * CHUNK + (unsigned int)E * (unsigned int)lane;
     volatile unsigned int *vs_tile = s_tile;
 
     // Read draw u into registers (values x, head bits hb), scan it within
@@ -132,20 +149,20 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
             if constexpr (sizeof(F) == 4) {
                 const int4 *sf = reinterpret_cast<const int4 *>(stage_buf + st * STAGE_U4 + TILE / 4) + (li0 >> 2);
 #pragma unroll
-                for (int r = 0; r < V; ++r) {
-                    x[r] = sv[32 * r];
-                    const int4 f = sf[32 * r];
-                    hb |= ((f.x != 0) | ((f.y != 0) << 1) | ((f.z != 0) << 2) | ((f.w != 0) << 3)) << (4 * r);
+                for (int i = 0; i < V; ++i) {
+                    x[i] = sv[u4_off(i)];
+                    const int4 f = sf[u4_off(i)];
+                    hb |= ((f.x != 0) | ((f.y != 0) << 1) | ((f.z != 0) << 2) | ((f.w != 0) << 3)) << (4 * i);
                 }
             } else {
                 // four byte flags in one word: byte c non-zero -> bit c of a nibble
                 const unsigned int *sf = reinterpret_cast<const unsigned int *>(stage_buf + st * STAGE_U4 + TILE / 4) +
                                          (li0 >> 2);
 #pragma unroll
-                for (int r = 0; r < V; ++r) {
-                    x[r] = sv[32 * r];
-                    const unsigned int m = __vcmpne4(sf[32 * r], 0u) & 0x08040201u;
-                    hb |= ((m * 0x01010101u) >> 24) << (4 * r);
+                for (int i = 0; i < V; ++i) {
+                    x[i] = sv[u4_off(i)];
+                    const unsigned int m = __vcmpne4(sf[u4_off(i)], 0u) & 0x08040201u;
+                    hb |= ((m * 0x01010101u) >> 24) << (4 * i);
                 }
             }
         } else {
@@ -154,48 +171,50 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
             const uint32_t *tv = vdata + tile_v0;
             const F *tf = vflags + tile_v0;
 #pragma unroll
-            for (int r = 0; r < V; ++r) {
+            for (int i = 0; i < V; ++i) {
                 unsigned int e[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const unsigned int li = li0 + 128 * r + c;
+                    const unsigned int li = li0 + 4 * u4_off(i) + c;
                     const bool in = li >= lo && li < hi;
                     e[c] = in ? tv[li] : 0u;
-                    if (in && tf[li] != 0) hb |= 1u << (4 * r + c);
+                    if (in && tf[li] != 0) hb |= 1u << (4 * i + c);
                 }
-                x[r] = make_uint4(e[0], e[1], e[2], e[3]);
+                x[i] = make_uint4(e[0], e[1], e[2], e[3]);
             }
         }
         // index 0 of the array always opens a segment
         if (tile_v0 <= head && head < tile_v0 + TILE) {
             const unsigned int li = (unsigned int)(head - tile_v0);
-            // element li belongs to warp li / CHUNK, lane (li % 128) / 4, round (li % CHUNK) / 128, c = li % 4
-            if (li / CHUNK == (unsigned int)warp && ((li % 128u) >> 2) == (unsigned int)lane)
-                hb |= 1u << (4 * ((li % CHUNK) / 128u) + (li & 3u));
+            // element li: warp li / CHUNK; within the warp's run, round
+            // rem / (32 E), lane (rem % (32 E)) / E, lane-local rem % E
+            const unsigned int rem = li % CHUNK, rr = rem / (32u * E), in_r = rem % (32u * E);
+            if (li / CHUNK == (unsigned int)warp && in_r / E == (unsigned int)lane) hb |= 1u << (E * rr + in_r % E);
         }
         // Per-round segmented scan within the warp, carry from round to round.
         unsigned int carry = 0;
         pfirst = kNoHead;
 #pragma unroll
-        for (int r = 0; r < V; ++r) {
-            const unsigned int b = (hb >> (4 * r)) & 0xfu;
-            const unsigned int e0 = x[r].x;
-            const unsigned int e1 = (b & 2u) ? x[r].y : e0 + x[r].y;
-            const unsigned int e2 = (b & 4u) ? x[r].z : e1 + x[r].z;
-            const unsigned int e3 = (b & 8u) ? x[r].w : e2 + x[r].w;
-            const unsigned int sl = warp_segmented_inclusive(e3, b != 0u, carry, lane);
+        for (int r = 0; r < R; ++r) {
+            const unsigned int b = (hb >> (E * r)) & kEMask;
+            // the lane's own E elements, scanned with resets at its heads
+            unsigned int e[E];
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+                const unsigned int v = comp(x[Q * r + i / 4], i % 4);
+                e[i] = (i == 0 || ((b >> i) & 1u)) ? v : e[i - 1] + v;
+            }
+            const unsigned int sl = warp_segmented_inclusive(e[E - 1], b != 0u, carry, lane);
             unsigned int cin = __shfl_up_sync(0xffffffffu, sl, 1);
             if (lane == 0) cin = carry;
-            x[r].x = (b & 1u) ? e0 : cin + e0;
-            x[r].y = (b & 3u) ? e1 : cin + e1;
-            x[r].z = (b & 7u) ? e2 : cin + e2;
-            x[r].w = (b & 15u) ? e3 : cin + e3;
+#pragma unroll
+            for (int i = 0; i < E; ++i) set_comp(x[Q * r + i / 4], i % 4, (b & ((2u << i) - 1u)) ? e[i] : cin + e[i]);
             carry = __shfl_sync(0xffffffffu, sl, 31);
             const unsigned int hm = __ballot_sync(0xffffffffu, b != 0u);
             if (pfirst == kNoHead && hm) {
                 const int lf = __ffs(hm) - 1;
                 const unsigned int bf = __shfl_sync(0xffffffffu, b, lf);
-                pfirst = 128u * r + 4u * lf + (unsigned int)(__ffs(bf) - 1);
+                pfirst = 32u * E * r + E * (unsigned int)lf + (unsigned int)(__ffs(bf) - 1);
             }
         }
         const unsigned int wcnt = __reduce_add_sync(0xffffffffu, (unsigned int)__popc(hb));
@@ -228,42 +247,47 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
         const unsigned long long last_v = head + n - 1 - tile_v0;
         const unsigned int last_li = last_v < TILE ? (unsigned int)last_v : TILE;
 #pragma unroll
-        for (int r = 0; r < V; ++r) {
-            const unsigned int p0 = 128u * r + 4u * lane;
-            const unsigned int y[4] = {x[r].x + (p0 + 0 < pfirst ? cin : 0u), x[r].y + (p0 + 1 < pfirst ? cin : 0u),
-                                       x[r].z + (p0 + 2 < pfirst ? cin : 0u), x[r].w + (p0 + 3 < pfirst ? cin : 0u)};
+        for (int r = 0; r < R; ++r) {
+            const unsigned int p0 = 32u * E * r + E * lane;  // warp-local index of the lane's first element
+            const unsigned int l0 = li0 + 32u * E * r;        // its tile-local index
+            unsigned int y[E];
+#pragma unroll
+            for (int i = 0; i < E; ++i) y[i] = comp(x[Q * r + i / 4], i % 4) + (p0 + i < pfirst ? cin : 0u);
             if (WRITE_SCAN) {
                 if (full) {
-                    __stcs(reinterpret_cast<uint4 *>(tv + li0 + 128 * r), make_uint4(y[0], y[1], y[2], y[3]));
+#pragma unroll
+                    for (int q = 0; q < Q; ++q)
+                        __stcs(reinterpret_cast<uint4 *>(tv + l0 + 4 * q),
+                               make_uint4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]));
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const unsigned int li = li0 + 128 * r + c;
-                        if (li >= lo && li < hi) tv[li] = y[c];
+                    for (int i = 0; i < E; ++i) {
+                        const unsigned int li = l0 + i;
+                        if (li >= lo && li < hi) tv[li] = y[i];
                     }
                 }
             }
             if (WANT_SUMS) {
-                const unsigned int b = (hb >> (4 * r)) & 0xfu;
+                const unsigned int b = (hb >> (E * r)) & kEMask;
                 // head bit of the element after this lane's last one
                 const unsigned int down = __shfl_down_sync(0xffffffffu, b & 1u, 1);
                 unsigned int wrap = next_first;
-                if (r + 1 < V) wrap = __shfl_sync(0xffffffffu, (hb >> (4 * (r + 1))) & 1u, 0);
+                if (r + 1 < R) wrap = __shfl_sync(0xffffffffu, (hb >> (E * (r + 1))) & 1u, 0);
                 const unsigned int after = lane < 31 ? down : wrap;
-                const unsigned int next_bits = (b >> 1) | (after << 3);  // bit c: element c + 1 is a head
-                const bool last_here = last_li - (li0 + 128 * r) < 4u;  // the array's last element is one of mine
+                const unsigned int next_bits = (b >> 1) | (after << (E - 1));  // bit i: element i + 1 is a head
+                const bool last_here = last_li - l0 < (unsigned int)E;  // the array's last element is one of mine
                 const unsigned int pc = (unsigned int)__popc(b);
                 // Most rounds of long segments hold no segment end: skip them.
                 if (__any_sync(0xffffffffu, next_bits != 0u || last_here)) {
                     const unsigned int incl = warp_inclusive_sum(pc, lane);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const unsigned int li = li0 + 128 * r + c;
-                        const bool end = li >= lo && li < hi && (((next_bits >> c) & 1u) || li == last_li);
+                    for (int i = 0; i < E; ++i) {
+                        const unsigned int li = l0 + i;
+                        const bool end = li >= lo && li < hi && (((next_bits >> i) & 1u) || li == last_li);
                         if (end) {
                             const unsigned long long k = (unsigned long long)hbase + (incl - pc) +
-                                                         (unsigned int)__popc(b & ((2u << c) - 1u)) - 1u;
-                            if (k < seg_cap) seg_sums[k] = y[c];
+                                                         (unsigned int)__popc(b & ((2u << i) - 1u)) - 1u;
+                            if (k < seg_cap) seg_sums[k] = y[i];
                         }
                     }
                 }
@@ -363,18 +387,43 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
     }
 }
 
-// Launch shape (512 threads, u32x4 per lane per tile, ring stages); chosen
-// by measurement on GB300, overridable at build time for tuning sweeps.
-#ifndef U32SCAN_S_V
-#define U32SCAN_S_V 7
-#endif
+// Launch shapes, chosen by measurement on GB300 per form and flag type:
+// writing the scan favours four elements a lane a round (one u32x4: the
+// stores and shared-memory reads stay unit-stride); the reduce, and the scan
+// with sums over byte flags, favour eight (half the warp-wide segmented-scan
+// work per element). A smaller flag stream leaves room for larger tiles.
+// Overridable at build time for tuning sweeps.
 #ifndef U32SCAN_S_STAGES
 #define U32SCAN_S_STAGES 2
 #endif
-constexpr int kSThreads = 512, kSV = U32SCAN_S_V, kSStages = U32SCAN_S_STAGES;
-constexpr unsigned long long kSTile = (unsigned long long)kSThreads * kSV * 4;
-template <typename F>
-constexpr size_t seg_smem() { return (size_t)kSStages * kSTile * (4 + sizeof(F)); }
+#ifndef U32SCAN_S_V1
+#define U32SCAN_S_V1 7  // u32x4 per lane, four elements a round
+#endif
+#ifndef U32SCAN_S_V2
+#define U32SCAN_S_V2 6  // u32x4 per lane, eight elements a round, int32 flags
+#endif
+#ifndef U32SCAN_S_V2B
+#define U32SCAN_S_V2B 8  // the same with byte flags
+#endif
+constexpr int kSThreads = 512, kSStages = U32SCAN_S_STAGES;
+template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
+constexpr int seg_q() { return (WRITE_SCAN && (!WANT_SUMS || sizeof(F) == 4)) ? 1 : 2; }
+template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
+constexpr int seg_v() {
+    return seg_q<WRITE_SCAN, WANT_SUMS, F>() == 1 ? U32SCAN_S_V1 : (sizeof(F) == 1 ? U32SCAN_S_V2B : U32SCAN_S_V2);
+}
+template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
+constexpr unsigned long long seg_tile() { return (unsigned long long)kSThreads * seg_v<WRITE_SCAN, WANT_SUMS, F>() * 4; }
+template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
+constexpr size_t seg_smem() { return (size_t)kSStages * seg_tile<WRITE_SCAN, WANT_SUMS, F>() * (4 + sizeof(F)); }
+static_assert(seg_smem<true, false, int32_t>() <= 227 * 1024 && seg_smem<true, true, int32_t>() <= 227 * 1024 &&
+                  seg_smem<false, true, int32_t>() <= 227 * 1024 && seg_smem<false, true, uint8_t>() <= 227 * 1024 &&
+                  seg_smem<true, true, uint8_t>() <= 227 * 1024,
+              "shared memory");
+// the smallest tile, which has the most tiles, sizes the workspace
+constexpr unsigned long long kSTile = (unsigned long long)kSThreads * 4 *
+                                      (U32SCAN_S_V1 < U32SCAN_S_V2 ? (U32SCAN_S_V1 < U32SCAN_S_V2B ? U32SCAN_S_V1 : U32SCAN_S_V2B)
+                                                                   : (U32SCAN_S_V2 < U32SCAN_S_V2B ? U32SCAN_S_V2 : U32SCAN_S_V2B));
 
 size_t segscan_workspace_bytes(unsigned long long n) {
     const unsigned long long tiles = (n + 3 + kSTile - 1) / kSTile;
@@ -403,9 +452,11 @@ static int segscan_launch(uint32_t *data, const F *flags, unsigned long long n, 
     const unsigned int head = (unsigned int)((reinterpret_cast<uintptr_t>(data) & 15) >> 2);
     // flags stream by bulk copy when they start a tile on a 16-byte boundary too
     const int aligned = ((reinterpret_cast<uintptr_t>(flags) - sizeof(F) * head) & 15) == 0;
-    const unsigned int n_tiles = (unsigned int)((n + head + kSTile - 1) / kSTile);
-    auto kern = segscan_u32_persistent<kSThreads, kSV, kSStages, WRITE_SCAN, WANT_SUMS, F>;
-    constexpr size_t smem = seg_smem<F>();
+    constexpr unsigned long long TILE = seg_tile<WRITE_SCAN, WANT_SUMS, F>();
+    const unsigned int n_tiles = (unsigned int)((n + head + TILE - 1) / TILE);
+    auto kern = segscan_u32_persistent<kSThreads, seg_v<WRITE_SCAN, WANT_SUMS, F>(), seg_q<WRITE_SCAN, WANT_SUMS, F>(),
+                                       kSStages, WRITE_SCAN, WANT_SUMS, F>;
+    constexpr size_t smem = seg_smem<WRITE_SCAN, WANT_SUMS, F>();
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return U32SCAN_ECUDA;
     int sms;

@@ -448,7 +448,7 @@ class CompactValuesOp(Op):
         test = "non-zero values" if self.nonzero else "int32 flags"
         self.metric = (f"compaction of values Gelem/s and HBM GB/s (fraction of peak) at n=2^27, "
                        f"kept with probability {self.p} ({test}), 1 GB300")
-        self.kernel = f"compact_values_persistent<512,{7 if self.nonzero else 4},3,{'false' if self.nonzero else 'true'}>"
+        self.kernel = f"compact_values_persistent<512,8,2,{'false' if self.nonzero else 'true'}>"
         self.kept = None
 
     def workload(self):

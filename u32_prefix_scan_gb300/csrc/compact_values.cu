@@ -9,16 +9,18 @@
 // (the page's `where xs[i] > 0` on unsigned values).
 //
 // Kernel: persistent, one block per SM, single pass with the look-back of
-// the plain scan (scan.cu) over the keep indicator. Each tile's values (and
-// flags) arrive by 1-D bulk copies into a ring of three shared-memory
-// stages. A round reads the next tile's keep bits, counts them and
-// publishes the count, then walks the current tile's look-back, stages its
-// kept values in shared memory at their tile-local rank and stores them as
-// one contiguous run. The current tile's values are read from its stage
-// during the store, so a stage is re-armed only after its tile is stored
-// (which is why this ring has three stages where the index compaction's
-// has two). Traffic: 4 bytes read per element (8 with flags), 4 written per
-// kept element.
+// the plain scan (scan.cu) over the keep indicator, the same two-stage
+// bulk-copy pipeline as the index compaction (compact.cu) over the stream
+// the keep bits come from (the flags, or the values themselves): a round
+// reads the next tile's keep bits, counts them and publishes the count (its
+// stage is re-armed at once), then walks the current tile's look-back,
+// stages the tile's kept values at their tile-local rank in shared memory
+// and stores them as one contiguous run. The values are read at the store,
+// from L2: the values' own bulk copy put them there, or, with flags, the
+// producer asks for an L2 prefetch of the tile's values when it starts the
+// flags' copy; every warp loads them before warp 0's look-back, so the
+// round trip overlaps it. Traffic: 4 bytes read per element (8 with flags),
+// 4 written per kept element.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -37,11 +39,10 @@ compact_values_persistent(const uint32_t *__restrict__ values, const int32_t *__
     constexpr unsigned int CHUNK = 128 * V;
     constexpr unsigned int TILE = THREADS * V * 4;
     constexpr unsigned int TILE_BYTES = TILE * 4;
-    constexpr unsigned int STAGE_U4 = (FLAGS ? 2 : 1) * TILE / 4;  // [values | flags] per stage
     static_assert(WARPS <= 32 && 4 * V <= 32, "one lane per warp; keep bits fit in a word");
-    static_assert(S >= 3, "a stage is re-armed only after its tile is stored");
-    extern __shared__ __align__(128) uint4 smem_dyn[];  // S stages, then TILE staged values
-    uint32_t *stage_out = reinterpret_cast<uint32_t *>(smem_dyn + S * STAGE_U4);
+    static_assert(S >= 2, "the pipeline reads one stage ahead");
+    extern __shared__ __align__(128) uint4 smem_dyn[];  // S stages of the keep stream, then TILE staged values
+    uint32_t *stage_out = reinterpret_cast<uint32_t *>(smem_dyn + S * (TILE / 4));
     __shared__ __align__(8) unsigned long long bar[S];
     __shared__ unsigned int s_tile[S];
     __shared__ unsigned int s_wt[2][WARPS];
@@ -50,12 +51,11 @@ compact_values_persistent(const uint32_t *__restrict__ values, const int32_t *__
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    // Every block draws exactly S ids past the end: S at the start, then one
-    // after each tile it stores, and it stores every tile it drew below
-    // n_tiles. The last of all draws re-arms the counter for the next call.
     const unsigned int last_draw = n_tiles + (unsigned int)S * gridDim.x - 1u;
     const uint32_t *vvals = reinterpret_cast<const uint32_t *>(reinterpret_cast<uintptr_t>(values) - 4ull * head);
     const int32_t *vflags = reinterpret_cast<const int32_t *>(reinterpret_cast<uintptr_t>(flags) - 4ull * head);
+    // the stream the keep bits come from: flags, or the values themselves
+    const uint4 *vkeep = FLAGS ? reinterpret_cast<const uint4 *>(vflags) : reinterpret_cast<const uint4 *>(vvals);
     const bool producer = threadIdx.x == THREADS - 32;
     unsigned int latest_parity = 0;  // bit st: parity of the latest phase armed on stage st
 
@@ -79,9 +79,9 @@ compact_values_persistent(const uint32_t *__restrict__ values, const int32_t *__
         const unsigned int b = smem_u32(&bar[st]);
         if (id < n_tiles && tile_full(id)) {
             const unsigned long long v0 = (unsigned long long)id * TILE;
-            mbar_arrive_expect_tx(b, (FLAGS ? 2 : 1) * TILE_BYTES);
-            bulk_load(smem_u32(smem_dyn + st * STAGE_U4), vvals + v0, TILE_BYTES, b);
-            if (FLAGS) bulk_load(smem_u32(smem_dyn + st * STAGE_U4 + TILE / 4), vflags + v0, TILE_BYTES, b);
+            mbar_arrive_expect_tx(b, TILE_BYTES);
+            bulk_load(smem_u32(smem_dyn + st * (TILE / 4)), vkeep + v0 / 4, TILE_BYTES, b);
+            if (FLAGS) bulk_prefetch_l2(vvals + v0, TILE_BYTES);  // the values, read at the store
         } else {
             mbar_arrive(b);  // nothing to copy: a partial tile reads global memory, a past-the-end draw stops
         }
@@ -114,7 +114,7 @@ compact_values_persistent(const uint32_t *__restrict__ values, const int32_t *__
         if (t >= n_tiles) return n_tiles;
         kb = 0;
         if (tile_full(t)) {
-            const uint4 *sk = smem_dyn + st * STAGE_U4 + (FLAGS ? TILE / 4 : 0) + (li0 >> 2);
+            const uint4 *sk = smem_dyn + st * (TILE / 4) + (li0 >> 2);
 #pragma unroll
             for (int r = 0; r < V; ++r) {
                 const uint4 f = sk[32 * r];
@@ -156,6 +156,11 @@ compact_values_persistent(const uint32_t *__restrict__ values, const int32_t *__
     unsigned int tc = read_tile(0, kbc, exc);
     unsigned int agg_c = 0, wex_c = 0;
     if (!__syncthreads_or(tc >= n_tiles)) {
+        if (producer) {
+            fence_proxy_async_smem();
+            issue(0);
+            latest_parity ^= 1u;
+        }
         if (warp == 0) {
             agg_c = block_aggregate(0, wex_c);
             if (lane == 0) publish_aggregate(desc, tc, agg_c, tag);
@@ -163,6 +168,34 @@ compact_values_persistent(const uint32_t *__restrict__ values, const int32_t *__
         for (unsigned int u = 1;; ++u) {
             const unsigned int tn = read_tile(u, kbn, exn);
             const bool more = !__syncthreads_or(tn >= n_tiles);  // barrier A
+            if (more && producer) {
+                fence_proxy_async_smem();
+                const int st = (int)(u % S);
+                issue(st);
+                latest_parity ^= 1u << st;
+            }
+            // The current tile's values for its kept elements, from L2 (the
+            // keep stream's bulk copy, or the producer's prefetch, brought
+            // them there); loaded before the look-back so the round trip
+            // overlaps it.
+            const unsigned long long tile_v0 = (unsigned long long)tc * TILE;
+            const bool full = tile_full(tc);
+            uint4 xv[V];
+#pragma unroll
+            for (int r = 0; r < V; ++r) {
+                const unsigned int b = (kbc >> (4 * r)) & 0xfu;
+                xv[r] = make_uint4(0u, 0u, 0u, 0u);
+                if (b == 0u) continue;
+                if (full) {
+                    xv[r] = __ldcg(reinterpret_cast<const uint4 *>(vvals + tile_v0 + li0 + 128 * r));
+                } else {
+                    const uint32_t *tb = vvals + tile_v0 + li0 + 128 * r;
+                    if (b & 1u) xv[r].x = tb[0];
+                    if (b & 2u) xv[r].y = tb[1];
+                    if (b & 4u) xv[r].z = tb[2];
+                    if (b & 8u) xv[r].w = tb[3];
+                }
+            }
             unsigned int agg_n = 0, wex_n = 0;
             if (warp == 0) {
                 if (more) {
@@ -181,38 +214,18 @@ compact_values_persistent(const uint32_t *__restrict__ values, const int32_t *__
                 }
             }
             __syncthreads();  // barrier B: the current tile's carries are visible
-
-            // ---- store the current tile (draw u - 1) ----
-            const int sc = (int)((u - 1u) % S);
             {
-                const unsigned long long tile_v0 = (unsigned long long)tc * TILE;
                 const unsigned int wbase = s_base[warp];
-                const bool full = tile_full(tc);
-                const uint4 *sv = smem_dyn + sc * STAGE_U4 + (li0 >> 2);
 #pragma unroll
                 for (int r = 0; r < V; ++r) {
                     const unsigned int b = (kbc >> (4 * r)) & 0xfu;
-                    if (b == 0u) continue;
-                    unsigned int e[4];
-                    if (full) {
-                        const uint4 x = sv[32 * r];
-                        e[0] = x.x; e[1] = x.y; e[2] = x.z; e[3] = x.w;
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) e[c] = (b >> c) & 1u ? vvals[tile_v0 + li0 + 128 * r + c] : 0u;
-                    }
+                    const unsigned int e[4] = {xv[r].x, xv[r].y, xv[r].z, xv[r].w};
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
                         if ((b >> c) & 1u) stage_out[wbase + exc[r] + __popc(b & ((1u << c) - 1u))] = e[c];
                 }
             }
-            __syncthreads();  // barrier C: kept values staged, stage sc read
-            if (producer) {
-                // re-arm stage sc with draw u - 1 + S
-                fence_proxy_async_smem();
-                issue(sc);
-                latest_parity ^= 1u << sc;
-            }
+            __syncthreads();  // barrier C: the tile's kept values are staged
             {
                 const unsigned int prefix = s_prefix, kept = s_kept;
                 for (unsigned int j = threadIdx.x; j < kept; j += THREADS) __stcs(out + prefix + j, stage_out[j]);
@@ -227,8 +240,8 @@ compact_values_persistent(const uint32_t *__restrict__ values, const int32_t *__
         }
     }
     // Leave no bulk copy in flight into this block's shared memory: wait
-    // (bounded) for the latest phase armed on each stage. Normally each is a
-    // past-the-end draw with nothing to copy; after a timeout it may not be.
+    // (bounded) for the latest phase armed on each stage (on the normal path
+    // the outstanding draws are past the end, with nothing to copy).
     if (producer) {
 #pragma unroll
         for (int st = 0; st < S; ++st)
@@ -237,25 +250,20 @@ compact_values_persistent(const uint32_t *__restrict__ values, const int32_t *__
 }
 
 // Launch shape, chosen by measurement on GB300 and overridable at build time
-// for tuning sweeps: ring stages, and u32x4 per lane with and without flags.
+// for tuning sweeps: ring stages and u32x4 per lane.
 #ifndef U32SCAN_CV_STAGES
-#define U32SCAN_CV_STAGES 3
+#define U32SCAN_CV_STAGES 2
 #endif
-#ifndef U32SCAN_CV_VF
-#define U32SCAN_CV_VF 4
+#ifndef U32SCAN_CV_V
+#define U32SCAN_CV_V 8
 #endif
-#ifndef U32SCAN_CV_VN
-#define U32SCAN_CV_VN 7
-#endif
-constexpr int kVThreads = 512, kVStages = U32SCAN_CV_STAGES;
-constexpr int kVVFlags = U32SCAN_CV_VF, kVVNonzero = U32SCAN_CV_VN;
-constexpr unsigned long long vtile(int v) { return (unsigned long long)kVThreads * v * 4; }
-constexpr size_t vsmem(int v, bool flags) { return ((size_t)kVStages * (flags ? 2 : 1) + 1) * vtile(v) * 4; }
-static_assert(vsmem(kVVFlags, true) <= 227 * 1024 && vsmem(kVVNonzero, false) <= 227 * 1024, "shared memory");
+constexpr int kVThreads = 512, kVStages = U32SCAN_CV_STAGES, kVV = U32SCAN_CV_V;
+constexpr unsigned long long kVTile = (unsigned long long)kVThreads * kVV * 4;
+constexpr size_t kVSmem = ((size_t)kVStages + 1) * kVTile * 4;
+static_assert(kVSmem <= 227 * 1024, "shared memory");
 
 size_t compact_values_workspace_bytes(unsigned long long n) {
-    constexpr unsigned long long small = vtile(kVVFlags < kVVNonzero ? kVVFlags : kVVNonzero);
-    const unsigned long long tiles = (n + 3 + small - 1) / small;
+    const unsigned long long tiles = (n + 3 + kVTile - 1) / kVTile;
     return round_up(kHeaderBytes + 8 * tiles, 256);
 }
 
@@ -267,9 +275,9 @@ template <bool FLAGS>
 static int compact_values_launch(const uint32_t *values, const int32_t *flags, unsigned long long n, uint32_t *out,
                                  int32_t *count, void *ws, size_t ws_bytes, cudaStream_t stream,
                                  unsigned long long limit_ns) {
-    constexpr int V = FLAGS ? kVVFlags : kVVNonzero;
-    constexpr unsigned long long TILE = vtile(V);
-    constexpr size_t SMEM = vsmem(V, FLAGS);
+    constexpr int V = kVV;
+    constexpr unsigned long long TILE = kVTile;
+    constexpr size_t SMEM = kVSmem;
     const unsigned int head = (unsigned int)((reinterpret_cast<uintptr_t>(values) & 15) >> 2);
     const int flags_aligned = ((reinterpret_cast<uintptr_t>(values) ^ reinterpret_cast<uintptr_t>(flags)) & 15) == 0;
     const unsigned int n_tiles = (unsigned int)((n + head + TILE - 1) / TILE);

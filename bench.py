@@ -644,7 +644,7 @@ class RunsOp(Op):
         self.name = "runs_owner_u32" + ("_skewed" if self.skewed else "")
         mix = "skewed counts, 1/16 of owners in [0,64)" if self.skewed else "counts uniform in [0,8)"
         self.metric = f"runs layout + owner row Gelem/s (owners) at n=2^25 owners ({mix}), 1 GB300"
-        self.kernel = "runs_owner_kernel<256,8> (merge path of ends with entry indices)"
+        self.kernel = "runs_owner_kernel<16 warps, 16 positions a lane> (merge path of ends with entry indices)"
         self.entries = None
 
     def workload(self):

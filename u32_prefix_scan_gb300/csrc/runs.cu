@@ -22,13 +22,16 @@
 // + i < p} owners, and an entry reached after i owners belongs to owner i.
 // Persistent warps take equal slices of the path -- owners plus entries, so
 // empty owners and long runs cost alike -- each finds its start by one
-// warp-wide search in global memory, then walks its slice in tiles of 256
-// positions with no block-wide barrier: the tile's owners are read once
-// (coalesced, eight independent loads a lane), each passed one marks the
-// count of owners passed so far at its end's offset in shared memory, a
-// warp max-scan turns the marks into every entry's owner, and the owners go
-// out as coalesced stores. Traffic: 4 bytes read per owner and 4 written per
-// entry.
+// warp-wide search in global memory, then walks its slice in tiles of 508
+// positions with no block-wide barrier. A tile tests its owners 32 at a
+// time (loaded while the previous tile was stored, as many chunks as that
+// tile needed plus one, more on demand) until one chunk holds an owner the
+// tile does not pass; each passed owner that ends a run of equal offsets
+// marks the count of owners passed so far at its end's offset in shared
+// memory; a warp max-scan turns the marks into every entry's owner, and each
+// lane writes its 16 owners from registers with 16-byte stores, in a frame
+// aligned to the owner row. Traffic: 4 bytes read per owner and 4 written
+// per entry.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -38,13 +41,13 @@
 namespace u32scan {
 
 #ifndef U32SCAN_RO_WARPS
-#define U32SCAN_RO_WARPS 8
+#define U32SCAN_RO_WARPS 16
 #endif
 #ifndef U32SCAN_RO_VT
-#define U32SCAN_RO_VT 8
+#define U32SCAN_RO_VT 16
 #endif
 #ifndef U32SCAN_RO_MINB
-#define U32SCAN_RO_MINB 6
+#define U32SCAN_RO_MINB 2
 #endif
 constexpr int kROWarps = U32SCAN_RO_WARPS, kROVT = U32SCAN_RO_VT, kROThreads = kROWarps * 32;
 constexpr int kFillThreads = 256;
@@ -122,7 +125,9 @@ __global__ void __launch_bounds__(WARPS * 32, U32SCAN_RO_MINB) runs_owner_kernel
                                                                 unsigned int n, int32_t *__restrict__ owner,
                                                                 unsigned long long cap) {
     constexpr unsigned int Dw = 32u * VT;
+    constexpr unsigned int TP = Dw - 4;  // path positions a tile: its entries fit the aligned frame
     constexpr unsigned int PADDED = Dw + Dw / 32;
+    static_assert(VT % 4 == 0 && 32 % VT == 0, "a lane's frame positions: whole 16-byte stores, one pad");
     // marks, then the tile's owners; zero between tiles
     __shared__ unsigned int s_buf[WARPS][PADDED];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -137,49 +142,48 @@ __global__ void __launch_bounds__(WARPS * 32, U32SCAN_RO_MINB) runs_owner_kernel
     const unsigned int E = total < cap ? total : (unsigned int)cap;
     if (E == 0) return;
     const unsigned long long L = (unsigned long long)n + E;
-    const unsigned long long tiles = (L + Dw - 1) / Dw;
+    const unsigned long long tiles = (L + TP - 1) / TP;
     const unsigned long long nwarps = (unsigned long long)gridDim.x * WARPS;
     const unsigned long long per = (tiles + nwarps - 1) / nwarps;
-    unsigned long long d0 = ((unsigned long long)blockIdx.x * WARPS + warp) * per * Dw;
+    unsigned long long d0 = ((unsigned long long)blockIdx.x * WARPS + warp) * per * TP;
     if (d0 >= L) return;
-    const unsigned long long d_end = d0 + per * Dw < L ? d0 + per * Dw : L;
+    const unsigned long long d_end = d0 + per * TP < L ? d0 + per * TP : L;
+    const unsigned int oa = (unsigned int)((reinterpret_cast<uintptr_t>(owner) >> 2) & 3u);  // owner's phase mod 16 B
     unsigned int i0 = (unsigned int)split_global(ends, d0 > E ? d0 - E : 0, d0 < n ? d0 : n, d0, E, lane);
 #pragma unroll
     for (unsigned int p = lane; p < PADDED; p += 32) buf[p] = 0u;
     __syncwarp();
+    unsigned int raw[VT];  // end values of the tile's first chunks, loaded ahead
+    int loaded = 0;        // chunks of the current tile in raw (warp-uniform)
 
     while (d0 < d_end) {
         const unsigned int j0 = (unsigned int)(d0 - i0);  // entries before the tile, <= E
-        const unsigned int q1 = (unsigned int)(d_end - d0 < Dw ? d_end - d0 : Dw);
+        const unsigned int q1 = (unsigned int)(d_end - d0 < TP ? d_end - d0 : TP);
         const unsigned int cnt = n - i0 < q1 ? n - i0 : q1;  // owners the tile can pass
-        const unsigned int *e_tile = ends + i0;
-        unsigned int rel[VT];
-#pragma unroll
-        for (int m = 0; m < VT; ++m) {
-            const unsigned int k = (unsigned int)lane + 32u * m;
-            unsigned int r = Dw;
-            if (k < cnt) {
-                const unsigned int v = __ldg(e_tile + k);
-                const unsigned int c = v < E ? v : E;
-                r = c > j0 ? (c - j0 < Dw ? c - j0 : Dw) : 0u;
-            }
-            rel[m] = r;
-        }
+        // Marks and owners live in a frame aligned to 16 bytes of the owner
+        // row: tile entry jl sits at frame position jl + s_al.
+        const unsigned int s_al = (oa + j0) & 3u;
+        // Chunks of 32 owners: the ones loaded ahead (while the previous
+        // tile stored), then more on demand until a chunk holds an owner the
+        // tile does not pass (the passed owners are a prefix).
         unsigned int pass = 0u;
+        int used = 0;
 #pragma unroll
         for (int m = 0; m < VT; ++m) {
+            if (32u * m >= cnt) break;
             const unsigned int k = (unsigned int)lane + 32u * m;
-            // the passed owners are a prefix: once a chunk's first owner is
-            // not passed, no later owner is (a warp-uniform test)
-            if (32u * m >= cnt || __shfl_sync(0xffffffffu, rel[m], 0) + 32u * m >= q1) break;
-            unsigned int rn = __shfl_down_sync(0xffffffffu, rel[m], 1);
-            const unsigned int first_next = m + 1 < VT ? __shfl_sync(0xffffffffu, rel[m + 1 < VT ? m + 1 : m], 0) : Dw;
-            if (lane == 31) rn = first_next;
-            if (k < cnt && rel[m] + k < q1) {
-                const bool next_passed = k + 1 < cnt && rn + k + 1 < q1;
-                if (!next_passed || rn != rel[m]) buf[pad(rel[m])] = k + 1;
-                if (!next_passed) pass = k + 1;
-            }
+            if (m >= loaded) raw[m] = k < cnt ? __ldg(ends + i0 + k) : 0xffffffffu;  // warp-uniform test
+            const unsigned int c = raw[m] < E ? raw[m] : E;
+            const unsigned int r = c > j0 ? (c - j0 < Dw ? c - j0 : Dw) : 0u;
+            const bool passed = k < cnt && r + k < q1;
+            // the last passed owner of each run of equal offsets in the chunk
+            // marks; a run crossing into the next chunk is settled by max
+            const unsigned int rn = __shfl_down_sync(0xffffffffu, r, 1);
+            const bool pn = __shfl_down_sync(0xffffffffu, passed ? 1u : 0u, 1) != 0u;
+            if (passed && (lane == 31 || !pn || rn != r)) atomicMax(&buf[pad(r + s_al)], k + 1);
+            if (passed) pass = k + 1;
+            used = m + 1;
+            if (__ballot_sync(0xffffffffu, passed) != 0xffffffffu) break;
         }
         // owners passed in the tile, held to what the entries left allow
         const unsigned int left = E - j0;
@@ -187,15 +191,38 @@ __global__ void __launch_bounds__(WARPS * 32, U32SCAN_RO_MINB) runs_owner_kernel
         unsigned int il1 = __reduce_max_sync(0xffffffffu, pass);
         il1 = il1 < lo1 ? lo1 : (il1 > cnt ? cnt : il1);
         const unsigned int jl1 = q1 - il1;
+        // load the next tile's first chunks now, so they arrive while this
+        // tile is scanned and stored: one more than this tile needed
+        {
+            const unsigned long long dn = d0 + q1;
+            const unsigned int in = i0 + il1;
+            loaded = used + 1 < VT ? used + 1 : VT;
+            if (dn < d_end) {
+                const unsigned int qn = (unsigned int)(d_end - dn < TP ? d_end - dn : TP);
+                const unsigned int cn = n - in < qn ? n - in : qn;
+#pragma unroll
+                for (int m = 0; m < VT; ++m) {
+                    if (m >= loaded) break;  // warp-uniform
+                    const unsigned int k = (unsigned int)lane + 32u * m;
+                    raw[m] = k < cn ? __ldg(ends + in + k) : 0xffffffffu;
+                }
+            }
+        }
         __syncwarp();
-        // inclusive max-scan of the marks over the tile's entries [0, jl1)
+        // Inclusive max-scan of the marks over the frame: lane l takes frame
+        // positions b0 = VT l .. b0 + VT - 1 (one padded base, VT words on:
+        // b0 is a multiple of VT, so the pad is the same for all of them),
+        // zeroes its marks as it reads them (every mark lies below the
+        // frame's end), and writes its owners straight from registers, two
+        // 16-byte stores when all are entries of the tile.
         const unsigned int b0 = (unsigned int)lane * VT;
-        unsigned int run = 0u;
+        unsigned int *mb = buf + pad(b0);
+        unsigned int run = 0u, xm[VT];
 #pragma unroll
         for (int v = 0; v < VT; ++v) {
-            const unsigned int x = b0 + v < jl1 ? buf[pad(b0 + v)] : 0u;
-            rel[v] = x;  // reuse the registers
-            run = x > run ? x : run;
+            xm[v] = mb[v];
+            mb[v] = 0u;
+            run = xm[v] > run ? xm[v] : run;
         }
         unsigned int inc = run;
 #pragma unroll
@@ -207,17 +234,21 @@ __global__ void __launch_bounds__(WARPS * 32, U32SCAN_RO_MINB) runs_owner_kernel
         if (lane == 0) run = 0u;
 #pragma unroll
         for (int v = 0; v < VT; ++v) {
-            run = rel[v] > run ? rel[v] : run;
-            buf[pad(b0 + v)] = b0 + v < jl1 ? i0 + run : 0u;
+            run = xm[v] > run ? xm[v] : run;
+            xm[v] = i0 + run;
         }
-        __syncwarp();
-        int32_t *dst = owner + (d0 - i0);
+        // frame position f is owner element j0 + (f - s_al); entries are f in [s_al, s_al + jl1)
+        if (b0 >= s_al && b0 + VT <= s_al + jl1) {
+            int32_t *dst = owner + j0 + (b0 - s_al);  // 16-byte aligned
 #pragma unroll
-        for (int m = 0; m < VT; ++m) {
-            const unsigned int p = (unsigned int)lane + 32u * m;
-            if (p < jl1) {
-                dst[p] = (int32_t)buf[pad(p)];
-                buf[pad(p)] = 0u;
+            for (int v = 0; v < VT; v += 4)
+                __stcs(reinterpret_cast<int4 *>(dst + v),
+                       make_int4((int)xm[v], (int)xm[v + 1], (int)xm[v + 2], (int)xm[v + 3]));
+        } else {
+#pragma unroll
+            for (int v = 0; v < VT; ++v) {
+                const unsigned int f = b0 + v;
+                if (f >= s_al && f < s_al + jl1) owner[j0 + (f - s_al)] = (int32_t)xm[v];
             }
         }
         __syncwarp();

@@ -194,21 +194,24 @@ __device__ __forceinline__ void publish_inclusive(unsigned long long *desc, unsi
 // the tile 32 * j + l + 1 places back (a virtual inclusive prefix holding
 // the operator's identity before tile 0).
 // Loading it early lets its L2 round trip overlap other work.
-template <int K, int OP = kAdd>
+// (STRIDE: words between consecutive tiles' words, for descriptors that
+// interleave several words a tile.)
+template <int K, int OP = kAdd, int STRIDE = 1>
 __device__ __forceinline__ void lookback_window(const unsigned long long *desc, long long pos,
                                                 unsigned long long tag, int lane, unsigned long long (&d)[K]) {
 #pragma unroll
     for (int j = 0; j < K; ++j) {
         const long long idx = pos - 32 * j - lane;
-        d[j] = idx >= 0 ? ld_relaxed(desc + idx) : (tag | kFlagP | Monoid<OP>::identity());
+        d[j] = idx >= 0 ? ld_relaxed(desc + STRIDE * idx) : (tag | kFlagP | Monoid<OP>::identity());
     }
 }
 
 // Fold (under OP) of tiles 0 .. t-1 (all 32 lanes call it), starting from a
 // first window `d` already loaded by lookback_window(desc, t - 1, ...).
-// Stops at the nearest word holding an inclusive prefix; a round needs
-// readiness only up to there, so slow far-away words are never waited for.
-template <int K, int OP = kAdd>
+// Stops at (and includes) the nearest word with a STOP flag (the inclusive
+// prefix, kFlagP, by default); a round needs readiness only up to there, so
+// slow far-away words are never waited for.
+template <int K, int OP = kAdd, int STRIDE = 1, unsigned long long STOP = kFlagP>
 __device__ __forceinline__ unsigned int lookback_prefix_wide(const unsigned long long *desc, unsigned int t,
                                                              unsigned long long tag, WsHeader *hdr,
                                                              unsigned long long limit_ns, int lane,
@@ -228,7 +231,7 @@ __device__ __forceinline__ unsigned int lookback_prefix_wide(const unsigned long
 #pragma unroll
             for (int j = K - 1; j >= 0; --j) {
                 const bool ready = (d[j] & kTagMask) == tag;
-                const unsigned int m = __ballot_sync(0xffffffffu, !ready || (d[j] & kFlagP));
+                const unsigned int m = __ballot_sync(0xffffffffu, !ready || (d[j] & STOP));
                 if (m) {
                     stop_j = j;
                     stop_lane = __ffs(m) - 1;
@@ -256,7 +259,7 @@ __device__ __forceinline__ unsigned int lookback_prefix_wide(const unsigned long
 #pragma unroll
             for (int j = 0; j < K; ++j) {
                 const long long idx = pos - 32 * j - lane;
-                if (idx >= 0 && (d[j] & kTagMask) != tag) d[j] = ld_relaxed(desc + idx);
+                if (idx >= 0 && (d[j] & kTagMask) != tag) d[j] = ld_relaxed(desc + STRIDE * idx);
             }
             const unsigned long long now = __shfl_sync(0xffffffffu, globaltimer(), 0);
             if (iter > 0 && (now - t0 > limit_ns || iter >= kMaxSpinIters)) {
@@ -267,7 +270,7 @@ __device__ __forceinline__ unsigned int lookback_prefix_wide(const unsigned long
             }
         }
         pos -= 32 * K;
-        lookback_window<K, OP>(desc, pos, tag, lane, d);
+        lookback_window<K, OP, STRIDE>(desc, pos, tag, lane, d);
     }
 }
 
@@ -361,6 +364,26 @@ __device__ __forceinline__ SegPrefix lookback_seg(const unsigned long long *desc
             }
         }
     }
+}
+
+// The same two look-backs, each with the library's windowed walk: word A
+// (stops at a word with a head or a final value) KA, word B (stops at a
+// final count) KB words a lane per round trip; both first windows are in
+// flight together. Word A usually stops one tile back (tiles that hold a
+// head); word B walks to the nearest tile whose count is final, which with
+// every SM's tiles in flight can be a block's worth of tiles back.
+template <int KA, int KB>
+__device__ __forceinline__ SegPrefix lookback_seg_wide(const unsigned long long *desc2, unsigned int t,
+                                                       unsigned long long tag, WsHeader *hdr,
+                                                       unsigned long long limit_ns, int lane) {
+    SegPrefix pre{0u, 0u};
+    if (t == 0) return pre;
+    unsigned long long wa[KA], wb[KB];
+    lookback_window<KA, kAdd, 2>(desc2, (long long)t - 1, tag, lane, wa);
+    lookback_window<KB, kAdd, 2>(desc2 + 1, (long long)t - 1, tag, lane, wb);
+    pre.seg = lookback_prefix_wide<KA, kAdd, 2, kFlagP | kFlagH>(desc2, t, tag, hdr, limit_ns, lane, wa);
+    pre.cnt = lookback_prefix_wide<KB, kAdd, 2, kFlagP>(desc2 + 1, t, tag, hdr, limit_ns, lane, wb);
+    return pre;
 }
 
 // ---------------------------------------------------------------------------

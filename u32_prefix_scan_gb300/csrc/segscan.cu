@@ -37,6 +37,13 @@
 
 #include "internal.cuh"
 
+#ifndef U32SCAN_S_LOOKA
+#define U32SCAN_S_LOOKA 1  // look-back words a lane per round trip: segmented value
+#endif
+#ifndef U32SCAN_S_LOOKB
+#define U32SCAN_S_LOOKB 1  // and head count
+#endif
+
 namespace u32scan {
 
 constexpr unsigned int kNoHead = 0xffffffffu;
@@ -50,7 +57,7 @@ __device__ __forceinline__ void set_comp(uint4 &v, int c, unsigned int a) {
 }
 
 template <int THREADS, int V, int Q, int S, bool WRITE_SCAN, bool WANT_SUMS, typename F>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 512 / THREADS)
 segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags, unsigned long long n,
                        uint32_t *seg_sums, unsigned long long seg_cap, uint32_t *nseg, WsHeader *hdr,
                        unsigned long long *desc2, unsigned int n_tiles, unsigned int head, int streams_aligned,
@@ -134,7 +141,8 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
     // Read draw u into registers (values x, head bits hb), scan it within
     // each warp and leave the warp aggregates in slot u & 1. Returns the
     // tile, or n_tiles and above past the end / on a timeout.
-    auto read_tile = [&](unsigned int u, uint4 (&x)[V], unsigned int &hb, unsigned int &pfirst) -> unsigned int {
+    auto read_tile = [&](unsigned int u, uint4 (&x)[V], unsigned int &hb, unsigned int &pfirst,
+                         unsigned int (&cl)[R]) -> unsigned int {
         const int st = (int)(u % S);
         if (!mbar_wait_bounded(smem_u32(&bar[st]), (u / S) & 1u, limit_ns)) {
             report_timeout(hdr, 0xfffffffeu);
@@ -204,13 +212,31 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
                 const unsigned int v = comp(x[Q * r + i / 4], i % 4);
                 e[i] = (i == 0 || ((b >> i) & 1u)) ? v : e[i - 1] + v;
             }
-            const unsigned int sl = warp_segmented_inclusive(e[E - 1], b != 0u, carry, lane);
-            unsigned int cin = __shfl_up_sync(0xffffffffu, sl, 1);
-            if (lane == 0) cin = carry;
-#pragma unroll
-            for (int i = 0; i < E; ++i) set_comp(x[Q * r + i / 4], i % 4, (b & ((2u << i) - 1u)) ? e[i] : cin + e[i]);
-            carry = __shfl_sync(0xffffffffu, sl, 31);
+            // The round's segmented scan across lanes with a zero carry; every
+            // shuffle works on carry-free values, so the rounds overlap and
+            // the carry enters by plain arithmetic: a lane gets it when no
+            // head lies at or before it in the round.
+            const unsigned int t = e[E - 1];
+            const unsigned int P = warp_inclusive_sum(t, lane);
             const unsigned int hm = __ballot_sync(0xffffffffu, b != 0u);
+            const unsigned int mle = hm & lanemask_le(lane);
+            const unsigned int bL = __shfl_sync(0xffffffffu, P - t, 31 - __clz(mle | 1u));
+            const unsigned int sl0 = mle ? P - bL : P;
+            const unsigned int T0 = __shfl_sync(0xffffffffu, sl0, 31);
+            const unsigned int up = __shfl_up_sync(0xffffffffu, sl0, 1);
+            const unsigned int cin = lane == 0 ? carry : up + ((hm & lanemask_lt(lane)) == 0u ? carry : 0u);
+            if constexpr (WRITE_SCAN) {
+#pragma unroll
+                for (int i = 0; i < E; ++i)
+                    set_comp(x[Q * r + i / 4], i % 4, (b & ((2u << i) - 1u)) ? e[i] : cin + e[i]);
+            } else {
+                // the reduce needs values at segment ends only: keep the
+                // lane-local ones and the lane's carry, added at the ends
+#pragma unroll
+                for (int i = 0; i < E; ++i) set_comp(x[Q * r + i / 4], i % 4, e[i]);
+                cl[r] = cin;
+            }
+            carry = hm ? T0 : carry + T0;
             if (pfirst == kNoHead && hm) {
                 const int lf = __ffs(hm) - 1;
                 const unsigned int bf = __shfl_sync(0xffffffffu, b, lf);
@@ -231,7 +257,8 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
     // Store the current tile (first-head slot cs): add each warp's carry-in to the
     // elements before its first head, write the scan, and write each
     // segment's sum at the segment's last element.
-    auto store_tile = [&](unsigned int t, int cs, const uint4 (&x)[V], unsigned int hb, unsigned int pfirst) {
+    auto store_tile = [&](unsigned int t, int cs, const uint4 (&x)[V], unsigned int hb, unsigned int pfirst,
+                          const unsigned int (&cl)[R]) {
         const unsigned long long tile_v0 = (unsigned long long)t * TILE;
         const unsigned int cin = s_bval[warp];
         const bool full = tile_full(t);
@@ -250,9 +277,20 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
         for (int r = 0; r < R; ++r) {
             const unsigned int p0 = 32u * E * r + E * lane;  // warp-local index of the lane's first element
             const unsigned int l0 = li0 + 32u * E * r;        // its tile-local index
+            // the scanned value of element i: for the reduce, the lane-local
+            // value plus the lane's carry before its first head (computed only
+            // where a sum is written)
+            auto yv = [&](int i) -> unsigned int {
+                unsigned int v = comp(x[Q * r + i / 4], i % 4) + (p0 + i < pfirst ? cin : 0u);
+                if constexpr (!WRITE_SCAN)
+                    if ((((hb >> (E * r)) & kEMask) & ((2u << i) - 1u)) == 0u) v += cl[r];
+                return v;
+            };
             unsigned int y[E];
+            if constexpr (WRITE_SCAN) {
 #pragma unroll
-            for (int i = 0; i < E; ++i) y[i] = comp(x[Q * r + i / 4], i % 4) + (p0 + i < pfirst ? cin : 0u);
+                for (int i = 0; i < E; ++i) y[i] = yv(i);
+            }
             if (WRITE_SCAN) {
                 if (full) {
 #pragma unroll
@@ -274,20 +312,29 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
                 unsigned int wrap = next_first;
                 if (r + 1 < R) wrap = __shfl_sync(0xffffffffu, (hb >> (E * (r + 1))) & 1u, 0);
                 const unsigned int after = lane < 31 ? down : wrap;
-                const unsigned int next_bits = (b >> 1) | (after << (E - 1));  // bit i: element i + 1 is a head
-                const bool last_here = last_li - l0 < (unsigned int)E;  // the array's last element is one of mine
+                // bit i: element i ends a segment (element i + 1 is a head, or
+                // element i is the array's last); only elements in the array
+                unsigned int ends = (b >> 1) | (after << (E - 1));
+                const unsigned int d_last = last_li - l0;
+                if (d_last < (unsigned int)E) ends |= 1u << d_last;
+                if (!full) {
+                    const unsigned int a0 = lo > l0 ? (lo - l0 < (unsigned int)E ? lo - l0 : (unsigned int)E) : 0u;
+                    const unsigned int a1 = hi > l0 ? (hi - l0 < (unsigned int)E ? hi - l0 : (unsigned int)E) : 0u;
+                    ends &= ((1u << a1) - 1u) & ~((1u << a0) - 1u);
+                }
                 const unsigned int pc = (unsigned int)__popc(b);
                 // Most rounds of long segments hold no segment end: skip them.
-                if (__any_sync(0xffffffffu, next_bits != 0u || last_here)) {
-                    const unsigned int incl = warp_inclusive_sum(pc, lane);
+                if (__any_sync(0xffffffffu, ends != 0u)) {
+                    // sum index of element i's segment: heads before this lane,
+                    // plus the lane's heads up to i, minus one (in 64 bits)
+                    const unsigned int kb = hbase + (warp_inclusive_sum(pc, lane) - pc);
 #pragma unroll
                     for (int i = 0; i < E; ++i) {
-                        const unsigned int li = l0 + i;
-                        const bool end = li >= lo && li < hi && (((next_bits >> i) & 1u) || li == last_li);
-                        if (end) {
-                            const unsigned long long k = (unsigned long long)hbase + (incl - pc) +
-                                                         (unsigned int)__popc(b & ((2u << i) - 1u)) - 1u;
-                            if (k < seg_cap) seg_sums[k] = y[i];
+                        if ((ends >> i) & 1u) {
+                            // at least one head (index 0's) lies at or before every end
+                            const unsigned long long k =
+                                (unsigned long long)kb + (unsigned int)__popc(b & ((2u << i) - 1u)) - 1ull;
+                            if (k < seg_cap) seg_sums[k] = WRITE_SCAN ? y[i] : yv(i);
                         }
                     }
                 }
@@ -297,8 +344,9 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
     };
 
     uint4 xc[V], xn[V];
+    unsigned int clc[R], cln[R];  // lanes' carries per round (the reduce only)
     unsigned int hbc = 0, hbn = 0, pfc = kNoHead, pfn = kNoHead;
-    unsigned int tc = read_tile(0, xc, hbc, pfc);
+    unsigned int tc = read_tile(0, xc, hbc, pfc, clc);
     // warp 0 keeps, per lane w < WARPS, what the look-back needs for the
     // current tile: the tile aggregate and warp w's exclusive offsets
     unsigned int agg_val = 0, agg_cnt = 0, wex_val = 0, wex_cnt = 0;
@@ -333,7 +381,7 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
         }
         if (warp == 0) block_aggregate(0, tc, agg_val, agg_head, agg_cnt, wex_val, head_before, wex_cnt);
         for (unsigned int u = 1;; ++u) {
-            const unsigned int tn = read_tile(u, xn, hbn, pfn);
+            const unsigned int tn = read_tile(u, xn, hbn, pfn, cln);
             const bool more = !__syncthreads_or(tn >= n_tiles);  // barrier A
             unsigned int n_val = 0, n_cnt = 0, n_xval = 0, n_xcnt = 0;
             bool n_head = false, n_before = false;
@@ -345,7 +393,7 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
             }
             if (warp == 0) {
                 if (more) block_aggregate((int)(u & 1u), tn, n_val, n_head, n_cnt, n_xval, n_before, n_xcnt);
-                const SegPrefix pre = lookback_seg(desc2, tc, tag, hdr, limit_ns, lane);
+                const SegPrefix pre = lookback_seg_wide<U32SCAN_S_LOOKA, U32SCAN_S_LOOKB>(desc2, tc, tag, hdr, limit_ns, lane);
                 if (lane == 0 && tc != 0 && tc != skip_tile) {
                     if (!agg_head) st_relaxed(desc2 + 2ull * tc, tag | kFlagP | (unsigned int)(pre.seg + agg_val));
                     st_relaxed(desc2 + 2ull * tc + 1, tag | kFlagP | (unsigned int)(pre.cnt + agg_cnt));
@@ -364,10 +412,12 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
                 }
             }
             __syncthreads();  // barrier B: carries of the current tile are visible
-            store_tile(tc, (int)((u - 1) % 3), xc, hbc, pfc);
+            store_tile(tc, (int)((u - 1) % 3), xc, hbc, pfc, clc);
             if (!more) break;
 #pragma unroll
             for (int r = 0; r < V; ++r) xc[r] = xn[r];
+#pragma unroll
+            for (int r = 0; r < R; ++r) clc[r] = cln[r];
             hbc = hbn;
             pfc = pfn;
             tc = tn;
@@ -405,25 +455,43 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
 #ifndef U32SCAN_S_V2B
 #define U32SCAN_S_V2B 8  // the same with byte flags
 #endif
-constexpr int kSThreads = 512, kSStages = U32SCAN_S_STAGES;
+#ifndef U32SCAN_S_T1
+#define U32SCAN_S_T1 512  // threads a block, scan only (512 / threads blocks an SM)
+#endif
+#ifndef U32SCAN_S_T2
+#define U32SCAN_S_T2 512  // threads a block, the forms that write sums
+#endif
+#ifndef U32SCAN_S_STAGES2
+#define U32SCAN_S_STAGES2 2  // ring stages of the eight-elements-a-round forms
+#endif
+template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
+constexpr int seg_threads() { return (WRITE_SCAN && !WANT_SUMS) ? U32SCAN_S_T1 : U32SCAN_S_T2; }
 template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
 constexpr int seg_q() { return (WRITE_SCAN && (!WANT_SUMS || sizeof(F) == 4)) ? 1 : 2; }
+template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
+constexpr int seg_stages() { return seg_q<WRITE_SCAN, WANT_SUMS, F>() == 1 ? U32SCAN_S_STAGES : U32SCAN_S_STAGES2; }
 template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
 constexpr int seg_v() {
     return seg_q<WRITE_SCAN, WANT_SUMS, F>() == 1 ? U32SCAN_S_V1 : (sizeof(F) == 1 ? U32SCAN_S_V2B : U32SCAN_S_V2);
 }
 template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
-constexpr unsigned long long seg_tile() { return (unsigned long long)kSThreads * seg_v<WRITE_SCAN, WANT_SUMS, F>() * 4; }
+constexpr unsigned long long seg_tile() {
+    return (unsigned long long)seg_threads<WRITE_SCAN, WANT_SUMS, F>() * seg_v<WRITE_SCAN, WANT_SUMS, F>() * 4;
+}
 template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
-constexpr size_t seg_smem() { return (size_t)kSStages * seg_tile<WRITE_SCAN, WANT_SUMS, F>() * (4 + sizeof(F)); }
+constexpr size_t seg_smem() {
+    return (size_t)seg_stages<WRITE_SCAN, WANT_SUMS, F>() * seg_tile<WRITE_SCAN, WANT_SUMS, F>() * (4 + sizeof(F));
+}
 static_assert(seg_smem<true, false, int32_t>() <= 227 * 1024 && seg_smem<true, true, int32_t>() <= 227 * 1024 &&
                   seg_smem<false, true, int32_t>() <= 227 * 1024 && seg_smem<false, true, uint8_t>() <= 227 * 1024 &&
                   seg_smem<true, true, uint8_t>() <= 227 * 1024,
               "shared memory");
 // the smallest tile, which has the most tiles, sizes the workspace
-constexpr unsigned long long kSTile = (unsigned long long)kSThreads * 4 *
-                                      (U32SCAN_S_V1 < U32SCAN_S_V2 ? (U32SCAN_S_V1 < U32SCAN_S_V2B ? U32SCAN_S_V1 : U32SCAN_S_V2B)
-                                                                   : (U32SCAN_S_V2 < U32SCAN_S_V2B ? U32SCAN_S_V2 : U32SCAN_S_V2B));
+constexpr unsigned long long min2(unsigned long long a, unsigned long long b) { return a < b ? a : b; }
+constexpr unsigned long long kSTile =
+    min2(min2(min2(seg_tile<true, false, int32_t>(), seg_tile<true, true, int32_t>()),
+              min2(seg_tile<false, true, int32_t>(), seg_tile<true, false, uint8_t>())),
+         min2(seg_tile<true, true, uint8_t>(), seg_tile<false, true, uint8_t>()));
 
 size_t segscan_workspace_bytes(unsigned long long n) {
     const unsigned long long tiles = (n + 3 + kSTile - 1) / kSTile;
@@ -454,8 +522,9 @@ static int segscan_launch(uint32_t *data, const F *flags, unsigned long long n, 
     const int aligned = ((reinterpret_cast<uintptr_t>(flags) - sizeof(F) * head) & 15) == 0;
     constexpr unsigned long long TILE = seg_tile<WRITE_SCAN, WANT_SUMS, F>();
     const unsigned int n_tiles = (unsigned int)((n + head + TILE - 1) / TILE);
-    auto kern = segscan_u32_persistent<kSThreads, seg_v<WRITE_SCAN, WANT_SUMS, F>(), seg_q<WRITE_SCAN, WANT_SUMS, F>(),
-                                       kSStages, WRITE_SCAN, WANT_SUMS, F>;
+    constexpr int THREADS = seg_threads<WRITE_SCAN, WANT_SUMS, F>();
+    auto kern = segscan_u32_persistent<THREADS, seg_v<WRITE_SCAN, WANT_SUMS, F>(), seg_q<WRITE_SCAN, WANT_SUMS, F>(),
+                                       seg_stages<WRITE_SCAN, WANT_SUMS, F>(), WRITE_SCAN, WANT_SUMS, F>;
     constexpr size_t smem = seg_smem<WRITE_SCAN, WANT_SUMS, F>();
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return U32SCAN_ECUDA;
@@ -473,10 +542,11 @@ static int segscan_launch(uint32_t *data, const F *flags, unsigned long long n, 
         }
         sms = g_seg_sms[dev];
     }
-    const unsigned int grid = n_tiles < (unsigned int)sms ? n_tiles : (unsigned int)sms;
+    const unsigned int slots = (unsigned int)sms * (512u / THREADS);  // blocks resident at once
+    const unsigned int grid = n_tiles < slots ? n_tiles : slots;
     WsHeader *hdr = static_cast<WsHeader *>(ws);
     unsigned long long *desc2 = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
-    kern<<<grid, kSThreads, smem, stream>>>(data, flags, n, seg_sums, seg_cap, nseg, hdr, desc2, n_tiles, head,
+    kern<<<grid, THREADS, smem, stream>>>(data, flags, n, seg_sums, seg_cap, nseg, hdr, desc2, n_tiles, head,
                                              aligned, skip_tile, limit_ns);
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }

@@ -305,68 +305,9 @@ struct SegPrefix {
     unsigned int cnt;  // heads before the tile
 };
 
-// Both look-backs of tile t (all 32 lanes call it), 32 words per round trip
-// each; word A stops at the nearest word with a head or a final value, word
-// B at the nearest final count.
-__device__ __forceinline__ SegPrefix lookback_seg(const unsigned long long *desc2, unsigned int t,
-                                                  unsigned long long tag, WsHeader *hdr,
-                                                  unsigned long long limit_ns, int lane) {
-    SegPrefix pre{0u, 0u};
-    if (t == 0) return pre;
-    long long pos_a = (long long)t - 1, pos_b = pos_a;
-    bool done_a = false, done_b = false;
-    unsigned long long wa = 0, wb = 0;
-    bool need_a = true, need_b = true;  // the window at pos_a / pos_b must be (re)loaded
-    unsigned long long t0 = 0;
-    for (unsigned int iter = 0;; ++iter) {
-        const long long ia = pos_a - lane, ib = pos_b - lane;
-        if (!done_a && need_a) wa = ia >= 0 ? ld_relaxed(desc2 + 2 * ia) : (tag | kFlagP);
-        if (!done_b && need_b) wb = ib >= 0 ? ld_relaxed(desc2 + 2 * ib + 1) : (tag | kFlagP);
-        bool waiting = false;
-        if (!done_a) {
-            const bool ready = (wa & kTagMask) == tag;
-            const unsigned int m = __ballot_sync(0xffffffffu, !ready || (wa & (kFlagP | kFlagH)));
-            const int k = m ? __ffs(m) - 1 : 31;
-            const bool k_ready = __shfl_sync(0xffffffffu, ready ? 1u : 0u, k) != 0;
-            if (k_ready) {
-                pre.seg += __reduce_add_sync(0xffffffffu, lane <= k ? (unsigned int)wa : 0u);
-                if (m) done_a = true; else pos_a -= 32;
-                need_a = true;
-            } else {
-                waiting = true;
-                need_a = !ready;  // reload only the words not ready yet
-            }
-        }
-        if (!done_b) {
-            const bool ready = (wb & kTagMask) == tag;
-            const unsigned int m = __ballot_sync(0xffffffffu, !ready || (wb & kFlagP));
-            const int k = m ? __ffs(m) - 1 : 31;
-            const bool k_ready = __shfl_sync(0xffffffffu, ready ? 1u : 0u, k) != 0;
-            if (k_ready) {
-                pre.cnt += __reduce_add_sync(0xffffffffu, lane <= k ? (unsigned int)wb : 0u);
-                if (m) done_b = true; else pos_b -= 32;
-                need_b = true;
-            } else {
-                waiting = true;
-                need_b = !ready;
-            }
-        }
-        if (done_a && done_b) return pre;
-        if (waiting) {
-            if (t0 == 0) t0 = __shfl_sync(0xffffffffu, globaltimer(), 0) | 1ull;
-            if (iter >= 8) __nanosleep(32);
-            const unsigned long long now = __shfl_sync(0xffffffffu, globaltimer(), 0);
-            if (now - t0 > limit_ns || iter >= kMaxSpinIters) {
-                if (lane == 0) report_timeout(hdr, t);
-                if (!done_a && (wa & kTagMask) != tag) wa = tag | kFlagP;
-                if (!done_b && (wb & kTagMask) != tag) wb = tag | kFlagP;
-                need_a = need_b = false;
-            }
-        }
-    }
-}
 
-// The same two look-backs, each with the library's windowed walk: word A
+// Both look-backs of tile t (all 32 lanes call it), each with the library's
+// windowed walk: word A
 // (stops at a word with a head or a final value) KA, word B (stops at a
 // final count) KB words a lane per round trip; both first windows are in
 // flight together. Word A usually stops one tile back (tiles that hold a

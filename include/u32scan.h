@@ -20,9 +20,10 @@
  *     u32scan_workspace_bytes(op, n) bytes (256-byte aligned). It must be
  *     zero-filled once before its first use (cudaMemset or
  *     u32scan_workspace_init); after that the library keeps it consistent
- *     itself, so it is reused across calls without clearing. A workspace
- *     serves one call at a time: calls that share one workspace must be
- *     ordered (the same stream, or events).
+ *     itself, so it is reused across calls and shared between operations
+ *     without clearing (the radix sort, which keeps data in it, clears what
+ *     it leaves where other operations keep tile state). A workspace serves one call at a time: calls that share one
+ *     workspace must be ordered (the same stream, or events).
  *   - Return value: U32SCAN_OK, or a negative status. Argument errors are
  *     found on the host before anything is launched; nothing is written
  *     then. U32SCAN_ECUDA reports a launch failure (cudaGetLastError).

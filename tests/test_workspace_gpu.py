@@ -80,3 +80,42 @@ def test_all_operations_share_one_workspace(u):
         ok, status = run_op(u, ws, which, n, 30 + k)
         assert status == _native.OK, (k, which, n)
         assert ok, (k, which, n)
+
+
+def test_radix_leaves_nothing_that_passes_for_tile_words(u):
+    """The radix sort keeps histograms and ping-pong buffers of keys and
+    indices in the workspace; with tie-heavy keys they hold small integers,
+    which (two to a 64-bit word) look like tile words tagged with a small
+    epoch. A fresh workspace keeps the epochs small, and each later call
+    here uses a size whose tile words cover where the sort's buffers were:
+    every result must still be exact."""
+    from u32_prefix_scan_gb300 import _native
+
+    lib = _native.lib()
+    big = 1 << 25
+    need = max([lib.u32scan_workspace_bytes(op, big) for op in (1, 2, 3, 6)] +
+               [lib.u32scan_workspace_bytes(4, 70001)])
+    for n_r in (1000, 70001):
+        for which in ("scan", "segscan", "compact", "values", "scan64"):
+            ws = u.Workspace(need, torch.device("cuda"))
+            k = inputs.radix_keys(n_r, 3, ties=True)
+            perm = u.radix_sort_perm_u32(dev32(k), workspace=ws)
+            assert np.array_equal(perm.cpu().numpy(), oracle.sort_perm(k))
+            if which in ("scan", "segscan", "compact"):
+                ok, status = run_op(u, ws, which, big, 5)
+            elif which == "values":
+                v, f = inputs.scan_values(big, 4), inputs.compact_flags(big, 4, 0.1)
+                out, count = u.compact_values_u32(dev32(v), dev32(f), workspace=ws)
+                want, used = oracle.compact_values(v, f, np.zeros(big, np.uint32))
+                ok = int(count.item()) == used and np.array_equal(host_u32(out)[:used], want[:used])
+                status = lib.u32scan_check(ws.ptr, torch.cuda.current_stream().cuda_stream)
+            else:
+                a = inputs.scan_values_u64(big, 5)
+                d = torch.from_numpy(a.view(np.int64).copy()).cuda()
+                total = u.scan_u64_op(d, "add", False, workspace=ws)
+                want, want_total = oracle.scan_op_u64(a, "add", False)
+                ok = np.array_equal(d.cpu().numpy().view(np.uint64), want) and \
+                    int(total.cpu().numpy().view(np.uint64)[0]) == want_total
+                status = lib.u32scan_check(ws.ptr, torch.cuda.current_stream().cuda_stream)
+            assert status == _native.OK, (n_r, which)
+            assert ok, (n_r, which)

@@ -17,11 +17,16 @@
 // stops waiting and finishes, so a kernel never hangs the GPU.
 //
 // Workspace: [header (256 B)] [tile words, 8 B each].
-// Descriptors carry a tag derived from a per-workspace call counter
-// ("epoch"), so words left by earlier calls read as "not ready" and the
-// workspace needs zeroing only once, before its first use. The block that
+// Descriptors carry a tag derived from a per-workspace launch counter
+// ("epoch"), so words left by earlier launches read as "not ready" and the
+// workspace needs zeroing only once, before its first use. That holds as
+// long as the workspace holds nothing but tile words at those offsets: the
+// radix sort, which also keeps histograms and its ping-pong buffers in the
+// workspace (stale small integers there could pass for tagged words), clears
+// its own tile words before its passes and, before it returns, the part of
+// the workspace any other operation's tile words can occupy. The block that
 // draws the last tile index resets the tile counter and advances the epoch
-// for the next call; every other block has read the epoch before its own
+// for the next launch; every other block has read the epoch before its own
 // draw, and the draw is an acq_rel RMW, so none can see the new epoch.
 #pragma once
 
@@ -54,6 +59,11 @@ constexpr unsigned long long kFlagH = 1ull << 33;
 constexpr unsigned long long kTagMask = ~((1ull << 34) - 1ull);
 
 __host__ __device__ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Clear workspace bytes on `stream` (see the workspace note above).
+static inline int clear_tile_words(void *p, size_t bytes, cudaStream_t stream) {
+    return cudaMemsetAsync(p, 0, bytes, stream) == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
+}
 
 __device__ __forceinline__ unsigned long long tag_of(unsigned int epoch) {
     return (unsigned long long)((epoch & 0x1FFFFFFFu) + 1u) << 34;

@@ -439,13 +439,25 @@ static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *per
         }
     }
     if (cudaMemsetAsync(hist, 0, 4 * 256 * 4, stream) != cudaSuccess) return U32SCAN_ECUDA;
+    // the digit passes' carry words (each pass's launch has its own tag)
+    if (const int rc = clear_tile_words(desc, 8ull * 256 * L.n_tiles, stream); rc != U32SCAN_OK) return rc;
     radix_histogram_kernel<<<1024, 512, 0, stream>>>(keys, n, hist);
     radix_plan_kernel<<<1, 128, 0, stream>>>(hist, n, plan, bases);
     for (int p = 0; p < 4; ++p)
         radix_onesweep_kernel<<<L.n_tiles, kRThreads, kRSmem, stream>>>(plan, p, keys, k1, k2, i1, perm, keys_out, n,
                                                                          L.n_tiles, bases, hdr, desc, kDefaultLimitNs);
     radix_identity_kernel<<<1024, 256, 0, stream>>>(plan, keys, perm, keys_out, n);
-    return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
+    if (cudaGetLastError() != cudaSuccess) return U32SCAN_ECUDA;
+    // Leave no data where another operation's tile words may go: the
+    // histograms, bases and ping-pong buffers hold small integers that could
+    // pass for tagged words. Any other operation's tile words lie within the
+    // largest workspace it can need (n below 2^32), a few MiB at most.
+    size_t reach = scan_workspace_bytes(0xffffffffull);
+    for (const size_t b : {segscan_workspace_bytes(0xffffffffull), compact_workspace_bytes(0xffffffffull),
+                           compact_values_workspace_bytes(0xffffffffull), scan64_workspace_bytes(0xffffffffull)})
+        reach = b > reach ? b : reach;
+    const size_t end = L.total < reach ? L.total : reach;
+    return clear_tile_words(w + kHeaderBytes, end - kHeaderBytes, stream);
 }
 
 }  // namespace u32scan

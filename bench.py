@@ -39,8 +39,11 @@ roofline   algorithmic bytes of one launch over its measured time, against
            same run (copy_gbs_same_run) and the nominal 7900 GB/s. For a
            step of several calls the dominant kernel is bracketed by its
            own events (kernel_ms).
-e2e        the same metric through the same C-ABI call, with pinned host
-           inputs copied in and the outputs copied out every step.
+e2e        the same metric end to end from pinned host memory: the add
+           scans call scan_{exclusive,inclusive}_u32_host, which streams the
+           host array through the device in chunks (copies in, scans and
+           copies out overlapped); the other ops copy their inputs in, make
+           the same C-ABI call and copy their outputs out, every step.
 cpu_baseline  the CPU oracle (one thread, as it stands) on a bounded sample.
 
 --impl reference times that oracle alone on the host cores (rank 0 only).
@@ -143,11 +146,18 @@ class ScanOp(Op):
         self.pinned_in = {"data": torch.from_numpy(host["data"].view(np.int32)).pin_memory()}
         self.pinned_out = {"data": torch.empty(self.n, dtype=torch.int32).pin_memory(),
                            "total": torch.empty(1, dtype=torch.int32).pin_memory()}
+        if self.monoid == "add":
+            self.host_fn = u.scan_inclusive_u32_host if self.inclusive else u.scan_exclusive_u32_host
+            self.ws_host = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_SCAN_HOST, self.n), dev)
 
     def step(self):
         self.fn(self.data, self.total, workspace=self.ws)
 
     def e2e_step(self):
+        if self.monoid == "add":  # host array in, host array out, through the device in overlapped chunks
+            self.host_fn(self.pinned_in["data"], self.pinned_out["data"], self.pinned_out["total"],
+                         workspace=self.ws_host)
+            return 4 * self.n, 4 * self.n + 4
         self.data.copy_(self.pinned_in["data"], non_blocking=True)
         self.step()
         self.pinned_out["data"].copy_(self.data, non_blocking=True)
@@ -163,6 +173,9 @@ class ScanOp(Op):
         k = min(self.n, 1 << 20)
         got = self.pinned_out["data"][:k].numpy().view(np.uint32)
         a = host["data"][:k]
+        total = int(self.pinned_out["total"].numpy().view(np.uint32)[0])
+        if total != int(host["data"].sum(dtype=np.uint64)) % (1 << 32):
+            return False
         if self.inclusive:
             return got[0] == a[0] and np.array_equal(got[1:] - got[:-1], a[1:])
         return got[0] == 0 and np.array_equal(got[1:] - got[:-1], a[:-1])
@@ -1051,6 +1064,8 @@ def run_ours(args, rank, local_rank, world):
         e_end.record(stream)
         torch.cuda.synchronize()
         op.u.check(workspace=op.ws)
+        if getattr(op, "ws_host", None) is not None:
+            op.u.check(workspace=op.ws_host)
         e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.e2e_steps, world)
         if not op.check_e2e(host):
             raise SystemExit("bench: e2e result fails its property check")

@@ -10,9 +10,11 @@
  * Conventions for every entry point below:
  *   - Pointers named as device pointers must point to memory the current
  *     CUDA device can access (cudaMalloc, torch tensors, managed memory),
- *     aligned to 4 bytes. 16-byte alignment is not required.
+ *     aligned to 4 bytes. 16-byte alignment is not required. Only the
+ *     *_host scans take host pointers, and say so.
  *   - Every call is asynchronous on `stream` (NULL = the legacy default
- *     stream). Results, totals and counts stay in device memory.
+ *     stream). Results, totals and counts stay in device memory (the
+ *     *_host scans write theirs to host memory).
  *   - The caller owns every buffer. The library allocates no memory and
  *     keeps no state between calls other than what lives in `ws` (and, for
  *     scan_exclusive_u32_noalloc, in that entry point's own static array).
@@ -22,8 +24,9 @@
  *     u32scan_workspace_init); after that the library keeps it consistent
  *     itself, so it is reused across calls and shared between operations
  *     without clearing (the radix sort, which keeps data in it, clears what
- *     it leaves where other operations keep tile state). A workspace serves one call at a time: calls that share one
- *     workspace must be ordered (the same stream, or events).
+ *     it leaves where other operations keep tile state). A workspace serves
+ *     one call at a time: calls that share one workspace must be ordered
+ *     (the same stream, or events).
  *   - Return value: U32SCAN_OK, or a negative status. Argument errors are
  *     found on the host before anything is launched; nothing is written
  *     then. U32SCAN_ECUDA reports a launch failure (cudaGetLastError).
@@ -69,6 +72,7 @@ typedef struct CUstream_st *u32scan_stream_t;
 #define U32SCAN_OP_RADIX 4     /* radix_sort_perm_u32, radix_sort_u32 */
 #define U32SCAN_OP_RUNS 5      /* runs_layout_u32 (runs_owner_u32 needs none) */
 #define U32SCAN_OP_SCAN64 6    /* scan_u64_op */
+#define U32SCAN_OP_SCAN_HOST 7 /* scan_exclusive_u32_host, scan_inclusive_u32_host */
 
 /* Bytes of device workspace an operation needs for n elements (a multiple
  * of 256, at least 256). Returns 0 for an unknown op. Pure host function. */
@@ -113,6 +117,38 @@ int scan_exclusive_u32(uint32_t *data, size_t n, uint32_t *total,
  */
 int scan_inclusive_u32(uint32_t *data, size_t n, uint32_t *total,
                        void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * The same two scans of an array in HOST memory, with the result written to
+ * host memory. Source: as scan_exclusive_u32 / scan_inclusive_u32
+ * ("scan.bend source", section API; CAIRN "scan"); the pages' arrays live in
+ * device memory, and these entry points carry a host array through the
+ * device scan. The array moves in chunks through staging slots in `ws`:
+ * copies in, chunk scans and copies out overlap on three streams (two
+ * created inside the call, released when their work completes), and each
+ * chunk's scan starts from the wrapped sum of the chunks before it.
+ *   host_in     HOST, uint32_t[n], page-locked (cudaHostAlloc, cudaMallocHost,
+ *               cudaHostRegister; torch pin_memory), read only.
+ *   host_out    HOST, uint32_t[n], page-locked: the scan. May be host_in
+ *               itself (in place); must not overlap it otherwise.
+ *   n           element count, any n below 2^62.
+ *   host_total  HOST, one page-locked uint32_t, or NULL: the wrapped total.
+ *   ws, ws_bytes  device, u32scan_workspace_bytes(U32SCAN_OP_SCAN_HOST, n)
+ *               bytes (at most about 64 MiB of staging plus the scan's
+ *               carry words), 256-byte aligned, zero-filled once.
+ *   stream      the scans run on it; the call returns at once, and the
+ *               outputs are complete when `stream` reaches the point of the
+ *               call (cudaStreamSynchronize(stream) waits for them).
+ * Errors: EINVAL (null in/out with n > 0, pointers not 4-byte aligned, host
+ * buffers not page-locked, partial overlap of in and out, total overlapping
+ * either, n >= 2^62), EWORKSPACE, ECUDA (a stream, event, copy or launch
+ * failed; work already queued still completes before later work on
+ * `stream`). A carry-wait timeout is reported by u32scan_check(ws, stream).
+ */
+int scan_exclusive_u32_host(const uint32_t *host_in, uint32_t *host_out, size_t n, uint32_t *host_total,
+                            void *ws, size_t ws_bytes, u32scan_stream_t stream);
+int scan_inclusive_u32_host(const uint32_t *host_in, uint32_t *host_out, size_t n, uint32_t *host_total,
+                            void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /*
  * Scan in place under any of the U32SCAN_ADD .. U32SCAN_MAX operators.

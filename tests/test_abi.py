@@ -222,3 +222,29 @@ def test_scan_u64_rejects_bad_arguments_on_host(lib):
     assert fn(0, 0, fake, 1 << 32, None, fake, need, None) == _native.EINVAL
     assert fn(0, 0, fake, 1000, None, None, need, None) == _native.EWORKSPACE
     assert fn(0, 0, fake, 1000, None, fake + 8, need, None) == _native.EWORKSPACE  # misaligned workspace
+
+
+@pytest.mark.parametrize("name", ["scan_exclusive_u32_host", "scan_inclusive_u32_host"])
+def test_host_scan_rejects_bad_arguments_on_host(lib, name):
+    fn = getattr(lib, name)
+    fake = 0x100000  # never dereferenced: every case below fails a check before any CUDA call
+    need = lib.u32scan_workspace_bytes(_native.OP_SCAN_HOST, 1000)
+    assert fn(None, fake, 10, None, fake, need, None) == _native.EINVAL                 # no input
+    assert fn(fake, None, 10, None, fake, need, None) == _native.EINVAL                 # no output
+    assert fn(fake + 2, fake + 8000, 10, None, fake, need, None) == _native.EINVAL      # misaligned input
+    assert fn(fake, fake + 8001, 10, None, fake, need, None) == _native.EINVAL          # misaligned output
+    assert fn(fake, fake + 8000, 10, fake + 9001, fake, need, None) == _native.EINVAL   # misaligned total
+    assert fn(fake, fake + 400, 1000, None, fake, need, None) == _native.EINVAL         # partial overlap
+    assert fn(fake + 400, fake, 1000, None, fake, need, None) == _native.EINVAL         # partial overlap
+    assert fn(fake, fake + 8000, 1 << 62, None, fake, 1 << 40, None) == _native.EINVAL  # n too large
+
+
+def test_host_scan_workspace_bytes(lib):
+    wb = lib.u32scan_workspace_bytes
+    for n in (1, 1000, (1 << 18) + 1, 1 << 22, (1 << 25) + 7, 1 << 28, 1 << 34):
+        b = wb(_native.OP_SCAN_HOST, n)
+        assert b % 256 == 0
+        # room for the whole array when it is short, else at least two 2^18-element staging slots
+        assert b >= 4 * min(n, 2 << 18)
+        # and never more than four 2^22-element slots plus the carry words
+        assert b <= 4 * 4 * (1 << 22) + wb(_native.OP_SCAN, 1 << 22) + wb(_native.OP_SCAN, (1 << 22) - 1) + 512

@@ -10,6 +10,8 @@ _API = {
     "Workspace",
     "scan_exclusive_u32",
     "scan_inclusive_u32",
+    "scan_exclusive_u32_host",
+    "scan_inclusive_u32_host",
     "scan_u32_op",
     "scan_u64_op",
     "segscan_inclusive_u32",

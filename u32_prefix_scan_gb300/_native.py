@@ -25,6 +25,7 @@ OP_COMPACT = 3
 OP_RADIX = 4
 OP_RUNS = 5
 OP_SCAN64 = 6
+OP_SCAN_HOST = 7
 
 _vp = ctypes.c_void_p
 _sz = ctypes.c_size_t
@@ -40,6 +41,8 @@ SIGNATURES = {
     "scan_exclusive_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
     "scan_inclusive_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
     "scan_exclusive_u32_noalloc": (_int, [_vp, _sz, _vp, _vp]),
+    "scan_exclusive_u32_host": (_int, [_vp, _vp, _sz, _vp, _vp, _sz, _vp]),
+    "scan_inclusive_u32_host": (_int, [_vp, _vp, _sz, _vp, _vp, _sz, _vp]),
     "scan_u32_op": (_int, [_int, _int, _vp, _sz, _vp, _vp, _sz, _vp]),
     "scan_u64_op": (_int, [_int, _int, _vp, _sz, _vp, _vp, _sz, _vp]),
     "segscan_inclusive_u32": (_int, [_vp, _vp, _sz, _vp, _sz, _vp, _vp, _sz, _vp]),

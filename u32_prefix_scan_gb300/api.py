@@ -21,6 +21,8 @@ __all__ = [
     "Workspace",
     "scan_exclusive_u32",
     "scan_inclusive_u32",
+    "scan_exclusive_u32_host",
+    "scan_inclusive_u32_host",
     "scan_u32_op",
     "scan_u64_op",
     "segscan_inclusive_u32",
@@ -125,6 +127,56 @@ def scan_inclusive_u32(data: torch.Tensor, total: torch.Tensor | None = None, *,
     """In place: data[j] <- data[0] + .. + data[j] (mod 2^32). Returns the
     one-element device tensor holding the wrapped total."""
     return _scan("scan_inclusive_u32", data, total, stream, workspace)
+
+
+def _require_pinned(t: torch.Tensor, name: str) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    # an empty tensor has no storage to pin and is never read
+    if t.device.type != "cpu" or (t.numel() > 0 and not t.is_pinned()):
+        raise ValueError(f"{name} must be a pinned (page-locked) CPU tensor")
+    if t.dtype not in _U32_DTYPES:
+        raise TypeError(f"{name} must have dtype in {_U32_DTYPES}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _scan_host(name: str, host_in: torch.Tensor, host_out, total, device, stream, workspace):
+    _require_pinned(host_in, "host_in")
+    if host_out is None:
+        host_out = torch.empty_like(host_in).pin_memory()
+    _require_pinned(host_out, "host_out")
+    if host_out.numel() != host_in.numel():
+        raise ValueError("host_in and host_out differ in length")
+    if total is None:
+        total = torch.empty(1, dtype=host_in.dtype).pin_memory()
+    _require_pinned(total, "total")
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    n = host_in.numel()
+    with torch.cuda.device(device):
+        sh = _stream_handle(stream)
+        ws = _ws(_native.OP_SCAN_HOST, n, device, sh, workspace)
+        fn = getattr(_native.lib(), name)
+        _native.check(fn(host_in.data_ptr(), host_out.data_ptr(), n, total.data_ptr(), ws.ptr, ws.nbytes, sh), name)
+    return host_out, total
+
+
+def scan_exclusive_u32_host(host_in: torch.Tensor, host_out: torch.Tensor | None = None,
+                            total: torch.Tensor | None = None, *, device=None, stream=None,
+                            workspace: Workspace | None = None):
+    """Exclusive scan of a pinned host array into a pinned host array (may be
+    host_in itself), through the device. Asynchronous on the stream: the
+    outputs are complete once the stream reaches the call. Returns
+    (host_out, total), total a one-element pinned tensor."""
+    return _scan_host("scan_exclusive_u32_host", host_in, host_out, total, device, stream, workspace)
+
+
+def scan_inclusive_u32_host(host_in: torch.Tensor, host_out: torch.Tensor | None = None,
+                            total: torch.Tensor | None = None, *, device=None, stream=None,
+                            workspace: Workspace | None = None):
+    """Inclusive scan of a pinned host array; otherwise as
+    scan_exclusive_u32_host."""
+    return _scan_host("scan_inclusive_u32_host", host_in, host_out, total, device, stream, workspace)
 
 
 def scan_u32_op(data: torch.Tensor, op: str, inclusive: bool = False, total: torch.Tensor | None = None, *,

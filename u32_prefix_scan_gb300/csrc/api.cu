@@ -23,6 +23,8 @@ extern "C" size_t u32scan_workspace_bytes(int op, size_t n) {
         return scan_workspace_bytes(n);
     case U32SCAN_OP_SCAN64:
         return scan64_workspace_bytes(n);
+    case U32SCAN_OP_SCAN_HOST:
+        return scan_host_workspace_bytes(n);
     default:
         return 0;
     }

@@ -419,13 +419,19 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 
 // Host-side workspace sizing of each operation (defined beside its kernels).
 size_t scan_workspace_bytes(unsigned long long n);
+size_t scan_workspace_bytes_upto(unsigned long long m);
+size_t scan_host_workspace_bytes(unsigned long long n);
 size_t segscan_workspace_bytes(unsigned long long n);
 size_t compact_workspace_bytes(unsigned long long n);
 size_t radix_workspace_bytes(unsigned long long n);
 size_t compact_values_workspace_bytes(unsigned long long n);
 size_t scan64_workspace_bytes(unsigned long long n);
 
-// In-library launch of the inclusive scan with its total (the runs layout).
+// In-library launches of the add-scan: one chunk of a longer array after a
+// device carry-in (the host-buffer pipeline), and the inclusive scan with
+// its total (the runs layout).
+int scan_chunk_launch(bool inclusive, uint32_t *data, unsigned long long n, const uint32_t *carry_in,
+                      uint32_t *total, void *ws, size_t ws_bytes, cudaStream_t stream);
 int scan_inclusive_launch(uint32_t *data, unsigned long long n, uint32_t *total, void *ws, size_t ws_bytes,
                           cudaStream_t stream);
 

@@ -84,7 +84,8 @@ __device__ __forceinline__ unsigned int warp_scan_rounds(uint4 (&x)[V], int lane
 // One tile per block, for short arrays: enough blocks to fill the GPU.
 template <int THREADS, int V, bool INCLUSIVE, int OP>
 __global__ void __launch_bounds__(THREADS, (THREADS >= 512 ? 2 : 4))
-scan_u32_kernel(uint32_t *__restrict__ data, unsigned long long n, uint32_t *total, WsHeader *hdr,
+scan_u32_kernel(uint32_t *__restrict__ data, unsigned long long n, uint32_t *total, const uint32_t *carry_in,
+                WsHeader *hdr,
                 unsigned long long *desc, unsigned int n_tiles, unsigned int head, unsigned int skip_tile,
                 unsigned long long limit_ns) {
     using M = Monoid<OP>;
@@ -143,10 +144,13 @@ scan_u32_kernel(uint32_t *__restrict__ data, unsigned long long n, uint32_t *tot
         const unsigned int agg = __shfl_sync(0xffffffffu, winc, 31);
         const unsigned int wex = M::warp_exclusive(winc, wt, lane);
         const bool publish = t != skip_tile;
-        if (lane == 0 && publish) publish_aggregate(desc, t, agg, tag);
+        // Everything before the array folds into tile 0: the carry-in, else the identity.
+        const unsigned int cin = (t == 0 && carry_in != nullptr) ? *carry_in : M::identity();
+        if (lane == 0 && publish) publish_aggregate(desc, t, M::apply(cin, agg), tag);
         unsigned long long win[1];
         lookback_window<1, OP>(desc, (long long)t - 1, tag, lane, win);
-        const unsigned int prefix = lookback_prefix_wide<1, OP>(desc, t, tag, hdr, limit_ns, lane, win);
+        const unsigned int prefix =
+            M::apply(cin, lookback_prefix_wide<1, OP>(desc, t, tag, hdr, limit_ns, lane, win));
         if (lane == 0 && publish && t != 0) publish_inclusive(desc, t, M::apply(prefix, agg), tag);
         if (lane < WARPS) s_warp[lane] = M::apply(prefix, wex);
         if (t == n_tiles - 1u && lane == 0 && total != nullptr) *total = M::apply(prefix, agg);
@@ -197,7 +201,8 @@ scan_u32_kernel(uint32_t *__restrict__ data, unsigned long long n, uint32_t *tot
 // last of the launch and re-arms the header.
 template <int THREADS, int V, int S, int K, bool INCLUSIVE, int OP>
 __global__ void __launch_bounds__(THREADS, U32SCAN_P_MINB)
-scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t *total, WsHeader *hdr,
+scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t *total, const uint32_t *carry_in,
+                    WsHeader *hdr,
                     unsigned long long *desc, unsigned int n_tiles, unsigned int head, unsigned int skip_tile,
                     unsigned long long limit_ns) {
     using M = Monoid<OP>;
@@ -243,6 +248,11 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
     };
     const unsigned int li0 = (unsigned int)warp * (128 * V) + 4u * (unsigned int)lane;
     volatile unsigned int *vs_tile = s_tile;
+    // The fold of everything before tile t's array start: the carry-in for
+    // tile 0 (when given), the identity otherwise.
+    auto carry_of = [&](unsigned int t) -> unsigned int {
+        return (t == 0 && carry_in != nullptr) ? *carry_in : M::identity();
+    };
 
     // Read draw number u (stage u % S) into x and scan it per warp; the warp
     // totals go to s_wt[u & 1]. Returns the tile index, n_tiles if the draw
@@ -352,7 +362,7 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
         }
         if (warp == 0) {
             agg_c = block_aggregate(0, wex_c);
-            if (lane == 0 && tc != skip_tile) publish_aggregate(desc, tc, agg_c, tag);
+            if (lane == 0 && tc != skip_tile) publish_aggregate(desc, tc, M::apply(carry_of(tc), agg_c), tag);
         }
         for (unsigned int u = 1;; ++u) {
             // Look ahead: read draw u and publish its aggregate.
@@ -368,12 +378,13 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
             if (warp == 0) {
                 if (more) {
                     agg_n = block_aggregate((int)(u & 1), wex_n);
-                    if (lane == 0 && tn != skip_tile) publish_aggregate(desc, tn, agg_n, tag);
+                    if (lane == 0 && tn != skip_tile) publish_aggregate(desc, tn, M::apply(carry_of(tn), agg_n), tag);
                 }
                 // Finish the current tile: its look-back, inclusive prefix, bases.
                 unsigned long long win[K];
                 lookback_window<K, OP>(desc, (long long)tc - 1, tag, lane, win);
-                const unsigned int prefix = lookback_prefix_wide<K, OP>(desc, tc, tag, hdr, limit_ns, lane, win);
+                const unsigned int prefix =
+                    M::apply(carry_of(tc), lookback_prefix_wide<K, OP>(desc, tc, tag, hdr, limit_ns, lane, win));
                 if (lane == 0 && tc != 0 && tc != skip_tile)
                     publish_inclusive(desc, tc, M::apply(prefix, agg_c), tag);
                 if (lane < WARPS) s_base[lane] = M::apply(prefix, wex_c);
@@ -458,12 +469,16 @@ static int persistent_grid(int *grid_out) {
 
 template <bool INCLUSIVE, int OP = kAdd>
 static int scan_launch(uint32_t *data, unsigned long long n, uint32_t *total, void *ws, size_t ws_bytes,
-                       cudaStream_t stream, unsigned int skip_tile, unsigned long long limit_ns) {
+                       cudaStream_t stream, unsigned int skip_tile, unsigned long long limit_ns,
+                       const uint32_t *carry_in = nullptr) {
     if ((n > 0 && data == nullptr) || n >= (1ull << 32)) return U32SCAN_EINVAL;
     if ((reinterpret_cast<uintptr_t>(data) & 3) || (reinterpret_cast<uintptr_t>(total) & 3))
         return U32SCAN_EINVAL;
     if (n == 0) {
-        if (total) {  // the fold of nothing is the operator's identity
+        if (total && carry_in) {  // nothing after the carry-in: the fold is the carry-in
+            if (cudaMemcpyAsync(total, carry_in, sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+                return U32SCAN_ECUDA;
+        } else if (total) {  // the fold of nothing is the operator's identity
             const unsigned int id = OP == kMul ? 1u : (OP == kAnd || OP == kMin) ? 0xffffffffu : 0u;
             if (cudaMemsetAsync(total, id ? 0xff : 0, sizeof(uint32_t), stream) != cudaSuccess) return U32SCAN_ECUDA;
             if (id == 1u && cudaMemcpyAsync(total, &kOne, sizeof(uint32_t), cudaMemcpyHostToDevice, stream) != cudaSuccess)
@@ -484,12 +499,32 @@ static int scan_launch(uint32_t *data, unsigned long long n, uint32_t *total, vo
         if (rc != U32SCAN_OK) return rc;
         if ((unsigned int)grid > n_tiles) grid = (int)n_tiles;
         scan_u32_persistent<kPThreads, kPV, kPStages, kPLook, INCLUSIVE, OP><<<grid, kPThreads, kPSmem, stream>>>(
-            data, n, total, hdr, desc, n_tiles, head, skip_tile, limit_ns);
+            data, n, total, carry_in, hdr, desc, n_tiles, head, skip_tile, limit_ns);
     } else {
-        scan_u32_kernel<256, 2, INCLUSIVE, OP><<<n_tiles, 256, 0, stream>>>(data, n, total, hdr, desc, n_tiles, head,
-                                                                        skip_tile, limit_ns);
+        scan_u32_kernel<256, 2, INCLUSIVE, OP><<<n_tiles, 256, 0, stream>>>(data, n, total, carry_in, hdr, desc,
+                                                                        n_tiles, head, skip_tile, limit_ns);
     }
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
+}
+
+// Workspace bytes that serve a scan of any length from 1 to m (the
+// one-tile-per-block kernel of lengths below the persistent threshold has
+// more, smaller tiles).
+size_t scan_workspace_bytes_upto(unsigned long long m) {
+    const size_t a = scan_workspace_bytes(m);
+    if (m < kPersistentMinN) return a;
+    const size_t b = scan_workspace_bytes(kPersistentMinN - 1);
+    return a > b ? a : b;
+}
+
+// One chunk of a longer add-scan: carry_in (device, or NULL for none) is
+// the wrapped sum of everything before the chunk; total gets the carry-in
+// plus the chunk's sum. total must not be carry_in: the block holding tile 0
+// may read the carry-in after the last tile has written the total.
+int scan_chunk_launch(bool inclusive, uint32_t *data, unsigned long long n, const uint32_t *carry_in,
+                      uint32_t *total, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return inclusive ? scan_launch<true>(data, n, total, ws, ws_bytes, stream, 0xffffffffu, kDefaultLimitNs, carry_in)
+                     : scan_launch<false>(data, n, total, ws, ws_bytes, stream, 0xffffffffu, kDefaultLimitNs, carry_in);
 }
 
 // The inclusive form with its total, for the runs layout.

@@ -134,8 +134,8 @@ int scan_inclusive_u32(uint32_t *data, size_t n, uint32_t *total,
  *   n           element count, any n below 2^62.
  *   host_total  HOST, one page-locked uint32_t, or NULL: the wrapped total.
  *   ws, ws_bytes  device, u32scan_workspace_bytes(U32SCAN_OP_SCAN_HOST, n)
- *               bytes (at most about 64 MiB of staging plus the scan's
- *               carry words), 256-byte aligned, zero-filled once.
+ *               bytes (at most 128 MiB of staging plus the scan's carry
+ *               words), 256-byte aligned, zero-filled once.
  *   stream      the scans run on it; the call returns at once, and the
  *               outputs are complete when `stream` reaches the point of the
  *               call (cudaStreamSynchronize(stream) waits for them).

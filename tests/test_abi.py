@@ -246,5 +246,5 @@ def test_host_scan_workspace_bytes(lib):
         assert b % 256 == 0
         # room for the whole array when it is short, else at least two 2^18-element staging slots
         assert b >= 4 * min(n, 2 << 18)
-        # and never more than four 2^22-element slots plus the carry words
-        assert b <= 4 * 4 * (1 << 22) + wb(_native.OP_SCAN, 1 << 22) + wb(_native.OP_SCAN, (1 << 22) - 1) + 512
+        # and never more than four 2^23-element slots plus the carry words
+        assert b <= 4 * 4 * (1 << 23) + wb(_native.OP_SCAN, 1 << 23) + wb(_native.OP_SCAN, (1 << 22) - 1) + 512

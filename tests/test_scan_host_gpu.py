@@ -46,7 +46,8 @@ def want(inclusive, a):
 
 
 # one chunk; 2^18-element chunks (2, 5 and 9 of them: the 4-slot ring wraps);
-# 2^22-element chunks with a short last chunk (persistent and small kernels)
+# eight chunks just over 2^22 elements with a last one just under (the
+# persistent and the one-tile-per-block kernels)
 SIZES = [1, 2, 5, 1000, (1 << 18) - 3, (1 << 18) + 7, 5 * (1 << 18) - 1, (1 << 21) + 12345,
          (1 << 25) + 777]
 

@@ -27,13 +27,16 @@
 
 namespace u32scan {
 
-// Chunk sizes in elements: at most 2^22 (16 MiB, about 0.1 ms on the link
+// Chunk sizes in elements: at most 2^23 (32 MiB, about 0.2 ms on the link
 // each way), at least 2^18, else about an eighth of the array so that short
-// arrays still overlap their copies. Staging slots: one being copied in, one
-// being scanned, one being copied out, and spares. Both can be overridden at
-// build time for sweeps.
+// arrays still overlap their copies. Each chunk costs about 6.5 us beyond
+// its bytes (measured on GB300 at n = 2^28: 2^20-element chunks 8.0 ms,
+// 2^21 7.4, 2^22 6.96, 2^23 6.75), so chunks are as long as the fill and
+// drain of the pipeline allow. Staging slots: one being copied in, one
+// being scanned, one being copied out, and a spare (3, 4 and 8 slots
+// measured alike). Both can be overridden at build time for sweeps.
 #ifndef U32SCAN_H_CHUNK_LOG2
-#define U32SCAN_H_CHUNK_LOG2 22
+#define U32SCAN_H_CHUNK_LOG2 23
 #endif
 #ifndef U32SCAN_H_RING
 #define U32SCAN_H_RING 4

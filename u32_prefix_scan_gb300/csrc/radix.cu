@@ -16,13 +16,14 @@
 // value come first) and finds digits that are equal for every key, whose
 // passes are skipped (exact: such a pass moves nothing). Each digit pass is
 // then one kernel over tiles of 8192 keys drawn in order: a tile ranks its
-// keys stably within itself (eight ballots per 32 keys give each key its
-// rank among the warp's keys of its digit value), publishes its 256 digit
-// counts, and finds for every digit value the count of that value in all
-// earlier tiles by a decoupled look-back (thread v walks back over the
-// earlier tiles' words for value v, several a round trip, until one holds an
-// inclusive count), so
-// each key's slot is base + earlier count + rank; the tile is ordered by
+// keys stably within itself (for each 32 keys of a warp, a per-warp
+// shared-memory mask per digit value collects the lanes holding that value,
+// which gives each key its rank among the warp's keys of its value),
+// publishes its 256 digit counts, and finds for every digit value the count
+// of that value in all earlier tiles by a decoupled look-back (thread v
+// walks back over the earlier tiles' words for value v, several a round
+// trip, until one holds an inclusive count), so each key's slot is
+// base + earlier count + rank; the tile is ordered by
 // digit value in shared memory and written out run by run. Which passes run,
 // and which buffers they read and write, is decided on the device, so the
 // call stays asynchronous. The last pass writes the indices into `perm` and,
@@ -36,12 +37,29 @@
 
 namespace u32scan {
 
-constexpr int kRThreads = 512;
-constexpr int kRKeys = 16;  // keys per thread per tile
+// Digit-pass shape: threads per block, keys per thread per tile, resident
+// blocks per SM (the launch bound); chosen by measurement on GB300 and
+// overridable at build time for sweeps.
+#ifndef U32SCAN_R_THREADS
+#define U32SCAN_R_THREADS 512
+#endif
+#ifndef U32SCAN_R_KEYS
+#define U32SCAN_R_KEYS 16
+#endif
+#ifndef U32SCAN_R_MINB
+#define U32SCAN_R_MINB 2
+#endif
+constexpr int kRThreads = U32SCAN_R_THREADS;
+constexpr int kRKeys = U32SCAN_R_KEYS;  // keys per thread per tile
 constexpr unsigned int kRTile = kRThreads * kRKeys;
 constexpr int kRWarps = kRThreads / 32;
+static_assert(kRThreads >= 256 && kRThreads % 32 == 0 && kRKeys <= 32, "a thread per digit value; key bits fit a word");
+// How a warp finds the lanes whose key has the same digit value:
+// 0: eight ballots, one per digit bit; 1: the match-any instruction;
+// 2: every lane sets its bit in a per-warp shared-memory mask word of its
+//    digit value (one shared atomic OR), and reads the word back.
 #ifndef U32SCAN_R_MATCH
-#define U32SCAN_R_MATCH 0  // 1: rank by the match-any instruction instead of eight ballots
+#define U32SCAN_R_MATCH 2
 #endif
 #ifndef U32SCAN_R_LOOK
 #define U32SCAN_R_LOOK 8
@@ -96,15 +114,17 @@ __global__ void radix_histogram_kernel(const uint32_t *__restrict__ keys, unsign
         atomicAdd(&s_h[2][(k >> 16) & 255u], 1u);
         atomicAdd(&s_h[3][k >> 24], 1u);
     };
-    // scalar head up to 16-byte alignment, 16-byte body, scalar tail
-    const unsigned long long head = ((16 - (reinterpret_cast<uintptr_t>(keys) & 15)) & 15) / 4;
-    const unsigned long long h = head < n ? head : n;
-    const unsigned long long nv = (n - h) / 4;
-    const unsigned long long gtid = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const unsigned long long gstride = (unsigned long long)gridDim.x * blockDim.x;
+    // scalar head up to 16-byte alignment, 16-byte body, scalar tail; n < 2^31
+    // for a radix sort, so 32-bit indices suffice
+    const unsigned int n32 = (unsigned int)n;
+    const unsigned int head = (unsigned int)((16 - (reinterpret_cast<uintptr_t>(keys) & 15)) & 15) / 4;
+    const unsigned int h = head < n32 ? head : n32;
+    const unsigned int nv = (n32 - h) / 4;
+    const unsigned int gtid = blockIdx.x * blockDim.x + threadIdx.x;
+    const unsigned int gstride = gridDim.x * blockDim.x;
     if (gtid < h) add(keys[gtid]);
     const uint4 *kv = reinterpret_cast<const uint4 *>(keys + h);
-    for (unsigned long long i = gtid; i < nv; i += gstride) {
+    for (unsigned int i = gtid; i < nv; i += gstride) {
         const uint4 q = kv[i];
         // a quad whose four keys agree on a digit (common when the digit is
         // constant over the keys) takes one atomic for it instead of four
@@ -123,7 +143,7 @@ __global__ void radix_histogram_kernel(const uint32_t *__restrict__ keys, unsign
             }
         }
     }
-    for (unsigned long long i = h + 4 * nv + gtid; i < n; i += gstride) add(keys[i]);
+    for (unsigned int i = h + 4 * nv + gtid; i < n32; i += gstride) add(keys[i]);
     __syncthreads();
     for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) {
         const unsigned int c = (&s_h[0][0])[i];
@@ -212,28 +232,41 @@ __device__ __forceinline__ PassBuffers pass_buffers(const RadixPlan &pl, const u
 __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restrict__ in_keys, unsigned long long n,
                                                         unsigned int t, int shift, uint32_t (&k)[kRKeys],
                                                         unsigned int (&wrank)[kRKeys], unsigned int (*s_cnt)[256],
-                                                        int lane, int warp) {
-    const unsigned long long base = (unsigned long long)t * kRTile + (unsigned long long)warp * (32 * kRKeys);
-    for (int i = lane; i < 256; i += 32) s_cnt[warp][i] = 0;
+                                                        unsigned int (*s_match)[256], int lane, int warp) {
+    // n < 2^31 for a radix sort, so key indices fit in 32 bits
+    const unsigned int n32 = (unsigned int)n;
+    const unsigned int base = t * kRTile + (unsigned int)warp * (32 * kRKeys);
+    for (int i = lane; i < 256; i += 32) {
+        s_cnt[warp][i] = 0;
+        if (U32SCAN_R_MATCH == 2) s_match[warp][i] = 0;
+    }
     __syncwarp();
     unsigned int valid_bits = 0;
 #pragma unroll
     for (int r = 0; r < kRKeys; ++r) {
-        const unsigned long long e = base + 32 * r + lane;
-        k[r] = e < n ? in_keys[e] : 0u;
-        valid_bits |= (e < n ? 1u : 0u) << r;
+        const unsigned int e = base + 32u * r + (unsigned int)lane;
+        k[r] = e < n32 ? in_keys[e] : 0u;
+        valid_bits |= (e < n32 ? 1u : 0u) << r;
     }
 #pragma unroll
     for (int r = 0; r < kRKeys; ++r) {
-        // lanes holding the same digit value: the AND over the digit's eight
-        // bits of the ballot (bit set) or its complement (bit clear), and
-        // the same for validity
         const bool valid = (valid_bits >> r) & 1u;
         const unsigned int dr = (k[r] >> shift) & 255u;
-#if U32SCAN_R_MATCH
+#if U32SCAN_R_MATCH == 2
+        // Each valid lane sets its bit in its digit value's mask word and
+        // reads the word back: the lanes holding the same digit value. After
+        // the read-back the lowest such lane (below == 0) clears the word and
+        // advances the value's count, so every word is zero again when the
+        // next round starts.
+        if (valid) atomicOr(&s_match[warp][dr], 1u << lane);
+        __syncwarp();
+        const unsigned int same = valid ? s_match[warp][dr] : 0u;
+#elif U32SCAN_R_MATCH == 1
         // invalid lanes get a label no valid digit has
         const unsigned int same = __match_any_sync(0xffffffffu, valid ? dr : 256u);
 #else
+        // the AND over the digit's eight bits of the ballot (bit set) or its
+        // complement (bit clear), and the same for validity
         const unsigned int vb = __ballot_sync(0xffffffffu, valid);
         unsigned int same = valid ? vb : ~vb;
 #pragma unroll
@@ -244,11 +277,15 @@ __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restri
         }
 #endif
         const unsigned int below = (unsigned int)__popc(same & lanemask_lt(lane));
-        unsigned int old = 0;
-        if (valid) old = s_cnt[warp][dr];
+        const unsigned int old = valid ? s_cnt[warp][dr] : 0u;
         wrank[r] = old + below;
         __syncwarp();
-        if (valid && below == 0) s_cnt[warp][dr] = old + (unsigned int)__popc(same);
+        if (valid && below == 0) {
+#if U32SCAN_R_MATCH == 2
+            s_match[warp][dr] = 0u;
+#endif
+            s_cnt[warp][dr] = old + (unsigned int)__popc(same);
+        }
         __syncwarp();
     }
     return valid_bits;
@@ -262,7 +299,7 @@ __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restri
 // words for each earlier tile): the library's tagged format, value = the
 // tile's count of v (aggregate) or the count of v in tiles 0..t (inclusive,
 // P bit).
-__global__ void __launch_bounds__(kRThreads, 2)
+__global__ void __launch_bounds__(kRThreads, U32SCAN_R_MINB)
 radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
                       int32_t *i1, int32_t *perm, uint32_t *keys_out, unsigned long long n, unsigned int n_tiles,
                       const unsigned int *__restrict__ bases, WsHeader *hdr, unsigned long long *desc,
@@ -271,6 +308,8 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     if (!pl.active) return;
     extern __shared__ __align__(16) unsigned int r_smem[];
     unsigned int(*s_cnt)[256] = reinterpret_cast<unsigned int(*)[256]>(r_smem);  // [kRWarps][256]
+    unsigned int(*s_match)[256] =
+        reinterpret_cast<unsigned int(*)[256]>(r_smem + kRWarps * 256 + 512 + 2 * kRTile);  // [kRWarps][256]
     unsigned int *s_tileoff = r_smem + kRWarps * 256;                           // [256] value's start in tile
     unsigned int *s_delta = s_tileoff + 256;                                    // [256] first slot - start
     unsigned int *s_keys = s_delta + 256;                                       // [kRTile]
@@ -287,10 +326,12 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     const unsigned int t = s_t;
     const unsigned long long tag = tag_of(s_epoch);
     const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm, keys_out);
+    // Key r of this thread is element base + 32 r + lane (n < 2^31: 32-bit indices).
+    const unsigned int base = t * kRTile + (unsigned int)warp * (32 * kRKeys);
     uint32_t k[kRKeys];
     unsigned int wrank[kRKeys];
     const int shift = 8 * p;
-    const unsigned int valid_bits = radix_rank_tile(b.in_keys, n, t, shift, k, wrank, s_cnt, lane, warp);
+    const unsigned int valid_bits = radix_rank_tile(b.in_keys, n, t, shift, k, wrank, s_cnt, s_match, lane, warp);
     __syncthreads();
     // Per digit value v (threads 0..255): warp offsets within the value's
     // run in this tile and the run's length, published at once.
@@ -322,16 +363,23 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     }
     __syncthreads();
     // Order the tile by digit value in shared memory (this frees the keys'
-    // registers before the look-back).
-    const unsigned long long base = (unsigned long long)t * kRTile + (unsigned long long)warp * (32 * kRKeys);
+    // registers before the look-back): keys first, keeping each key's
+    // position in wrank, then the indices.
 #pragma unroll
     for (int r = 0; r < kRKeys; ++r) {
         if ((valid_bits >> r) & 1u) {
-            const unsigned long long e = base + 32 * r + lane;
             const unsigned int v = (k[r] >> shift) & 255u;
-            const unsigned int pos = s_cnt[warp][v] + wrank[r];
-            s_keys[pos] = k[r];
-            if (b.out_idx) s_idx[pos] = b.in_idx ? b.in_idx[e] : (int32_t)e;
+            wrank[r] += s_cnt[warp][v];
+            s_keys[wrank[r]] = k[r];
+        }
+    }
+    if (b.out_idx) {
+#pragma unroll
+        for (int r = 0; r < kRKeys; ++r) {
+            if ((valid_bits >> r) & 1u) {
+                const unsigned int e = base + 32u * r + (unsigned int)lane;
+                s_idx[wrank[r]] = b.in_idx ? b.in_idx[e] : (int32_t)e;
+            }
         }
     }
     // Look back (threads 0..255, value v): the count of v in all earlier
@@ -387,7 +435,7 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     }
 }
 
-constexpr size_t kRSmem = (size_t)(kRWarps * 256 + 512 + 2 * kRTile) * 4;
+constexpr size_t kRSmem = (size_t)(kRWarps * 256 + 512 + 2 * kRTile + (U32SCAN_R_MATCH == 2 ? kRWarps * 256 : 0)) * 4;
 
 // All digits constant (every key equal): the permutation is the identity.
 __global__ void radix_identity_kernel(const RadixPlan *__restrict__ plan, const uint32_t *keys, int32_t *perm,

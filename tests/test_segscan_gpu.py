@@ -73,7 +73,9 @@ def check_segscan(u, a, f, offset_a=0, offset_f=0, cap=None):
     assert np.all(host(sums)[k:cap] == 0xFFFFFFFF)  # nothing written past the segments / capacity
 
 
-SIZES = [1, 2, 5, 4096 + 3, 8192, 8192 + 1, 3 * 8192 + 77, 100003, (1 << 20) + 5]
+# around the tiles of the forms that write the scan (10240 elements with
+# int32 flags) and of the reduce (14336), with ragged tails
+SIZES = [1, 2, 5, 4096 + 3, 10240, 10240 + 1, 3 * 10240 + 77, 14336 + 1, 3 * 14336 + 77, 100003, (1 << 20) + 5]
 
 
 @pytest.mark.parametrize("kind", ["geometric", "geometric16", "regular4", "regular7", "all", "none", "half"])
@@ -83,7 +85,7 @@ def test_segscan_parity(u, kind, n):
 
 
 @pytest.mark.parametrize("offsets", [(1, 1), (2, 2), (3, 3), (1, 2), (0, 3), (3, 0)])
-@pytest.mark.parametrize("n", [7, 8192 * 3 + 5, (1 << 18) + 3])
+@pytest.mark.parametrize("n", [7, 10240 * 3 + 5, 14336 * 3 + 5, (1 << 18) + 3])
 def test_segscan_misaligned(u, offsets, n):
     check_segscan(u, inputs.scan_values(n, 5), heads("half", n, 5), *offsets)
 
@@ -94,7 +96,7 @@ def test_segscan_capacity_below_count(u):
 
 
 @pytest.mark.parametrize("kind", ["geometric", "regular4", "half", "none"])
-@pytest.mark.parametrize("n", [1, 8192 + 1, 100003, (1 << 20) + 5])
+@pytest.mark.parametrize("n", [1, 14336 + 1, 3 * 14336 + 77, 100003, (1 << 20) + 5])
 def test_segreduce_parity(u, kind, n):
     a, f = inputs.scan_values(n, 3), heads(kind, n)
     d, fl = dev(a), dev(f)

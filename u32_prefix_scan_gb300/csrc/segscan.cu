@@ -25,12 +25,18 @@
 // words (internal.cuh): the segmented value and the running head count; the
 // head count gives every segment end its index into the sums.
 //
-// Layout inside a tile: warp w owns the w-th run of 128 * V elements; in
-// round r (of V / Q) lane l holds the E = 4 Q consecutive elements at
-// 32 E r + E l of that run, as Q u32x4. Head flags become one bit per
-// element (bit 4 i + c for component c of the lane's i-th u32x4); byte flags
-// are read four to a word and tested bytewise. Each round costs one warp-wide
-// segmented scan, so more elements a lane a round means fewer per element.
+// Layout inside a tile (lane runs): lane l of warp w owns the E = 4R
+// consecutive elements at w * 32E + l * E of the tile (R u32x4, R odd: a
+// warp reading its lanes' i-th u32x4 from the linear shared-memory stage then
+// hits eight different 16-byte bank groups in every quarter-warp, so the
+// reads are free of bank conflicts). Head flags become one bit per element
+// (bit j: element j of the run); byte flags are read four to a word and
+// tested bytewise. A lane scans its run sequentially with resets at its
+// heads; one warp-wide segmented scan of the lanes' run values then serves
+// E elements a lane, and a lane's segment ends take consecutive indices into
+// the sums. The forms that write the scan put it in a shared-memory output
+// buffer (the same layout, conflict free) and store each full tile with one
+// 1-D bulk copy.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -46,8 +52,6 @@
 
 namespace u32scan {
 
-constexpr unsigned int kNoHead = 0xffffffffu;
-
 // Component c of a u32x4.
 __device__ __forceinline__ unsigned int comp(const uint4 &v, int c) {
     return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
@@ -56,35 +60,30 @@ __device__ __forceinline__ void set_comp(uint4 &v, int c, unsigned int a) {
     if (c == 0) v.x = a; else if (c == 1) v.y = a; else if (c == 2) v.z = a; else v.w = a;
 }
 
-template <int THREADS, int V, int Q, int S, bool WRITE_SCAN, bool WANT_SUMS, typename F>
+// The kernel: persistent, one 512-thread block per SM; tile layout, pipeline
+// and look-back as described at the top of this file.
+template <int THREADS, int R, int S, bool WRITE_SCAN, bool WANT_SUMS, typename F, bool OUTBUF>
 __global__ void __launch_bounds__(THREADS, 512 / THREADS)
-segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags, unsigned long long n,
-                       uint32_t *seg_sums, unsigned long long seg_cap, uint32_t *nseg, WsHeader *hdr,
-                       unsigned long long *desc2, unsigned int n_tiles, unsigned int head, int streams_aligned,
-                       unsigned int skip_tile, unsigned long long limit_ns) {
+segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags, unsigned long long n,
+                         uint32_t *seg_sums, unsigned long long seg_cap, uint32_t *nseg, WsHeader *hdr,
+                         unsigned long long *desc2, unsigned int n_tiles, unsigned int head, int streams_aligned,
+                         unsigned int skip_tile, unsigned long long limit_ns) {
     constexpr int WARPS = THREADS / 32;
-    constexpr unsigned int CHUNK = 128 * V;  // elements per warp
-    constexpr unsigned int TILE = THREADS * V * 4;
-    // A lane takes E = 4 Q consecutive elements a round (Q u32x4), R rounds.
-    constexpr int R = V / Q, E = 4 * Q;
-    constexpr unsigned int kEMask = (1u << E) - 1u;
-    static_assert(V % Q == 0 && E <= 16, "whole rounds of u32x4");
-    // x[i] holds lane-local elements 4i .. 4i + 3: round i / Q, part i % Q;
-    // u4_off(i) is its offset from the lane's first element, in u32x4.
-    auto u4_off = [](int i) -> unsigned int { return 32u * Q * (unsigned int)(i / Q) + (unsigned int)(i % Q); };
-    constexpr unsigned int TILE_BYTES = TILE * 4;  // values
+    constexpr int E = 4 * R;                    // elements a lane
+    constexpr unsigned int CHUNK = 32u * E;     // elements a warp
+    constexpr unsigned int TILE = WARPS * CHUNK;
+    constexpr unsigned int TILE_BYTES = TILE * 4;
     constexpr unsigned int FLAG_BYTES = TILE * (unsigned int)sizeof(F);
     constexpr unsigned int STAGE_U4 = (TILE_BYTES + FLAG_BYTES) / 16;
-    static_assert(WARPS <= 32 && 4 * V <= 32, "one lane per warp; head bits fit in a word");
+    static_assert(R % 2 == 1 && E <= 32, "odd u32x4 count a lane; a lane's head bits fit a word");
+    static_assert(WARPS <= 32 && FLAG_BYTES % 16 == 0, "one lane per warp; whole 16-byte flag stages");
     static_assert(sizeof(F) == 4 || sizeof(F) == 1, "int32 or byte head flags");
-    extern __shared__ __align__(128) uint4 stage_buf[];  // S stages of [values | flags]
+    static_assert(WRITE_SCAN || !OUTBUF, "the output buffer holds the scan");
+    extern __shared__ __align__(128) uint4 stage_buf[];  // S stages of [values | flags] (+ the output buffer)
     __shared__ __align__(8) unsigned long long bar[S];
     __shared__ unsigned int s_tile[S];
     __shared__ unsigned int s_wval[2][WARPS], s_wcnt[2][WARPS], s_whas[2][WARPS];
-    // Head bit of each warp's first element, read after barrier B by the
-    // previous warp; three slots, so a warp already reading the next tile
-    // never overwrites the slot of a tile still being stored.
-    __shared__ unsigned int s_wfirst[3][WARPS];
+    __shared__ unsigned int s_wfirst[3][WARPS];  // head bit of each warp's first element, three tiles deep
     __shared__ unsigned int s_bval[WARPS], s_bcnt[WARPS], s_nexthead;
     __shared__ unsigned int s_epoch;
 
@@ -95,6 +94,7 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
     const F *vflags = reinterpret_cast<const F *>(reinterpret_cast<uintptr_t>(flags) - sizeof(F) * head);
     const bool producer = threadIdx.x == THREADS - 32;
     unsigned int latest_parity = 0;
+    const unsigned int li0 = (unsigned int)warp * CHUNK + (unsigned int)E * (unsigned int)lane;  // lane's first element
 
     auto tile_full = [&](unsigned int id) {
         const unsigned long long v0 = (unsigned long long)id * TILE;
@@ -135,14 +135,21 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
     }
     __syncthreads();
     const unsigned long long tag = tag_of(s_epoch);
-    const unsigned int li0 = (unsigned int)warp * CHUNK + (unsigned int)E * (unsigned int)lane;
     volatile unsigned int *vs_tile = s_tile;
 
-    // Read draw u into registers (values x, head bits hb), scan it within
-    // each warp and leave the warp aggregates in slot u & 1. Returns the
-    // tile, or n_tiles and above past the end / on a timeout.
-    auto read_tile = [&](unsigned int u, uint4 (&x)[V], unsigned int &hb, unsigned int &pfirst,
-                         unsigned int (&cl)[R]) -> unsigned int {
+    // What a lane keeps of a tile between reading it and storing it.
+    struct LaneRun {
+        uint4 x[R];           // the run, then its segmented scan from the lane's start
+        unsigned int hb;      // head bits (bit j: element j of the run)
+        unsigned int cin;     // segmented value flowing in from the warp's earlier lanes
+        unsigned int cex;     // heads in the warp's earlier lanes (the forms with sums)
+        bool head_before;     // a head in the warp's earlier lanes
+    };
+
+    // Read draw u (stage u % S) into a lane run, scan it, and leave the warp
+    // aggregates in slot u & 1. Returns the tile, n_tiles past the end, or
+    // n_tiles + 1 on a timeout.
+    auto read_tile = [&](unsigned int u, LaneRun &L) -> unsigned int {
         const int st = (int)(u % S);
         if (!mbar_wait_bounded(smem_u32(&bar[st]), (u / S) & 1u, limit_ns)) {
             report_timeout(hdr, 0xfffffffeu);
@@ -151,25 +158,25 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
         const unsigned int t = vs_tile[st];
         if (t >= n_tiles) return n_tiles;
         const unsigned long long tile_v0 = (unsigned long long)t * TILE;
-        hb = 0;
+        unsigned int hb = 0;
         if (tile_full(t)) {
             const uint4 *sv = stage_buf + st * STAGE_U4 + (li0 >> 2);
             if constexpr (sizeof(F) == 4) {
                 const int4 *sf = reinterpret_cast<const int4 *>(stage_buf + st * STAGE_U4 + TILE / 4) + (li0 >> 2);
 #pragma unroll
-                for (int i = 0; i < V; ++i) {
-                    x[i] = sv[u4_off(i)];
-                    const int4 f = sf[u4_off(i)];
+                for (int i = 0; i < R; ++i) {
+                    L.x[i] = sv[i];
+                    const int4 f = sf[i];
                     hb |= ((f.x != 0) | ((f.y != 0) << 1) | ((f.z != 0) << 2) | ((f.w != 0) << 3)) << (4 * i);
                 }
             } else {
                 // four byte flags in one word: byte c non-zero -> bit c of a nibble
-                const unsigned int *sf = reinterpret_cast<const unsigned int *>(stage_buf + st * STAGE_U4 + TILE / 4) +
-                                         (li0 >> 2);
+                const unsigned int *sf =
+                    reinterpret_cast<const unsigned int *>(stage_buf + st * STAGE_U4 + TILE / 4) + (li0 >> 2);
 #pragma unroll
-                for (int i = 0; i < V; ++i) {
-                    x[i] = sv[u4_off(i)];
-                    const unsigned int m = __vcmpne4(sf[u4_off(i)], 0u) & 0x08040201u;
+                for (int i = 0; i < R; ++i) {
+                    L.x[i] = sv[i];
+                    const unsigned int m = __vcmpne4(sf[i], 0u) & 0x08040201u;
                     hb |= ((m * 0x01010101u) >> 24) << (4 * i);
                 }
             }
@@ -179,174 +186,136 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
             const uint32_t *tv = vdata + tile_v0;
             const F *tf = vflags + tile_v0;
 #pragma unroll
-            for (int i = 0; i < V; ++i) {
+            for (int i = 0; i < R; ++i) {
                 unsigned int e[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const unsigned int li = li0 + 4 * u4_off(i) + c;
+                    const unsigned int li = li0 + 4 * i + c;
                     const bool in = li >= lo && li < hi;
                     e[c] = in ? tv[li] : 0u;
                     if (in && tf[li] != 0) hb |= 1u << (4 * i + c);
                 }
-                x[i] = make_uint4(e[0], e[1], e[2], e[3]);
+                L.x[i] = make_uint4(e[0], e[1], e[2], e[3]);
             }
         }
         // index 0 of the array always opens a segment
         if (tile_v0 <= head && head < tile_v0 + TILE) {
             const unsigned int li = (unsigned int)(head - tile_v0);
-            // element li: warp li / CHUNK; within the warp's run, round
-            // rem / (32 E), lane (rem % (32 E)) / E, lane-local rem % E
-            const unsigned int rem = li % CHUNK, rr = rem / (32u * E), in_r = rem % (32u * E);
-            if (li / CHUNK == (unsigned int)warp && in_r / E == (unsigned int)lane) hb |= 1u << (E * rr + in_r % E);
+            if (li - li0 < (unsigned int)E) hb |= 1u << (li - li0);
         }
-        // Per-round segmented scan within the warp, carry from round to round.
-        unsigned int carry = 0;
-        pfirst = kNoHead;
+        // the lane's run, scanned with resets at its heads
+        unsigned int s = 0;
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const unsigned int b = (hb >> (E * r)) & kEMask;
-            // the lane's own E elements, scanned with resets at its heads
-            unsigned int e[E];
-#pragma unroll
-            for (int i = 0; i < E; ++i) {
-                const unsigned int v = comp(x[Q * r + i / 4], i % 4);
-                e[i] = (i == 0 || ((b >> i) & 1u)) ? v : e[i - 1] + v;
-            }
-            // The round's segmented scan across lanes with a zero carry; every
-            // shuffle works on carry-free values, so the rounds overlap and
-            // the carry enters by plain arithmetic: a lane gets it when no
-            // head lies at or before it in the round.
-            const unsigned int t = e[E - 1];
-            const unsigned int P = warp_inclusive_sum(t, lane);
-            const unsigned int hm = __ballot_sync(0xffffffffu, b != 0u);
-            const unsigned int mle = hm & lanemask_le(lane);
-            const unsigned int bL = __shfl_sync(0xffffffffu, P - t, 31 - __clz(mle | 1u));
-            const unsigned int sl0 = mle ? P - bL : P;
-            const unsigned int T0 = __shfl_sync(0xffffffffu, sl0, 31);
-            const unsigned int up = __shfl_up_sync(0xffffffffu, sl0, 1);
-            const unsigned int cin = lane == 0 ? carry : up + ((hm & lanemask_lt(lane)) == 0u ? carry : 0u);
-            if constexpr (WRITE_SCAN) {
-#pragma unroll
-                for (int i = 0; i < E; ++i)
-                    set_comp(x[Q * r + i / 4], i % 4, (b & ((2u << i) - 1u)) ? e[i] : cin + e[i]);
-            } else {
-                // the reduce needs values at segment ends only: keep the
-                // lane-local ones and the lane's carry, added at the ends
-#pragma unroll
-                for (int i = 0; i < E; ++i) set_comp(x[Q * r + i / 4], i % 4, e[i]);
-                cl[r] = cin;
-            }
-            carry = hm ? T0 : carry + T0;
-            if (pfirst == kNoHead && hm) {
-                const int lf = __ffs(hm) - 1;
-                const unsigned int bf = __shfl_sync(0xffffffffu, b, lf);
-                pfirst = 32u * E * r + E * (unsigned int)lf + (unsigned int)(__ffs(bf) - 1);
-            }
+        for (int j = 0; j < E; ++j) {
+            const unsigned int v = comp(L.x[j / 4], j % 4);
+            s = ((hb >> j) & 1u) ? v : s + v;
+            set_comp(L.x[j / 4], j % 4, s);
         }
-        const unsigned int wcnt = __reduce_add_sync(0xffffffffu, (unsigned int)__popc(hb));
-        if (lane == 0) {
+        // across the warp's lanes: the value at the end of lane l's run with
+        // no carry into the warp is P[l] - P[L-1], L the last lane at or
+        // before l holding a head (P[l] when there is none)
+        const unsigned int P = warp_inclusive_sum(s, lane);
+        const unsigned int hm = __ballot_sync(0xffffffffu, hb != 0u);
+        const unsigned int mle = hm & lanemask_le(lane);
+        const unsigned int bL = __shfl_sync(0xffffffffu, P - s, 31 - __clz(mle | 1u));
+        const unsigned int incl = mle ? P - bL : P;
+        const unsigned int up = __shfl_up_sync(0xffffffffu, incl, 1);
+        L.cin = lane == 0 ? 0u : up;
+        L.head_before = (hm & lanemask_lt(lane)) != 0u;
+        L.hb = hb;
+        const unsigned int pc = (unsigned int)__popc(hb);
+        L.cex = WANT_SUMS ? warp_inclusive_sum(pc, lane) - pc : 0u;
+        const unsigned int wcnt = __reduce_add_sync(0xffffffffu, pc);
+        if (lane == 31) {
             const int slot = (int)(u & 1u);
-            s_wval[slot][warp] = carry;
+            s_wval[slot][warp] = incl;
             s_wcnt[slot][warp] = wcnt;
-            s_whas[slot][warp] = pfirst != kNoHead;
-            s_wfirst[u % 3][warp] = hb & 1u;
+            s_whas[slot][warp] = hm != 0u;
         }
+        if (lane == 0) s_wfirst[u % 3][warp] = hb & 1u;
         return t;
     };
 
-    // Store the current tile (first-head slot cs): add each warp's carry-in to the
-    // elements before its first head, write the scan, and write each
-    // segment's sum at the segment's last element.
-    auto store_tile = [&](unsigned int t, int cs, const uint4 (&x)[V], unsigned int hb, unsigned int pfirst,
-                          const unsigned int (&cl)[R]) {
+    // Store the current tile (first-head slot cs): each lane adds its carry
+    // to the elements before its first head, writes the scan, and writes the
+    // sum of each segment that ends in its run.
+    auto store_tile = [&](unsigned int t, int cs, const LaneRun &L) {
         const unsigned long long tile_v0 = (unsigned long long)t * TILE;
-        const unsigned int cin = s_bval[warp];
         const bool full = tile_full(t);
         unsigned int lo = 0, hi = TILE;
         if (!full) tile_range(t, lo, hi);
         uint32_t *tv = vdata + tile_v0;
-        unsigned int hbase = 0, next_first = 0;
-        if (WANT_SUMS) {
-            hbase = s_bcnt[warp];
-            next_first = warp + 1 < WARPS ? s_wfirst[cs][warp + 1] : s_nexthead;
+        const unsigned int wc = s_bval[warp];
+        const unsigned int lc = L.head_before ? L.cin : wc + L.cin;  // flows into the lane's run
+        const unsigned int f = L.hb ? (unsigned int)(__ffs(L.hb) - 1) : (unsigned int)E;  // first head
+        auto y = [&](int j) -> unsigned int { return comp(L.x[j / 4], j % 4) + ((unsigned int)j < f ? lc : 0u); };
+        if (WRITE_SCAN) {
+            if (full && OUTBUF) {
+                // through the output buffer (same lane-run layout, conflict
+                // free), then one 1-D bulk copy of the whole tile; thread 0
+                // waited for its previous copy to read the buffer before
+                // barrier B, and tile_full(t) is the same for every thread
+                uint4 *ob = stage_buf + S * STAGE_U4 + (li0 >> 2);
+#pragma unroll
+                for (int i = 0; i < R; ++i) ob[i] = make_uint4(y(4 * i), y(4 * i + 1), y(4 * i + 2), y(4 * i + 3));
+                fence_proxy_async_smem();
+                __syncthreads();  // barrier C: the output buffer is complete
+                if (threadIdx.x == 0) bulk_store(tv, smem_u32(stage_buf + S * STAGE_U4), TILE_BYTES);
+            } else if (full) {
+#pragma unroll
+                for (int i = 0; i < R; ++i)
+                    *reinterpret_cast<uint4 *>(tv + li0 + 4 * i) = make_uint4(y(4 * i), y(4 * i + 1), y(4 * i + 2), y(4 * i + 3));
+            } else {
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const unsigned int li = li0 + j;
+                    if (li >= lo && li < hi) tv[li] = y(j);
+                }
+            }
         }
-        // tile-local index of the array's last element (TILE when outside)
-        const unsigned long long last_v = head + n - 1 - tile_v0;
-        const unsigned int last_li = last_v < TILE ? (unsigned int)last_v : TILE;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const unsigned int p0 = 32u * E * r + E * lane;  // warp-local index of the lane's first element
-            const unsigned int l0 = li0 + 32u * E * r;        // its tile-local index
-            // the scanned value of element i: for the reduce, the lane-local
-            // value plus the lane's carry before its first head (computed only
-            // where a sum is written)
-            auto yv = [&](int i) -> unsigned int {
-                unsigned int v = comp(x[Q * r + i / 4], i % 4) + (p0 + i < pfirst ? cin : 0u);
-                if constexpr (!WRITE_SCAN)
-                    if ((((hb >> (E * r)) & kEMask) & ((2u << i) - 1u)) == 0u) v += cl[r];
-                return v;
-            };
-            unsigned int y[E];
-            if constexpr (WRITE_SCAN) {
-#pragma unroll
-                for (int i = 0; i < E; ++i) y[i] = yv(i);
+        if (WANT_SUMS) {
+            // element j ends a segment when element j + 1 is a head (the next
+            // lane's, warp's or tile's first element after the run's last) or
+            // j is the array's last element; only elements in the array count
+            const unsigned int down = __shfl_down_sync(0xffffffffu, L.hb & 1u, 1);
+            const unsigned int next_first = warp + 1 < WARPS ? s_wfirst[cs][warp + 1] : s_nexthead;
+            const unsigned int after = lane < 31 ? down : next_first;
+            unsigned int ends = (L.hb >> 1) | (after << (E - 1));
+            const unsigned long long last_v = head + n - 1 - tile_v0;
+            const unsigned int last_li = last_v < TILE ? (unsigned int)last_v : TILE;
+            const unsigned int d_last = last_li - li0;
+            if (d_last < (unsigned int)E) ends |= 1u << d_last;
+            if (!full) {
+                const unsigned int a0 = lo > li0 ? (lo - li0 < (unsigned int)E ? lo - li0 : (unsigned int)E) : 0u;
+                const unsigned int a1 = hi > li0 ? (hi - li0 < (unsigned int)E ? hi - li0 : (unsigned int)E) : 0u;
+                ends &= (unsigned int)(((1ull << a1) - 1ull) & ~((1ull << a0) - 1ull));
             }
-            if (WRITE_SCAN) {
-                if (full) {
+            ends &= (unsigned int)((1ull << E) - 1ull);
+            if (__any_sync(0xffffffffu, ends != 0u)) {
+                // segment index of element j: the heads before the run plus
+                // those of the run up to j, minus one (index 0's head lies at
+                // or before every end)
+                unsigned int k = s_bcnt[warp] + L.cex - 1u;
 #pragma unroll
-                    for (int q = 0; q < Q; ++q)
-                        __stcs(reinterpret_cast<uint4 *>(tv + l0 + 4 * q),
-                               make_uint4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]));
-                } else {
-#pragma unroll
-                    for (int i = 0; i < E; ++i) {
-                        const unsigned int li = l0 + i;
-                        if (li >= lo && li < hi) tv[li] = y[i];
-                    }
+                for (int j = 0; j < E; ++j) {
+                    k += (L.hb >> j) & 1u;
+                    if (((ends >> j) & 1u) && (unsigned long long)k < seg_cap) seg_sums[k] = y(j);
                 }
-            }
-            if (WANT_SUMS) {
-                const unsigned int b = (hb >> (E * r)) & kEMask;
-                // head bit of the element after this lane's last one
-                const unsigned int down = __shfl_down_sync(0xffffffffu, b & 1u, 1);
-                unsigned int wrap = next_first;
-                if (r + 1 < R) wrap = __shfl_sync(0xffffffffu, (hb >> (E * (r + 1))) & 1u, 0);
-                const unsigned int after = lane < 31 ? down : wrap;
-                // bit i: element i ends a segment (element i + 1 is a head, or
-                // element i is the array's last); only elements in the array
-                unsigned int ends = (b >> 1) | (after << (E - 1));
-                const unsigned int d_last = last_li - l0;
-                if (d_last < (unsigned int)E) ends |= 1u << d_last;
-                if (!full) {
-                    const unsigned int a0 = lo > l0 ? (lo - l0 < (unsigned int)E ? lo - l0 : (unsigned int)E) : 0u;
-                    const unsigned int a1 = hi > l0 ? (hi - l0 < (unsigned int)E ? hi - l0 : (unsigned int)E) : 0u;
-                    ends &= ((1u << a1) - 1u) & ~((1u << a0) - 1u);
-                }
-                const unsigned int pc = (unsigned int)__popc(b);
-                // Most rounds of long segments hold no segment end: skip them.
-                if (__any_sync(0xffffffffu, ends != 0u)) {
-                    // sum index of element i's segment: heads before this lane,
-                    // plus the lane's heads up to i, minus one (in 64 bits)
-                    const unsigned int kb = hbase + (warp_inclusive_sum(pc, lane) - pc);
-#pragma unroll
-                    for (int i = 0; i < E; ++i) {
-                        if ((ends >> i) & 1u) {
-                            // at least one head (index 0's) lies at or before every end
-                            const unsigned long long k =
-                                (unsigned long long)kb + (unsigned int)__popc(b & ((2u << i) - 1u)) - 1ull;
-                            if (k < seg_cap) seg_sums[k] = WRITE_SCAN ? y[i] : yv(i);
-                        }
-                    }
-                }
-                hbase += __reduce_add_sync(0xffffffffu, pc);
             }
         }
     };
 
-    uint4 xc[V], xn[V];
-    unsigned int clc[R], cln[R];  // lanes' carries per round (the reduce only)
-    unsigned int hbc = 0, hbn = 0, pfc = kNoHead, pfn = kNoHead;
-    unsigned int tc = read_tile(0, xc, hbc, pfc, clc);
+    // Head flag of the element just after tile t (warp 0, lane 0, the forms
+    // with sums): loaded one round before it is needed, when the tile is
+    // read, so that its latency stays off the look-back's path.
+    auto head_after = [&](unsigned int t) -> unsigned int {
+        const unsigned long long after = (unsigned long long)(t + 1) * TILE;
+        return after < head + n && vflags[after] != 0 ? 1u : 0u;
+    };
+    LaneRun Lc, Ln;
+    unsigned int tc = read_tile(0, Lc);
+    unsigned int nh_c = 0, nh_n = 0;
+    if (WANT_SUMS && threadIdx.x == 0 && tc < n_tiles) nh_c = head_after(tc);
     // warp 0 keeps, per lane w < WARPS, what the look-back needs for the
     // current tile: the tile aggregate and warp w's exclusive offsets
     unsigned int agg_val = 0, agg_cnt = 0, wex_val = 0, wex_cnt = 0;
@@ -354,18 +323,18 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
     auto block_aggregate = [&](int slot, unsigned int t, unsigned int &a_val, bool &a_head, unsigned int &a_cnt,
                                unsigned int &x_val, bool &h_before, unsigned int &x_cnt) {
         const unsigned int wv = lane < WARPS ? s_wval[slot][lane] : 0u;
-        const unsigned int wc = lane < WARPS ? s_wcnt[slot][lane] : 0u;
+        const unsigned int wcn = lane < WARPS ? s_wcnt[slot][lane] : 0u;
         const bool wh = lane < WARPS ? s_whas[slot][lane] != 0 : false;
         const unsigned int sw = warp_segmented_inclusive(wv, wh, 0u, lane);
         const unsigned int hm = __ballot_sync(0xffffffffu, wh);
         a_val = __shfl_sync(0xffffffffu, sw, 31);
         a_head = hm != 0;
-        const unsigned int cw = warp_inclusive_sum(wc, lane);
+        const unsigned int cw = warp_inclusive_sum(wcn, lane);
         a_cnt = __shfl_sync(0xffffffffu, cw, 31);
         x_val = __shfl_up_sync(0xffffffffu, sw, 1);
         if (lane == 0) x_val = 0;
         h_before = (hm & lanemask_lt(lane)) != 0;
-        x_cnt = cw - wc;
+        x_cnt = cw - wcn;
         if (lane == 0 && t != skip_tile) {
             // a tile holding a head knows its segmented carry at once
             st_relaxed(desc2 + 2ull * t, tag | (a_head || t == 0 ? (kFlagH | kFlagP) : 0ull) | a_val);
@@ -381,8 +350,9 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
         }
         if (warp == 0) block_aggregate(0, tc, agg_val, agg_head, agg_cnt, wex_val, head_before, wex_cnt);
         for (unsigned int u = 1;; ++u) {
-            const unsigned int tn = read_tile(u, xn, hbn, pfn, cln);
+            const unsigned int tn = read_tile(u, Ln);
             const bool more = !__syncthreads_or(tn >= n_tiles);  // barrier A
+            if (WANT_SUMS && threadIdx.x == 0 && more) nh_n = head_after(tn);
             unsigned int n_val = 0, n_cnt = 0, n_xval = 0, n_xcnt = 0;
             bool n_head = false, n_before = false;
             if (more && producer) {
@@ -393,7 +363,8 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
             }
             if (warp == 0) {
                 if (more) block_aggregate((int)(u & 1u), tn, n_val, n_head, n_cnt, n_xval, n_before, n_xcnt);
-                const SegPrefix pre = lookback_seg_wide<U32SCAN_S_LOOKA, U32SCAN_S_LOOKB>(desc2, tc, tag, hdr, limit_ns, lane);
+                const SegPrefix pre =
+                    lookback_seg_wide<U32SCAN_S_LOOKA, U32SCAN_S_LOOKB>(desc2, tc, tag, hdr, limit_ns, lane);
                 if (lane == 0 && tc != 0 && tc != skip_tile) {
                     if (!agg_head) st_relaxed(desc2 + 2ull * tc, tag | kFlagP | (unsigned int)(pre.seg + agg_val));
                     st_relaxed(desc2 + 2ull * tc + 1, tag | kFlagP | (unsigned int)(pre.cnt + agg_cnt));
@@ -404,23 +375,16 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
                 }
                 if (lane == 0) {
                     if (tc == n_tiles - 1u && nseg != nullptr) *nseg = pre.cnt + agg_cnt;
-                    if (WANT_SUMS) {
-                        // head flag of the element just after the tile
-                        const unsigned long long after = (unsigned long long)(tc + 1) * TILE;
-                        s_nexthead = after < head + n && vflags[after] != 0 ? 1u : 0u;
-                    }
+                    if (WANT_SUMS) s_nexthead = nh_c;
                 }
             }
+            if (OUTBUF && threadIdx.x == 0) bulk_wait_read();  // output buffer free again
             __syncthreads();  // barrier B: carries of the current tile are visible
-            store_tile(tc, (int)((u - 1) % 3), xc, hbc, pfc, clc);
+            store_tile(tc, (int)((u - 1) % 3), Lc);
             if (!more) break;
-#pragma unroll
-            for (int r = 0; r < V; ++r) xc[r] = xn[r];
-#pragma unroll
-            for (int r = 0; r < R; ++r) clc[r] = cln[r];
-            hbc = hbn;
-            pfc = pfn;
+            Lc = Ln;
             tc = tn;
+            nh_c = nh_n;
             agg_val = n_val;
             agg_head = n_head;
             agg_cnt = n_cnt;
@@ -429,69 +393,63 @@ segscan_u32_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags,
             wex_cnt = n_xcnt;
         }
     }
-    // Leave no bulk copy in flight into this block's shared memory.
+    // Leave no bulk copy in flight into or out of this block's shared memory.
     if (producer) {
 #pragma unroll
         for (int st = 0; st < S; ++st)
             (void)mbar_wait_bounded(smem_u32(&bar[st]), (latest_parity >> st) & 1u, limit_ns);
     }
+    if (OUTBUF && threadIdx.x == 0) bulk_wait_all();
 }
 
-// Launch shapes, chosen by measurement on GB300 per form and flag type:
-// writing the scan favours four elements a lane a round (one u32x4: the
-// stores and shared-memory reads stay unit-stride); the reduce, and the scan
-// with sums over byte flags, favour eight (half the warp-wide segmented-scan
-// work per element). A smaller flag stream leaves room for larger tiles.
-// Overridable at build time for tuning sweeps.
-#ifndef U32SCAN_S_STAGES
-#define U32SCAN_S_STAGES 2
+// Launch shapes, chosen by measurement on GB300 (n = 2^26) and overridable
+// at build time for tuning sweeps: R u32x4 a lane (odd), ring stages, and
+// whether the forms that write the scan go through an output buffer and a
+// bulk copy. Writing the scan from registers (each lane's 16-byte stores
+// fill half a 32-byte sector: twice the store requests of unit-stride
+// stores) measured slower than the buffer; the buffer leaves room for R = 5
+// with int32 flags and R = 7 with byte flags.
+#ifndef U32SCAN_S_LR
+#define U32SCAN_S_LR 7  // the reduce: u32x4 a lane
 #endif
-#ifndef U32SCAN_S_V1
-#define U32SCAN_S_V1 7  // u32x4 per lane, four elements a round
+#ifndef U32SCAN_S_LSTAGES4
+#define U32SCAN_S_LSTAGES4 2  // the reduce: ring stages with int32 flags
 #endif
-#ifndef U32SCAN_S_V2
-#define U32SCAN_S_V2 6  // u32x4 per lane, eight elements a round, int32 flags
+#ifndef U32SCAN_S_LSTAGES1
+#define U32SCAN_S_LSTAGES1 3  // and with byte flags
 #endif
-#ifndef U32SCAN_S_V2B
-#define U32SCAN_S_V2B 8  // the same with byte flags
+#ifndef U32SCAN_S_WOUT
+#define U32SCAN_S_WOUT 1  // the forms writing the scan: through an output buffer and a bulk copy
 #endif
-#ifndef U32SCAN_S_T1
-#define U32SCAN_S_T1 512  // threads a block, scan only (512 / threads blocks an SM)
+#ifndef U32SCAN_S_WR4
+#define U32SCAN_S_WR4 5  // the forms writing the scan: u32x4 a lane with int32 flags
 #endif
-#ifndef U32SCAN_S_T2
-#define U32SCAN_S_T2 512  // threads a block, the forms that write sums
+#ifndef U32SCAN_S_WR1
+#define U32SCAN_S_WR1 7  // and with byte flags
 #endif
-#ifndef U32SCAN_S_STAGES2
-#define U32SCAN_S_STAGES2 2  // ring stages of the eight-elements-a-round forms
-#endif
-template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
-constexpr int seg_threads() { return (WRITE_SCAN && !WANT_SUMS) ? U32SCAN_S_T1 : U32SCAN_S_T2; }
-template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
-constexpr int seg_q() { return (WRITE_SCAN && (!WANT_SUMS || sizeof(F) == 4)) ? 1 : 2; }
-template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
-constexpr int seg_stages() { return seg_q<WRITE_SCAN, WANT_SUMS, F>() == 1 ? U32SCAN_S_STAGES : U32SCAN_S_STAGES2; }
-template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
-constexpr int seg_v() {
-    return seg_q<WRITE_SCAN, WANT_SUMS, F>() == 1 ? U32SCAN_S_V1 : (sizeof(F) == 1 ? U32SCAN_S_V2B : U32SCAN_S_V2);
+template <bool WRITE_SCAN, typename F>
+constexpr bool lanes_out() { return WRITE_SCAN && U32SCAN_S_WOUT; }
+template <bool WRITE_SCAN, typename F>
+constexpr int lanes_r() { return !WRITE_SCAN ? U32SCAN_S_LR : sizeof(F) == 1 ? U32SCAN_S_WR1 : U32SCAN_S_WR4; }
+template <bool WRITE_SCAN, typename F>
+constexpr int lanes_stages() {
+    return lanes_out<WRITE_SCAN, F>() ? 2 : sizeof(F) == 1 ? U32SCAN_S_LSTAGES1 : U32SCAN_S_LSTAGES4;
 }
-template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
-constexpr unsigned long long seg_tile() {
-    return (unsigned long long)seg_threads<WRITE_SCAN, WANT_SUMS, F>() * seg_v<WRITE_SCAN, WANT_SUMS, F>() * 4;
+template <bool WRITE_SCAN, typename F>
+constexpr unsigned long long lanes_tile() { return 512ull * 4 * lanes_r<WRITE_SCAN, F>(); }
+template <bool WRITE_SCAN, typename F>
+constexpr size_t lanes_smem() {
+    return (size_t)lanes_stages<WRITE_SCAN, F>() * lanes_tile<WRITE_SCAN, F>() * (4 + sizeof(F)) +
+           (lanes_out<WRITE_SCAN, F>() ? lanes_tile<WRITE_SCAN, F>() * 4 : 0);
 }
-template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
-constexpr size_t seg_smem() {
-    return (size_t)seg_stages<WRITE_SCAN, WANT_SUMS, F>() * seg_tile<WRITE_SCAN, WANT_SUMS, F>() * (4 + sizeof(F));
-}
-static_assert(seg_smem<true, false, int32_t>() <= 227 * 1024 && seg_smem<true, true, int32_t>() <= 227 * 1024 &&
-                  seg_smem<false, true, int32_t>() <= 227 * 1024 && seg_smem<false, true, uint8_t>() <= 227 * 1024 &&
-                  seg_smem<true, true, uint8_t>() <= 227 * 1024,
+static_assert(lanes_smem<false, int32_t>() <= 227 * 1024 && lanes_smem<false, uint8_t>() <= 227 * 1024 &&
+                  lanes_smem<true, int32_t>() <= 227 * 1024 && lanes_smem<true, uint8_t>() <= 227 * 1024,
               "shared memory");
+
 // the smallest tile, which has the most tiles, sizes the workspace
 constexpr unsigned long long min2(unsigned long long a, unsigned long long b) { return a < b ? a : b; }
-constexpr unsigned long long kSTile =
-    min2(min2(min2(seg_tile<true, false, int32_t>(), seg_tile<true, true, int32_t>()),
-              min2(seg_tile<false, true, int32_t>(), seg_tile<true, false, uint8_t>())),
-         min2(seg_tile<true, true, uint8_t>(), seg_tile<false, true, uint8_t>()));
+constexpr unsigned long long kSTile = min2(min2(lanes_tile<false, int32_t>(), lanes_tile<false, uint8_t>()),
+                                           min2(lanes_tile<true, int32_t>(), lanes_tile<true, uint8_t>()));
 
 size_t segscan_workspace_bytes(unsigned long long n) {
     const unsigned long long tiles = (n + 3 + kSTile - 1) / kSTile;
@@ -520,12 +478,12 @@ static int segscan_launch(uint32_t *data, const F *flags, unsigned long long n, 
     const unsigned int head = (unsigned int)((reinterpret_cast<uintptr_t>(data) & 15) >> 2);
     // flags stream by bulk copy when they start a tile on a 16-byte boundary too
     const int aligned = ((reinterpret_cast<uintptr_t>(flags) - sizeof(F) * head) & 15) == 0;
-    constexpr unsigned long long TILE = seg_tile<WRITE_SCAN, WANT_SUMS, F>();
+    constexpr unsigned long long TILE = lanes_tile<WRITE_SCAN, F>();
     const unsigned int n_tiles = (unsigned int)((n + head + TILE - 1) / TILE);
-    constexpr int THREADS = seg_threads<WRITE_SCAN, WANT_SUMS, F>();
-    auto kern = segscan_u32_persistent<THREADS, seg_v<WRITE_SCAN, WANT_SUMS, F>(), seg_q<WRITE_SCAN, WANT_SUMS, F>(),
-                                       seg_stages<WRITE_SCAN, WANT_SUMS, F>(), WRITE_SCAN, WANT_SUMS, F>;
-    constexpr size_t smem = seg_smem<WRITE_SCAN, WANT_SUMS, F>();
+    constexpr int THREADS = 512;
+    auto kern = segscan_lanes_persistent<THREADS, lanes_r<WRITE_SCAN, F>(), lanes_stages<WRITE_SCAN, F>(), WRITE_SCAN,
+                                         WANT_SUMS, F, lanes_out<WRITE_SCAN, F>()>;
+    constexpr size_t smem = lanes_smem<WRITE_SCAN, F>();
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return U32SCAN_ECUDA;
     int sms;

@@ -62,7 +62,7 @@ __device__ __forceinline__ void set_comp(uint4 &v, int c, unsigned int a) {
 
 // The kernel: persistent, one 512-thread block per SM; tile layout, pipeline
 // and look-back as described at the top of this file.
-template <int THREADS, int R, int S, bool WRITE_SCAN, bool WANT_SUMS, typename F, bool OUTBUF>
+template <int THREADS, int R, int S, bool WRITE_SCAN, bool WANT_SUMS, typename F, bool BUF>
 __global__ void __launch_bounds__(THREADS, 512 / THREADS)
 segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags, unsigned long long n,
                          uint32_t *seg_sums, unsigned long long seg_cap, uint32_t *nseg, WsHeader *hdr,
@@ -78,8 +78,11 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
     static_assert(R % 2 == 1 && E <= 32, "odd u32x4 count a lane; a lane's head bits fit a word");
     static_assert(WARPS <= 32 && FLAG_BYTES % 16 == 0, "one lane per warp; whole 16-byte flag stages");
     static_assert(sizeof(F) == 4 || sizeof(F) == 1, "int32 or byte head flags");
-    static_assert(WRITE_SCAN || !OUTBUF, "the output buffer holds the scan");
-    extern __shared__ __align__(128) uint4 stage_buf[];  // S stages of [values | flags] (+ the output buffer)
+    // BUF: a tile-sized shared-memory buffer after the stages, in the lane-run
+    // layout. The forms writing the scan put the tile's scan there and store
+    // it with one bulk copy; the reduce keeps each lane's scanned run in its
+    // own part of it, to read the values at segment ends by index.
+    extern __shared__ __align__(128) uint4 stage_buf[];  // S stages of [values | flags] (+ the buffer)
     __shared__ __align__(8) unsigned long long bar[S];
     __shared__ unsigned int s_tile[S];
     __shared__ unsigned int s_wval[2][WARPS], s_wcnt[2][WARPS], s_whas[2][WARPS];
@@ -249,13 +252,13 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
         const unsigned int lc = L.head_before ? L.cin : wc + L.cin;  // flows into the lane's run
         const unsigned int f = L.hb ? (unsigned int)(__ffs(L.hb) - 1) : (unsigned int)E;  // first head
         auto y = [&](int j) -> unsigned int { return comp(L.x[j / 4], j % 4) + ((unsigned int)j < f ? lc : 0u); };
+        uint4 *ob = stage_buf + S * STAGE_U4 + (li0 >> 2);  // this lane's run in the buffer (BUF)
         if (WRITE_SCAN) {
-            if (full && OUTBUF) {
+            if (full && BUF) {
                 // through the output buffer (same lane-run layout, conflict
                 // free), then one 1-D bulk copy of the whole tile; thread 0
                 // waited for its previous copy to read the buffer before
                 // barrier B, and tile_full(t) is the same for every thread
-                uint4 *ob = stage_buf + S * STAGE_U4 + (li0 >> 2);
 #pragma unroll
                 for (int i = 0; i < R; ++i) ob[i] = make_uint4(y(4 * i), y(4 * i + 1), y(4 * i + 2), y(4 * i + 3));
                 fence_proxy_async_smem();
@@ -291,11 +294,26 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
                 ends &= (unsigned int)(((1ull << a1) - 1ull) & ~((1ull << a0) - 1ull));
             }
             ends &= (unsigned int)((1ull << E) - 1ull);
-            if (__any_sync(0xffffffffu, ends != 0u)) {
-                // segment index of element j: the heads before the run plus
-                // those of the run up to j, minus one (index 0's head lies at
-                // or before every end)
-                unsigned int k = s_bcnt[warp] + L.cex - 1u;
+            // segment index of element j: the heads before the run plus those
+            // of the run up to j, minus one (index 0's head lies at or before
+            // every end)
+            const unsigned int k0 = s_bcnt[warp] + L.cex - 1u;
+            if (BUF && full) {
+                // the run's scan is in the buffer (the forms writing the scan
+                // put it there above; the reduce writes it now, into this
+                // lane's own part): visit the ends only
+                if (!WRITE_SCAN && ends != 0u) {
+#pragma unroll
+                    for (int i = 0; i < R; ++i) ob[i] = make_uint4(y(4 * i), y(4 * i + 1), y(4 * i + 2), y(4 * i + 3));
+                }
+                const uint32_t *run = reinterpret_cast<const uint32_t *>(ob);
+                for (unsigned int e = ends; e != 0u; e &= e - 1u) {
+                    const unsigned int j = (unsigned int)(__ffs(e) - 1);
+                    const unsigned int k = k0 + (unsigned int)__popc(L.hb & ((2u << j) - 1u));
+                    if ((unsigned long long)k < seg_cap) seg_sums[k] = run[j];
+                }
+            } else if (__any_sync(0xffffffffu, ends != 0u)) {
+                unsigned int k = k0;
 #pragma unroll
                 for (int j = 0; j < E; ++j) {
                     k += (L.hb >> j) & 1u;
@@ -378,7 +396,7 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
                     if (WANT_SUMS) s_nexthead = nh_c;
                 }
             }
-            if (OUTBUF && threadIdx.x == 0) bulk_wait_read();  // output buffer free again
+            if (WRITE_SCAN && BUF && threadIdx.x == 0) bulk_wait_read();  // output buffer free again
             __syncthreads();  // barrier B: carries of the current tile are visible
             store_tile(tc, (int)((u - 1) % 3), Lc);
             if (!more) break;
@@ -399,7 +417,7 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
         for (int st = 0; st < S; ++st)
             (void)mbar_wait_bounded(smem_u32(&bar[st]), (latest_parity >> st) & 1u, limit_ns);
     }
-    if (OUTBUF && threadIdx.x == 0) bulk_wait_all();
+    if (WRITE_SCAN && BUF && threadIdx.x == 0) bulk_wait_all();
 }
 
 // Launch shapes, chosen by measurement on GB300 (n = 2^26) and overridable
@@ -421,6 +439,16 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
 #ifndef U32SCAN_S_WOUT
 #define U32SCAN_S_WOUT 1  // the forms writing the scan: through an output buffer and a bulk copy
 #endif
+// The reduce with the runs kept in a shared-memory buffer (and the shapes of
+// the forms writing the scan), per flag type. Measured (Gelem/s, geometric /
+// length-4 heads): int32 flags 472 / 396 with the buffer (R = 5) against 523
+// / 451 without (R = 7, larger tiles); byte flags 622 / 458 against 547 / 479.
+#ifndef U32SCAN_S_RBUF4
+#define U32SCAN_S_RBUF4 0
+#endif
+#ifndef U32SCAN_S_RBUF1
+#define U32SCAN_S_RBUF1 1
+#endif
 #ifndef U32SCAN_S_WR4
 #define U32SCAN_S_WR4 5  // the forms writing the scan: u32x4 a lane with int32 flags
 #endif
@@ -428,9 +456,9 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
 #define U32SCAN_S_WR1 7  // and with byte flags
 #endif
 template <bool WRITE_SCAN, typename F>
-constexpr bool lanes_out() { return WRITE_SCAN && U32SCAN_S_WOUT; }
+constexpr bool lanes_out() { return WRITE_SCAN ? U32SCAN_S_WOUT : sizeof(F) == 1 ? U32SCAN_S_RBUF1 : U32SCAN_S_RBUF4; }
 template <bool WRITE_SCAN, typename F>
-constexpr int lanes_r() { return !WRITE_SCAN ? U32SCAN_S_LR : sizeof(F) == 1 ? U32SCAN_S_WR1 : U32SCAN_S_WR4; }
+constexpr int lanes_r() { return !lanes_out<WRITE_SCAN, F>() ? U32SCAN_S_LR : sizeof(F) == 1 ? U32SCAN_S_WR1 : U32SCAN_S_WR4; }
 template <bool WRITE_SCAN, typename F>
 constexpr int lanes_stages() {
     return lanes_out<WRITE_SCAN, F>() ? 2 : sizeof(F) == 1 ? U32SCAN_S_LSTAGES1 : U32SCAN_S_LSTAGES4;

@@ -49,8 +49,32 @@
 #ifndef U32SCAN_S_LOOKB
 #define U32SCAN_S_LOOKB 1  // and head count
 #endif
+#ifndef U32SCAN_S_FEWENDS
+#define U32SCAN_S_FEWENDS 2  // segment ends a lane up to which its sums are visited end by end (no buffer)
+#endif
 
 namespace u32scan {
+
+// Element j (0 <= j < 4R, known only at run time) of a run held in
+// registers, by predicated moves: the u32x4 first, then the component.
+template <int R>
+__device__ __forceinline__ unsigned int pick(const uint4 (&x)[R], unsigned int j) {
+    // bitwise blends under an all-ones / all-zeros mask, so that the run stays
+    // in registers (no indexed copy in local memory)
+    const unsigned int qi = j >> 2;
+    uint4 q = x[0];
+#pragma unroll
+    for (int i = 1; i < R; ++i) {
+        const unsigned int m = 0u - (unsigned int)(qi == (unsigned int)i);
+        q.x = (x[i].x & m) | (q.x & ~m);
+        q.y = (x[i].y & m) | (q.y & ~m);
+        q.z = (x[i].z & m) | (q.z & ~m);
+        q.w = (x[i].w & m) | (q.w & ~m);
+    }
+    const unsigned int c = j & 3u;
+    const unsigned int lo = (c & 1u) ? q.y : q.x, hi = (c & 1u) ? q.w : q.z;
+    return (c & 2u) ? hi : lo;
+}
 
 // Component c of a u32x4.
 __device__ __forceinline__ unsigned int comp(const uint4 &v, int c) {
@@ -312,12 +336,21 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
                     const unsigned int k = k0 + (unsigned int)__popc(L.hb & ((2u << j) - 1u));
                     if ((unsigned long long)k < seg_cap) seg_sums[k] = run[j];
                 }
-            } else if (__any_sync(0xffffffffu, ends != 0u)) {
+            } else if (__any_sync(0xffffffffu, __popc(ends) > U32SCAN_S_FEWENDS)) {
+                // many ends in some lane: one pass over the run's elements
                 unsigned int k = k0;
 #pragma unroll
                 for (int j = 0; j < E; ++j) {
                     k += (L.hb >> j) & 1u;
                     if (((ends >> j) & 1u) && (unsigned long long)k < seg_cap) seg_sums[k] = y(j);
+                }
+            } else {
+                // few ends a lane: visit them, picking each value out of the registers
+                for (unsigned int e = ends; e != 0u; e &= e - 1u) {
+                    const unsigned int j = (unsigned int)(__ffs(e) - 1);
+                    const unsigned int k = k0 + (unsigned int)__popc(L.hb & ((2u << j) - 1u));
+                    const unsigned int v = pick<R>(L.x, j) + (j < f ? lc : 0u);
+                    if ((unsigned long long)k < seg_cap) seg_sums[k] = v;
                 }
             }
         }
@@ -440,14 +473,16 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
 #define U32SCAN_S_WOUT 1  // the forms writing the scan: through an output buffer and a bulk copy
 #endif
 // The reduce with the runs kept in a shared-memory buffer (and the shapes of
-// the forms writing the scan), per flag type. Measured (Gelem/s, geometric /
-// length-4 heads): int32 flags 472 / 396 with the buffer (R = 5) against 523
-// / 451 without (R = 7, larger tiles); byte flags 622 / 458 against 547 / 479.
+// the forms writing the scan), per flag type; without it, a lane with few
+// segment ends picks their values out of its registers. Measured (Gelem/s,
+// geometric / length-4 heads): int32 flags 472 / 396 with the buffer (R = 5)
+// against 588 / 449 without (R = 7, larger tiles); byte flags 620 / 456
+// against 631 / 475.
 #ifndef U32SCAN_S_RBUF4
 #define U32SCAN_S_RBUF4 0
 #endif
 #ifndef U32SCAN_S_RBUF1
-#define U32SCAN_S_RBUF1 1
+#define U32SCAN_S_RBUF1 0
 #endif
 #ifndef U32SCAN_S_WR4
 #define U32SCAN_S_WR4 5  // the forms writing the scan: u32x4 a lane with int32 flags

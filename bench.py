@@ -71,6 +71,7 @@ if str(ROOT) not in sys.path:
 
 UNIT = "Gelem/s"
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1000 * 1000  # GB300's L2
 REF_SAMPLE = 1 << 24  # elements per reference-arm step
 
 
@@ -790,6 +791,8 @@ def parse_args(argv=None):
     p.add_argument("--monoid", choices=["add", "mul", "and", "or", "xor", "min", "max"], default="max",
                    help="scan_op: the operator")
     p.add_argument("--inclusive", action="store_true", help="scan_op: inclusive instead of exclusive")
+    p.add_argument("--graph", action="store_true",
+                   help="capture the timed steps in one CUDA graph and time its replay (launch-bound sizes)")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -1032,13 +1035,29 @@ def run_ours(args, rank, local_rank, world):
     marked = hasattr(op, "step_marked")
     marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in range(args.steps if marked else 0)]
+    graph = None
+    if args.graph:
+        # the K timed steps captured once, replayed once inside the timed
+        # region: no host launch cost between steps (for L2-resident sizes,
+        # where the host's launch rate would otherwise be what is timed)
+        if marked:
+            raise SystemExit("bench: --graph times plain steps; this op brackets its dominant kernel with events")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(args.steps):
+                op.step()
+        graph.replay()  # one untimed replay
+        torch.cuda.synchronize()
     w0 = time.time()
     start.record(stream)
-    for k in range(args.steps):
-        if marked:
-            op.step_marked(*marks[k])
-        else:
-            op.step()
+    if graph is not None:
+        graph.replay()
+    else:
+        for k in range(args.steps):
+            if marked:
+                op.step_marked(*marks[k])
+            else:
+                op.step()
     end.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
@@ -1090,7 +1109,9 @@ def run_ours(args, rank, local_rank, world):
         "data": "synthetic",
         "config": {"workload": op.workload() if full else f"profiling case: {op.workload()}", "n": op.n,
                    "op": args.op, "per_rank": "one independent replica per GPU",
-                   "l2": "inputs larger than the 129 MB L2; no flush between steps"},
+                   "l2": ("inputs larger than the 129 MB L2; no flush between steps" if nbytes > L2_BYTES
+                          else "inputs resident in the 129 MB L2: a latency figure, no roofline claim"),
+                   **({"launch": "the timed steps replayed from one CUDA graph"} if graph is not None else {})},
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,

@@ -52,7 +52,8 @@ def run(u, inclusive, a, offset=0):
 
 
 SIZES = [1, 2, 3, 4, 5, 31, 32, 33, 127, 1000, 2047, 2048, 2049, 3 * 2048 + 77, 8192 * 5 + 3,
-         65536, 65536 + 1, (1 << 22) - 1, 1 << 22, (1 << 22) + 1, 3 * 16384 * 100 + 12345]
+         65536, 65536 + 1, (1 << 19) - 1, 1 << 19, (1 << 19) + 1, (1 << 22) - 1, 1 << 22, (1 << 22) + 1,
+         3 * 16384 * 100 + 12345]
 
 
 @pytest.mark.parametrize("inclusive", [False, True])
@@ -67,7 +68,7 @@ def test_parity_sizes(u, inclusive, n):
 
 @pytest.mark.parametrize("inclusive", [False, True])
 @pytest.mark.parametrize("offset", [1, 2, 3])
-@pytest.mark.parametrize("n", [5, 2049, 65536 + 7, (1 << 22) + 5])
+@pytest.mark.parametrize("n", [5, 2049, 65536 + 7, (1 << 19) + 5, (1 << 22) + 5])
 def test_parity_misaligned_start(u, inclusive, offset, n):
     a = inputs.scan_values(n, 7)
     got, total = run(u, inclusive, a, offset)

@@ -419,7 +419,10 @@ constexpr int kPThreads = U32SCAN_P_THREADS, kPV = U32SCAN_P_V, kPStages = U32SC
               kPLook = U32SCAN_P_LOOK;
 constexpr unsigned long long kPTile = (unsigned long long)kPThreads * kPV * 4;
 constexpr size_t kPSmem = (size_t)(kPStages + (U32SCAN_P_BULKSTORE ? 1 : 0)) * kPTile * 4;
-constexpr unsigned long long kPersistentMinN = 1ull << 22;
+#ifndef U32SCAN_P_MINN_LOG2
+#define U32SCAN_P_MINN_LOG2 19  // arrays of at least 2^this elements take the persistent kernel
+#endif
+constexpr unsigned long long kPersistentMinN = 1ull << U32SCAN_P_MINN_LOG2;
 
 struct ScanShape {
     bool persistent;

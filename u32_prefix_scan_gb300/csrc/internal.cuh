@@ -397,14 +397,14 @@ __device__ __forceinline__ void bulk_load(unsigned int dst_smem, const void *src
         : "memory");
 }
 
-// Shared memory -> global 1-D bulk copy (16-byte aligned, size a multiple of
-// 16), tracked as a bulk-async group of the issuing thread.
 // Ask for `bytes` at `src` (16-byte aligned, a multiple of 16) to be brought
 // into L2, without waiting.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, unsigned int bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Shared memory -> global 1-D bulk copy (16-byte aligned, size a multiple of
+// 16), tracked as a bulk-async group of the issuing thread.
 __device__ __forceinline__ void bulk_store(void *dst, unsigned int src_smem, unsigned int bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem), "r"(bytes)
                  : "memory");

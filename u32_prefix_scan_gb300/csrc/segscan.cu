@@ -49,6 +49,9 @@
 #ifndef U32SCAN_S_LOOKB
 #define U32SCAN_S_LOOKB 1  // and head count
 #endif
+#ifndef U32SCAN_S_STAGEMIN
+#define U32SCAN_S_STAGEMIN 64  // fewest ends a warp for which its sums are staged
+#endif
 #ifndef U32SCAN_S_FEWENDS
 #define U32SCAN_S_FEWENDS 2  // segment ends a lane up to which its sums are visited end by end (no buffer)
 #endif
@@ -86,7 +89,7 @@ __device__ __forceinline__ void set_comp(uint4 &v, int c, unsigned int a) {
 
 // The kernel: persistent, one 512-thread block per SM; tile layout, pipeline
 // and look-back as described at the top of this file.
-template <int THREADS, int R, int S, bool WRITE_SCAN, bool WANT_SUMS, typename F, bool BUF>
+template <int THREADS, int R, int S, bool WRITE_SCAN, bool WANT_SUMS, typename F, bool BUF, int SUMCAP>
 __global__ void __launch_bounds__(THREADS, 512 / THREADS)
 segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags, unsigned long long n,
                          uint32_t *seg_sums, unsigned long long seg_cap, uint32_t *nseg, WsHeader *hdr,
@@ -322,6 +325,39 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
             // of the run up to j, minus one (index 0's head lies at or before
             // every end)
             const unsigned int k0 = s_bcnt[warp] + L.cex - 1u;
+            // A warp's ends take consecutive segment indices (one head lies
+            // between two ends), so a warp with at most SUMCAP ends in a full
+            // tile puts its sums in its own shared-memory slots (the m-th end
+            // of a lane at the lane's exclusive end count + m) and writes them
+            // with unit-stride stores; otherwise each lane stores its own.
+            bool staged = false;
+            unsigned int ecx = 0, cw = 0, kw = 0;
+            uint32_t *stg = nullptr;
+            if constexpr (SUMCAP > 0) {
+                if (full) {
+                    const unsigned int ne = (unsigned int)__popc(ends);
+                    cw = __reduce_add_sync(0xffffffffu, ne);
+                    // the same for the whole warp; few ends go straight out
+                    staged = cw >= U32SCAN_S_STAGEMIN && cw <= (unsigned int)SUMCAP;
+                    if (staged) {
+                        ecx = warp_inclusive_sum(ne, lane) - ne;
+                        // the warp's first end: its lowest lane with ends, that lane's first
+                        const unsigned int hmE = __ballot_sync(0xffffffffu, ne != 0u);
+                        const unsigned int j0 = ends ? (unsigned int)(__ffs(ends) - 1) : 0u;
+                        const unsigned int kf = k0 + (unsigned int)__popc(L.hb & ((2u << j0) - 1u));
+                        kw = __shfl_sync(0xffffffffu, kf, hmE ? __ffs(hmE) - 1 : 0);
+                        stg = reinterpret_cast<uint32_t *>(stage_buf + S * STAGE_U4 + (BUF ? TILE / 4 : 0)) +
+                              (unsigned int)warp * SUMCAP;
+                    }
+                }
+            }
+            // the m-th end of this lane, in segment k, with value v
+            auto emit = [&](unsigned int m, unsigned int k, unsigned int v) {
+                if (staged)
+                    stg[ecx + m] = v;
+                else if ((unsigned long long)k < seg_cap)
+                    seg_sums[k] = v;
+            };
             if (BUF && full) {
                 // the run's scan is in the buffer (the forms writing the scan
                 // put it there above; the reduce writes it now, into this
@@ -331,27 +367,33 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
                     for (int i = 0; i < R; ++i) ob[i] = make_uint4(y(4 * i), y(4 * i + 1), y(4 * i + 2), y(4 * i + 3));
                 }
                 const uint32_t *run = reinterpret_cast<const uint32_t *>(ob);
-                for (unsigned int e = ends; e != 0u; e &= e - 1u) {
+                unsigned int m = 0;
+                for (unsigned int e = ends; e != 0u; e &= e - 1u, ++m) {
                     const unsigned int j = (unsigned int)(__ffs(e) - 1);
-                    const unsigned int k = k0 + (unsigned int)__popc(L.hb & ((2u << j) - 1u));
-                    if ((unsigned long long)k < seg_cap) seg_sums[k] = run[j];
+                    emit(m, staged ? 0u : k0 + (unsigned int)__popc(L.hb & ((2u << j) - 1u)), run[j]);
                 }
             } else if (__any_sync(0xffffffffu, __popc(ends) > U32SCAN_S_FEWENDS)) {
                 // many ends in some lane: one pass over the run's elements
-                unsigned int k = k0;
+                unsigned int k = k0, m = 0;
 #pragma unroll
                 for (int j = 0; j < E; ++j) {
                     k += (L.hb >> j) & 1u;
-                    if (((ends >> j) & 1u) && (unsigned long long)k < seg_cap) seg_sums[k] = y(j);
+                    if ((ends >> j) & 1u) emit(m++, k, y(j));
                 }
             } else {
                 // few ends a lane: visit them, picking each value out of the registers
-                for (unsigned int e = ends; e != 0u; e &= e - 1u) {
+                unsigned int m = 0;
+                for (unsigned int e = ends; e != 0u; e &= e - 1u, ++m) {
                     const unsigned int j = (unsigned int)(__ffs(e) - 1);
-                    const unsigned int k = k0 + (unsigned int)__popc(L.hb & ((2u << j) - 1u));
-                    const unsigned int v = pick<R>(L.x, j) + (j < f ? lc : 0u);
-                    if ((unsigned long long)k < seg_cap) seg_sums[k] = v;
+                    emit(m, staged ? 0u : k0 + (unsigned int)__popc(L.hb & ((2u << j) - 1u)),
+                         pick<R>(L.x, j) + (j < f ? lc : 0u));
                 }
+            }
+            if (staged) {
+                __syncwarp();
+                for (unsigned int i = (unsigned int)lane; i < cw; i += 32u)
+                    if ((unsigned long long)(kw + i) < seg_cap) seg_sums[kw + i] = stg[i];
+                __syncwarp();
             }
         }
     };
@@ -508,6 +550,23 @@ constexpr size_t lanes_smem() {
 static_assert(lanes_smem<false, int32_t>() <= 227 * 1024 && lanes_smem<false, uint8_t>() <= 227 * 1024 &&
                   lanes_smem<true, int32_t>() <= 227 * 1024 && lanes_smem<true, uint8_t>() <= 227 * 1024,
               "shared memory");
+// Segment sums staged per warp (the forms writing the scan with sums, where
+// the shared memory left over allows at least 64 slots a warp, 2 KB kept for
+// static shared memory): slots a warp, a multiple of 32, at most a warp's
+// elements + 1. Measured (n = 2^26, Gelem/s, geometric / length-4 heads):
+// scan + sums 406 / 334 -> 402 / 349, byte flags 544 / 386 -> 537 / 452;
+// the byte-flag reduce gained nothing (639 / 476 -> 622 / 473) and does not
+// stage.
+#ifndef U32SCAN_S_STAGESUMS
+#define U32SCAN_S_STAGESUMS 1
+#endif
+template <bool WRITE_SCAN, bool WANT_SUMS, typename F>
+constexpr int lanes_sumcap() {
+    constexpr long long spare = 227LL * 1024 - 2048 - (long long)lanes_smem<WRITE_SCAN, F>();
+    constexpr long long cap = spare / (16 * 4) / 32 * 32;
+    constexpr long long chunk = 128LL * lanes_r<WRITE_SCAN, F>() + 32;
+    return (!U32SCAN_S_STAGESUMS || !WANT_SUMS || !WRITE_SCAN || cap < 64) ? 0 : (int)(cap < chunk ? cap : chunk);
+}
 
 // the smallest tile, which has the most tiles, sizes the workspace
 constexpr unsigned long long min2(unsigned long long a, unsigned long long b) { return a < b ? a : b; }
@@ -544,9 +603,11 @@ static int segscan_launch(uint32_t *data, const F *flags, unsigned long long n, 
     constexpr unsigned long long TILE = lanes_tile<WRITE_SCAN, F>();
     const unsigned int n_tiles = (unsigned int)((n + head + TILE - 1) / TILE);
     constexpr int THREADS = 512;
+    constexpr int SUMCAP = lanes_sumcap<WRITE_SCAN, WANT_SUMS, F>();
     auto kern = segscan_lanes_persistent<THREADS, lanes_r<WRITE_SCAN, F>(), lanes_stages<WRITE_SCAN, F>(), WRITE_SCAN,
-                                         WANT_SUMS, F, lanes_out<WRITE_SCAN, F>()>;
-    constexpr size_t smem = lanes_smem<WRITE_SCAN, F>();
+                                         WANT_SUMS, F, lanes_out<WRITE_SCAN, F>(), SUMCAP>;
+    constexpr size_t smem = lanes_smem<WRITE_SCAN, F>() + (size_t)16 * 4 * SUMCAP;
+    static_assert(smem <= 227 * 1024 - 2048, "shared memory");
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return U32SCAN_ECUDA;
     int sms;

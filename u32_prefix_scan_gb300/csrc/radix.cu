@@ -224,30 +224,16 @@ __device__ __forceinline__ PassBuffers pass_buffers(const RadixPlan &pl, const u
     return b;
 }
 
-// Load this thread's keys of tile t (warp-striped: round r of warp w covers
-// 32 consecutive keys) and rank them stably within the tile: after the call
-// wrank[r] is the key's rank among the keys of its digit value in this warp
-// (in tile order) and s_cnt[w][v] the warp's count of digit value v. Bit r
-// of the returned mask says whether key r lies inside the array.
-__device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restrict__ in_keys, unsigned long long n,
-                                                        unsigned int t, int shift, uint32_t (&k)[kRKeys],
-                                                        unsigned int (&wrank)[kRKeys], unsigned int (*s_cnt)[256],
-                                                        unsigned int (*s_match)[256], int lane, int warp) {
-    // n < 2^31 for a radix sort, so key indices fit in 32 bits
-    const unsigned int n32 = (unsigned int)n;
-    const unsigned int base = t * kRTile + (unsigned int)warp * (32 * kRKeys);
+// Rank a warp's keys (held as in radix_rank_tile, bit r of valid_bits set
+// for the keys inside the array) stably within the warp.
+__device__ __forceinline__ void radix_rank_keys(const uint32_t (&k)[kRKeys], unsigned int valid_bits, int shift,
+                                                unsigned int (&wrank)[kRKeys], unsigned int (*s_cnt)[256],
+                                                unsigned int (*s_match)[256], int lane, int warp) {
     for (int i = lane; i < 256; i += 32) {
         s_cnt[warp][i] = 0;
         if (U32SCAN_R_MATCH == 2) s_match[warp][i] = 0;
     }
     __syncwarp();
-    unsigned int valid_bits = 0;
-#pragma unroll
-    for (int r = 0; r < kRKeys; ++r) {
-        const unsigned int e = base + 32u * r + (unsigned int)lane;
-        k[r] = e < n32 ? in_keys[e] : 0u;
-        valid_bits |= (e < n32 ? 1u : 0u) << r;
-    }
 #pragma unroll
     for (int r = 0; r < kRKeys; ++r) {
         const bool valid = (valid_bits >> r) & 1u;
@@ -288,6 +274,28 @@ __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restri
         }
         __syncwarp();
     }
+}
+
+// Load this thread's keys of tile t (warp-striped: round r of warp w covers
+// 32 consecutive keys) and rank them stably within the tile: after the call
+// wrank[r] is the key's rank among the keys of its digit value in this warp
+// (in tile order) and s_cnt[w][v] the warp's count of digit value v. Bit r
+// of the returned mask says whether key r lies inside the array.
+__device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restrict__ in_keys, unsigned long long n,
+                                                        unsigned int t, int shift, uint32_t (&k)[kRKeys],
+                                                        unsigned int (&wrank)[kRKeys], unsigned int (*s_cnt)[256],
+                                                        unsigned int (*s_match)[256], int lane, int warp) {
+    // n < 2^31 for a radix sort, so key indices fit in 32 bits
+    const unsigned int n32 = (unsigned int)n;
+    const unsigned int base = t * kRTile + (unsigned int)warp * (32 * kRKeys);
+    unsigned int valid_bits = 0;
+#pragma unroll
+    for (int r = 0; r < kRKeys; ++r) {
+        const unsigned int e = base + 32u * r + (unsigned int)lane;
+        k[r] = e < n32 ? in_keys[e] : 0u;
+        valid_bits |= (e < n32 ? 1u : 0u) << r;
+    }
+    radix_rank_keys(k, valid_bits, shift, wrank, s_cnt, s_match, lane, warp);
     return valid_bits;
 }
 

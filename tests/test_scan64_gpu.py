@@ -57,7 +57,8 @@ def check(u, a, op, inclusive, offset=0, ws=None):
     assert int(host(total)[0]) == want_total
 
 
-SIZES = [1, 2, 3, 1023, 1024, 1025, 3 * 1024 + 7, 100003, (1 << 21) - 1, 1 << 21, (1 << 21) + 4097, 3_000_001]
+SIZES = [1, 2, 3, 1023, 1024, 1025, 3 * 1024 + 7, 100003, (1 << 20) - 1, 1 << 20, (1 << 20) + 1, (1 << 21) - 1,
+         1 << 21, (1 << 21) + 4097, 3_000_001]
 
 
 @pytest.mark.parametrize("op", OPS)
@@ -67,7 +68,7 @@ def test_parity(u, op, inclusive, n):
     check(u, values(op, n, 2), op, inclusive)
 
 
-@pytest.mark.parametrize("n", [5, 100003, (1 << 21) + 77])
+@pytest.mark.parametrize("n", [5, 100003, (1 << 20) + 3, (1 << 21) + 77])
 @pytest.mark.parametrize("op", ["add", "max"])
 def test_row_8_bytes_past_16_byte_boundary(u, n, op):
     check(u, values(op, n, 3), op, False, offset=1)

@@ -442,7 +442,10 @@ scan_u64_persistent(unsigned long long *__restrict__ data, unsigned long long n,
 #define U32SCAN_S64_STAGES 2
 #endif
 constexpr int kS64T = 512, kS64V = U32SCAN_S64_V, kS64S = U32SCAN_S64_STAGES;
-constexpr unsigned long long kScan64LargeMinN = 1ull << 21;
+#ifndef U32SCAN_S64_MINN_LOG2
+#define U32SCAN_S64_MINN_LOG2 20  // rows of at least 2^this elements take the persistent kernel
+#endif
+constexpr unsigned long long kScan64LargeMinN = 1ull << U32SCAN_S64_MINN_LOG2;
 constexpr size_t kS64Smem = (size_t)(kS64S + 1) * kS64T * kS64V * 2 * 8;
 static_assert(kS64Smem <= 227 * 1024, "shared memory");
 struct Scan64Shape {

@@ -399,6 +399,22 @@ int u32scan_test_scan_skip_publish(uint32_t *data, size_t n, uint32_t *total,
                                    unsigned long long limit_ns,
                                    u32scan_stream_t stream);
 
+/*
+ * The same test hook for the segmented scan's two carry words (segmented
+ * value and head count): runs segscan_inclusive_u32 (with or without
+ * `seg_sums`), except that tile `skip_tile` of the launch publishes neither
+ * word, so the tiles after it that need them wait `limit_ns` nanoseconds,
+ * give up, and the next u32scan_check() on `ws` returns U32SCAN_ETIMEOUT.
+ * The results are then wrong by design; `ws` stays usable. Tiles hold
+ * 10240 elements with these int32 flags.
+ */
+int u32scan_test_segscan_skip_publish(uint32_t *data, const int32_t *head_flags, size_t n,
+                                      uint32_t *seg_sums, size_t seg_capacity, uint32_t *nseg,
+                                      void *ws, size_t ws_bytes,
+                                      unsigned int skip_tile,
+                                      unsigned long long limit_ns,
+                                      u32scan_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -2,8 +2,9 @@
 oracle, through the C ABI: bit-exact scans, sums and counts over head
 patterns from one segment to all heads, geometric and length-4 segments,
 ragged tails, misaligned and differently aligned streams, a capacity below
-the segment count, repeated calls on one workspace, and both benchmark
-workloads at full size (n = 2^26)."""
+the segment count, repeated calls on one workspace, both benchmark
+workloads at full size (n = 2^26), and the bounded carry wait (a tile that
+never publishes its carry words is reported, and the workspace recovers)."""
 
 import numpy as np
 import pytest
@@ -162,3 +163,36 @@ def test_workload_2_26_full_parity(u, kind):
     want_sums, want_nseg = oracle.segreduce(a, f)
     assert int(host(nseg)[0]) == want_nseg
     assert np.array_equal(host(sums)[:want_nseg], want_sums)
+
+
+@pytest.mark.parametrize("with_sums", [False, True], ids=["scan", "scan+sums"])
+@pytest.mark.parametrize("kind", ["none", "regular4"])
+@pytest.mark.parametrize("n,skip", [(10240 * 8 + 7, 2), ((1 << 22) + 12345, 3)], ids=["9-tiles", "411-tiles"])
+def test_timeout_is_reported_and_workspace_recovers(u, n, skip, kind, with_sums):
+    # Tile `skip` never publishes its two carry words: the tiles after it
+    # that need them wait the given limit, give up, and the status says so;
+    # the workspace then serves a normal call.
+    from u32_prefix_scan_gb300 import _native
+
+    lib = _native.lib()
+    a, f = inputs.scan_values(n, 13), heads(kind, n, 13)
+    d, fl = dev(a), dev(f)
+    sums = torch.zeros(n, dtype=torch.int32, device="cuda")
+    nseg = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = u.Workspace(lib.u32scan_workspace_bytes(_native.OP_SEGSCAN, n), torch.device("cuda"))
+    s = torch.cuda.current_stream().cuda_stream
+    rc = lib.u32scan_test_segscan_skip_publish(d.data_ptr(), fl.data_ptr(), n, sums.data_ptr() if with_sums else None,
+                                               n if with_sums else 0, nseg.data_ptr(), ws.ptr, ws.nbytes, skip,
+                                               20_000_000, s)
+    assert rc == _native.OK
+    assert lib.u32scan_check(ws.ptr, s) == _native.ETIMEOUT
+    assert lib.u32scan_check(ws.ptr, s) == _native.OK  # the status was cleared
+    d = dev(a)
+    sums = torch.full((n,), -1, dtype=torch.int32, device="cuda") if with_sums else None
+    nseg = u.segscan_inclusive_u32(d, fl, sums, workspace=ws)
+    assert lib.u32scan_check(ws.ptr, s) == _native.OK
+    want_sums, want_nseg = oracle.segreduce(a, f)
+    assert np.array_equal(host(d), oracle.segscan_inclusive(a, f))
+    assert int(host(nseg)[0]) == want_nseg
+    if with_sums:
+        assert np.array_equal(host(sums)[:want_nseg], want_sums)

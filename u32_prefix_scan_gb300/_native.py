@@ -56,6 +56,8 @@ SIGNATURES = {
     "runs_layout_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp, _sz, _vp]),
     "runs_owner_u32": (_int, [_vp, _sz, _vp, _sz, _vp]),
     "u32scan_test_scan_skip_publish": (_int, [_vp, _sz, _vp, _vp, _sz, ctypes.c_uint, ctypes.c_ulonglong, _vp]),
+    "u32scan_test_segscan_skip_publish": (_int, [_vp, _vp, _sz, _vp, _sz, _vp, _vp, _sz, ctypes.c_uint,
+                                                  ctypes.c_ulonglong, _vp]),
 }
 
 _lib = None

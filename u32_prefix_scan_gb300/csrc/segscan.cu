@@ -674,3 +674,14 @@ extern "C" int segreduce_u32_u8heads(const uint32_t *data, const uint8_t *head_f
                                        seg_sums ? seg_capacity : 0, nseg, ws, ws_bytes, (cudaStream_t)stream,
                                        0xffffffffu, kDefaultLimitNs);
 }
+
+extern "C" int u32scan_test_segscan_skip_publish(uint32_t *data, const int32_t *head_flags, size_t n,
+                                                 uint32_t *seg_sums, size_t seg_capacity, uint32_t *nseg, void *ws,
+                                                 size_t ws_bytes, unsigned int skip_tile, unsigned long long limit_ns,
+                                                 u32scan_stream_t stream) {
+    if (seg_sums != nullptr)
+        return segscan_launch<true, true>(data, head_flags, n, seg_sums, seg_capacity, nseg, ws, ws_bytes,
+                                          (cudaStream_t)stream, skip_tile, limit_ns);
+    return segscan_launch<true, false>(data, head_flags, n, nullptr, 0, nseg, ws, ws_bytes, (cudaStream_t)stream,
+                                       skip_tile, limit_ns);
+}

@@ -279,10 +279,13 @@ class SegOp(Op):
         fl = ", u8 head flags" if args.u8heads else ""
         self.metric = f"U32 {what} Gelem/s and HBM GB/s (fraction of peak) at n=2^26 ({lengths}{fl}), 1 GB300"
         kind = {"segscan": "true,false", "segscan_sums": "true,true", "segreduce": "false,true"}[mode]
-        # (u32x4 per lane, u32x4 per lane per round) as the library picks them
-        shape = "7,1" if mode != "segreduce" and (mode == "segscan" or not args.u8heads) else (
-            "8,2" if args.u8heads else "6,2")
-        self.kernel = f"segscan_u32_persistent<512,{shape},2,{kind},{'uint8' if args.u8heads else 'int32'}>"
+        # (u32x4 a lane, ring stages, output buffer) as the library picks them
+        if mode == "segreduce":
+            r, stages, buf = 7, 3 if args.u8heads else 2, 0
+        else:
+            r, stages, buf = 7 if args.u8heads else 5, 2, 1
+        ftype = "uint8" if args.u8heads else "int32"
+        self.kernel = f"segscan_lanes_persistent<512,{r},{stages},{kind},{ftype},{buf}>"
         self.nseg = None
 
     def workload(self):

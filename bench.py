@@ -45,6 +45,9 @@ e2e        the same metric end to end from pinned host memory: the add
            copies out overlapped); the other ops copy their inputs in, make
            the same C-ABI call and copy their outputs out, every step.
 cpu_baseline  the CPU oracle (one thread, as it stands) on a bounded sample.
+library_context  (--library-context, the add scans) PyTorch's CUDA cumsum
+           over the same values, timed the same way, with a bit-for-bit
+           comparison against scan_inclusive_u32: context, not a baseline.
 
 --impl reference times that oracle alone on the host cores (rank 0 only).
 Under torchrun each rank runs its own replica of the workload on its own GPU
@@ -180,6 +183,38 @@ class ScanOp(Op):
         if self.inclusive:
             return got[0] == a[0] and np.array_equal(got[1:] - got[:-1], a[1:])
         return got[0] == 0 and np.array_equal(got[1:] - got[:-1], a[:-1])
+
+    def library_context(self, host, steps: int):
+        """PyTorch's own CUDA scan of the same values, timed the same way, for
+        context: torch.cumsum over int32 with an int32 result wraps exactly
+        as the U32 inclusive scan does (two's-complement addition), out of
+        place, so it moves the same 8 B/element. Its bits are compared with
+        this library's inclusive scan of the same input."""
+        import numpy as np
+        import torch
+
+        x = torch.from_numpy(host["data"].view(np.int32)).to(self.data.device)
+        y = torch.empty_like(x)
+        z = x.clone()
+        self.u.scan_inclusive_u32(z, workspace=self.ws)
+        torch.cumsum(x, 0, dtype=torch.int32, out=y)
+        torch.cuda.synchronize()
+        same = bool(torch.equal(y, z))
+        del z
+        for _ in range(3):
+            torch.cumsum(x, 0, dtype=torch.int32, out=y)
+        stream = torch.cuda.current_stream()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(steps):
+            torch.cumsum(x, 0, dtype=torch.int32, out=y)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        return {"call": "torch.cumsum(int32 values, dtype=int32, out=...) on the same device array", "ms_per_step": ms,
+                "value": self.n / (ms * 1e-3) / 1e9, "unit": UNIT, "hbm_gbs": 8 * self.n / (ms * 1e-3) / 1e9,
+                "bits_equal_to_scan_inclusive_u32": same}
 
     def oracle_step(self, lib, arrays):
         ptr = arrays["data"].ctypes.data_as(ctypes.POINTER(ctypes.c_uint32))
@@ -796,6 +831,8 @@ def parse_args(argv=None):
     p.add_argument("--inclusive", action="store_true", help="scan_op: inclusive instead of exclusive")
     p.add_argument("--graph", action="store_true",
                    help="capture the timed steps in one CUDA graph and time its replay (launch-bound sizes)")
+    p.add_argument("--library-context", action="store_true",
+                   help="scan ops: also time torch.cumsum on the same values (context, not a baseline)")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -1092,6 +1129,12 @@ def run_ours(args, rank, local_rank, world):
         if not op.check_e2e(host):
             raise SystemExit("bench: e2e result fails its property check")
 
+    library = None
+    if args.library_context:
+        if not hasattr(op, "library_context") or getattr(op, "monoid", "add") != "add":
+            raise SystemExit("bench: --library-context applies to the U32 add scans")
+        library = op.library_context(host, args.steps)
+
     peak, peak_kind = load_peak()
     nbytes = op.algorithmic_bytes()
     achieved = nbytes / (kernel_ms * 1e-3) / 1e9
@@ -1126,6 +1169,9 @@ def run_ours(args, rank, local_rank, world):
         "clocks": clocks,
         "gpu_launches": args.steps * op.launches_per_step,
     }
+    if library is not None:
+        library["frac"] = library["hbm_gbs"] / peak
+        result["library_context"] = library
     if rank == 0 and not args.no_cpu_baseline:
         v, reps, el = time_oracle(op, host, args.cpu_seconds, op.n)
         result["cpu_baseline"] = {"value": v / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",

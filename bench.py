@@ -45,9 +45,10 @@ e2e        the same metric end to end from pinned host memory: the add
            copies out overlapped); the other ops copy their inputs in, make
            the same C-ABI call and copy their outputs out, every step.
 cpu_baseline  the CPU oracle (one thread, as it stands) on a bounded sample.
-library_context  (--library-context, the add scans) PyTorch's CUDA cumsum
-           over the same values, timed the same way, with a bit-for-bit
-           comparison against scan_inclusive_u32: context, not a baseline.
+library_context  (--library-context) PyTorch's CUDA cumsum over the
+           same values (the add scans), or its stable sort of the same keys
+           (radix), timed the same way, with a bit-for-bit comparison
+           against this library's result: context, not a baseline.
 
 --impl reference times that oracle alone on the host cores (rank 0 only).
 Under torchrun each rank runs its own replica of the workload on its own GPU
@@ -669,6 +670,37 @@ class RadixOp(Op):
             ok &= bool(np.array_equal(self.pinned_out["keys_out"].numpy().view(np.uint32), np.sort(host["keys"])))
         return ok
 
+    def library_context(self, host, steps: int):
+        """PyTorch's CUDA stable sort of the same keys, for context:
+        torch.sort(stable=True) over int32 keys with the sign bit flipped
+        (signed order of k ^ 2^31 is the unsigned order of k; the flip is
+        done once, outside the timing) returns the sorted keys and int64
+        indices, which are compared with this library's permutation."""
+        import numpy as np
+        import torch
+
+        flipped = torch.from_numpy((host["keys"] ^ np.uint32(1 << 31)).view(np.int32)).to(self.keys.device)
+        perm = torch.empty(self.n, dtype=torch.int32, device=self.keys.device)
+        self.u.radix_sort_perm_u32(self.keys, perm, workspace=self.ws)
+        _, idx = torch.sort(flipped, stable=True)
+        torch.cuda.synchronize()
+        same = bool(torch.equal(idx.to(torch.int32), perm))
+        del perm, idx
+        for _ in range(3):
+            torch.sort(flipped, stable=True)
+        stream = torch.cuda.current_stream()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(steps):
+            torch.sort(flipped, stable=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        return {"call": "torch.sort(int32 keys ^ 2^31, stable=True) -> sorted keys + int64 indices, same device keys",
+                "ms_per_step": ms, "value": self.n / (ms * 1e-3) / 1e9, "unit": UNIT,
+                "indices_equal_to_radix_sort_perm_u32": same}
+
     def oracle_step(self, lib, arrays):
         import numpy as np
 
@@ -832,7 +864,7 @@ def parse_args(argv=None):
     p.add_argument("--graph", action="store_true",
                    help="capture the timed steps in one CUDA graph and time its replay (launch-bound sizes)")
     p.add_argument("--library-context", action="store_true",
-                   help="scan ops: also time torch.cumsum on the same values (context, not a baseline)")
+                   help="add scans / radix: also time torch.cumsum / torch.sort on the same inputs (context)")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -1132,7 +1164,7 @@ def run_ours(args, rank, local_rank, world):
     library = None
     if args.library_context:
         if not hasattr(op, "library_context") or getattr(op, "monoid", "add") != "add":
-            raise SystemExit("bench: --library-context applies to the U32 add scans")
+            raise SystemExit("bench: --library-context applies to the U32 add scans and the radix sort")
         library = op.library_context(host, args.steps)
 
     peak, peak_kind = load_peak()
@@ -1170,7 +1202,8 @@ def run_ours(args, rank, local_rank, world):
         "gpu_launches": args.steps * op.launches_per_step,
     }
     if library is not None:
-        library["frac"] = library["hbm_gbs"] / peak
+        if "hbm_gbs" in library:
+            library["frac"] = library["hbm_gbs"] / peak
         result["library_context"] = library
     if rank == 0 and not args.no_cpu_baseline:
         v, reps, el = time_oracle(op, host, args.cpu_seconds, op.n)

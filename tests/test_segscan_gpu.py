@@ -72,6 +72,11 @@ def check_segscan(u, a, f, offset_a=0, offset_f=0, cap=None):
     k = min(cap, want_nseg)
     assert np.array_equal(host(sums)[:k], want_sums[:k])
     assert np.all(host(sums)[k:cap] == 0xFFFFFFFF)  # nothing written past the segments / capacity
+    # the form without sums (its own count path) on the same input
+    d2 = dev(a, offset_a)
+    c2 = u.segscan_inclusive_u32(d2, fl)
+    u.check()
+    assert np.array_equal(host(d2), host(d)) and int(host(c2)[0]) == want_nseg
 
 
 # around the tiles of the forms that write the scan (10240 elements with

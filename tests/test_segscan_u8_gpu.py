@@ -79,6 +79,10 @@ def check(u, a, f, off_a=0, off_f=0, cap=None):
     k = min(cap, want_nseg)
     assert np.array_equal(host(sums)[:k], want_sums[:k])
     assert np.all(host(sums)[k:cap] == 0xFFFFFFFF)
+    d3 = dev32(a, off_a)  # the form without sums, on the same input
+    c3 = u.segscan_inclusive_u32(d3, fl)
+    u.check()
+    assert np.array_equal(host(d3), host(d)) and int(host(c3)[0]) == want_nseg
     d2 = dev32(a, off_a)
     s2, c2 = u.segreduce_u32(d2, fl)
     u.check()

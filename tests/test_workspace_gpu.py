@@ -1,5 +1,5 @@
 """Every operation keeps the shared 256-byte workspace header (tile counter,
-call epoch, device status) valid: interleaving all operations on one
+call epoch, device status, the segment count word) valid: interleaving all operations on one
 workspace, in every order, must give oracle-exact results and a clean
 status after each call."""
 
@@ -47,11 +47,13 @@ def run_op(u, ws, which, n, seed):
         a = inputs.splitmix_u32(seed, 0, n)
         f = inputs.segment_heads_geometric(n, seed, log2_mean=6)
         d, fl = dev32(a), dev32(f)
-        sums = torch.empty(n, dtype=torch.int32, device="cuda")
+        # with sums, or without (the segment count then goes through a
+        # header word of its own)
+        sums = torch.empty(n, dtype=torch.int32, device="cuda") if seed % 2 else None
         nseg = u.segscan_inclusive_u32(d, fl, sums, workspace=ws)
         want_sums, want_n = oracle.segreduce(a, f)
         ok = (np.array_equal(host_u32(d), oracle.segscan_inclusive(a, f)) and int(nseg.item()) == want_n
-              and np.array_equal(host_u32(sums)[:want_n], want_sums))
+              and (sums is None or np.array_equal(host_u32(sums)[:want_n], want_sums)))
     elif which == "compact":
         f = inputs.compact_flags(n, seed, 0.1)
         offsets, indices, count = u.compact_indices_u32(dev32(f), workspace=ws)

@@ -23,7 +23,9 @@
 // the next tile and publishes its aggregate, then walks the current tile's
 // look-back, adds the carry and stores. Per tile the look-back carries two
 // words (internal.cuh): the segmented value and the running head count; the
-// head count gives every segment end its index into the sums.
+// head count gives every segment end its index into the sums. The forms
+// without sums need no such index: they walk the value alone, and count
+// the segments with one atomic add a tile.
 //
 // Layout inside a tile (lane runs): lane l of warp w owns the E = 4R
 // consecutive elements at w * 32E + l * E of the tile (R u32x4, R odd: a
@@ -55,8 +57,35 @@
 #ifndef U32SCAN_S_FEWENDS
 #define U32SCAN_S_FEWENDS 2  // segment ends a lane up to which its sums are visited end by end (no buffer)
 #endif
+#ifndef U32SCAN_S_ATOMCOUNT
+#define U32SCAN_S_ATOMCOUNT 1  // without sums: the segment count by one atomic add a tile, no count look-back
+#endif
 
 namespace u32scan {
+
+// The segment count of the forms without sums, which need no segment index
+// per tile: every tile adds 2^32 + (its head count) to one 64-bit word of
+// the workspace header (a spare word no other kernel uses, at byte 128, away
+// from the 128-byte line of the tile counter). The add that finds
+// n_tiles - 1 tiles counted before it is the last, so its old value plus
+// its own count is the total; that tile puts the word back to zero for the
+// next call. The heads of a whole array number fewer than 2^32, so they
+// never carry into the tile count. (A compare-and-swap loop on a word in
+// the tile counter's line measured 13 times slower than the look-back.)
+__device__ __forceinline__ unsigned long long *seg_count_word(WsHeader *hdr) {
+    return reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(hdr) + 128);
+}
+static_assert(sizeof(WsHeader) >= 136, "the count word lies inside the header");
+
+__device__ __forceinline__ bool seg_count_add(WsHeader *hdr, unsigned int n_tiles, unsigned int heads,
+                                              unsigned int &total) {
+    unsigned long long *w = seg_count_word(hdr);
+    const unsigned long long old = atomicAdd(w, (1ull << 32) | (unsigned long long)heads);
+    if ((unsigned int)(old >> 32) != n_tiles - 1u) return false;
+    total = (unsigned int)old + heads;
+    atomicExch(w, 0ull);
+    return true;
+}
 
 // Element j (0 <= j < 4R, known only at run time) of a run held in
 // registers, by predicated moves: the u32x4 first, then the component.
@@ -96,6 +125,7 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
                          unsigned long long *desc2, unsigned int n_tiles, unsigned int head, int streams_aligned,
                          unsigned int skip_tile, unsigned long long limit_ns) {
     constexpr int WARPS = THREADS / 32;
+    constexpr bool ATOM_COUNT = !WANT_SUMS && U32SCAN_S_ATOMCOUNT;  // the count serves no segment index
     constexpr int E = 4 * R;                    // elements a lane
     constexpr unsigned int CHUNK = 32u * E;     // elements a warp
     constexpr unsigned int TILE = WARPS * CHUNK;
@@ -431,7 +461,7 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
         if (lane == 0 && t != skip_tile) {
             // a tile holding a head knows its segmented carry at once
             st_relaxed(desc2 + 2ull * t, tag | (a_head || t == 0 ? (kFlagH | kFlagP) : 0ull) | a_val);
-            st_relaxed(desc2 + 2ull * t + 1, tag | (t == 0 ? kFlagP : 0ull) | a_cnt);
+            if (!ATOM_COUNT) st_relaxed(desc2 + 2ull * t + 1, tag | (t == 0 ? kFlagP : 0ull) | a_cnt);
         }
     };
 
@@ -456,18 +486,33 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
             }
             if (warp == 0) {
                 if (more) block_aggregate((int)(u & 1u), tn, n_val, n_head, n_cnt, n_xval, n_before, n_xcnt);
-                const SegPrefix pre =
-                    lookback_seg_wide<U32SCAN_S_LOOKA, U32SCAN_S_LOOKB>(desc2, tc, tag, hdr, limit_ns, lane);
+                SegPrefix pre{0u, 0u};
+                if constexpr (ATOM_COUNT) {
+                    if (tc != 0) {
+                        unsigned long long wa[U32SCAN_S_LOOKA];
+                        lookback_window<U32SCAN_S_LOOKA, kAdd, 2>(desc2, (long long)tc - 1, tag, lane, wa);
+                        pre.seg = lookback_prefix_wide<U32SCAN_S_LOOKA, kAdd, 2, kFlagP | kFlagH>(desc2, tc, tag, hdr,
+                                                                                                limit_ns, lane, wa);
+                    }
+                } else {
+                    pre = lookback_seg_wide<U32SCAN_S_LOOKA, U32SCAN_S_LOOKB>(desc2, tc, tag, hdr, limit_ns, lane);
+                }
                 if (lane == 0 && tc != 0 && tc != skip_tile) {
                     if (!agg_head) st_relaxed(desc2 + 2ull * tc, tag | kFlagP | (unsigned int)(pre.seg + agg_val));
-                    st_relaxed(desc2 + 2ull * tc + 1, tag | kFlagP | (unsigned int)(pre.cnt + agg_cnt));
+                    if (!ATOM_COUNT)
+                        st_relaxed(desc2 + 2ull * tc + 1, tag | kFlagP | (unsigned int)(pre.cnt + agg_cnt));
                 }
                 if (lane < WARPS) {
                     s_bval[lane] = head_before ? wex_val : pre.seg + wex_val;
                     s_bcnt[lane] = pre.cnt + wex_cnt;
                 }
                 if (lane == 0) {
-                    if (tc == n_tiles - 1u && nseg != nullptr) *nseg = pre.cnt + agg_cnt;
+                    unsigned int total;
+                    if (ATOM_COUNT) {
+                        if (nseg != nullptr && seg_count_add(hdr, n_tiles, agg_cnt, total)) *nseg = total;
+                    } else if (tc == n_tiles - 1u && nseg != nullptr) {
+                        *nseg = pre.cnt + agg_cnt;
+                    }
                     if (WANT_SUMS) s_nexthead = nh_c;
                 }
             }

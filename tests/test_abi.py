@@ -248,3 +248,26 @@ def test_host_scan_workspace_bytes(lib):
         assert b >= 4 * min(n, 2 << 18)
         # and never more than four 2^23-element slots plus the carry words
         assert b <= 4 * 4 * (1 << 23) + wb(_native.OP_SCAN, 1 << 23) + wb(_native.OP_SCAN, (1 << 22) - 1) + 512
+
+
+def test_readme_c_example_compiles_and_links(lib, tmp_path):
+    # the README's C example, built as a caller would build it: the header,
+    # the CUDA runtime header, and a link against the library (no GPU call)
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda = pathlib.Path("/usr/local/cuda")
+    if cc is None or not (cuda / "include" / "cuda_runtime.h").exists():
+        pytest.skip("no C compiler or CUDA headers")
+    text = (ROOT / "README.md").read_text()
+    code = re.search(r"```c\n(.*?)```", text, flags=re.S).group(1)
+    src = tmp_path / "example.c"
+    src.write_text(code + "\nint main(int argc, char **argv) { (void)argv; return argc > 1 ? scan_in_place(0, 0, 0, 0) : 0; }\n")
+    so = pathlib.Path(_native.__file__).with_name("libu32scan.so")
+    libdirs = [d for d in (cuda / "lib64", cuda / "targets" / "sbsa-linux" / "lib", cuda / "targets" / "x86_64-linux" / "lib")
+               if d.exists()]
+    cmd = [cc, "-std=c99", "-Wall", "-Werror", str(src), "-I", str(ROOT / "include"), "-I", str(cuda / "include"),
+           str(so), *[f"-L{d}" for d in libdirs], "-lcudart", f"-Wl,-rpath,{so.parent}", "-o", str(tmp_path / "ex")]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr

@@ -250,8 +250,8 @@ def test_host_scan_workspace_bytes(lib):
         assert b <= 4 * 4 * (1 << 23) + wb(_native.OP_SCAN, 1 << 23) + wb(_native.OP_SCAN, (1 << 22) - 1) + 512
 
 
-def test_readme_c_example_compiles_and_links(lib, tmp_path):
-    # the README's C example, built as a caller would build it: the header,
+def test_c_example_compiles_and_links(lib, tmp_path):
+    # examples/scan_in_place.c built as a caller would build it: the header,
     # the CUDA runtime header, and a link against the library (no GPU call)
     import shutil
     import subprocess
@@ -260,10 +260,7 @@ def test_readme_c_example_compiles_and_links(lib, tmp_path):
     cuda = pathlib.Path("/usr/local/cuda")
     if cc is None or not (cuda / "include" / "cuda_runtime.h").exists():
         pytest.skip("no C compiler or CUDA headers")
-    text = (ROOT / "README.md").read_text()
-    code = re.search(r"```c\n(.*?)```", text, flags=re.S).group(1)
-    src = tmp_path / "example.c"
-    src.write_text(code + "\nint main(int argc, char **argv) { (void)argv; return argc > 1 ? scan_in_place(0, 0, 0, 0) : 0; }\n")
+    src = ROOT / "examples" / "scan_in_place.c"
     so = pathlib.Path(_native.__file__).with_name("libu32scan.so")
     libdirs = [d for d in (cuda / "lib64", cuda / "targets" / "sbsa-linux" / "lib", cuda / "targets" / "x86_64-linux" / "lib")
                if d.exists()]

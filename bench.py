@@ -105,6 +105,10 @@ class Op:
     def algorithmic_bytes(self) -> int:
         raise NotImplementedError
 
+    def is_marked(self) -> bool:
+        """Whether a step brackets its dominant kernel with events (step_marked)."""
+        return hasattr(self, "step_marked")
+
 
 class ScanOp(Op):
     log2n = 28
@@ -114,6 +118,11 @@ class ScanOp(Op):
         super().__init__(args)
         self.inclusive = inclusive
         self.monoid = monoid
+        # under torchrun: rank r scans its shard of one array of N * n elements
+        self.world, self.rank = getattr(args, "world", 1), getattr(args, "rank", 0)
+        self.sharded = self.world > 1 and monoid == "add"
+        if self.sharded:
+            self.launches_per_step = 3  # fold, scan of the gathered sums, scan from the carry-in
         form = "inclusive" if inclusive else "exclusive"
         self.name = f"scan_{form}_u32" if monoid == "add" else f"scan_{monoid}_{form}_u32"
         what = "" if monoid == "add" else f"{monoid} "
@@ -123,15 +132,24 @@ class ScanOp(Op):
     def workload(self):
         form = "inclusive" if self.inclusive else "exclusive"
         what = "" if self.monoid == "add" else f"{self.monoid}-"
-        return f"u32 {what}{form} scan in place + total, n=2^{self.n.bit_length() - 1}, uniform u32 seed 2"
+        lg = self.n.bit_length() - 1
+        if self.sharded:
+            return (f"u32 {form} scan in place + total of one array of {self.world} x 2^{lg} elements (uniform u32 "
+                    f"seed 2), sharded: rank r holds elements [r 2^{lg}, (r+1) 2^{lg})")
+        return f"u32 {what}{form} scan in place + total, n=2^{lg}, uniform u32 seed 2"
 
     def algorithmic_bytes(self):
-        return 8 * self.n  # read 4 + write 4 per element
+        return 8 * self.n  # read 4 + write 4 per element (the scan kernel; the sharded fold reads 4 more)
 
     def host_inputs(self):
         from u32_prefix_scan_gb300 import inputs
 
+        if self.sharded:
+            return {"data": inputs.splitmix_u32(2, 0, self.n, start=self.rank * self.n)}
         return {"data": inputs.scan_values(self.n, 2)}
+
+    def is_marked(self) -> bool:
+        return self.sharded
 
     def setup(self, dev, host):
         import numpy as np
@@ -147,7 +165,14 @@ class ScanOp(Op):
             self.fn = lambda d, t, workspace: u.scan_u32_op(d, self.monoid, self.inclusive, t, workspace=workspace)
         self.data = torch.from_numpy(host["data"].view(np.int32)).to(dev)
         self.total = torch.empty(1, dtype=torch.int32, device=dev)
-        self.ws = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_SCAN, self.n), dev)
+        lib = _native.lib()
+        self.ws = u.Workspace(max(lib.u32scan_workspace_bytes(_native.OP_SCAN, self.n),
+                                  lib.u32scan_workspace_bytes(_native.OP_REDUCE, self.n)), dev)
+        if self.sharded:
+            from u32_prefix_scan_gb300 import shard
+
+            self.shard = shard
+            self.steps = shard.KernelSteps(workspace=self.ws)
         self.pinned_in = {"data": torch.from_numpy(host["data"].view(np.int32)).pin_memory()}
         self.pinned_out = {"data": torch.empty(self.n, dtype=torch.int32).pin_memory(),
                            "total": torch.empty(1, dtype=torch.int32).pin_memory()}
@@ -156,9 +181,23 @@ class ScanOp(Op):
             self.ws_host = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_SCAN_HOST, self.n), dev)
 
     def step(self):
-        self.fn(self.data, self.total, workspace=self.ws)
+        if self.sharded:
+            self.total = self.shard.sharded_scan(self.data, self.inclusive, steps=self.steps)
+        else:
+            self.fn(self.data, self.total, workspace=self.ws)
+
+    def step_marked(self, before, after):
+        """The sharded step with events around its scan from the carry-in,
+        the kernel that moves 8 of its 12 bytes an element."""
+        self.total = self.shard.sharded_scan(self.data, self.inclusive, steps=self.steps, marks=(before, after))
 
     def e2e_step(self):
+        if self.sharded:  # the shard in from pinned host memory, the sharded scan, the shard and total out
+            self.data.copy_(self.pinned_in["data"], non_blocking=True)
+            self.step()
+            self.pinned_out["data"].copy_(self.data, non_blocking=True)
+            self.pinned_out["total"].copy_(self.total, non_blocking=True)
+            return 4 * self.n, 4 * self.n + 4
         if self.monoid == "add":  # host array in, host array out, through the device in overlapped chunks
             self.host_fn(self.pinned_in["data"], self.pinned_out["data"], self.pinned_out["total"],
                          workspace=self.ws_host)
@@ -178,6 +217,8 @@ class ScanOp(Op):
         k = min(self.n, 1 << 20)
         got = self.pinned_out["data"][:k].numpy().view(np.uint32)
         a = host["data"][:k]
+        if self.sharded:  # the shard starts from its carry-in; the total is the whole array's
+            return np.array_equal(got[1:] - got[:-1], a[1:] if self.inclusive else a[:-1])
         total = int(self.pinned_out["total"].numpy().view(np.uint32)[0])
         if total != int(host["data"].sum(dtype=np.uint64)) % (1 << 32):
             return False
@@ -866,6 +907,8 @@ def parse_args(argv=None):
     p.add_argument("--library-context", action="store_true",
                    help="add scans / radix: also time torch.cumsum / torch.sort on the same inputs (context)")
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--soak-seconds", type=float, default=1.0,
+                   help="after the timed region, repeat timed windows of the same steps this long (clock record)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--log2n", type=int, default=None,
@@ -978,12 +1021,9 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
-    def window(self, t0, t1):
-        self.t0, self.t1 = t0, t1
-
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            return
         time.sleep(0.12)
         self.proc.terminate()
         try:
@@ -991,7 +1031,13 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.reader.join(timeout=2)
-        rows = [l for (t, l) in self.lines if self.t0 is None or (self.t0 - 0.06 <= t <= self.t1 + 0.06)]
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, its maximum and the throttle reasons seen in
+        [t0, t1] (the samples around it when none fall inside)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = [l for (t, l) in self.lines if t0 is None or (t0 - 0.06 <= t <= t1 + 0.06)]
         if not rows and self.lines:
             rows = [self.lines[-1][1]]
         sm, smax, reasons = [], [], set()
@@ -1089,6 +1135,7 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.current_stream()
+    args.world, args.rank = world, rank
     op = make_op(args)
     host = op.host_inputs()
     op.setup(dev, host)
@@ -1104,7 +1151,7 @@ def run_ours(args, rank, local_rank, world):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # an op whose step runs several calls brackets its dominant kernel with
     # events on the launching stream; the roofline uses that kernel's time
-    marked = hasattr(op, "step_marked")
+    marked = op.is_marked()
     marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in range(args.steps if marked else 0)]
     graph = None
@@ -1134,8 +1181,26 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.synchronize()
     w1 = time.time()
     barrier(world)
-    sampler.window(w0, w1)
-    clocks = sampler.stop()
+    # Repeat windows of the same K steps for about --soak-seconds (timed
+    # each, reported apart from the timed region), so that the clock record
+    # holds more than the few samples a short timed region gets.
+    soak = []
+    w2 = time.time()
+    while args.soak_seconds > 0 and time.time() - w2 < args.soak_seconds:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            for k in range(args.steps):
+                op.step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        soak.append(a.elapsed_time(b) / args.steps)
+    w3 = time.time()
+    barrier(world)
+    sampler.stop()
+    clocks = sampler.summary(w0, w1)
     op.u.check(workspace=op.ws)
     ms = start.elapsed_time(end) / args.steps
     ms_max = max_over_ranks(ms, world)
@@ -1201,6 +1266,15 @@ def run_ours(args, rank, local_rank, world):
         "clocks": clocks,
         "gpu_launches": args.steps * op.launches_per_step,
     }
+    if soak:
+        soak.sort()
+        result["repeat_windows"] = {"windows": len(soak), "steps_each": args.steps,
+                                    "ms_per_step_median": soak[len(soak) // 2], "ms_per_step_min": soak[0],
+                                    "ms_per_step_max": soak[-1], "clocks": sampler.summary(w2, w3)}
+    if getattr(op, "sharded", False):
+        result["scaling"] = "weak"
+        result["config"]["per_rank"] = ("one shard of one global scan: fold (4 B/elem), all-gather of the "
+                                        f"{world} shard sums over NCCL, scan from the carry-in (8 B/elem)")
     if library is not None:
         if "hbm_gbs" in library:
             library["frac"] = library["hbm_gbs"] / peak

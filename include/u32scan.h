@@ -24,9 +24,12 @@
  *     u32scan_workspace_init); after that the library keeps it consistent
  *     itself, so it is reused across calls and shared between operations
  *     without clearing (the radix sort, which keeps data in it, clears what
- *     it leaves where other operations keep tile state). A workspace serves
- *     one call at a time: calls that share one workspace must be ordered
- *     (the same stream, or events).
+ *     it leaves where other operations keep tile state). This holds for any
+ *     number of calls: carry words are tagged with a per-workspace launch
+ *     count whose tags repeat every 2^29 launches, and the launch that ends
+ *     such a period zeroes the carry words (up to a few MiB of ws) before the
+ *     next one starts. A workspace serves one call at a time: calls that
+ *     share one workspace must be ordered (the same stream, or events).
  *   - Return value: U32SCAN_OK, or a negative status. Argument errors are
  *     found on the host before anything is launched; nothing is written
  *     then. U32SCAN_ECUDA reports a launch failure (cudaGetLastError).
@@ -73,6 +76,7 @@ typedef struct CUstream_st *u32scan_stream_t;
 #define U32SCAN_OP_RUNS 5      /* runs_layout_u32 (runs_owner_u32 needs none) */
 #define U32SCAN_OP_SCAN64 6    /* scan_u64_op */
 #define U32SCAN_OP_SCAN_HOST 7 /* scan_exclusive_u32_host, scan_inclusive_u32_host */
+#define U32SCAN_OP_REDUCE 8    /* reduce_u32_op (the same size for every n) */
 
 /* Bytes of device workspace an operation needs for n elements (a multiple
  * of 256, at least 256). Returns 0 for an unknown op. Pure host function. */
@@ -83,7 +87,10 @@ int u32scan_workspace_init(void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /* Wait for `stream`, then read and clear the device-side status that the
  * calls using `ws` left: U32SCAN_OK, or U32SCAN_ETIMEOUT when a tile gave up
- * waiting for its predecessor's carry (its results are then wrong).
+ * waiting for its predecessor's carry or a block gave up waiting for a tile's
+ * bulk copy (the results of that call are then wrong). After a timeout,
+ * zero-fill the workspace again (u32scan_workspace_init) before reusing it:
+ * a launch whose blocks stopped early may leave its tile counter unreset.
  * U32SCAN_ECUDA if the synchronisation or the read fails. */
 int u32scan_check(void *ws, u32scan_stream_t stream);
 
@@ -117,6 +124,50 @@ int scan_exclusive_u32(uint32_t *data, size_t n, uint32_t *total,
  */
 int scan_inclusive_u32(uint32_t *data, size_t n, uint32_t *total,
                        void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * The two scans of one piece of a longer array: the piece starts after a
+ * carry-in, the wrapped sum of everything before it (a device word, so that
+ * it can come from an earlier kernel or a collective without a host round
+ * trip). Source: "scan.bend source", section Driver (each block is rescanned
+ * from its base, the scan of the block sums before it) and section API; one
+ * level up, the pieces are the shards of an array split across GPUs.
+ *   data, n, ws, ws_bytes, stream  as scan_exclusive_u32.
+ *   carry_in  device, one uint32_t (4-byte aligned), or NULL for 0:
+ *             exclusive: data[j] = carry_in + data[0] + .. + data[j-1];
+ *             inclusive: through data[j].
+ *   total     device, one uint32_t or NULL: carry_in + data[0] + .. +
+ *             data[n-1] (wrapping); must not be carry_in itself (the block
+ *             holding the first tile may read the carry-in after the last
+ *             tile has written the total).
+ * Errors: EINVAL (as scan_exclusive_u32, a misaligned carry_in, total ==
+ * carry_in), EWORKSPACE, ECUDA.
+ */
+int scan_exclusive_u32_carry(uint32_t *data, size_t n, const uint32_t *carry_in, uint32_t *total,
+                             void *ws, size_t ws_bytes, u32scan_stream_t stream);
+int scan_inclusive_u32_carry(uint32_t *data, size_t n, const uint32_t *carry_in, uint32_t *total,
+                             void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * The fold of an array under one of U32SCAN_ADD .. U32SCAN_MAX, reading it
+ * once (4 bytes an element) and writing nothing else. Source: the CAIRN
+ * "Concurrency" page, section "reduce and compact" (`reduce` with add_wrap,
+ * mul_wrap, &, |, ^, min, max; sums and products wrap at 2^32). Every such
+ * operator is associative and commutative, so the result does not depend on
+ * the order in which the device folds.
+ *   op        U32SCAN_ADD .. U32SCAN_MAX.
+ *   data      device, uint32_t[n], 4-byte aligned, read only.
+ *   n         element count, below 2^62.
+ *   total     device, one uint32_t (4-byte aligned): the fold (the
+ *             operator's identity when n == 0).
+ *   ws, ws_bytes  u32scan_workspace_bytes(U32SCAN_OP_REDUCE, n) bytes (a
+ *             few KiB, the same for every n), 256-byte aligned, zero-filled
+ *             once; shared with the other operations like any workspace.
+ * Errors: EINVAL (unknown op, null data with n > 0, null total, misaligned
+ * pointers), EWORKSPACE, ECUDA.
+ */
+int reduce_u32_op(int op, const uint32_t *data, size_t n, uint32_t *total,
+                  void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /*
  * The same two scans of an array in HOST memory, with the result written to
@@ -371,18 +422,30 @@ int runs_owner_u32(const uint32_t *ends, size_t n, int32_t *owner, size_t capaci
  * every GPU that loads the library until the process exits). The first
  * call on each device looks up that array's device address
  * (cudaGetSymbolAddress) with the device current; make that first call
- * before any stream capture. Each call enqueues a 4-byte cudaMemsetAsync on
- * `stream` (re-arming the array's tile counter) and then the scan kernel;
- * it calls no cudaMalloc or cudaFree.
+ * before any stream capture. Each call enqueues the scan kernel alone on
+ * `stream`; it calls no cudaMalloc, cudaFree or memset. The array keeps
+ * its state between calls: each launch leaves it ready for the next.
  * All calls share the one array: calls that overlap on the GPU (different
  * streams, or different host threads without ordering) race and give wrong
  * results. Order them, e.g. on one stream.
  * Errors: EINVAL for n > 2^31 (the scratch limit) and as scan_exclusive_u32;
  * ECUDA if the set-up or a launch fails. A carry-wait timeout is recorded
- * in the internal array only and is not reported by this entry point.
+ * in the array's status word: read it with u32scan_check_noalloc.
  */
 int scan_exclusive_u32_noalloc(uint32_t *data, size_t n, uint32_t *total,
                                u32scan_stream_t stream);
+
+/*
+ * The device-side status of the allocation-free scan (no counterpart on the
+ * pages): waits for `stream`, then reads and clears the status word of the
+ * library's fixed array, as u32scan_check does for a workspace. Returns
+ * U32SCAN_OK, or U32SCAN_ETIMEOUT when a call since the last check gave up
+ * waiting (its results are then wrong; the array is then zero-filled on
+ * `stream` and waited for, so later calls start afresh); U32SCAN_ECUDA if
+ * the set-up, the synchronisation, the read or the fill fails. Allocates
+ * nothing.
+ */
+int u32scan_check_noalloc(u32scan_stream_t stream);
 
 /*
  * Test hook for the bounded carry wait (no counterpart on the pages; the
@@ -414,6 +477,24 @@ int u32scan_test_segscan_skip_publish(uint32_t *data, const int32_t *head_flags,
                                       unsigned int skip_tile,
                                       unsigned long long limit_ns,
                                       u32scan_stream_t stream);
+
+/*
+ * The same test hook for the allocation-free scan (no counterpart on the
+ * pages): runs scan_exclusive_u32_noalloc with tile `skip_tile` never
+ * publishing its carry, so the next u32scan_check_noalloc() returns
+ * U32SCAN_ETIMEOUT. Tiles hold 2048 elements below 2^19 elements, 16384
+ * from there. The results are then wrong by design; later calls are not
+ * affected.
+ */
+int u32scan_test_noalloc_skip_publish(uint32_t *data, size_t n, uint32_t *total, unsigned int skip_tile,
+                                      unsigned long long limit_ns, u32scan_stream_t stream);
+
+/*
+ * Test hook (no counterpart on the pages): sets the launch count of the
+ * allocation-free scan's fixed array, ordered on `stream`, so that a test
+ * can reach the end of a tag period (2^29 launches) without making them.
+ */
+int u32scan_test_noalloc_set_epoch(unsigned int epoch, u32scan_stream_t stream);
 
 #ifdef __cplusplus
 }

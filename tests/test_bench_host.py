@@ -97,3 +97,20 @@ def test_two_gloo_ranks_barrier_max_and_reference_on_rank0(tmp_path):
     r1 = json.loads((tmp_path / "rank1.json").read_text())
     assert r0["max"] == r1["max"] == 2.5  # the slowest rank's time
     assert r0["ref"] == "reference" and r1["ref"] is None
+
+
+def test_scan_under_several_ranks_is_one_sharded_scan():
+    args = bench.parse_args([])
+    args.world, args.rank = 4, 2
+    op = bench.make_op(args)
+    assert op.sharded and op.is_marked() and op.launches_per_step == 3
+    assert "4 x 2^28" in op.workload()
+    # rank 2's shard continues the seed-2 stream where rank 1's ends
+    from u32_prefix_scan_gb300 import inputs
+
+    args.log2n = 10
+    op = bench.make_op(args)
+    whole = inputs.splitmix_u32(2, 0, 4 << 10)
+    assert (op.host_inputs()["data"] == whole[2 << 10: 3 << 10]).all()
+    args.world, args.rank = 1, 0
+    assert not bench.make_op(args).sharded

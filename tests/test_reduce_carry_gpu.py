@@ -1,0 +1,131 @@
+"""GPU parity of the fold (reduce_u32_op), the scans from a carry-in
+(scan_*_u32_carry) and their composition into a sharded scan, against the
+CPU oracle, through the C ABI.
+
+The fold is checked under every CAIRN integer operator against the oracle's
+scan total; a scan from a carry-in c against the oracle scan plus c (the
+scan of the piece as part of a longer array whose earlier elements sum to
+c). The composition splits one array into pieces and scans each from the
+exclusive scan of the pieces' folds ("scan.bend source", section Driver,
+with pieces for blocks): the pieces put back together must equal the
+oracle's scan of the whole array. On one GPU the pieces' exchange is
+emulated by concatenation (no kernel waits on another), and the
+collective-driven form runs on a one-rank NCCL group.
+"""
+
+import os
+import socket
+
+import numpy as np
+import pytest
+
+import oracle
+from u32_prefix_scan_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+SIZES = [0, 1, 3, 4, 1000, 4 * 512 * 4 * 2 + 5, (1 << 20) + 3, (1 << 24) + 12345]
+
+
+@pytest.fixture(scope="module")
+def u():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from u32_prefix_scan_gb300 import build
+
+    build.build()
+    import u32_prefix_scan_gb300 as u
+
+    return u
+
+
+def dev32(a, offset=0):
+    buf = torch.empty(a.size + offset + 4, dtype=torch.int32, device="cuda")
+    view = buf[offset: offset + a.size]
+    view.copy_(torch.from_numpy(np.ascontiguousarray(a).view(np.int32)))
+    return view
+
+
+def host_u32(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+@pytest.mark.parametrize("op", ["add", "mul", "and", "or", "xor", "min", "max"])
+@pytest.mark.parametrize("n", SIZES)
+def test_fold_matches_the_oracle(u, op, n):
+    a = inputs.splitmix_u32(61, 0, n)
+    if op == "mul":
+        a = a | 1  # odd factors: the product stays informative instead of reaching 0
+    for offset in (0, 1, 3):  # every 4-byte phase of the start
+        d = dev32(a, offset)
+        total = u.reduce_u32_op(d, op)
+        u.check()
+        assert int(host_u32(total)[0]) == oracle.scan_op(a, op, False)[1], (op, n, offset)
+        assert np.array_equal(host_u32(d), a)  # read only
+
+
+@pytest.mark.parametrize("inclusive", [False, True], ids=["exclusive", "inclusive"])
+@pytest.mark.parametrize("n", SIZES)
+def test_scan_from_a_carry_in(u, n, inclusive):
+    a = inputs.splitmix_u32(62, 0, n)
+    c = np.uint32(0xDEADBEEF)
+    want, want_total = (oracle.scan_inclusive if inclusive else oracle.scan_exclusive)(a)
+    fn = u.scan_inclusive_u32_carry if inclusive else u.scan_exclusive_u32_carry
+    for offset in (0, 2):
+        d = dev32(a, offset)
+        carry = torch.from_numpy(np.array([c], np.uint32).view(np.int32)).cuda()
+        total = fn(d, carry)
+        u.check()
+        assert np.array_equal(host_u32(d), (want + c).astype(np.uint32)), (n, offset)
+        assert int(host_u32(total)[0]) == (want_total + int(c)) % (1 << 32)
+    # no carry-in: the plain scan
+    d = dev32(a)
+    total = fn(d, None)
+    u.check()
+    assert np.array_equal(host_u32(d), want) and int(host_u32(total)[0]) == want_total
+
+
+@pytest.mark.parametrize("inclusive", [False, True], ids=["exclusive", "inclusive"])
+@pytest.mark.parametrize("cuts", [[70001, 0, (1 << 22) + 9, 123], [(1 << 21) + 1, (1 << 21) + 1, 5]],
+                         ids=["uneven-with-empty", "two-long-one-short"])
+def test_pieces_scanned_from_their_carries_make_the_whole_scan(u, cuts, inclusive):
+    from u32_prefix_scan_gb300.shard import KernelSteps
+
+    whole = inputs.splitmix_u32(63, 0, sum(cuts))
+    steps = KernelSteps()
+    bounds = np.cumsum([0] + cuts)
+    pieces = [dev32(whole[bounds[r]:bounds[r + 1]]) for r in range(len(cuts))]
+    row = torch.cat([steps.reduce(p) for p in pieces])  # the all-gather, emulated
+    grand = steps.scan_row(row)
+    for r, p in enumerate(pieces):
+        steps.scan_from(p, row[r:r + 1], inclusive)
+    u.check()
+    want, want_total = (oracle.scan_inclusive if inclusive else oracle.scan_exclusive)(whole)
+    got = np.concatenate([host_u32(p) for p in pieces])
+    assert np.array_equal(got, want)
+    assert int(host_u32(grand)[0]) == want_total
+
+
+def test_sharded_scan_on_a_one_rank_nccl_group(u):
+    import torch.distributed as dist
+
+    from u32_prefix_scan_gb300 import shard
+
+    if dist.is_initialized():
+        pytest.skip("a process group already exists")
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", rank=0, world_size=1)
+    try:
+        a = inputs.splitmix_u32(64, 0, (1 << 22) + 77)
+        d = dev32(a)
+        total = shard.sharded_scan(d)
+        u.check()
+        want, want_total = oracle.scan_exclusive(a)
+        assert np.array_equal(host_u32(d), want) and int(host_u32(total)[0]) == want_total
+    finally:
+        dist.destroy_process_group()

@@ -1,0 +1,95 @@
+"""The sharded scan's composition on two gloo ranks (CPU, no GPU).
+
+u32_prefix_scan_gb300.shard.sharded_scan splits one array's scan across
+ranks: each rank folds its shard, the shard sums are all-gathered, their
+exclusive scan gives each rank its carry-in, and each rank scans its shard
+from it ("scan.bend source", section Driver, one level up). Here the three
+local steps are taken by the CPU oracle (fold = the oracle scan's total; a
+scan from a carry-in = the oracle scan of the shard plus the carry) and the
+exchange is a real gloo all-gather between two processes; the shards put
+back together must equal the oracle's scan of the whole array, bit for bit.
+"""
+
+import json
+import os
+import socket
+
+import numpy as np
+import pytest
+
+import oracle
+from u32_prefix_scan_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+
+
+def free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _u32(t):
+    return t.numpy().view(np.uint32)
+
+
+class OracleSteps:
+    """The composition's local steps, computed by the CPU oracle."""
+
+    def reduce(self, shard):
+        return torch.from_numpy(np.array([oracle.scan_exclusive(_u32(shard))[1]], np.uint32).view(np.int32))
+
+    def scan_row(self, row):
+        out, total = oracle.scan_exclusive(_u32(row))
+        row.copy_(torch.from_numpy(out.view(np.int32)))
+        return torch.from_numpy(np.array([total], np.uint32).view(np.int32))
+
+    def scan_from(self, shard, carry, inclusive):
+        out, total = (oracle.scan_inclusive if inclusive else oracle.scan_exclusive)(_u32(shard))
+        c = _u32(carry)[0]
+        shard.copy_(torch.from_numpy((out + c).astype(np.uint32).view(np.int32)))  # wraps mod 2^32
+        return torch.from_numpy(np.array([total + c], np.uint64).astype(np.uint32).view(np.int32))
+
+
+CASES = {
+    "uneven": (100003, [40000, 60003]),
+    "empty_first": (5000, [0, 5000]),
+    "empty_last": (70001, [70001, 0]),
+    "tiny": (3, [1, 2]),
+}
+
+
+def _rank_main(rank, world, port, out_dir, case, inclusive):
+    import torch.distributed as dist
+
+    from u32_prefix_scan_gb300 import shard as sh
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        n, cuts = CASES[case]
+        whole = inputs.splitmix_u32(77, 0, n)
+        lo = sum(cuts[:rank])
+        piece = torch.from_numpy(whole[lo:lo + cuts[rank]].view(np.int32).copy())
+        total = sh.sharded_scan(piece, inclusive=inclusive, steps=OracleSteps())
+        np.save(os.path.join(out_dir, f"rank{rank}.npy"), _u32(piece))
+        with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as fh:
+            json.dump({"total": int(_u32(total)[0])}, fh)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("inclusive", [False, True], ids=["exclusive", "inclusive"])
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_two_gloo_ranks_compose_the_whole_scan(tmp_path, case, inclusive):
+    import torch.multiprocessing as mp
+
+    world = 2
+    mp.spawn(_rank_main, args=(world, free_port(), str(tmp_path), case, inclusive), nprocs=world, join=True)
+    n, _ = CASES[case]
+    whole = inputs.splitmix_u32(77, 0, n)
+    want, want_total = (oracle.scan_inclusive if inclusive else oracle.scan_exclusive)(whole)
+    got = np.concatenate([np.load(tmp_path / f"rank{r}.npy") for r in range(world)])
+    assert np.array_equal(got, want)
+    for r in range(world):
+        assert json.loads((tmp_path / f"rank{r}.json").read_text())["total"] == want_total

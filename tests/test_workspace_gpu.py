@@ -121,3 +121,75 @@ def test_radix_leaves_nothing_that_passes_for_tile_words(u):
                 status = lib.u32scan_check(ws.ptr, torch.cuda.current_stream().cuda_stream)
             assert status == _native.OK, (n_r, which)
             assert ok, (n_r, which)
+
+
+# Header words (32-bit) of a workspace: tile counter, launch count (epoch),
+# status, detail, blocks finished.
+H_COUNTER, H_EPOCH, H_DONE = 0, 1, 4
+TAG_PERIOD = 1 << 29  # carry-word tags repeat every 2^29 launches
+
+
+def header(ws):
+    return ws.buf[:256].view(torch.int32).cpu().numpy().view(np.uint32)
+
+
+def set_epoch(ws, e):
+    ws.buf[4 * H_EPOCH: 4 * H_EPOCH + 4].copy_(
+        torch.tensor([e & 0xffffffff], dtype=torch.int64).to(torch.int32).view(torch.uint8))
+
+
+def run_exact(u, ws, which, n, seed):
+    """One call of `which` on ws, checked element by element against the oracle."""
+    from u32_prefix_scan_gb300 import _native
+
+    lib = _native.lib()
+    if which in ("scan", "segscan", "compact"):
+        return run_op(u, ws, which, n, seed)
+    if which == "segscan_nosums":
+        a, f = inputs.splitmix_u32(seed, 0, n), inputs.segment_heads_geometric(n, seed, log2_mean=6)
+        d = dev32(a)
+        nseg = u.segscan_inclusive_u32(d, dev32(f), workspace=ws)
+        ok = (np.array_equal(host_u32(d), oracle.segscan_inclusive(a, f))
+              and int(nseg.item()) == oracle.segreduce(a, f)[1])
+    elif which == "values":
+        v, f = inputs.scan_values(n, seed), inputs.compact_flags(n, seed, 0.9)
+        out, count = u.compact_values_u32(dev32(v), dev32(f), workspace=ws)
+        want, used = oracle.compact_values(v, f, np.zeros(n, np.uint32))
+        ok = int(count.item()) == used and np.array_equal(host_u32(out)[:used], want[:used])
+    else:  # scan64
+        a = inputs.scan_values_u64(n, seed)
+        d = torch.from_numpy(a.view(np.int64).copy()).cuda()
+        total = u.scan_u64_op(d, "add", False, workspace=ws)
+        want, want_total = oracle.scan_op_u64(a, "add", False)
+        ok = np.array_equal(d.cpu().numpy().view(np.uint64), want) and \
+            int(total.cpu().numpy().view(np.uint64)[0]) == want_total
+    return ok, lib.u32scan_check(ws.ptr, torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.parametrize("which,big", [("scan", (1 << 22) + 77), ("scan", 300001), ("segscan", (1 << 22) + 5),
+                                       ("segscan_nosums", (1 << 22) + 5), ("compact", (1 << 22) + 9),
+                                       ("values", (1 << 22) + 9), ("scan64", (1 << 21) + 3)])
+def test_tag_period_end_clears_old_carry_words(u, which, big):
+    """Carry-word tags repeat every 2^29 launches on a workspace. A long call
+    leaves tagged words far out; shorter calls then advance the launch count
+    (here: set directly in the header) without touching those words. The
+    launch that ends the tag period must zero them, or the next long call
+    whose tag matches the old one would add them in as published carries."""
+    from u32_prefix_scan_gb300 import _native
+
+    op = {"scan": 1, "segscan": 2, "segscan_nosums": 2, "compact": 3, "values": 3, "scan64": 6}[which]
+    ws = u.Workspace(_native.lib().u32scan_workspace_bytes(op, big), torch.device("cuda"))
+    set_epoch(ws, TAG_PERIOD - 2)
+    ok, status = run_exact(u, ws, which, big, 41)  # the long call: tag of launch 2^29 - 2
+    assert status == _native.OK and ok
+    h = header(ws)
+    assert h[H_EPOCH] == TAG_PERIOD - 1 and h[H_COUNTER] == 0 and h[H_DONE] == 0
+    ok, status = run_exact(u, ws, which, 1000, 42)  # launch 2^29 - 1 ends the period
+    assert status == _native.OK and ok
+    assert header(ws)[H_EPOCH] == TAG_PERIOD
+    set_epoch(ws, 2 * TAG_PERIOD - 2)  # the same tag as the long call's
+    ok, status = run_exact(u, ws, which, big, 43)
+    assert status == _native.OK
+    assert ok, "a carry word from the previous tag period was taken as published"
+    h = header(ws)
+    assert h[H_EPOCH] == 2 * TAG_PERIOD - 1 and h[H_COUNTER] == 0 and h[H_DONE] == 0

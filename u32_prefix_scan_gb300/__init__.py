@@ -10,6 +10,9 @@ _API = {
     "Workspace",
     "scan_exclusive_u32",
     "scan_inclusive_u32",
+    "scan_exclusive_u32_carry",
+    "scan_inclusive_u32_carry",
+    "reduce_u32_op",
     "scan_exclusive_u32_host",
     "scan_inclusive_u32_host",
     "scan_u32_op",

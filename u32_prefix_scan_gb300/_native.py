@@ -26,6 +26,7 @@ OP_RADIX = 4
 OP_RUNS = 5
 OP_SCAN64 = 6
 OP_SCAN_HOST = 7
+OP_REDUCE = 8
 
 _vp = ctypes.c_void_p
 _sz = ctypes.c_size_t
@@ -41,6 +42,9 @@ SIGNATURES = {
     "scan_exclusive_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
     "scan_inclusive_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
     "scan_exclusive_u32_noalloc": (_int, [_vp, _sz, _vp, _vp]),
+    "scan_exclusive_u32_carry": (_int, [_vp, _sz, _vp, _vp, _vp, _sz, _vp]),
+    "scan_inclusive_u32_carry": (_int, [_vp, _sz, _vp, _vp, _vp, _sz, _vp]),
+    "reduce_u32_op": (_int, [_int, _vp, _sz, _vp, _vp, _sz, _vp]),
     "scan_exclusive_u32_host": (_int, [_vp, _vp, _sz, _vp, _vp, _sz, _vp]),
     "scan_inclusive_u32_host": (_int, [_vp, _vp, _sz, _vp, _vp, _sz, _vp]),
     "scan_u32_op": (_int, [_int, _int, _vp, _sz, _vp, _vp, _sz, _vp]),
@@ -58,6 +62,9 @@ SIGNATURES = {
     "u32scan_test_scan_skip_publish": (_int, [_vp, _sz, _vp, _vp, _sz, ctypes.c_uint, ctypes.c_ulonglong, _vp]),
     "u32scan_test_segscan_skip_publish": (_int, [_vp, _vp, _sz, _vp, _sz, _vp, _vp, _sz, ctypes.c_uint,
                                                   ctypes.c_ulonglong, _vp]),
+    "u32scan_check_noalloc": (_int, [_vp]),
+    "u32scan_test_noalloc_skip_publish": (_int, [_vp, _sz, _vp, ctypes.c_uint, ctypes.c_ulonglong, _vp]),
+    "u32scan_test_noalloc_set_epoch": (_int, [ctypes.c_uint, _vp]),
 }
 
 _lib = None

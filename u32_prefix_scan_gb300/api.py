@@ -21,6 +21,9 @@ __all__ = [
     "Workspace",
     "scan_exclusive_u32",
     "scan_inclusive_u32",
+    "scan_exclusive_u32_carry",
+    "scan_inclusive_u32_carry",
+    "reduce_u32_op",
     "scan_exclusive_u32_host",
     "scan_inclusive_u32_host",
     "scan_u32_op",
@@ -127,6 +130,53 @@ def scan_inclusive_u32(data: torch.Tensor, total: torch.Tensor | None = None, *,
     """In place: data[j] <- data[0] + .. + data[j] (mod 2^32). Returns the
     one-element device tensor holding the wrapped total."""
     return _scan("scan_inclusive_u32", data, total, stream, workspace)
+
+
+def _scan_carry(name: str, data: torch.Tensor, carry_in, total, stream, workspace) -> torch.Tensor:
+    _require_cuda(data, "data")
+    if carry_in is not None:
+        _require_cuda(carry_in, "carry_in")
+        if carry_in.numel() < 1:
+            raise ValueError("carry_in must hold at least one element")
+    total = _scalar_out(total, data, data.dtype)
+    n = data.numel()
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_SCAN, n, data.device, sh, workspace)
+    fn = getattr(_native.lib(), name)
+    _native.check(fn(data.data_ptr(), n, carry_in.data_ptr() if carry_in is not None else None, total.data_ptr(),
+                     ws.ptr, ws.nbytes, sh), name)
+    return total
+
+
+def scan_exclusive_u32_carry(data: torch.Tensor, carry_in: torch.Tensor | None, total: torch.Tensor | None = None,
+                             *, stream=None, workspace: Workspace | None = None) -> torch.Tensor:
+    """In place: data[j] <- carry_in + data[0] + .. + data[j-1] (mod 2^32),
+    carry_in a one-element device tensor (None: 0). Returns the one-element
+    device tensor holding carry_in + the wrapped sum of data."""
+    return _scan_carry("scan_exclusive_u32_carry", data, carry_in, total, stream, workspace)
+
+
+def scan_inclusive_u32_carry(data: torch.Tensor, carry_in: torch.Tensor | None, total: torch.Tensor | None = None,
+                             *, stream=None, workspace: Workspace | None = None) -> torch.Tensor:
+    """In place: data[j] <- carry_in + data[0] + .. + data[j] (mod 2^32).
+    Returns carry_in + the wrapped sum of data (one-element device tensor)."""
+    return _scan_carry("scan_inclusive_u32_carry", data, carry_in, total, stream, workspace)
+
+
+def reduce_u32_op(data: torch.Tensor, op: str = "add", total: torch.Tensor | None = None, *, stream=None,
+                  workspace: Workspace | None = None) -> torch.Tensor:
+    """The fold of data under op in {add, mul, and, or, xor, min, max} (u32;
+    add and mul wrap), read once. Returns a one-element device tensor."""
+    if op not in _native.SCAN_OPS:
+        raise ValueError(f"op must be one of {sorted(_native.SCAN_OPS)}")
+    _require_cuda(data, "data")
+    total = _scalar_out(total, data, data.dtype)
+    n = data.numel()
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_REDUCE, n, data.device, sh, workspace)
+    _native.check(_native.lib().reduce_u32_op(_native.SCAN_OPS[op], data.data_ptr(), n, total.data_ptr(), ws.ptr,
+                                              ws.nbytes, sh), "reduce_u32_op")
+    return total
 
 
 def _require_pinned(t: torch.Tensor, name: str) -> None:

@@ -5,6 +5,27 @@
 
 #include "internal.cuh"
 
+namespace u32scan {
+
+// The largest span, from the workspace start, that any operation's tile
+// words can take: the largest workspace of the operations that keep nothing
+// but tile words there, over every n below 2^32 (a few MiB).
+size_t tile_word_reach() {
+    size_t reach = scan_workspace_bytes(0xffffffffull);
+    for (const size_t b : {segscan_workspace_bytes(0xffffffffull), compact_workspace_bytes(0xffffffffull),
+                           compact_values_workspace_bytes(0xffffffffull), scan64_workspace_bytes(0xffffffffull)})
+        reach = b > reach ? b : reach;
+    return reach;
+}
+
+unsigned long long tile_words_to_clear(size_t ws_bytes) {
+    const size_t reach = tile_word_reach();
+    const size_t end = ws_bytes < reach ? ws_bytes : reach;
+    return end > kHeaderBytes ? (end - kHeaderBytes) / 8 : 0ull;
+}
+
+}  // namespace u32scan
+
 using namespace u32scan;
 
 extern "C" size_t u32scan_workspace_bytes(int op, size_t n) {
@@ -25,6 +46,8 @@ extern "C" size_t u32scan_workspace_bytes(int op, size_t n) {
         return scan64_workspace_bytes(n);
     case U32SCAN_OP_SCAN_HOST:
         return scan_host_workspace_bytes(n);
+    case U32SCAN_OP_REDUCE:
+        return reduce_workspace_bytes();
     default:
         return 0;
     }

@@ -43,7 +43,8 @@ template <int THREADS, int V, int S>
 __global__ void __launch_bounds__(THREADS, 1)
 compact_persistent(const int32_t *__restrict__ flags, unsigned long long n, int32_t *offsets,
                    int32_t *__restrict__ indices, int32_t *count, WsHeader *hdr, unsigned long long *desc,
-                   unsigned int n_tiles, unsigned int head, int offsets_aligned, unsigned long long limit_ns) {
+                   unsigned int n_tiles, unsigned int head, int offsets_aligned, unsigned long long limit_ns,
+                   unsigned long long clear_words) {
     constexpr int WARPS = THREADS / 32;
     constexpr unsigned int CHUNK = 128 * V;
     constexpr unsigned int TILE = THREADS * V * 4;
@@ -262,6 +263,7 @@ compact_persistent(const int32_t *__restrict__ flags, unsigned long long n, int3
         for (int st = 0; st < S; ++st)
             (void)mbar_wait_bounded(smem_u32(&bar[st]), (latest_parity >> st) & 1u, limit_ns);
     }
+    finish_period(hdr, s_epoch, desc, clear_words);
 }
 
 constexpr int kCThreads = 512, kCV = U32SCAN_C_V, kCStages = U32SCAN_C_STAGES;
@@ -314,7 +316,7 @@ static int compact_launch(const int32_t *flags, unsigned long long n, int32_t *o
     WsHeader *hdr = static_cast<WsHeader *>(ws);
     unsigned long long *desc = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
     kern<<<grid, kCThreads, kCSmem, stream>>>(flags, n, offsets, indices, count, hdr, desc, n_tiles, head,
-                                             offsets_aligned, limit_ns);
+                                             offsets_aligned, limit_ns, tile_words_to_clear(ws_bytes));
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }
 

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 compact_values_persistent(const uint32_t *__restrict__ values, const int32_t *__restrict__ flags,
                           unsigned long long n, uint32_t *__restrict__ out, int32_t *count, WsHeader *hdr,
                           unsigned long long *desc, unsigned int n_tiles, unsigned int head, int flags_aligned,
-                          unsigned long long limit_ns) {
+                          unsigned long long limit_ns, unsigned long long clear_words) {
     constexpr int WARPS = THREADS / 32;
     constexpr unsigned int CHUNK = 128 * V;
     constexpr unsigned int TILE = THREADS * V * 4;
@@ -247,6 +247,7 @@ compact_values_persistent(const uint32_t *__restrict__ values, const int32_t *__
         for (int st = 0; st < S; ++st)
             (void)mbar_wait_bounded(smem_u32(&bar[st]), (latest_parity >> st) & 1u, limit_ns);
     }
+    finish_period(hdr, s_epoch, desc, clear_words);
 }
 
 // Launch shape, chosen by measurement on GB300 and overridable at build time
@@ -301,7 +302,7 @@ static int compact_values_launch(const uint32_t *values, const int32_t *flags, u
     WsHeader *hdr = static_cast<WsHeader *>(ws);
     unsigned long long *desc = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
     kern<<<grid, kVThreads, SMEM, stream>>>(values, flags, n, out, count, hdr, desc, n_tiles, head, flags_aligned,
-                                           limit_ns);
+                                           limit_ns, tile_words_to_clear(ws_bytes));
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }
 

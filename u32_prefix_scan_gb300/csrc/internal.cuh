@@ -24,10 +24,20 @@
 // radix sort, which also keeps histograms and its ping-pong buffers in the
 // workspace (stale small integers there could pass for tagged words), clears
 // its own tile words before its passes and, before it returns, the part of
-// the workspace any other operation's tile words can occupy. The block that
-// draws the last tile index resets the tile counter and advances the epoch
-// for the next launch; every other block has read the epoch before its own
-// draw, and the draw is an acq_rel RMW, so none can see the new epoch.
+// the workspace any other operation's tile words can occupy.
+//
+// Re-arming. Every block reads the epoch before its first draw; the block
+// that draws the launch's last index resets the tile counter and advances
+// the epoch for the next launch (every other block has read the epoch
+// before its own draw, and the draw is an acq_rel RMW, so none can see the
+// new epoch). A tag holds 29 bits of the epoch, so tags repeat every 2^29
+// launches. Every block knows from its epoch whether its launch is the last
+// of a tag period; in that launch alone the blocks count themselves out as
+// they finish (finish_period), and the last one out zeroes the tile words,
+// so no word from the period that ends can pass for a word of the next one.
+// Other launches pay nothing for this. (A launch whose blocks stop early on
+// a bulk-copy timeout may leave the tile counter unreset; the timeout is
+// reported, and the workspace must be zero-filled again before reuse.)
 #pragma once
 
 #include <cstdint>
@@ -42,7 +52,10 @@ struct WsHeader {
     unsigned int epoch;     // call generation
     unsigned int status;    // device-side error bits (kStatus*)
     unsigned int detail;    // first tile that timed out, + 1 (0 = none)
-    unsigned int pad[60];
+    unsigned int done;      // blocks of the running launch that have finished
+    unsigned int pad0[27];
+    unsigned long long seg_count;  // segmented scans: tiles counted and heads (byte 128, its own line)
+    unsigned int pad1[30];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -65,8 +78,11 @@ static inline int clear_tile_words(void *p, size_t bytes, cudaStream_t stream) {
     return cudaMemsetAsync(p, 0, bytes, stream) == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }
 
+// Launches per tag period: tag_of(e) == tag_of(e + kTagPeriod).
+constexpr unsigned int kTagPeriod = 1u << 29;
+
 __device__ __forceinline__ unsigned long long tag_of(unsigned int epoch) {
-    return (unsigned long long)((epoch & 0x1FFFFFFFu) + 1u) << 34;
+    return (unsigned long long)((epoch & (kTagPeriod - 1u)) + 1u) << 34;
 }
 
 __device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long *p) {
@@ -105,14 +121,36 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 // epoch of this call; the block drawing index n_tiles - 1 re-arms the header.
 __device__ __forceinline__ unsigned int draw_tile(WsHeader *hdr, unsigned int n_tiles,
                                                   unsigned int *epoch_out) {
-    unsigned int e = ld_relaxed_u32(&hdr->epoch);
-    unsigned int t = atom_add_acq_rel(&hdr->counter, 1u);
+    const unsigned int e = ld_relaxed_u32(&hdr->epoch);
+    const unsigned int t = atom_add_acq_rel(&hdr->counter, 1u);
     if (t == n_tiles - 1u) {
         st_relaxed_u32(&hdr->counter, 0u);
         st_relaxed_u32(&hdr->epoch, e + 1u);
     }
     *epoch_out = e;
     return t;
+}
+
+// The end of a tag period (all threads of every block call it, once, after
+// the block's last access to the workspace; a no-op unless this launch,
+// epoch `epoch`, is the period's last). Then each block counts itself out,
+// and the last one out zeroes the first `clear_words` tile words (`words`:
+// the tile words after the header), which must cover every tile word a
+// later launch on this workspace can read.
+__device__ __forceinline__ void finish_period(WsHeader *hdr, unsigned int epoch, unsigned long long *words,
+                                              unsigned long long clear_words) {
+    if (((epoch + 1u) & (kTagPeriod - 1u)) != 0u || clear_words == 0ull) return;  // the same in every block
+    __shared__ unsigned int s_last_out;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const bool last = atom_add_acq_rel(&hdr->done, 1u) == gridDim.x - 1u;
+        if (last) st_relaxed_u32(&hdr->done, 0u);
+        s_last_out = last ? 1u : 0u;
+    }
+    __syncthreads();
+    if (s_last_out)
+        for (unsigned long long i = threadIdx.x; i < clear_words; i += blockDim.x) words[i] = 0ull;
 }
 
 __device__ __forceinline__ void report_timeout(WsHeader *hdr, unsigned int tile) {
@@ -417,6 +455,12 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 // Wait until this thread's bulk stores have completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Tile words (8 bytes each, after the header) that the last launch of a tag
+// period zeroes in a workspace of ws_bytes: all of them, up to the largest
+// span any operation's tile words can take (defined in api.cu).
+unsigned long long tile_words_to_clear(size_t ws_bytes);
+size_t tile_word_reach();
+
 // Host-side workspace sizing of each operation (defined beside its kernels).
 size_t scan_workspace_bytes(unsigned long long n);
 size_t scan_workspace_bytes_upto(unsigned long long m);
@@ -426,6 +470,7 @@ size_t compact_workspace_bytes(unsigned long long n);
 size_t radix_workspace_bytes(unsigned long long n);
 size_t compact_values_workspace_bytes(unsigned long long n);
 size_t scan64_workspace_bytes(unsigned long long n);
+size_t reduce_workspace_bytes();
 
 // In-library launches of the add-scan: one chunk of a longer array after a
 // device carry-in (the host-buffer pipeline), and the inclusive scan with

@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS >= 512 ? 2 : 4))
 scan_u32_kernel(uint32_t *__restrict__ data, unsigned long long n, uint32_t *total, const uint32_t *carry_in,
                 WsHeader *hdr,
                 unsigned long long *desc, unsigned int n_tiles, unsigned int head, unsigned int skip_tile,
-                unsigned long long limit_ns) {
+                unsigned long long limit_ns, unsigned long long clear_words) {
     using M = Monoid<OP>;
     constexpr int WARPS = THREADS / 32;
     constexpr unsigned long long TILE = (unsigned long long)THREADS * V * 4;
@@ -179,6 +179,7 @@ scan_u32_kernel(uint32_t *__restrict__ data, unsigned long long n, uint32_t *tot
             }
         }
     }
+    finish_period(hdr, s_epoch, desc, clear_words);
 }
 
 // Persistent form for long arrays. Each block loops over tiles drawn from
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(THREADS, U32SCAN_P_MINB)
 scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t *total, const uint32_t *carry_in,
                     WsHeader *hdr,
                     unsigned long long *desc, unsigned int n_tiles, unsigned int head, unsigned int skip_tile,
-                    unsigned long long limit_ns) {
+                    unsigned long long limit_ns, unsigned long long clear_words) {
     using M = Monoid<OP>;
     constexpr int WARPS = THREADS / 32;
     constexpr unsigned int TILE = THREADS * V * 4;
@@ -411,6 +412,7 @@ scan_u32_persistent(uint32_t *__restrict__ data, unsigned long long n, uint32_t 
             (void)mbar_wait_bounded(smem_u32(&bar[st]), (latest_parity >> st) & 1u, limit_ns);
     }
     if (U32SCAN_P_BULKSTORE && threadIdx.x == 0) bulk_wait_all();
+    finish_period(hdr, s_epoch, desc, clear_words);
 }
 
 // Launch shapes, chosen by n: long arrays use the persistent kernel, short
@@ -496,16 +498,18 @@ static int scan_launch(uint32_t *data, unsigned long long n, uint32_t *total, vo
     const unsigned int n_tiles = (unsigned int)((n + head + sh.tile() - 1) / sh.tile());
     WsHeader *hdr = static_cast<WsHeader *>(ws);
     unsigned long long *desc = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
+    const unsigned long long clear_words = tile_words_to_clear(ws_bytes);
     if (sh.persistent) {
         int grid = 0;
         const int rc = persistent_grid<INCLUSIVE, OP>(&grid);
         if (rc != U32SCAN_OK) return rc;
         if ((unsigned int)grid > n_tiles) grid = (int)n_tiles;
         scan_u32_persistent<kPThreads, kPV, kPStages, kPLook, INCLUSIVE, OP><<<grid, kPThreads, kPSmem, stream>>>(
-            data, n, total, carry_in, hdr, desc, n_tiles, head, skip_tile, limit_ns);
+            data, n, total, carry_in, hdr, desc, n_tiles, head, skip_tile, limit_ns, clear_words);
     } else {
         scan_u32_kernel<256, 2, INCLUSIVE, OP><<<n_tiles, 256, 0, stream>>>(data, n, total, carry_in, hdr, desc,
-                                                                        n_tiles, head, skip_tile, limit_ns);
+                                                                        n_tiles, head, skip_tile, limit_ns,
+                                                                        clear_words);
     }
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }
@@ -548,6 +552,20 @@ extern "C" int scan_exclusive_u32(uint32_t *data, size_t n, uint32_t *total, voi
 extern "C" int scan_inclusive_u32(uint32_t *data, size_t n, uint32_t *total, void *ws, size_t ws_bytes,
                                   u32scan_stream_t stream) {
     return scan_launch<true>(data, n, total, ws, ws_bytes, (cudaStream_t)stream, 0xffffffffu, kDefaultLimitNs);
+}
+
+extern "C" int scan_exclusive_u32_carry(uint32_t *data, size_t n, const uint32_t *carry_in, uint32_t *total,
+                                        void *ws, size_t ws_bytes, u32scan_stream_t stream) {
+    if (n > 0 && total != nullptr && total == carry_in) return U32SCAN_EINVAL;
+    if (reinterpret_cast<uintptr_t>(carry_in) & 3) return U32SCAN_EINVAL;
+    return scan_chunk_launch(false, data, n, carry_in, total, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" int scan_inclusive_u32_carry(uint32_t *data, size_t n, const uint32_t *carry_in, uint32_t *total,
+                                        void *ws, size_t ws_bytes, u32scan_stream_t stream) {
+    if (n > 0 && total != nullptr && total == carry_in) return U32SCAN_EINVAL;
+    if (reinterpret_cast<uintptr_t>(carry_in) & 3) return U32SCAN_EINVAL;
+    return scan_chunk_launch(true, data, n, carry_in, total, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 extern "C" int scan_u32_op(int op, int inclusive, uint32_t *data, size_t n, uint32_t *total, void *ws,
@@ -620,6 +638,9 @@ static int static_scratch(void **out) {
     return U32SCAN_OK;
 }
 
+// Sets the array's epoch (test hook below): one thread, on the stream.
+__global__ void static_set_epoch_kernel(WsHeader *hdr, unsigned int epoch) { hdr->epoch = epoch; }
+
 }  // namespace u32scan
 
 extern "C" int scan_exclusive_u32_noalloc(uint32_t *data, size_t n, uint32_t *total, u32scan_stream_t stream) {
@@ -631,11 +652,41 @@ extern "C" int scan_exclusive_u32_noalloc(uint32_t *data, size_t n, uint32_t *to
     if (rc != U32SCAN_OK) return rc;
     if (scan_workspace_bytes(n) > kStaticScratchBytes) return U32SCAN_EINVAL;
     // The array keeps the previous call's contents. Carry words are tagged
-    // with a call counter, so stale ones are never taken for current ones;
-    // only the tile counter must read zero when a launch starts. Each launch
-    // leaves it at zero, and it is cleared here as well, in case an earlier
-    // launch on this array never completed.
-    if (cudaMemsetAsync(ws, 0, sizeof(unsigned int), (cudaStream_t)stream) != cudaSuccess) return U32SCAN_ECUDA;
+    // with a call counter, and the last block out of each launch resets the
+    // tile counter and advances that call counter (also after a launch that
+    // stopped early on a timeout), so nothing needs clearing between calls.
     return scan_launch<false>(data, n, total, ws, kStaticScratchBytes, (cudaStream_t)stream, 0xffffffffu,
                               kDefaultLimitNs);
+}
+
+extern "C" int u32scan_check_noalloc(u32scan_stream_t stream) {
+    void *ws = nullptr;
+    int rc = static_scratch(&ws);
+    if (rc != U32SCAN_OK) return rc;
+    rc = u32scan_check(ws, stream);
+    if (rc == U32SCAN_ETIMEOUT) {
+        // a launch that stopped early may have left the tile counter unreset:
+        // start the array afresh (every caller's next call finds it zeroed)
+        if (cudaMemsetAsync(ws, 0, kStaticScratchBytes, (cudaStream_t)stream) != cudaSuccess ||
+            cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess)
+            return U32SCAN_ECUDA;
+    }
+    return rc;
+}
+
+extern "C" int u32scan_test_noalloc_skip_publish(uint32_t *data, size_t n, uint32_t *total, unsigned int skip_tile,
+                                                 unsigned long long limit_ns, u32scan_stream_t stream) {
+    if (n > kStaticMaxN) return U32SCAN_EINVAL;
+    void *ws = nullptr;
+    const int rc = static_scratch(&ws);
+    if (rc != U32SCAN_OK) return rc;
+    return scan_launch<false>(data, n, total, ws, kStaticScratchBytes, (cudaStream_t)stream, skip_tile, limit_ns);
+}
+
+extern "C" int u32scan_test_noalloc_set_epoch(unsigned int epoch, u32scan_stream_t stream) {
+    void *ws = nullptr;
+    const int rc = static_scratch(&ws);
+    if (rc != U32SCAN_OK) return rc;
+    static_set_epoch_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(static_cast<WsHeader *>(ws), epoch);
+    return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }

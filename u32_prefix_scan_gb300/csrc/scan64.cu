@@ -132,7 +132,7 @@ template <int THREADS, int V, int MINB, bool INCLUSIVE, int OP>
 __global__ void __launch_bounds__(THREADS, MINB)
 scan_u64_kernel(unsigned long long *__restrict__ data, unsigned long long n, unsigned long long *total,
                 WsHeader *hdr, unsigned long long *desc2, unsigned int n_tiles, unsigned int head,
-                unsigned long long limit_ns) {
+                unsigned long long limit_ns, unsigned long long clear_words) {
     using M = Monoid64<OP>;
     constexpr int WARPS = THREADS / 32;
     constexpr unsigned long long TILE = (unsigned long long)THREADS * V * 2;
@@ -224,6 +224,7 @@ scan_u64_kernel(unsigned long long *__restrict__ data, unsigned long long n, uns
             if (a + 1 >= lo && a + 1 < hi) tbase[a + 1] = x[r].y;
         }
     }
+    finish_period(hdr, s_epoch, desc2, clear_words);
 }
 
 // Persistent form for long rows, the u64 counterpart of scan.cu's
@@ -238,7 +239,7 @@ template <int THREADS, int V, int S, bool INCLUSIVE, int OP>
 __global__ void __launch_bounds__(THREADS, 1)
 scan_u64_persistent(unsigned long long *__restrict__ data, unsigned long long n, unsigned long long *total,
                     WsHeader *hdr, unsigned long long *desc2, unsigned int n_tiles, unsigned int head,
-                    unsigned long long limit_ns) {
+                    unsigned long long limit_ns, unsigned long long clear_words) {
     using M = Monoid64<OP>;
     constexpr int WARPS = THREADS / 32;
     constexpr unsigned int TILE = THREADS * V * 2;
@@ -430,6 +431,7 @@ scan_u64_persistent(unsigned long long *__restrict__ data, unsigned long long n,
             (void)mbar_wait_bounded(smem_u32(&bar[st]), (latest_parity >> st) & 1u, limit_ns);
     }
     if (threadIdx.x == 0) bulk_wait_all();
+    finish_period(hdr, s_epoch, desc2, clear_words);
 }
 
 // Shapes: short rows take one small tile per block (enough blocks to fill
@@ -505,16 +507,17 @@ static int scan64_launch(unsigned long long *data, unsigned long long n, unsigne
     const unsigned int n_tiles = (unsigned int)((n + head + sh.tile() - 1) / sh.tile());
     WsHeader *hdr = static_cast<WsHeader *>(ws);
     unsigned long long *desc2 = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
+    const unsigned long long clear_words = tile_words_to_clear(ws_bytes);
     if (n >= kScan64LargeMinN) {
         int grid = 0;
         const int rc = scan64_grid<INCLUSIVE, OP>(&grid);
         if (rc != U32SCAN_OK) return rc;
         if ((unsigned int)grid > n_tiles) grid = (int)n_tiles;
         scan_u64_persistent<kS64T, kS64V, kS64S, INCLUSIVE, OP><<<grid, kS64T, kS64Smem, stream>>>(
-            data, n, total, hdr, desc2, n_tiles, head, kDefaultLimitNs);
+            data, n, total, hdr, desc2, n_tiles, head, kDefaultLimitNs, clear_words);
     } else
         scan_u64_kernel<256, 2, 4, INCLUSIVE, OP><<<n_tiles, 256, 0, stream>>>(data, n, total, hdr, desc2, n_tiles,
-                                                                            head, kDefaultLimitNs);
+                                                                            head, kDefaultLimitNs, clear_words);
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }
 

@@ -72,10 +72,7 @@ namespace u32scan {
 // next call. The heads of a whole array number fewer than 2^32, so they
 // never carry into the tile count. (A compare-and-swap loop on a word in
 // the tile counter's line measured 13 times slower than the look-back.)
-__device__ __forceinline__ unsigned long long *seg_count_word(WsHeader *hdr) {
-    return reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(hdr) + 128);
-}
-static_assert(sizeof(WsHeader) >= 136, "the count word lies inside the header");
+__device__ __forceinline__ unsigned long long *seg_count_word(WsHeader *hdr) { return &hdr->seg_count; }
 
 __device__ __forceinline__ bool seg_count_add(WsHeader *hdr, unsigned int n_tiles, unsigned int heads,
                                               unsigned int &total) {
@@ -123,7 +120,7 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
 segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flags, unsigned long long n,
                          uint32_t *seg_sums, unsigned long long seg_cap, uint32_t *nseg, WsHeader *hdr,
                          unsigned long long *desc2, unsigned int n_tiles, unsigned int head, int streams_aligned,
-                         unsigned int skip_tile, unsigned long long limit_ns) {
+                         unsigned int skip_tile, unsigned long long limit_ns, unsigned long long clear_words) {
     constexpr int WARPS = THREADS / 32;
     constexpr bool ATOM_COUNT = !WANT_SUMS && U32SCAN_S_ATOMCOUNT;  // the count serves no segment index
     constexpr int E = 4 * R;                    // elements a lane
@@ -538,6 +535,7 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
             (void)mbar_wait_bounded(smem_u32(&bar[st]), (latest_parity >> st) & 1u, limit_ns);
     }
     if (WRITE_SCAN && BUF && threadIdx.x == 0) bulk_wait_all();
+    finish_period(hdr, s_epoch, desc2, clear_words);
 }
 
 // Launch shapes, chosen by measurement on GB300 (n = 2^26) and overridable
@@ -674,7 +672,7 @@ static int segscan_launch(uint32_t *data, const F *flags, unsigned long long n, 
     WsHeader *hdr = static_cast<WsHeader *>(ws);
     unsigned long long *desc2 = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
     kern<<<grid, THREADS, smem, stream>>>(data, flags, n, seg_sums, seg_cap, nseg, hdr, desc2, n_tiles, head,
-                                             aligned, skip_tile, limit_ns);
+                                             aligned, skip_tile, limit_ns, tile_words_to_clear(ws_bytes));
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }
 

@@ -1,0 +1,87 @@
+"""Scans of one U32 array split across ranks, one contiguous shard a rank.
+
+Source: "scan.bend source", header comment (pass 2 scans the block sums) and
+section Driver: the blocks are summed, the block sums are scanned, and each
+block is rescanned from its base. Here the blocks are the ranks' shards, in
+rank order (rank r holds the r-th piece of the array; pieces may differ in
+length, and may be empty):
+
+  1. every rank folds its shard to its wrapped sum (reduce_u32_op: 4 bytes
+     read an element);
+  2. one all-gather of the G shard sums (G words: all that crosses between
+     GPUs);
+  3. the exclusive scan of the gathered row (scan_exclusive_u32, on the
+     device) gives rank r its carry-in, the wrapped sum of every element on
+     the ranks before it, and the row's total is the whole array's;
+  4. every rank scans its shard from its carry-in (scan_*_u32_carry: 8 bytes
+     an element).
+
+So a sharded scan moves 12 bytes an element against 8 on one GPU, with one
+collective of G words and no host round trip. Sums wrap at 2^32 and are
+associative, so the result has the bits of a one-GPU scan of the whole
+array.
+
+The composition takes its three local steps from a `steps` object (fold a
+shard, scan the gathered row in place, scan a shard from a carry-in): by
+default this library's kernels on CUDA tensors; the CPU tests pass other
+implementations of the same steps and run the composition on gloo ranks.
+This module only sequences the steps and the collective; it does no
+arithmetic on the data itself.
+"""
+
+from __future__ import annotations
+
+import torch
+import torch.distributed as dist
+
+from . import api
+
+
+class KernelSteps:
+    """The three local steps as this library's kernels (CUDA tensors)."""
+
+    def __init__(self, workspace: api.Workspace | None = None):
+        self.workspace = workspace
+
+    def reduce(self, shard: torch.Tensor) -> torch.Tensor:
+        return api.reduce_u32_op(shard, "add", workspace=self.workspace)
+
+    def scan_row(self, row: torch.Tensor) -> torch.Tensor:
+        return api.scan_exclusive_u32(row, workspace=self.workspace)
+
+    def scan_from(self, shard: torch.Tensor, carry: torch.Tensor, inclusive: bool) -> torch.Tensor:
+        fn = api.scan_inclusive_u32_carry if inclusive else api.scan_exclusive_u32_carry
+        return fn(shard, carry, workspace=self.workspace)
+
+
+def _all_gather(x: torch.Tensor, group) -> torch.Tensor:
+    """The G one-word tensors of the group's ranks, as one row in rank order."""
+    world = dist.get_world_size(group)
+    if dist.get_backend(group) == "nccl":
+        row = torch.empty(world, dtype=x.dtype, device=x.device)
+        dist.all_gather_into_tensor(row, x, group=group)
+        return row
+    parts = [torch.empty_like(x) for _ in range(world)]
+    dist.all_gather(parts, x, group=group)
+    return torch.cat(parts)
+
+
+def sharded_scan(shard: torch.Tensor, inclusive: bool = False, group=None, steps=None, marks=None) -> torch.Tensor:
+    """Scan this rank's shard in place as its piece of the whole array's
+    exclusive (or inclusive) scan. Every rank of `group` calls it, in the
+    same order as its other collectives. Returns the whole array's wrapped
+    total (one-element tensor, on the shard's device), the same on every rank.
+    `marks`: an optional pair of CUDA events recorded on the current stream
+    just before and after the scan from the carry-in (for timing it).
+    """
+    steps = KernelSteps() if steps is None else steps
+    rank = dist.get_rank(group)
+    own = steps.reduce(shard)
+    row = _all_gather(own.reshape(1), group)
+    whole = steps.scan_row(row)  # row now holds each rank's carry-in
+    if marks is not None:
+        marks[0].record()
+    steps.scan_from(shard, row[rank:rank + 1], inclusive)
+    if marks is not None:
+        marks[1].record()
+    return whole

@@ -16,19 +16,29 @@
 // value come first) and finds digits that are equal for every key, whose
 // passes are skipped (exact: such a pass moves nothing). Each digit pass is
 // then one kernel over tiles of 8192 keys drawn in order: a tile ranks its
-// keys stably within itself (for each 32 keys of a warp, a per-warp
-// shared-memory mask per digit value collects the lanes holding that value,
-// which gives each key its rank among the warp's keys of its value),
-// publishes its 256 digit counts, and finds for every digit value the count
-// of that value in all earlier tiles by a decoupled look-back (thread v
-// walks back over the earlier tiles' words for value v, several a round
-// trip, until one holds an inclusive count), so each key's slot is
-// base + earlier count + rank; the tile is ordered by
+// keys stably within itself, publishes its 256 digit counts, and finds for
+// every digit value the count of that value in all earlier tiles by a
+// decoupled look-back (thread v walks back over the earlier tiles' words
+// for value v, several a round trip, until one holds an inclusive count), so
+// each key's slot is base + earlier count + rank; the tile is ordered by
 // digit value in shared memory and written out run by run. Which passes run,
 // and which buffers they read and write, is decided on the device, so the
 // call stays asynchronous. The last pass writes the indices into `perm` and,
 // for radix_sort_u32, the sorted keys into `keys_out`; a keys-only sort moves
 // no indices at all.
+//
+// Ranking. For the 32 keys of one warp round (one per lane), eight ballots,
+// one per digit bit, give each lane the mask of lanes holding its digit
+// value; the lowest lane of each value adds the value's count to the warp's
+// running counter for it (one shared atomic add, whose old value is
+// broadcast to the value's lanes), and a lane's rank is that old value plus
+// the lanes below it in the mask. So a round costs one shared-memory access
+// per distinct digit value; the shared tables a round reads and writes at
+// random digit values (and their bank conflicts) are what bound a pass
+// otherwise. A tile's input indices come into shared memory by one bulk copy
+// issued when the tile is drawn, so their latency hides behind the ranking,
+// and each block asks L2 for the keys and indices of the tile drawn one
+// resident grid later.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -53,18 +63,25 @@ constexpr int kRThreads = U32SCAN_R_THREADS;
 constexpr int kRKeys = U32SCAN_R_KEYS;  // keys per thread per tile
 constexpr unsigned int kRTile = kRThreads * kRKeys;
 constexpr int kRWarps = kRThreads / 32;
+constexpr unsigned int kRWarpKeys = 32 * kRKeys;  // a warp's run of the tile
 static_assert(kRThreads >= 256 && kRThreads % 32 == 0 && kRKeys <= 32, "a thread per digit value; key bits fit a word");
 // How a warp finds the lanes whose key has the same digit value:
-// 0: eight ballots, one per digit bit; 1: the match-any instruction;
-// 2: every lane sets its bit in a per-warp shared-memory mask word of its
-//    digit value (one shared atomic OR), and reads the word back.
+// 0: eight ballots, one per digit bit; 1: the match-any instruction.
 #ifndef U32SCAN_R_MATCH
-#define U32SCAN_R_MATCH 2
+#define U32SCAN_R_MATCH 0
 #endif
 #ifndef U32SCAN_R_LOOK
 #define U32SCAN_R_LOOK 8
 #endif
 constexpr int kRLook = U32SCAN_R_LOOK;  // earlier tiles read per look-back round trip
+// 1: each block asks L2 for the tile one resident grid ahead.
+#ifndef U32SCAN_R_PREFETCH
+#define U32SCAN_R_PREFETCH 1
+#endif
+// 1: a full tile's input indices arrive by one bulk copy into shared memory.
+#ifndef U32SCAN_R_STAGE
+#define U32SCAN_R_STAGE 0
+#endif
 
 // One pass's role, decided on the device from the histograms.
 struct RadixPlan {
@@ -102,20 +119,35 @@ struct RadixLayout {
     }
 };
 
-// Counts of all four digits over all keys (one read), for the plan.
-__global__ void radix_histogram_kernel(const uint32_t *__restrict__ keys, unsigned long long n,
-                                       unsigned int *__restrict__ hist) {
-    __shared__ unsigned int s_h[4][256];
-    for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) (&s_h[0][0])[i] = 0;
+// Counts of all four digits over all keys (one read), for the plan. One
+// block of 1024 threads per SM. The counters are lane columns: row
+// (digit, value) holds 32 words, one per lane, so the 32 atomic adds of a
+// warp instruction always fall in 32 different banks whatever the keys.
+constexpr int kHThreads = 1024;
+constexpr size_t kHSmem = (size_t)4 * 256 * 32 * 4;  // 128 KiB
+
+__global__ void __launch_bounds__(kHThreads, 1)
+radix_histogram_kernel(const uint32_t *__restrict__ keys, unsigned long long n, unsigned int *__restrict__ hist) {
+    extern __shared__ __align__(16) unsigned int h_cols[];  // [4 * 256][32]
+    for (int i = threadIdx.x; i < 4 * 256 * 32; i += kHThreads) h_cols[i] = 0;
     __syncthreads();
+    const unsigned int lane = threadIdx.x & 31;
+    unsigned int *col = h_cols + lane;
     auto add = [&](uint32_t k) {
-        atomicAdd(&s_h[0][k & 255u], 1u);
-        atomicAdd(&s_h[1][(k >> 8) & 255u], 1u);
-        atomicAdd(&s_h[2][(k >> 16) & 255u], 1u);
-        atomicAdd(&s_h[3][k >> 24], 1u);
+        atomicAdd(col + 32 * (k & 255u), 1u);
+        atomicAdd(col + 32 * (256 + ((k >> 8) & 255u)), 1u);
+        atomicAdd(col + 32 * (512 + ((k >> 16) & 255u)), 1u);
+        atomicAdd(col + 32 * (768 + (k >> 24)), 1u);
     };
-    // scalar head up to 16-byte alignment, 16-byte body, scalar tail; n < 2^31
-    // for a radix sort, so 32-bit indices suffice
+    auto add4 = [&](const uint4 &q) {
+        add(q.x);
+        add(q.y);
+        add(q.z);
+        add(q.w);
+    };
+    // scalar head up to 16-byte alignment, 16-byte body (four loads in
+    // flight a thread), scalar tail; n < 2^31 for a radix sort, so 32-bit
+    // indices suffice
     const unsigned int n32 = (unsigned int)n;
     const unsigned int head = (unsigned int)((16 - (reinterpret_cast<uintptr_t>(keys) & 15)) & 15) / 4;
     const unsigned int h = head < n32 ? head : n32;
@@ -124,30 +156,25 @@ __global__ void radix_histogram_kernel(const uint32_t *__restrict__ keys, unsign
     const unsigned int gstride = gridDim.x * blockDim.x;
     if (gtid < h) add(keys[gtid]);
     const uint4 *kv = reinterpret_cast<const uint4 *>(keys + h);
-    for (unsigned int i = gtid; i < nv; i += gstride) {
-        const uint4 q = kv[i];
-        // a quad whose four keys agree on a digit (common when the digit is
-        // constant over the keys) takes one atomic for it instead of four
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const unsigned int s = 8 * p;
-            const unsigned int a = (q.x >> s) & 255u, b = (q.y >> s) & 255u, c = (q.z >> s) & 255u,
-                               d = (q.w >> s) & 255u;
-            if (a == b && b == c && c == d) {
-                atomicAdd(&s_h[p][a], 4u);
-            } else {
-                atomicAdd(&s_h[p][a], 1u);
-                atomicAdd(&s_h[p][b], 1u);
-                atomicAdd(&s_h[p][c], 1u);
-                atomicAdd(&s_h[p][d], 1u);
-            }
-        }
+    unsigned int i = gtid;
+    for (; i + 3 * gstride < nv; i += 4 * gstride) {
+        const uint4 q0 = __ldcs(kv + i), q1 = __ldcs(kv + i + gstride), q2 = __ldcs(kv + i + 2 * gstride),
+                    q3 = __ldcs(kv + i + 3 * gstride);
+        add4(q0);
+        add4(q1);
+        add4(q2);
+        add4(q3);
     }
-    for (unsigned int i = h + 4 * nv + gtid; i < n32; i += gstride) add(keys[i]);
+    for (; i < nv; i += gstride) add4(__ldcs(kv + i));
+    for (unsigned int j = h + 4 * nv + gtid; j < n32; j += gstride) add(keys[j]);
     __syncthreads();
-    for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) {
-        const unsigned int c = (&s_h[0][0])[i];
-        if (c) atomicAdd(hist + i, c);
+    // thread r sums row r over the lanes, starting at its own lane's column
+    // so that the 32 reads of a warp instruction fall in different banks
+    for (int r = threadIdx.x; r < 4 * 256; r += kHThreads) {
+        unsigned int sum = 0;
+#pragma unroll 8
+        for (int c = 0; c < 32; ++c) sum += h_cols[32 * r + ((c + (int)lane) & 31)];
+        if (sum) atomicAdd(hist + r, sum);
     }
 }
 
@@ -224,79 +251,68 @@ __device__ __forceinline__ PassBuffers pass_buffers(const RadixPlan &pl, const u
     return b;
 }
 
-// Rank a warp's keys (held as in radix_rank_tile, bit r of valid_bits set
-// for the keys inside the array) stably within the warp.
-__device__ __forceinline__ void radix_rank_keys(const uint32_t (&k)[kRKeys], unsigned int valid_bits, int shift,
-                                                unsigned int (&wrank)[kRKeys], unsigned int (*s_cnt)[256],
-                                                unsigned int (*s_match)[256], int lane, int warp) {
-    for (int i = lane; i < 256; i += 32) {
-        s_cnt[warp][i] = 0;
-        if (U32SCAN_R_MATCH == 2) s_match[warp][i] = 0;
-    }
-    __syncwarp();
-#pragma unroll
-    for (int r = 0; r < kRKeys; ++r) {
-        const bool valid = (valid_bits >> r) & 1u;
-        const unsigned int dr = (k[r] >> shift) & 255u;
-#if U32SCAN_R_MATCH == 2
-        // Each valid lane sets its bit in its digit value's mask word and
-        // reads the word back: the lanes holding the same digit value. After
-        // the read-back the lowest such lane (below == 0) clears the word and
-        // advances the value's count, so every word is zero again when the
-        // next round starts.
-        if (valid) atomicOr(&s_match[warp][dr], 1u << lane);
-        __syncwarp();
-        const unsigned int same = valid ? s_match[warp][dr] : 0u;
-#elif U32SCAN_R_MATCH == 1
-        // invalid lanes get a label no valid digit has
-        const unsigned int same = __match_any_sync(0xffffffffu, valid ? dr : 256u);
+// The lanes of this warp round whose key has digit value d (all lanes call
+// it; an invalid lane takes part in no mask and gets 0).
+template <bool FULL>
+__device__ __forceinline__ unsigned int radix_same_digit(unsigned int d, bool valid) {
+#if U32SCAN_R_MATCH == 1
+    const unsigned int m = __match_any_sync(0xffffffffu, (FULL || valid) ? d : 256u);
+    return (FULL || valid) ? m : 0u;
 #else
-        // the AND over the digit's eight bits of the ballot (bit set) or its
-        // complement (bit clear), and the same for validity
-        const unsigned int vb = __ballot_sync(0xffffffffu, valid);
-        unsigned int same = valid ? vb : ~vb;
+    unsigned int same = FULL ? 0xffffffffu : __ballot_sync(0xffffffffu, valid);
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const bool bit = (dr >> b) & 1u;
-            const unsigned int bb = __ballot_sync(0xffffffffu, bit);
-            same &= bit ? bb : ~bb;
-        }
-#endif
-        const unsigned int below = (unsigned int)__popc(same & lanemask_lt(lane));
-        const unsigned int old = valid ? s_cnt[warp][dr] : 0u;
-        wrank[r] = old + below;
-        __syncwarp();
-        if (valid && below == 0) {
-#if U32SCAN_R_MATCH == 2
-            s_match[warp][dr] = 0u;
-#endif
-            s_cnt[warp][dr] = old + (unsigned int)__popc(same);
-        }
-        __syncwarp();
+    for (int b = 0; b < 8; ++b) {
+        const unsigned int bit = (d >> b) & 1u;
+        const unsigned int bb = __ballot_sync(0xffffffffu, bit != 0u);
+        same &= bb ^ (bit - 1u);  // the ballot where the bit is set, its complement where clear
     }
+    return (FULL || valid) ? same : 0u;
+#endif
 }
 
 // Load this thread's keys of tile t (warp-striped: round r of warp w covers
-// 32 consecutive keys) and rank them stably within the tile: after the call
-// wrank[r] is the key's rank among the keys of its digit value in this warp
-// (in tile order) and s_cnt[w][v] the warp's count of digit value v. Bit r
-// of the returned mask says whether key r lies inside the array.
-__device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restrict__ in_keys, unsigned long long n,
-                                                        unsigned int t, int shift, uint32_t (&k)[kRKeys],
-                                                        unsigned int (&wrank)[kRKeys], unsigned int (*s_cnt)[256],
-                                                        unsigned int (*s_match)[256], int lane, int warp) {
-    // n < 2^31 for a radix sort, so key indices fit in 32 bits
-    const unsigned int n32 = (unsigned int)n;
-    const unsigned int base = t * kRTile + (unsigned int)warp * (32 * kRKeys);
-    unsigned int valid_bits = 0;
+// the 32 consecutive keys at t * kRTile + w * kRWarpKeys + 32 r) and rank
+// them stably within the warp: afterwards wrank[r] is the key's rank among
+// the warp's keys of its digit value (in tile order) and s_wcnt[v] the
+// warp's count of value v. FULL: every key of the tile lies in the array.
+template <bool FULL>
+__device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restrict__ in_keys, unsigned int n32,
+                                                        unsigned int wbase, int shift, uint32_t (&k)[kRKeys],
+                                                        unsigned int (&wrank)[kRKeys], unsigned int *s_wcnt,
+                                                        int lane) {
+    unsigned int valid_bits = FULL ? 0xffffffffu : 0u;
 #pragma unroll
     for (int r = 0; r < kRKeys; ++r) {
-        const unsigned int e = base + 32u * r + (unsigned int)lane;
-        k[r] = e < n32 ? in_keys[e] : 0u;
-        valid_bits |= (e < n32 ? 1u : 0u) << r;
+        const unsigned int e = wbase + 32u * r + (unsigned int)lane;
+        if (FULL) {
+            k[r] = __ldcs(in_keys + e);
+        } else {
+            k[r] = e < n32 ? __ldcs(in_keys + e) : 0u;
+            valid_bits |= (e < n32 ? 1u : 0u) << r;
+        }
     }
-    radix_rank_keys(k, valid_bits, shift, wrank, s_cnt, s_match, lane, warp);
+    for (int i = lane; i < 256; i += 32) s_wcnt[i] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < kRKeys; ++r) {
+        const bool valid = FULL || ((valid_bits >> r) & 1u);
+        const unsigned int d = (k[r] >> shift) & 255u;
+        const unsigned int same = radix_same_digit<FULL>(d, valid);
+        const unsigned int below = (unsigned int)__popc(same & lanemask_lt(lane));
+        unsigned int old = 0;
+        if (valid && below == 0) old = atomicAdd(s_wcnt + d, (unsigned int)__popc(same));
+        const int leader = same ? __ffs(same) - 1 : 0;
+        wrank[r] = __shfl_sync(0xffffffffu, old, leader) + below;
+        __syncwarp();  // orders this round's counter updates before the next round's
+    }
     return valid_bits;
+}
+
+// The 16-byte-aligned interior of [p, p + bytes), requested into L2.
+__device__ __forceinline__ void prefetch_l2_interior(const void *p, unsigned long long bytes) {
+    const uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15);
+    const uintptr_t e = (reinterpret_cast<uintptr_t>(p) + bytes) & ~uintptr_t(15);
+    if (e > a) bulk_prefetch_l2(reinterpret_cast<const void *>(a), (unsigned int)(e - a));
 }
 
 // One digit pass over tile t (drawn in order): rank, carry each digit
@@ -306,40 +322,70 @@ __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restri
 // desc[256 t + v] (tile-major: the 32 values of a warp read 32 consecutive
 // words for each earlier tile): the library's tagged format, value = the
 // tile's count of v (aggregate) or the count of v in tiles 0..t (inclusive,
-// P bit).
+// P bit). `ahead`: tiles between a block's tile and the one it prefetches.
 __global__ void __launch_bounds__(kRThreads, U32SCAN_R_MINB)
 radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
                       int32_t *i1, int32_t *perm, uint32_t *keys_out, unsigned long long n, unsigned int n_tiles,
                       const unsigned int *__restrict__ bases, WsHeader *hdr, unsigned long long *desc,
-                      unsigned long long limit_ns) {
+                      unsigned long long limit_ns, unsigned int ahead) {
     const RadixPlan pl = plan[p];
     if (!pl.active) return;
-    extern __shared__ __align__(16) unsigned int r_smem[];
-    unsigned int(*s_cnt)[256] = reinterpret_cast<unsigned int(*)[256]>(r_smem);  // [kRWarps][256]
-    unsigned int(*s_match)[256] =
-        reinterpret_cast<unsigned int(*)[256]>(r_smem + kRWarps * 256 + 512 + 2 * kRTile);  // [kRWarps][256]
-    unsigned int *s_tileoff = r_smem + kRWarps * 256;                           // [256] value's start in tile
-    unsigned int *s_delta = s_tileoff + 256;                                    // [256] first slot - start
-    unsigned int *s_keys = s_delta + 256;                                       // [kRTile]
-    int32_t *s_idx = reinterpret_cast<int32_t *>(s_keys + kRTile);              // [kRTile]
-    __shared__ unsigned int s_part[kRThreads / 32];
-    __shared__ unsigned int s_t, s_epoch;
+    // Shared memory (32-bit words): per-warp digit counters, later the warp
+    // offsets in the tile-ordered buffer [kRWarps][256]; each value's run
+    // start in the tile [256]; its first output slot minus that start [256];
+    // the tile's keys in digit order [kRTile]; its input indices, first in
+    // tile order (bulk copy), then in digit order [kRTile].
+    extern __shared__ __align__(128) unsigned int r_smem[];
+    unsigned int(*s_cnt)[256] = reinterpret_cast<unsigned int(*)[256]>(r_smem);
+    unsigned int *s_tileoff = r_smem + kRWarps * 256;
+    unsigned int *s_delta = s_tileoff + 256;
+    unsigned int *s_keys = s_delta + 256;
+    int32_t *s_idx = reinterpret_cast<int32_t *>(s_keys + kRTile);
+    __shared__ unsigned int s_part[kRWarps];
+    __shared__ unsigned int s_t, s_epoch, s_staged;
+    __shared__ __align__(8) unsigned long long s_bar;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm, keys_out);
+    // n < 2^31 for a radix sort: 32-bit element indices
+    const unsigned int n32 = (unsigned int)n;
     if (threadIdx.x == 0) {
         unsigned int e;
-        s_t = draw_tile(hdr, n_tiles, &e);
+        const unsigned int t = draw_tile(hdr, n_tiles, &e);
+        s_t = t;
         s_epoch = e;
+        const unsigned int tile0 = t * kRTile;
+        const bool full = n32 - tile0 >= kRTile;
+        // input indices of a full tile by bulk copy, when they start on a
+        // 16-byte boundary (tile starts are 32 KiB apart)
+        const bool staged = U32SCAN_R_STAGE && b.out_idx != nullptr && b.in_idx != nullptr && full &&
+                            (reinterpret_cast<uintptr_t>(b.in_idx) & 15) == 0;
+        s_staged = staged ? 1u : 0u;
+        if (staged) {
+            const unsigned int bar = smem_u32(&s_bar);
+            mbar_init(bar, 1u);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(bar, kRTile * 4u);
+            bulk_load(smem_u32(s_idx), b.in_idx + tile0, kRTile * 4u, bar);
+        }
+        if (U32SCAN_R_PREFETCH && ahead != 0u && t + ahead < n_tiles) {
+            const unsigned int f0 = (t + ahead) * kRTile;
+            const unsigned int cnt = n32 - f0 < kRTile ? n32 - f0 : kRTile;
+            prefetch_l2_interior(b.in_keys + f0, 4ull * cnt);
+            if (b.in_idx != nullptr && b.out_idx != nullptr) prefetch_l2_interior(b.in_idx + f0, 4ull * cnt);
+        }
     }
     __syncthreads();
     const unsigned int t = s_t;
     const unsigned long long tag = tag_of(s_epoch);
-    const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm, keys_out);
-    // Key r of this thread is element base + 32 r + lane (n < 2^31: 32-bit indices).
-    const unsigned int base = t * kRTile + (unsigned int)warp * (32 * kRKeys);
+    const bool staged = s_staged != 0u;
+    const unsigned int tile0 = t * kRTile;
+    const bool full = n32 - tile0 >= kRTile;
+    const unsigned int wbase = tile0 + (unsigned int)warp * kRWarpKeys;
+    const int shift = 8 * p;
     uint32_t k[kRKeys];
     unsigned int wrank[kRKeys];
-    const int shift = 8 * p;
-    const unsigned int valid_bits = radix_rank_tile(b.in_keys, n, t, shift, k, wrank, s_cnt, s_match, lane, warp);
+    const unsigned int valid_bits = full ? radix_rank_tile<true>(b.in_keys, n32, wbase, shift, k, wrank, s_cnt[warp], lane)
+                                         : radix_rank_tile<false>(b.in_keys, n32, wbase, shift, k, wrank, s_cnt[warp], lane);
     __syncthreads();
     // Per digit value v (threads 0..255): warp offsets within the value's
     // run in this tile and the run's length, published at once.
@@ -370,30 +416,51 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
         for (int w = 0; w < kRWarps; ++w) s_cnt[w][threadIdx.x] += start;
     }
     __syncthreads();
-    // Order the tile by digit value in shared memory (this frees the keys'
-    // registers before the look-back): keys first, keeping each key's
-    // position in wrank, then the indices.
+    // Order the keys by digit value in shared memory; wrank becomes each
+    // key's position in the tile-ordered buffer.
 #pragma unroll
     for (int r = 0; r < kRKeys; ++r) {
-        if ((valid_bits >> r) & 1u) {
+        if (full || ((valid_bits >> r) & 1u)) {
             const unsigned int v = (k[r] >> shift) & 255u;
             wrank[r] += s_cnt[warp][v];
             s_keys[wrank[r]] = k[r];
         }
     }
+    // The indices, in digit order: from the staged copy (read in tile order,
+    // then a barrier before the buffer is overwritten), from global memory,
+    // or the element indices themselves on the first pass.
     if (b.out_idx) {
+        int32_t idx[kRKeys];
+        if (staged) {
+            if (!mbar_wait_bounded(smem_u32(&s_bar), 0u, limit_ns) && lane == 0) report_timeout(hdr, t);
 #pragma unroll
-        for (int r = 0; r < kRKeys; ++r) {
-            if ((valid_bits >> r) & 1u) {
-                const unsigned int e = base + 32u * r + (unsigned int)lane;
-                s_idx[wrank[r]] = b.in_idx ? b.in_idx[e] : (int32_t)e;
+            for (int r = 0; r < kRKeys; ++r) idx[r] = s_idx[warp * kRWarpKeys + 32 * r + lane];
+            __syncthreads();
+        } else {
+#pragma unroll
+            for (int r = 0; r < kRKeys; ++r) {
+                const unsigned int e = wbase + 32u * r + (unsigned int)lane;
+                idx[r] = b.in_idx ? ((full || e < n32) ? __ldcs(b.in_idx + e) : 0) : (int32_t)e;
             }
+        }
+#pragma unroll
+        for (int r = 0; r < kRKeys; ++r)
+            if (full || ((valid_bits >> r) & 1u)) s_idx[wrank[r]] = idx[r];
+    }
+    // First look-back window of value v (threads 0..255): the words of the
+    // kRLook tiles before t.
+    unsigned long long wd[kRLook];
+    if (threadIdx.x < 256) {
+#pragma unroll
+        for (int j = 0; j < kRLook; ++j) {
+            const long long q = (long long)t - 1 - j;
+            wd[j] = q >= 0 ? ld_relaxed(desc + 256ull * (unsigned long long)q + threadIdx.x) : (tag | kFlagP);
         }
     }
     // Look back (threads 0..255, value v): the count of v in all earlier
-    // tiles, W tiles a round trip: load the words of tiles pos-W+1 .. pos
-    // together and add them from pos down to the first inclusive one; a word
-    // not yet published ends the round and is loaded again.
+    // tiles. Window word j holds tile pos - j (a virtual inclusive zero
+    // before tile 0); fold from pos down to the first inclusive word; a word
+    // not yet published ends the round, and the window is reloaded from it.
     if (threadIdx.x < 256) {
         const int v = threadIdx.x;
         const unsigned long long *col = desc + v;  // value v's word of tile q at col[256 q]
@@ -401,12 +468,9 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
         long long pos = (long long)t - 1;
         unsigned long long t0 = 0;
         unsigned int iter = 0;
-        while (pos >= 0) {
-            unsigned long long wd[kRLook];
-#pragma unroll
-            for (int j = 0; j < kRLook; ++j)
-                wd[j] = pos - j >= 0 ? ld_relaxed(col + 256ull * (unsigned long long)(pos - j)) : (tag | kFlagP);
+        while (true) {
             bool done = false, stalled = false;
+            int used = 0;
 #pragma unroll
             for (int j = 0; j < kRLook; ++j) {
                 if (done || stalled) continue;
@@ -415,35 +479,41 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
                     continue;
                 }
                 before += (unsigned int)wd[j];
-                --pos;
+                ++used;
                 if (wd[j] & kFlagP) done = true;
             }
             if (done) break;
-            if (!stalled) continue;
-            // a word not published yet: wait, bounded
-            if (iter == 0) t0 = globaltimer();
-            ++iter;
-            if (iter >= 8) __nanosleep(64);
-            if (iter >= kMaxSpinIters || globaltimer() - t0 > limit_ns) {
-                report_timeout(hdr, t);
-                break;
+            pos -= used;
+            if (stalled) {  // a word not published yet: wait, bounded
+                if (iter == 0) t0 = globaltimer();
+                ++iter;
+                if (iter >= 8) __nanosleep(64);
+                if (iter >= kMaxSpinIters || globaltimer() - t0 > limit_ns) {
+                    report_timeout(hdr, t);
+                    break;
+                }
             }
+#pragma unroll
+            for (int j = 0; j < kRLook; ++j)
+                wd[j] = pos - j >= 0 ? ld_relaxed(col + 256ull * (unsigned long long)(pos - j)) : (tag | kFlagP);
         }
         if (t != 0) st_relaxed(my, tag | kFlagP | (before + tot));
         s_delta[v] = bases[256 * p + v] + before - s_tileoff[v];
     }
     __syncthreads();
-    const unsigned long long tile0 = (unsigned long long)t * kRTile;
-    const unsigned int count = n - tile0 < kRTile ? (unsigned int)(n - tile0) : kRTile;
+    const unsigned int count = full ? kRTile : n32 - tile0;
     for (unsigned int i = threadIdx.x; i < count; i += kRThreads) {
         const unsigned int key = s_keys[i];
         const unsigned int slot = s_delta[(key >> shift) & 255u] + i;
         if (b.out_keys) b.out_keys[slot] = key;
         if (b.out_idx) b.out_idx[slot] = s_idx[i];
     }
+    // leave no bulk copy in flight into this block's shared memory
+    if (staged && threadIdx.x == 0) (void)mbar_wait_bounded(smem_u32(&s_bar), 0u, limit_ns);
+    // (no period clear: this pass's own carry words are cleared before each call)
 }
 
-constexpr size_t kRSmem = (size_t)(kRWarps * 256 + 512 + 2 * kRTile + (U32SCAN_R_MATCH == 2 ? kRWarps * 256 : 0)) * 4;
+constexpr size_t kRSmem = (size_t)(kRWarps * 256 + 512 + 2 * kRTile) * 4;
 
 // All digits constant (every key equal): the permutation is the identity.
 __global__ void radix_identity_kernel(const RadixPlan *__restrict__ plan, const uint32_t *keys, int32_t *perm,
@@ -481,37 +551,46 @@ static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *per
     uint32_t *k1 = reinterpret_cast<uint32_t *>(w + L.k1);
     uint32_t *k2 = reinterpret_cast<uint32_t *>(w + L.k2);
     int32_t *i1 = reinterpret_cast<int32_t *>(w + L.i1);
+    // per device, once: shared-memory limits, SM count, resident digit-pass blocks
+    int sms = 0, resident = 0;
     {
         static std::mutex mu;
-        static bool attr_set[64];
+        static int dev_sms[64], dev_resident[64];
         int dev = -1;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return U32SCAN_ECUDA;
         std::lock_guard<std::mutex> lock(mu);
-        if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(radix_onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kRSmem) != cudaSuccess)
+        if (dev_sms[dev] == 0) {
+            int s = 0, bps = 0;
+            if (cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaFuncSetAttribute(radix_onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kRSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(radix_histogram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kHSmem) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, radix_onesweep_kernel, kRThreads, kRSmem) !=
+                    cudaSuccess)
                 return U32SCAN_ECUDA;
-            attr_set[dev] = true;
+            dev_resident[dev] = s * (bps > 0 ? bps : 1);
+            dev_sms[dev] = s;
         }
+        sms = dev_sms[dev];
+        resident = dev_resident[dev];
     }
     if (cudaMemsetAsync(hist, 0, 4 * 256 * 4, stream) != cudaSuccess) return U32SCAN_ECUDA;
     // the digit passes' carry words (each pass's launch has its own tag)
     if (const int rc = clear_tile_words(desc, 8ull * 256 * L.n_tiles, stream); rc != U32SCAN_OK) return rc;
-    radix_histogram_kernel<<<1024, 512, 0, stream>>>(keys, n, hist);
+    radix_histogram_kernel<<<sms, kHThreads, kHSmem, stream>>>(keys, n, hist);
     radix_plan_kernel<<<1, 128, 0, stream>>>(hist, n, plan, bases);
     for (int p = 0; p < 4; ++p)
         radix_onesweep_kernel<<<L.n_tiles, kRThreads, kRSmem, stream>>>(plan, p, keys, k1, k2, i1, perm, keys_out, n,
-                                                                         L.n_tiles, bases, hdr, desc, kDefaultLimitNs);
+                                                                         L.n_tiles, bases, hdr, desc, kDefaultLimitNs,
+                                                                         (unsigned int)resident);
     radix_identity_kernel<<<1024, 256, 0, stream>>>(plan, keys, perm, keys_out, n);
     if (cudaGetLastError() != cudaSuccess) return U32SCAN_ECUDA;
     // Leave no data where another operation's tile words may go: the
     // histograms, bases and ping-pong buffers hold small integers that could
     // pass for tagged words. Any other operation's tile words lie within the
     // largest workspace it can need (n below 2^32), a few MiB at most.
-    size_t reach = scan_workspace_bytes(0xffffffffull);
-    for (const size_t b : {segscan_workspace_bytes(0xffffffffull), compact_workspace_bytes(0xffffffffull),
-                           compact_values_workspace_bytes(0xffffffffull), scan64_workspace_bytes(0xffffffffull)})
-        reach = b > reach ? b : reach;
+    const size_t reach = tile_word_reach();
     const size_t end = L.total < reach ? L.total : reach;
     return clear_tile_words(w + kHeaderBytes, end - kHeaderBytes, stream);
 }

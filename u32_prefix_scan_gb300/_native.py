@@ -76,6 +76,17 @@ class U32ScanError(RuntimeError):
         super().__init__(f"{what}: {strerror(status)} (status {status})")
 
 
+def load(path) -> ctypes.CDLL:
+    """A library built from these sources at `path` (e.g. with other launch
+    shapes), with the same signatures declared."""
+    handle = ctypes.CDLL(str(path))
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
 def lib() -> ctypes.CDLL:
     """The loaded library with its signatures declared."""
     global _lib
@@ -84,12 +95,7 @@ def lib() -> ctypes.CDLL:
             raise RuntimeError(
                 f"{SO.name} is not built: run `python -c 'import __graft_entry__ as g; g.build()'` "
                 "(needs nvcc); this package has no CPU fallback")
-        handle = ctypes.CDLL(str(SO))
-        for name, (res, args) in SIGNATURES.items():
-            fn = getattr(handle, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = handle
+        _lib = load(SO)
     return _lib
 
 

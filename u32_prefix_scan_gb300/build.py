@@ -70,6 +70,42 @@ def build(force: bool = False, verbose: bool = False) -> pathlib.Path:
     return SO
 
 
+def build_variant(tag: str, defines: list[str], verbose: bool = False) -> pathlib.Path:
+    """Compile the library with extra preprocessor definitions (other launch
+    shapes: the U32SCAN_* macros of the kernel files) into
+    _build/variants/<tag>/libu32scan.so, if its sources or definitions
+    changed since the last build. For tests that compare launch shapes; the
+    package itself always loads the default library."""
+    out = BUILD / "variants" / tag
+    so = out / SO.name
+    stamp = out / "defines.txt"
+    want = " ".join(defines)
+    if so.exists() and stamp.exists() and stamp.read_text() == want:
+        newest = max(p.stat().st_mtime for p in list(CSRC.iterdir()) + list(INCLUDE.glob("*.h")))
+        if so.stat().st_mtime >= newest:
+            return so
+    nvcc = _nvcc()
+    out.mkdir(parents=True, exist_ok=True)
+    procs = []
+    for src in sources():
+        obj = out / (src.stem + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *defines, "-c", str(src), "-o", str(obj)]
+        procs.append((src, obj, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
+    objs = []
+    for src, obj, p in procs:
+        text = p.communicate()[0].decode()
+        if verbose or p.returncode:
+            sys.stderr.write(text)
+        if p.returncode:
+            raise RuntimeError(f"nvcc failed on {src.name} with {defines}")
+        objs.append(obj)
+    tmp = so.with_name(f"{so.name}.tmp{os.getpid()}")
+    subprocess.check_call([nvcc, *ARCH, "-shared", "-o", str(tmp), *map(str, objs)])
+    os.replace(tmp, so)
+    stamp.write_text(want)
+    return so
+
+
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose="-v" in sys.argv)
     print(SO)

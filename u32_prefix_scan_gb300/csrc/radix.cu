@@ -35,10 +35,8 @@
 // the lanes below it in the mask. So a round costs one shared-memory access
 // per distinct digit value; the shared tables a round reads and writes at
 // random digit values (and their bank conflicts) are what bound a pass
-// otherwise. A tile's input indices come into shared memory by one bulk copy
-// issued when the tile is drawn, so their latency hides behind the ranking,
-// and each block asks L2 for the keys and indices of the tile drawn one
-// resident grid later.
+// otherwise. Each block asks L2 for the keys and indices of the tile drawn
+// one resident grid later.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -65,11 +63,6 @@ constexpr unsigned int kRTile = kRThreads * kRKeys;
 constexpr int kRWarps = kRThreads / 32;
 constexpr unsigned int kRWarpKeys = 32 * kRKeys;  // a warp's run of the tile
 static_assert(kRThreads >= 256 && kRThreads % 32 == 0 && kRKeys <= 32, "a thread per digit value; key bits fit a word");
-// How a warp finds the lanes whose key has the same digit value:
-// 0: eight ballots, one per digit bit; 1: the match-any instruction.
-#ifndef U32SCAN_R_MATCH
-#define U32SCAN_R_MATCH 0
-#endif
 #ifndef U32SCAN_R_LOOK
 #define U32SCAN_R_LOOK 8
 #endif
@@ -78,11 +71,6 @@ constexpr int kRLook = U32SCAN_R_LOOK;  // earlier tiles read per look-back roun
 #ifndef U32SCAN_R_PREFETCH
 #define U32SCAN_R_PREFETCH 1
 #endif
-// 1: a full tile's input indices arrive by one bulk copy into shared memory.
-#ifndef U32SCAN_R_STAGE
-#define U32SCAN_R_STAGE 0
-#endif
-
 // One pass's role, decided on the device from the histograms.
 struct RadixPlan {
     int active;  // this digit differs between keys
@@ -253,12 +241,9 @@ __device__ __forceinline__ PassBuffers pass_buffers(const RadixPlan &pl, const u
 
 // The lanes of this warp round whose key has digit value d (all lanes call
 // it; an invalid lane takes part in no mask and gets 0).
+// (Eight ballots measured faster than the match-any instruction.)
 template <bool FULL>
 __device__ __forceinline__ unsigned int radix_same_digit(unsigned int d, bool valid) {
-#if U32SCAN_R_MATCH == 1
-    const unsigned int m = __match_any_sync(0xffffffffu, (FULL || valid) ? d : 256u);
-    return (FULL || valid) ? m : 0u;
-#else
     unsigned int same = FULL ? 0xffffffffu : __ballot_sync(0xffffffffu, valid);
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
@@ -267,7 +252,6 @@ __device__ __forceinline__ unsigned int radix_same_digit(unsigned int d, bool va
         same &= bb ^ (bit - 1u);  // the ballot where the bit is set, its complement where clear
     }
     return (FULL || valid) ? same : 0u;
-#endif
 }
 
 // Load this thread's keys of tile t (warp-striped: round r of warp w covers
@@ -315,14 +299,15 @@ __device__ __forceinline__ void prefetch_l2_interior(const void *p, unsigned lon
     if (e > a) bulk_prefetch_l2(reinterpret_cast<const void *>(a), (unsigned int)(e - a));
 }
 
-// One digit pass over tile t (drawn in order): rank, carry each digit
-// value's count across tiles by decoupled look-back, order the tile by
-// digit value in shared memory, write each value's run of (key, index)
-// pairs to consecutive slots. Carry word of (tile t, value v) at
-// desc[256 t + v] (tile-major: the 32 values of a warp read 32 consecutive
-// words for each earlier tile): the library's tagged format, value = the
-// tile's count of v (aggregate) or the count of v in tiles 0..t (inclusive,
-// P bit). `ahead`: tiles between a block's tile and the one it prefetches.
+// One digit pass: tiles drawn in order; per tile: rank, carry each digit
+// value's count across tiles by decoupled look-back, order the tile by digit
+// value in shared memory, write each value's run of (key, index) pairs to
+// consecutive slots. Carry word of (tile t, value v) at desc[256 t + v]
+// (tile-major: the 32 values of a warp read 32 consecutive words for each
+// earlier tile): the library's tagged format, value = the tile's count of v
+// (aggregate) or the count of v in tiles 0..t (inclusive, P bit).
+// One tile per block; `ahead`: tiles between a block's tile and the one it
+// asks L2 for (the resident grid).
 __global__ void __launch_bounds__(kRThreads, U32SCAN_R_MINB)
 radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
                       int32_t *i1, int32_t *perm, uint32_t *keys_out, unsigned long long n, unsigned int n_tiles,
@@ -333,8 +318,8 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     // Shared memory (32-bit words): per-warp digit counters, later the warp
     // offsets in the tile-ordered buffer [kRWarps][256]; each value's run
     // start in the tile [256]; its first output slot minus that start [256];
-    // the tile's keys in digit order [kRTile]; its input indices, first in
-    // tile order (bulk copy), then in digit order [kRTile].
+    // the tile's keys in digit order [kRTile]; its indices in digit order
+    // [kRTile].
     extern __shared__ __align__(128) unsigned int r_smem[];
     unsigned int(*s_cnt)[256] = reinterpret_cast<unsigned int(*)[256]>(r_smem);
     unsigned int *s_tileoff = r_smem + kRWarps * 256;
@@ -342,46 +327,32 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     unsigned int *s_keys = s_delta + 256;
     int32_t *s_idx = reinterpret_cast<int32_t *>(s_keys + kRTile);
     __shared__ unsigned int s_part[kRWarps];
-    __shared__ unsigned int s_t, s_epoch, s_staged;
-    __shared__ __align__(8) unsigned long long s_bar;
+    __shared__ unsigned int s_t, s_epoch;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm, keys_out);
+    const int shift = 8 * p;
     // n < 2^31 for a radix sort: 32-bit element indices
     const unsigned int n32 = (unsigned int)n;
+    // Ask L2 for tile f's keys (and indices, when the pass moves them).
+    auto prefetch_tile = [&](unsigned int f) {
+        const unsigned int f0 = f * kRTile;
+        const unsigned int cnt = n32 - f0 < kRTile ? n32 - f0 : kRTile;
+        prefetch_l2_interior(b.in_keys + f0, 4ull * cnt);
+        if (b.in_idx != nullptr && b.out_idx != nullptr) prefetch_l2_interior(b.in_idx + f0, 4ull * cnt);
+    };
     if (threadIdx.x == 0) {
         unsigned int e;
         const unsigned int t = draw_tile(hdr, n_tiles, &e);
         s_t = t;
         s_epoch = e;
-        const unsigned int tile0 = t * kRTile;
-        const bool full = n32 - tile0 >= kRTile;
-        // input indices of a full tile by bulk copy, when they start on a
-        // 16-byte boundary (tile starts are 32 KiB apart)
-        const bool staged = U32SCAN_R_STAGE && b.out_idx != nullptr && b.in_idx != nullptr && full &&
-                            (reinterpret_cast<uintptr_t>(b.in_idx) & 15) == 0;
-        s_staged = staged ? 1u : 0u;
-        if (staged) {
-            const unsigned int bar = smem_u32(&s_bar);
-            mbar_init(bar, 1u);
-            fence_mbar_init();
-            mbar_arrive_expect_tx(bar, kRTile * 4u);
-            bulk_load(smem_u32(s_idx), b.in_idx + tile0, kRTile * 4u, bar);
-        }
-        if (U32SCAN_R_PREFETCH && ahead != 0u && t + ahead < n_tiles) {
-            const unsigned int f0 = (t + ahead) * kRTile;
-            const unsigned int cnt = n32 - f0 < kRTile ? n32 - f0 : kRTile;
-            prefetch_l2_interior(b.in_keys + f0, 4ull * cnt);
-            if (b.in_idx != nullptr && b.out_idx != nullptr) prefetch_l2_interior(b.in_idx + f0, 4ull * cnt);
-        }
+        if (U32SCAN_R_PREFETCH && ahead != 0u && t + ahead < n_tiles) prefetch_tile(t + ahead);
     }
     __syncthreads();
     const unsigned int t = s_t;
     const unsigned long long tag = tag_of(s_epoch);
-    const bool staged = s_staged != 0u;
     const unsigned int tile0 = t * kRTile;
     const bool full = n32 - tile0 >= kRTile;
     const unsigned int wbase = tile0 + (unsigned int)warp * kRWarpKeys;
-    const int shift = 8 * p;
     uint32_t k[kRKeys];
     unsigned int wrank[kRKeys];
     const unsigned int valid_bits = full ? radix_rank_tile<true>(b.in_keys, n32, wbase, shift, k, wrank, s_cnt[warp], lane)
@@ -417,7 +388,10 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     }
     __syncthreads();
     // Order the keys by digit value in shared memory; wrank becomes each
-    // key's position in the tile-ordered buffer.
+    // key's position in the tile-ordered buffer. Then the indices: read from
+    // the previous pass's buffer (all sixteen loads first, then the stores:
+    // a load and its store taken in turn measured 16 % slower), or the
+    // element indices on the first pass.
 #pragma unroll
     for (int r = 0; r < kRKeys; ++r) {
         if (full || ((valid_bits >> r) & 1u)) {
@@ -426,36 +400,16 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
             s_keys[wrank[r]] = k[r];
         }
     }
-    // The indices, in digit order: from the staged copy (read in tile order,
-    // then a barrier before the buffer is overwritten), from global memory,
-    // or the element indices themselves on the first pass.
     if (b.out_idx) {
         int32_t idx[kRKeys];
-        if (staged) {
-            if (!mbar_wait_bounded(smem_u32(&s_bar), 0u, limit_ns) && lane == 0) report_timeout(hdr, t);
 #pragma unroll
-            for (int r = 0; r < kRKeys; ++r) idx[r] = s_idx[warp * kRWarpKeys + 32 * r + lane];
-            __syncthreads();
-        } else {
-#pragma unroll
-            for (int r = 0; r < kRKeys; ++r) {
-                const unsigned int e = wbase + 32u * r + (unsigned int)lane;
-                idx[r] = b.in_idx ? ((full || e < n32) ? __ldcs(b.in_idx + e) : 0) : (int32_t)e;
-            }
+        for (int r = 0; r < kRKeys; ++r) {
+            const unsigned int e = wbase + 32u * r + (unsigned int)lane;
+            idx[r] = b.in_idx ? ((full || ((valid_bits >> r) & 1u)) ? __ldcs(b.in_idx + e) : 0) : (int32_t)e;
         }
 #pragma unroll
         for (int r = 0; r < kRKeys; ++r)
             if (full || ((valid_bits >> r) & 1u)) s_idx[wrank[r]] = idx[r];
-    }
-    // First look-back window of value v (threads 0..255): the words of the
-    // kRLook tiles before t.
-    unsigned long long wd[kRLook];
-    if (threadIdx.x < 256) {
-#pragma unroll
-        for (int j = 0; j < kRLook; ++j) {
-            const long long q = (long long)t - 1 - j;
-            wd[j] = q >= 0 ? ld_relaxed(desc + 256ull * (unsigned long long)q + threadIdx.x) : (tag | kFlagP);
-        }
     }
     // Look back (threads 0..255, value v): the count of v in all earlier
     // tiles. Window word j holds tile pos - j (a virtual inclusive zero
@@ -464,6 +418,12 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     if (threadIdx.x < 256) {
         const int v = threadIdx.x;
         const unsigned long long *col = desc + v;  // value v's word of tile q at col[256 q]
+        unsigned long long wd[kRLook];
+#pragma unroll
+        for (int j = 0; j < kRLook; ++j) {
+            const long long q = (long long)t - 1 - j;
+            wd[j] = q >= 0 ? ld_relaxed(col + 256ull * (unsigned long long)q) : (tag | kFlagP);
+        }
         unsigned int before = 0;
         long long pos = (long long)t - 1;
         unsigned long long t0 = 0;
@@ -501,16 +461,15 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
         s_delta[v] = bases[256 * p + v] + before - s_tileoff[v];
     }
     __syncthreads();
-    const unsigned int count = full ? kRTile : n32 - tile0;
-    for (unsigned int i = threadIdx.x; i < count; i += kRThreads) {
-        const unsigned int key = s_keys[i];
-        const unsigned int slot = s_delta[(key >> shift) & 255u] + i;
-        if (b.out_keys) b.out_keys[slot] = key;
-        if (b.out_idx) b.out_idx[slot] = s_idx[i];
+    {
+        const unsigned int count = full ? kRTile : n32 - tile0;
+        for (unsigned int i = threadIdx.x; i < count; i += kRThreads) {
+            const unsigned int key = s_keys[i];
+            const unsigned int slot = s_delta[(key >> shift) & 255u] + i;
+            if (b.out_keys) b.out_keys[slot] = key;
+            if (b.out_idx) b.out_idx[slot] = s_idx[i];
+        }
     }
-    // leave no bulk copy in flight into this block's shared memory
-    if (staged && threadIdx.x == 0) (void)mbar_wait_bounded(smem_u32(&s_bar), 0u, limit_ns);
-    // (no period clear: this pass's own carry words are cleared before each call)
 }
 
 constexpr size_t kRSmem = (size_t)(kRWarps * 256 + 512 + 2 * kRTile) * 4;

@@ -466,10 +466,22 @@ class CompactOp(Op):
         self.metric = (f"stream compaction Gelem/s and HBM GB/s (fraction of peak) at n=2^27, "
                        f"Bernoulli p={self.p} int32 flags, 1 GB300")
         self.kernel = "compact_persistent<512,8,2>"
+        # under torchrun: rank r compacts its shard of one array of N * n flags
+        self.world, self.rank = getattr(args, "world", 1), getattr(args, "rank", 0)
+        self.sharded = self.world > 1
+        if self.sharded:
+            self.launches_per_step = 4  # count, two scans of the gathered words, compaction from the carry-ins
 
     def workload(self):
-        return (f"compaction of n=2^{self.n.bit_length() - 1} int32 flags, Bernoulli p={self.p} (seed 4): "
+        lg = self.n.bit_length() - 1
+        if self.sharded:
+            return (f"compaction of one array of {self.world} x 2^{lg} int32 flags, Bernoulli p={self.p} (seed 4), "
+                    f"sharded: rank r holds flags [r 2^{lg}, (r+1) 2^{lg}); whole-array offsets and indices, counts")
+        return (f"compaction of n=2^{lg} int32 flags, Bernoulli p={self.p} (seed 4): "
                 f"inclusive offsets, kept indices with -1 tail, count")
+
+    def is_marked(self) -> bool:
+        return self.sharded
 
     def algorithmic_bytes(self):
         return 12 * self.n + 4  # flags read; offsets and one index slot written per element; the count
@@ -477,7 +489,7 @@ class CompactOp(Op):
     def host_inputs(self):
         from u32_prefix_scan_gb300 import inputs
 
-        return {"flags": inputs.compact_flags(self.n, 4, self.p)}
+        return {"flags": inputs.compact_flags(self.n, 4, self.p, start=self.rank * self.n)}
 
     def setup(self, dev, host):
         import torch
@@ -486,17 +498,35 @@ class CompactOp(Op):
         from u32_prefix_scan_gb300 import _native
 
         self.u = u
+        if self.sharded:
+            from u32_prefix_scan_gb300 import shard
+
+            self.shard = shard
         self.flags = torch.from_numpy(host["flags"]).to(dev)
         self.offsets = torch.empty(self.n, dtype=torch.int32, device=dev)
         self.indices = torch.empty(self.n, dtype=torch.int32, device=dev)
         self.count = torch.empty(1, dtype=torch.int32, device=dev)
-        self.ws = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_COMPACT, self.n), dev)
+        lib = _native.lib()
+        self.ws = u.Workspace(max(lib.u32scan_workspace_bytes(_native.OP_COMPACT, self.n),
+                                  lib.u32scan_workspace_bytes(_native.OP_SCAN, self.world),
+                                  lib.u32scan_workspace_bytes(_native.OP_REDUCE, self.n)), dev)
+        if self.sharded:
+            self.steps = shard.KernelSteps(workspace=self.ws)
         self.pinned_in = {"flags": torch.from_numpy(host["flags"]).pin_memory()}
         self.pinned_out = {k: torch.empty(self.n, dtype=torch.int32).pin_memory() for k in ("offsets", "indices")}
         self.pinned_out["count"] = torch.empty(1, dtype=torch.int32).pin_memory()
 
     def step(self):
-        self.u.compact_indices_u32(self.flags, self.offsets, self.indices, self.count, workspace=self.ws)
+        if self.sharded:
+            self.offsets, self.indices, self.count, _ = self.shard.sharded_compact(self.flags, steps=self.steps)
+        else:
+            self.u.compact_indices_u32(self.flags, self.offsets, self.indices, self.count, workspace=self.ws)
+
+    def step_marked(self, before, after):
+        """The sharded step with events around its compaction from the
+        carry-ins, the kernel that moves 12 of its 16 bytes an element."""
+        self.offsets, self.indices, self.count, _ = self.shard.sharded_compact(self.flags, steps=self.steps,
+                                                                              marks=(before, after))
 
     def e2e_step(self):
         self.flags.copy_(self.pinned_in["flags"], non_blocking=True)
@@ -510,6 +540,9 @@ class CompactOp(Op):
         import numpy as np
 
         c = int(self.pinned_out["count"][0])
+        if self.sharded:  # whole-array offsets: the last one exceeds the shard's count by what lies before
+            return (c == int(np.count_nonzero(host["flags"])) and int(self.pinned_out["offsets"][-1]) >= c
+                    and (c == self.n or int(self.pinned_out["indices"][c]) == -1))
         return (c == int(np.count_nonzero(host["flags"])) and int(self.pinned_out["offsets"][-1]) == c
                 and (c == self.n or int(self.pinned_out["indices"][c]) == -1))
 
@@ -1273,8 +1306,11 @@ def run_ours(args, rank, local_rank, world):
                                     "ms_per_step_max": soak[-1], "clocks": sampler.summary(w2, w3)}
     if getattr(op, "sharded", False):
         result["scaling"] = "weak"
-        result["config"]["per_rank"] = ("one shard of one global scan: fold (4 B/elem), all-gather of the "
-                                        f"{world} shard sums over NCCL, scan from the carry-in (8 B/elem)")
+        result["config"]["per_rank"] = (
+            f"one shard of one global compaction: count (4 B/elem), all-gather of the {world} (count, length) "
+            "pairs over NCCL, compaction from the carry-ins (12 B/elem)" if isinstance(op, CompactOp) else
+            "one shard of one global scan: fold (4 B/elem), all-gather of the "
+            f"{world} shard sums over NCCL, scan from the carry-in (8 B/elem)")
     if library is not None:
         if "hbm_gbs" in library:
             library["frac"] = library["hbm_gbs"] / peak

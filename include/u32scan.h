@@ -170,6 +170,20 @@ int reduce_u32_op(int op, const uint32_t *data, size_t n, uint32_t *total,
                   void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /*
+ * The number of non-zero elements, read once: the count of a compaction
+ * without its offsets. Source: the "parallel" package reference (entelechy
+ * docs), graph `compact`: compact_total is the number of kept elements, and a
+ * non-zero flag keeps its element.
+ *   data   device, uint32_t[n] (int32 flags may be passed as is), read only.
+ *   n      element count, below 2^62; count wraps at 2^32.
+ *   count  device, one uint32_t: the number of data[i] != 0 (0 when n == 0).
+ *   ws, ws_bytes  as reduce_u32_op (U32SCAN_OP_REDUCE).
+ * Errors: as reduce_u32_op.
+ */
+int count_nonzero_u32(const uint32_t *data, size_t n, uint32_t *count,
+                      void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
  * The same two scans of an array in HOST memory, with the result written to
  * host memory. Source: as scan_exclusive_u32 / scan_inclusive_u32
  * ("scan.bend source", section API; CAIRN "scan"); the pages' arrays live in
@@ -333,6 +347,31 @@ int compact_indices_u32(const int32_t *flags, size_t n, int32_t *offsets,
  */
 int compact_values_u32(const uint32_t *values, const int32_t *flags, size_t n, uint32_t *out,
                        int32_t *count, void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
+ * compact_indices_u32 of one piece of a longer flag array: what lies before
+ * the piece comes in as two device words (so that they can come from a
+ * collective without a host round trip), and the piece's results are its
+ * part of the whole array's. Source: as compact_indices_u32; the pieces
+ * compose as the scan.bend source's blocks do (section Driver): a piece's
+ * offsets start from the kept count before it.
+ *   kept_before  device, one int32_t or NULL for 0: kept elements before the
+ *                piece; offsets[i] = kept_before + kept in flags[0..i].
+ *   first_index  device, one int32_t or NULL for 0: the whole array's index
+ *                of flags[0]; the kept indices written are whole-array
+ *                indices (first_index + i).
+ *   flags, n, offsets, indices, count, ws, ws_bytes, stream: as
+ *                compact_indices_u32; indices and count are the piece's own
+ *                (its kept indices in order at the front, -1 after them, and
+ *                its kept count). The whole array's compacted indices are the
+ *                pieces' fronts one after another. Whole-array indices must
+ *                stay below 2^31.
+ * Errors: as compact_indices_u32, and EINVAL for a misaligned kept_before or
+ * first_index.
+ */
+int compact_indices_u32_carry(const int32_t *flags, size_t n, const int32_t *kept_before,
+                              const int32_t *first_index, int32_t *offsets, int32_t *indices, int32_t *count,
+                              void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /*
  * Stable LSD radix-sort permutation of U32 keys.

@@ -114,3 +114,15 @@ def test_scan_under_several_ranks_is_one_sharded_scan():
     assert (op.host_inputs()["data"] == whole[2 << 10: 3 << 10]).all()
     args.world, args.rank = 1, 0
     assert not bench.make_op(args).sharded
+
+
+def test_compaction_under_several_ranks_is_one_sharded_compaction():
+    args = bench.parse_args(["--op", "compact", "--log2n", "10"])
+    args.world, args.rank = 2, 1
+    op = bench.make_op(args)
+    assert op.sharded and op.is_marked() and op.launches_per_step == 4
+    assert "2 x 2^10" in op.workload()
+    from u32_prefix_scan_gb300 import inputs
+
+    whole = inputs.compact_flags(2 << 10, 4, 0.1)
+    assert (op.host_inputs()["flags"] == whole[1 << 10:]).all()

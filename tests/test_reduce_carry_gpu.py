@@ -129,3 +129,84 @@ def test_sharded_scan_on_a_one_rank_nccl_group(u):
         assert np.array_equal(host_u32(d), want) and int(host_u32(total)[0]) == want_total
     finally:
         dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("p", [0.1, 0.9])
+@pytest.mark.parametrize("n", [0, 1, 5, 1000, (1 << 20) + 3, (1 << 24) + 12345])
+def test_count_nonzero_matches_the_oracle(u, n, p):
+    f = inputs.compact_flags(n, 65, p)
+    f[::7] = -7  # any non-zero flag keeps its element
+    for offset in (0, 3):
+        d = dev32(f.view(np.uint32), offset)
+        count = u.count_nonzero_u32(d)
+        u.check()
+        assert int(host_u32(count)[0]) == oracle.compact_indices(f)[2], (n, offset)
+
+
+@pytest.mark.parametrize("n", [1, 1000, 100003, (1 << 22) + 77])
+def test_compaction_from_carry_ins(u, n):
+    f = inputs.compact_flags(n, 66, 0.1)
+    want_off, want_idx, want_cnt = oracle.compact_indices(f)
+    kb = torch.tensor([12345], dtype=torch.int32, device="cuda")
+    ib = torch.tensor([1 << 24], dtype=torch.int32, device="cuda")
+    off, idx, cnt = u.compact_indices_u32_carry(dev32(f.view(np.uint32), 1).view(torch.int32), kb, ib)
+    u.check()
+    assert int(cnt.item()) == want_cnt
+    assert np.array_equal(off.cpu().numpy(), want_off + 12345)
+    got = idx.cpu().numpy()
+    assert np.array_equal(got[:want_cnt], want_idx[:want_cnt] + (1 << 24)) and (got[want_cnt:] == -1).all()
+    # no carry-ins: the plain compaction
+    off, idx, cnt = u.compact_indices_u32_carry(dev32(f.view(np.uint32)).view(torch.int32), None, None)
+    u.check()
+    assert np.array_equal(off.cpu().numpy(), want_off) and np.array_equal(idx.cpu().numpy(), want_idx)
+
+
+@pytest.mark.parametrize("cuts", [[70001, 0, (1 << 22) + 9, 123], [(1 << 21) + 1, (1 << 21) + 1, 5]],
+                         ids=["uneven-with-empty", "two-long-one-short"])
+def test_pieces_compacted_from_their_carries_make_the_whole_compaction(u, cuts):
+    from u32_prefix_scan_gb300.shard import KernelSteps
+
+    whole = inputs.compact_flags(sum(cuts), 67, 0.1)
+    steps = KernelSteps()
+    bounds = np.cumsum([0] + cuts)
+    pieces = [dev32(whole[bounds[r]:bounds[r + 1]].view(np.uint32)).view(torch.int32) for r in range(len(cuts))]
+    counts = torch.cat([steps.count(p) for p in pieces])  # the all-gather, emulated
+    lengths = torch.tensor(cuts, dtype=torch.int32, device="cuda")
+    grand = steps.scan_row(counts)
+    steps.scan_row(lengths)
+    got_off, got_idx = [], []
+    for r, p in enumerate(pieces):
+        off, idx, cnt = steps.compact_from(p, counts[r:r + 1], lengths[r:r + 1])
+        k = int(cnt.item())
+        got_off.append(off.cpu().numpy())
+        got_idx.append(idx.cpu().numpy()[:k])
+        assert (idx.cpu().numpy()[k:] == -1).all()
+    u.check()
+    want_off, want_idx, want_cnt = oracle.compact_indices(whole)
+    assert np.array_equal(np.concatenate(got_off), want_off)
+    assert np.array_equal(np.concatenate(got_idx), want_idx[:want_cnt])
+    assert int(grand.item()) == want_cnt
+
+
+def test_sharded_compaction_on_a_one_rank_nccl_group(u):
+    import torch.distributed as dist
+
+    from u32_prefix_scan_gb300 import shard
+
+    if dist.is_initialized():
+        pytest.skip("a process group already exists")
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", rank=0, world_size=1)
+    try:
+        f = inputs.compact_flags((1 << 22) + 77, 68, 0.9)
+        off, idx, cnt, total = shard.sharded_compact(dev32(f.view(np.uint32)).view(torch.int32))
+        u.check()
+        want_off, want_idx, want_cnt = oracle.compact_indices(f)
+        assert np.array_equal(off.cpu().numpy(), want_off) and np.array_equal(idx.cpu().numpy(), want_idx)
+        assert int(cnt.item()) == want_cnt == int(total.item())
+    finally:
+        dist.destroy_process_group()

@@ -50,6 +50,19 @@ class OracleSteps:
         shard.copy_(torch.from_numpy((out + c).astype(np.uint32).view(np.int32)))  # wraps mod 2^32
         return torch.from_numpy(np.array([total + c], np.uint64).astype(np.uint32).view(np.int32))
 
+    def count(self, flags):
+        return torch.tensor([oracle.compact_indices(flags.numpy())[2]], dtype=torch.int32)
+
+    def compact_from(self, flags, kept_before, first_index):
+        # the shard's compaction as part of the whole array: offsets from the
+        # kept elements before it, indices from the shard's first index
+        off, idx, cnt = oracle.compact_indices(flags.numpy())
+        kb, ib = int(kept_before[0]), int(first_index[0])
+        idx = idx.copy()
+        idx[:cnt] += ib
+        return (torch.from_numpy((off + kb).astype(np.int32)), torch.from_numpy(idx.astype(np.int32)),
+                torch.tensor([cnt], dtype=torch.int32))
+
 
 CASES = {
     "uneven": (100003, [40000, 60003]),
@@ -93,3 +106,49 @@ def test_two_gloo_ranks_compose_the_whole_scan(tmp_path, case, inclusive):
     assert np.array_equal(got, want)
     for r in range(world):
         assert json.loads((tmp_path / f"rank{r}.json").read_text())["total"] == want_total
+
+
+COMPACT_CASES = {
+    "uneven": (100003, [40000, 60003], 0.1),
+    "dense": (50001, [25000, 25001], 0.9),
+    "empty_first": (7001, [0, 7001], 0.1),
+}
+
+
+def _compact_rank_main(rank, world, port, out_dir, case):
+    import torch.distributed as dist
+
+    from u32_prefix_scan_gb300 import shard as sh
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        n, cuts, p = COMPACT_CASES[case]
+        whole = inputs.compact_flags(n, 78, p)
+        lo = sum(cuts[:rank])
+        piece = torch.from_numpy(whole[lo:lo + cuts[rank]].copy())
+        offsets, indices, count, total = sh.sharded_compact(piece, steps=OracleSteps())
+        np.save(os.path.join(out_dir, f"off{rank}.npy"), offsets.numpy())
+        np.save(os.path.join(out_dir, f"idx{rank}.npy"), indices.numpy()[:int(count[0])])
+        np.save(os.path.join(out_dir, f"tail{rank}.npy"), indices.numpy()[int(count[0]):])
+        with open(os.path.join(out_dir, f"c{rank}.json"), "w") as fh:
+            json.dump({"total": int(total[0])}, fh)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("case", sorted(COMPACT_CASES))
+def test_two_gloo_ranks_compose_the_whole_compaction(tmp_path, case):
+    import torch.multiprocessing as mp
+
+    world = 2
+    mp.spawn(_compact_rank_main, args=(world, free_port(), str(tmp_path), case), nprocs=world, join=True)
+    n, _, p = COMPACT_CASES[case]
+    want_off, want_idx, want_count = oracle.compact_indices(inputs.compact_flags(n, 78, p))
+    got_off = np.concatenate([np.load(tmp_path / f"off{r}.npy") for r in range(world)])
+    got_idx = np.concatenate([np.load(tmp_path / f"idx{r}.npy") for r in range(world)])
+    assert np.array_equal(got_off, want_off)
+    assert np.array_equal(got_idx, want_idx[:want_count])
+    for r in range(world):
+        assert (np.load(tmp_path / f"tail{r}.npy") == -1).all()
+        assert json.loads((tmp_path / f"c{r}.json").read_text())["total"] == want_count

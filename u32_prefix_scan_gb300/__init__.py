@@ -13,6 +13,8 @@ _API = {
     "scan_exclusive_u32_carry",
     "scan_inclusive_u32_carry",
     "reduce_u32_op",
+    "count_nonzero_u32",
+    "compact_indices_u32_carry",
     "scan_exclusive_u32_host",
     "scan_inclusive_u32_host",
     "scan_u32_op",

@@ -24,6 +24,8 @@ __all__ = [
     "scan_exclusive_u32_carry",
     "scan_inclusive_u32_carry",
     "reduce_u32_op",
+    "count_nonzero_u32",
+    "compact_indices_u32_carry",
     "scan_exclusive_u32_host",
     "scan_inclusive_u32_host",
     "scan_u32_op",
@@ -341,6 +343,54 @@ def compact_indices_u32(flags: torch.Tensor, offsets: torch.Tensor | None = None
         flags.data_ptr(), n, offsets.data_ptr() if offsets is not None else None, indices.data_ptr(),
         count.data_ptr(), ws.ptr, ws.nbytes, sh), "compact_indices_u32")
     return offsets, indices, count
+
+
+def compact_indices_u32_carry(flags: torch.Tensor, kept_before: torch.Tensor | None,
+                              first_index: torch.Tensor | None, offsets: torch.Tensor | None = None,
+                              indices: torch.Tensor | None = None, count: torch.Tensor | None = None, *,
+                              stream=None, workspace: Workspace | None = None):
+    """compact_indices_u32 of one piece of a longer flag array: kept_before
+    and first_index (one-element int32 device tensors, or None for 0) are
+    the kept elements and the elements before the piece. Returns (offsets,
+    indices, count) as compact_indices_u32, with whole-array offsets and
+    indices and the piece's own count."""
+    _require_cuda(flags, "flags", (torch.int32,))
+    for name, t in (("kept_before", kept_before), ("first_index", first_index)):
+        if t is not None:
+            _require_cuda(t, name, (torch.int32,))
+            if t.numel() < 1:
+                raise ValueError(f"{name} must hold at least one element")
+    n = flags.numel()
+    if offsets is None:
+        offsets = torch.empty(n, dtype=torch.int32, device=flags.device)
+    _require_cuda(offsets, "offsets", (torch.int32,))
+    if indices is None:
+        indices = torch.empty(n, dtype=torch.int32, device=flags.device)
+    _require_cuda(indices, "indices", (torch.int32,))
+    if offsets.numel() != n or indices.numel() != n:
+        raise ValueError("offsets and indices must have n elements")
+    count = _scalar_out(count, flags, torch.int32)
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_COMPACT, n, flags.device, sh, workspace)
+    _native.check(_native.lib().compact_indices_u32_carry(
+        flags.data_ptr(), n, kept_before.data_ptr() if kept_before is not None else None,
+        first_index.data_ptr() if first_index is not None else None, offsets.data_ptr(), indices.data_ptr(),
+        count.data_ptr(), ws.ptr, ws.nbytes, sh), "compact_indices_u32_carry")
+    return offsets, indices, count
+
+
+def count_nonzero_u32(data: torch.Tensor, count: torch.Tensor | None = None, *, stream=None,
+                      workspace: Workspace | None = None) -> torch.Tensor:
+    """The number of non-zero elements of data (u32 or int32 flags), read
+    once. Returns a one-element device tensor."""
+    _require_cuda(data, "data")
+    count = _scalar_out(count, data, data.dtype)
+    n = data.numel()
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_REDUCE, n, data.device, sh, workspace)
+    _native.check(_native.lib().count_nonzero_u32(data.data_ptr(), n, count.data_ptr(), ws.ptr, ws.nbytes, sh),
+                  "count_nonzero_u32")
+    return count
 
 
 def compact_values_u32(values: torch.Tensor, flags: torch.Tensor | None = None, out: torch.Tensor | None = None,

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 compact_persistent(const int32_t *__restrict__ flags, unsigned long long n, int32_t *offsets,
                    int32_t *__restrict__ indices, int32_t *count, WsHeader *hdr, unsigned long long *desc,
                    unsigned int n_tiles, unsigned int head, int offsets_aligned, unsigned long long limit_ns,
-                   unsigned long long clear_words) {
+                   unsigned long long clear_words, const int32_t *kept_before, const int32_t *first_index) {
     constexpr int WARPS = THREADS / 32;
     constexpr unsigned int CHUNK = 128 * V;
     constexpr unsigned int TILE = THREADS * V * 4;
@@ -58,6 +58,7 @@ compact_persistent(const int32_t *__restrict__ flags, unsigned long long n, int3
     __shared__ unsigned int s_base[WARPS];  // kept before warp w of the current tile (tile-local)
     __shared__ unsigned int s_prefix;       // kept before the current tile
     __shared__ unsigned int s_kept;         // kept in the current tile
+    __shared__ unsigned int s_kbase, s_ibase;  // carry-ins: kept elements and elements before the array
     __shared__ unsigned int s_epoch;
 
     const int lane = threadIdx.x & 31;
@@ -103,8 +104,13 @@ compact_persistent(const int32_t *__restrict__ flags, unsigned long long n, int3
 #pragma unroll
         for (int st = 0; st < S; ++st) issue(st);
     }
+    if (threadIdx.x == 0) {  // the array as one piece of a longer one: what lies before it
+        s_kbase = kept_before ? (unsigned int)*kept_before : 0u;
+        s_ibase = first_index ? (unsigned int)*first_index : 0u;
+    }
     __syncthreads();
     const unsigned long long tag = tag_of(s_epoch);
+    const unsigned int kbase = s_kbase, ibase = s_ibase;
     const unsigned int li0 = (unsigned int)warp * CHUNK + 4u * (unsigned int)lane;
     volatile unsigned int *vs_tile = s_tile;
 
@@ -215,7 +221,7 @@ compact_persistent(const int32_t *__restrict__ flags, unsigned long long n, int3
 #pragma unroll
                     for (int r = 0; r < V; ++r) {
                         const unsigned int b = (kbc >> (4 * r)) & 0xfu;
-                        const unsigned int o = prefix + wbase + exc[r];
+                        const unsigned int o = kbase + prefix + wbase + exc[r];
                         const int4 y = make_int4((int)(o + (b & 1u)), (int)(o + __popc(b & 3u)),
                                                  (int)(o + __popc(b & 7u)), (int)(o + __popc(b)));
                         if (vec) {
@@ -237,7 +243,7 @@ compact_persistent(const int32_t *__restrict__ flags, unsigned long long n, int3
                     for (int c = 0; c < 4; ++c)
                         if ((b >> c) & 1u)
                             stage_idx[wbase + exc[r] + __popc(b & ((1u << c) - 1u))] =
-                                (int32_t)(e0 + li0 + 128 * r + c);
+                                (int32_t)(ibase + e0 + li0 + 128 * r + c);
                 }
                 __syncthreads();  // barrier C: the tile's kept indices are staged
                 for (unsigned int j = threadIdx.x; j < kept; j += THREADS) __stcs(indices + prefix + j, stage_idx[j]);
@@ -281,11 +287,13 @@ static bool g_cmp_attr[64];
 
 static int compact_launch(const int32_t *flags, unsigned long long n, int32_t *offsets, int32_t *indices,
                           int32_t *count, void *ws, size_t ws_bytes, cudaStream_t stream,
-                          unsigned long long limit_ns) {
+                          unsigned long long limit_ns, const int32_t *kept_before = nullptr,
+                          const int32_t *first_index = nullptr) {
     if (n >= (1ull << 31)) return U32SCAN_EINVAL;
     if (n > 0 && (flags == nullptr || indices == nullptr)) return U32SCAN_EINVAL;
     if ((reinterpret_cast<uintptr_t>(flags) & 3) || (reinterpret_cast<uintptr_t>(offsets) & 3) ||
-        (reinterpret_cast<uintptr_t>(indices) & 3) || (reinterpret_cast<uintptr_t>(count) & 3))
+        (reinterpret_cast<uintptr_t>(indices) & 3) || (reinterpret_cast<uintptr_t>(count) & 3) ||
+        (reinterpret_cast<uintptr_t>(kept_before) & 3) || (reinterpret_cast<uintptr_t>(first_index) & 3))
         return U32SCAN_EINVAL;
     if (n == 0) {
         if (count && cudaMemsetAsync(count, 0, sizeof(int32_t), stream) != cudaSuccess) return U32SCAN_ECUDA;
@@ -316,7 +324,8 @@ static int compact_launch(const int32_t *flags, unsigned long long n, int32_t *o
     WsHeader *hdr = static_cast<WsHeader *>(ws);
     unsigned long long *desc = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
     kern<<<grid, kCThreads, kCSmem, stream>>>(flags, n, offsets, indices, count, hdr, desc, n_tiles, head,
-                                             offsets_aligned, limit_ns, tile_words_to_clear(ws_bytes));
+                                             offsets_aligned, limit_ns, tile_words_to_clear(ws_bytes), kept_before,
+                                             first_index);
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }
 
@@ -327,4 +336,11 @@ using namespace u32scan;
 extern "C" int compact_indices_u32(const int32_t *flags, size_t n, int32_t *offsets, int32_t *indices,
                                    int32_t *count, void *ws, size_t ws_bytes, u32scan_stream_t stream) {
     return compact_launch(flags, n, offsets, indices, count, ws, ws_bytes, (cudaStream_t)stream, kDefaultLimitNs);
+}
+
+extern "C" int compact_indices_u32_carry(const int32_t *flags, size_t n, const int32_t *kept_before,
+                                         const int32_t *first_index, int32_t *offsets, int32_t *indices,
+                                         int32_t *count, void *ws, size_t ws_bytes, u32scan_stream_t stream) {
+    return compact_launch(flags, n, offsets, indices, count, ws, ws_bytes, (cudaStream_t)stream, kDefaultLimitNs,
+                          kept_before, first_index);
 }

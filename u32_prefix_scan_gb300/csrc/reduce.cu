@@ -6,6 +6,10 @@
 // and products wrap at 2^32). Each is associative and commutative, so the
 // fold may be taken in any grouping and order and gives the same bits.
 //
+// count_nonzero_u32 folds (x != 0) with add instead: the number of kept
+// elements of a compaction (the entelechy `compact` graph's count), read
+// without writing offsets.
+//
 // Kernel: a grid of resident blocks strides over the array with four 16-byte
 // loads in flight a thread; each block folds its share (lanes, then warps)
 // into one partial in the workspace, and the last block to finish (counted
@@ -24,7 +28,9 @@ constexpr int kFMaxGrid = 1024;  // partials in the workspace
 
 size_t reduce_workspace_bytes() { return kHeaderBytes + round_up(4 * kFMaxGrid, 256); }
 
-template <int OP>
+// NZ: fold (x != 0) instead of x (with OP = add: the count of non-zero
+// elements, the kept count of a compaction).
+template <int OP, bool NZ>
 __global__ void __launch_bounds__(kFThreads, 2)
 reduce_u32_kernel(const uint32_t *__restrict__ data, unsigned long long n, uint32_t *total, WsHeader *hdr,
                   unsigned int *partials) {
@@ -38,10 +44,13 @@ reduce_u32_kernel(const uint32_t *__restrict__ data, unsigned long long n, uint3
     const unsigned long long nv = (n - h) / 4;
     const unsigned long long gtid = (unsigned long long)blockIdx.x * kFThreads + threadIdx.x;
     const unsigned long long gstride = (unsigned long long)gridDim.x * kFThreads;
+    auto val = [](unsigned int x) -> unsigned int { return NZ ? (x != 0u ? 1u : 0u) : x; };
     unsigned int acc = M::identity();
-    if (gtid < h) acc = M::apply(acc, data[gtid]);
+    if (gtid < h) acc = M::apply(acc, val(data[gtid]));
     const uint4 *dv = reinterpret_cast<const uint4 *>(data + h);
-    auto fold4 = [&](const uint4 &q) { acc = M::apply(acc, M::apply(M::apply(q.x, q.y), M::apply(q.z, q.w))); };
+    auto fold4 = [&](const uint4 &q) {
+        acc = M::apply(acc, M::apply(M::apply(val(q.x), val(q.y)), M::apply(val(q.z), val(q.w))));
+    };
     unsigned long long i = gtid;
     for (; i + 3 * gstride < nv; i += 4 * gstride) {
         const uint4 q0 = __ldcs(dv + i), q1 = __ldcs(dv + i + gstride), q2 = __ldcs(dv + i + 2 * gstride),
@@ -52,7 +61,7 @@ reduce_u32_kernel(const uint32_t *__restrict__ data, unsigned long long n, uint3
         fold4(q3);
     }
     for (; i < nv; i += gstride) fold4(__ldcs(dv + i));
-    for (unsigned long long j = h + 4 * nv + gtid; j < n; j += gstride) acc = M::apply(acc, data[j]);
+    for (unsigned long long j = h + 4 * nv + gtid; j < n; j += gstride) acc = M::apply(acc, val(data[j]));
     acc = M::warp_fold(acc);
     if (lane == 0) s_warp[warp] = acc;
     __syncthreads();
@@ -83,7 +92,7 @@ reduce_u32_kernel(const uint32_t *__restrict__ data, unsigned long long n, uint3
 static std::mutex g_red_mu;
 static int g_red_grid[64];
 
-template <int OP>
+template <int OP, bool NZ = false>
 static int reduce_launch(const uint32_t *data, unsigned long long n, uint32_t *total, void *ws, size_t ws_bytes,
                          cudaStream_t stream) {
     if ((n > 0 && data == nullptr) || total == nullptr || n >= (1ull << 62)) return U32SCAN_EINVAL;
@@ -117,7 +126,7 @@ static int reduce_launch(const uint32_t *data, unsigned long long n, uint32_t *t
     if (want < (unsigned long long)grid) grid = want > 0 ? (int)want : 1;
     WsHeader *hdr = static_cast<WsHeader *>(ws);
     unsigned int *partials = reinterpret_cast<unsigned int *>(static_cast<char *>(ws) + kHeaderBytes);
-    reduce_u32_kernel<OP><<<grid, kFThreads, 0, stream>>>(data, n, total, hdr, partials);
+    reduce_u32_kernel<OP, NZ><<<grid, kFThreads, 0, stream>>>(data, n, total, hdr, partials);
     return cudaGetLastError() == cudaSuccess ? U32SCAN_OK : U32SCAN_ECUDA;
 }
 
@@ -138,4 +147,9 @@ extern "C" int reduce_u32_op(int op, const uint32_t *data, size_t n, uint32_t *t
     case kMax: return reduce_launch<kMax>(data, n, total, ws, ws_bytes, s);
     default: return U32SCAN_EINVAL;
     }
+}
+
+extern "C" int count_nonzero_u32(const uint32_t *data, size_t n, uint32_t *count, void *ws, size_t ws_bytes,
+                                 u32scan_stream_t stream) {
+    return reduce_launch<kAdd, true>(data, n, count, ws, ws_bytes, (cudaStream_t)stream);
 }

@@ -119,11 +119,12 @@ def segment_heads_regular(n: int, length: int) -> np.ndarray:
     return flags
 
 
-def compact_flags(n: int, seed: int, p: float) -> np.ndarray:
-    """int32 flags, 1 with probability p (p in COMPACT_THRESHOLD), else 0."""
+def compact_flags(n: int, seed: int, p: float, start: int = 0) -> np.ndarray:
+    """int32 flags, 1 with probability p (p in COMPACT_THRESHOLD), else 0;
+    elements start .. start + n - 1 of the stream."""
     if p not in COMPACT_THRESHOLD:
         raise ValueError(f"p must be one of {sorted(COMPACT_THRESHOLD)}")
-    draw = splitmix_u32(seed, 1, n)
+    draw = splitmix_u32(seed, 1, n, start=start)
     return (draw < np.uint32(COMPACT_THRESHOLD[p])).astype(np.int32)
 
 

@@ -21,6 +21,15 @@ collective of G words and no host round trip. Sums wrap at 2^32 and are
 associative, so the result has the bits of a one-GPU scan of the whole
 array.
 
+The compaction of a sharded flag array (the entelechy `compact` graph)
+composes the same way: every rank counts its kept flags (count_nonzero_u32,
+4 bytes read an element), one all-gather collects the G (count, length)
+pairs, their exclusive scans give rank r the kept elements and the elements
+before its shard, and every rank compacts its shard from those two device
+words (compact_indices_u32_carry: whole-array offsets and kept indices, 12
+bytes an element). The whole array's compacted indices are the ranks'
+kept fronts in rank order.
+
 The composition takes its three local steps from a `steps` object (fold a
 shard, scan the gathered row in place, scan a shard from a carry-in): by
 default this library's kernels on CUDA tensors; the CPU tests pass other
@@ -53,12 +62,19 @@ class KernelSteps:
         fn = api.scan_inclusive_u32_carry if inclusive else api.scan_exclusive_u32_carry
         return fn(shard, carry, workspace=self.workspace)
 
+    def count(self, flags: torch.Tensor) -> torch.Tensor:
+        return api.count_nonzero_u32(flags, workspace=self.workspace)
+
+    def compact_from(self, flags: torch.Tensor, kept_before: torch.Tensor, first_index: torch.Tensor):
+        return api.compact_indices_u32_carry(flags, kept_before, first_index, workspace=self.workspace)
+
 
 def _all_gather(x: torch.Tensor, group) -> torch.Tensor:
-    """The G one-word tensors of the group's ranks, as one row in rank order."""
+    """The group's ranks' copies of the small 1-D tensor x, one after another
+    in rank order, as one row."""
     world = dist.get_world_size(group)
     if dist.get_backend(group) == "nccl":
-        row = torch.empty(world, dtype=x.dtype, device=x.device)
+        row = torch.empty(world * x.numel(), dtype=x.dtype, device=x.device)
         dist.all_gather_into_tensor(row, x, group=group)
         return row
     parts = [torch.empty_like(x) for _ in range(world)]
@@ -85,3 +101,28 @@ def sharded_scan(shard: torch.Tensor, inclusive: bool = False, group=None, steps
     if marks is not None:
         marks[1].record()
     return whole
+
+
+def sharded_compact(flags: torch.Tensor, group=None, steps=None, marks=None):
+    """Compact this rank's shard of int32 flags as its piece of the whole
+    array's compaction. Every rank of `group` calls it. Returns (offsets,
+    indices, count, total): whole-array inclusive offsets for the shard, the
+    shard's kept whole-array indices at the front of `indices` (-1 after
+    them), the shard's kept count, and the whole array's kept count (the same
+    on every rank). The whole array must hold fewer than 2^31 elements.
+    `marks`: an optional pair of CUDA events recorded around the shard's
+    compaction (for timing it)."""
+    steps = KernelSteps() if steps is None else steps
+    rank = dist.get_rank(group)
+    own = steps.count(flags).reshape(1).to(torch.int32)
+    length = torch.full((1,), flags.numel(), dtype=torch.int32, device=flags.device)
+    row = _all_gather(torch.cat([own, length]), group)  # (count, length) of each rank, in rank order
+    counts, lengths = row[0::2].contiguous(), row[1::2].contiguous()
+    total = steps.scan_row(counts)  # counts now hold the kept elements before each rank
+    steps.scan_row(lengths)  # lengths now hold each rank's first whole-array index
+    if marks is not None:
+        marks[0].record()
+    offsets, indices, count = steps.compact_from(flags, counts[rank:rank + 1], lengths[rank:rank + 1])
+    if marks is not None:
+        marks[1].record()
+    return offsets, indices, count, total

@@ -364,12 +364,25 @@ class SegOp(Op):
         ftype = "uint8" if args.u8heads else "int32"
         self.kernel = f"segscan_lanes_persistent<512,{r},{stages},{kind},{ftype},{buf}>"
         self.nseg = None
+        # under torchrun, the segmented scan with int32 flags: rank r scans its
+        # shard of one array of N * n elements
+        self.world, self.rank = getattr(args, "world", 1), getattr(args, "rank", 0)
+        self.sharded = self.world > 1 and mode == "segscan" and not args.u8heads
+        if self.sharded:
+            self.launches_per_step = 6  # scan, summary, carries, first head, fix (+ its init)
 
     def workload(self):
         lengths = "Bernoulli(2^-10) heads" if self.heads == "geometric" else "a head every 4th index"
         ftype = "u8" if self.fbytes == 1 else "int32"
-        return (f"u32 {self.mode} n=2^{self.n.bit_length() - 1}, values uniform u32 seed 3, {ftype} head "
+        lg = self.n.bit_length() - 1
+        if self.sharded:
+            return (f"u32 segmented scan of one array of {self.world} x 2^{lg} elements, values uniform u32 seed 3, "
+                    f"int32 head flags: {lengths}; sharded: rank r holds elements [r 2^{lg}, (r+1) 2^{lg})")
+        return (f"u32 {self.mode} n=2^{lg}, values uniform u32 seed 3, {ftype} head "
                 f"flags: {lengths}")
+
+    def is_marked(self) -> bool:
+        return self.sharded
 
     def algorithmic_bytes(self):
         n, nseg, fb = self.n, self.nseg, self.fbytes
@@ -384,12 +397,13 @@ class SegOp(Op):
 
         from u32_prefix_scan_gb300 import inputs
 
-        f = (inputs.segment_heads_geometric(self.n, 3) if self.heads == "geometric"
-             else inputs.segment_heads_regular(self.n, 4))
+        start = self.rank * self.n if self.sharded else 0
+        f = (inputs.segment_heads_geometric(self.n, 3, start=start) if self.heads == "geometric"
+             else inputs.segment_heads_regular(self.n, 4))  # n is a multiple of 4: every shard alike
         self.nseg = int(np.count_nonzero(f))
         if self.fbytes == 1:
             f = f.astype(np.uint8)
-        return {"data": inputs.scan_values(self.n, 3), "flags": f}
+        return {"data": inputs.splitmix_u32(3, 0, self.n, start=start), "flags": f}
 
     def setup(self, dev, host):
         import numpy as np
@@ -404,6 +418,11 @@ class SegOp(Op):
         self.sums = torch.empty(self.nseg, dtype=torch.int32, device=dev) if self.mode != "segscan" else None
         self.count = torch.empty(1, dtype=torch.int32, device=dev)
         self.ws = u.Workspace(_native.lib().u32scan_workspace_bytes(_native.OP_SEGSCAN, self.n), dev)
+        if self.sharded:
+            from u32_prefix_scan_gb300 import shard
+
+            self.shard = shard
+            self.steps = shard.KernelSteps(workspace=self.ws)
         self.pinned_in = {"data": torch.from_numpy(host["data"].view(np.int32)).pin_memory(),
                           "flags": torch.from_numpy(host["flags"]).pin_memory()}
         self.pinned_out = {"count": torch.empty(1, dtype=torch.int32).pin_memory()}
@@ -413,10 +432,17 @@ class SegOp(Op):
             self.pinned_out["sums"] = torch.empty(self.nseg, dtype=torch.int32).pin_memory()
 
     def step(self):
-        if self.mode == "segreduce":
+        if self.sharded:
+            self.count = self.shard.sharded_segscan(self.data, self.flags, steps=self.steps)
+        elif self.mode == "segreduce":
             self.u.segreduce_u32(self.data, self.flags, self.sums, self.count, workspace=self.ws)
         else:
             self.u.segscan_inclusive_u32(self.data, self.flags, self.sums, self.count, workspace=self.ws)
+
+    def step_marked(self, before, after):
+        """The sharded step with events around the shard's own segmented scan,
+        the kernel that moves its 12 bytes an element."""
+        self.count = self.shard.sharded_segscan(self.data, self.flags, steps=self.steps, marks=(before, after))
 
     def e2e_step(self):
         self.data.copy_(self.pinned_in["data"], non_blocking=True)
@@ -433,6 +459,8 @@ class SegOp(Op):
         return (4 + self.fbytes) * self.n, d2h
 
     def check_e2e(self, host):
+        if self.sharded:  # the whole array's count: at least this shard's heads
+            return int(self.pinned_out["count"][0]) >= self.nseg
         return int(self.pinned_out["count"][0]) == self.nseg
 
     def oracle_step(self, lib, arrays):
@@ -1309,6 +1337,9 @@ def run_ours(args, rank, local_rank, world):
         result["config"]["per_rank"] = (
             f"one shard of one global compaction: count (4 B/elem), all-gather of the {world} (count, length) "
             "pairs over NCCL, compaction from the carry-ins (12 B/elem)" if isinstance(op, CompactOp) else
+            f"one shard of one global segmented scan: its own scan (12 B/elem), all-gather of the {world} "
+            "(head, tail, count) summaries over NCCL, the carry-in added before its first head"
+            if isinstance(op, SegOp) else
             "one shard of one global scan: fold (4 B/elem), all-gather of the "
             f"{world} shard sums over NCCL, scan from the carry-in (8 B/elem)")
     if library is not None:

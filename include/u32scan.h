@@ -288,6 +288,48 @@ int segreduce_u32(const uint32_t *data, const int32_t *head_flags, size_t n,
                   void *ws, size_t ws_bytes, u32scan_stream_t stream);
 
 /*
+ * The segmented scan of one array split into pieces (one per rank, say):
+ * each piece is scanned on its own with segscan_inclusive_u32, then summed
+ * up, the summaries combined in piece order, and each piece fixed from its
+ * carry-in. Source: "Futhark.Pass.ExtractKernels.Segmented"
+ * (regularSegmentedScan) for the operation; the scan.bend source's Driver
+ * (block sums, their scan, each block finished from its base) for the
+ * composition. The segmented operator over a piece is (has a head, the
+ * segmented value at its end); the value flowing into piece r + 1 is piece
+ * r's tail when piece r holds a head, else the value flowing into piece r
+ * plus that tail. Only the elements before a piece's first head depend on
+ * it.
+ *
+ * segscan_piece_summary_u32: one piece's summary, three uint32_t at
+ * `summary` (device): whether the piece holds a head (any non-zero flag,
+ * element 0 included), the scanned value of its last element, and its
+ * segment count as a piece of the whole array (segments that start in it).
+ *   scanned      device, uint32_t[n]: the piece after segscan_inclusive_u32.
+ *   head_flags   device, int32_t[n]: the piece's flags.
+ *   nseg         device, one uint32_t: the count segscan_inclusive_u32 gave.
+ *   first_opens  non-zero for the first piece (its element 0 opens the
+ *                array's first segment), 0 for the others.
+ *   n == 0 gives (0, 0, 0).
+ * segscan_piece_carries_u32: from the g pieces' summaries in piece order
+ * (device, uint32_t[3 g]), each piece's carry-in (device, uint32_t[g]; the
+ * first is 0) and the whole array's segment count (device, one uint32_t, or
+ * NULL).
+ * segscan_fix_u32: adds the carry-in (device, one uint32_t) to the elements
+ * of the scanned piece `data` before its first head (all of them when it
+ * has none); `ws`: any workspace of the library (at least its 256-byte
+ * header), zero-filled once; the call keeps it so.
+ * All three are asynchronous on `stream`. Errors: EINVAL (null pointers the
+ * call needs, misaligned pointers, n >= 2^32), EWORKSPACE, ECUDA.
+ */
+int segscan_piece_summary_u32(const uint32_t *scanned, const int32_t *head_flags, size_t n,
+                              const uint32_t *nseg, int first_opens, uint32_t *summary,
+                              u32scan_stream_t stream);
+int segscan_piece_carries_u32(const uint32_t *summaries, size_t g, uint32_t *carries, uint32_t *nseg_total,
+                              u32scan_stream_t stream);
+int segscan_fix_u32(uint32_t *data, const int32_t *head_flags, size_t n, const uint32_t *carry,
+                    void *ws, size_t ws_bytes, u32scan_stream_t stream);
+
+/*
  * The same two operations with one byte per head flag: a non-zero byte at j
  * opens a segment at j (the entelechy reading of a flag: non-zero is set).
  * Arguments, results, workspace (U32SCAN_OP_SEGSCAN) and errors as in

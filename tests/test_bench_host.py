@@ -126,3 +126,18 @@ def test_compaction_under_several_ranks_is_one_sharded_compaction():
 
     whole = inputs.compact_flags(2 << 10, 4, 0.1)
     assert (op.host_inputs()["flags"] == whole[1 << 10:]).all()
+
+
+def test_segmented_scan_under_several_ranks_is_one_sharded_scan():
+    from u32_prefix_scan_gb300 import inputs
+
+    args = bench.parse_args(["--op", "segscan", "--log2n", "10"])
+    args.world, args.rank = 3, 2
+    op = bench.make_op(args)
+    assert op.sharded and op.is_marked()
+    h = op.host_inputs()
+    whole_f = inputs.segment_heads_geometric(3 << 10, 3)
+    assert (h["flags"] == whole_f[2 << 10:]).all() and (h["data"] == inputs.splitmix_u32(3, 0, 3 << 10)[2 << 10:]).all()
+    args = bench.parse_args(["--op", "segscan_sums"])
+    args.world, args.rank = 2, 0
+    assert not bench.make_op(args).sharded  # only the plain segmented scan shards

@@ -210,3 +210,76 @@ def test_sharded_compaction_on_a_one_rank_nccl_group(u):
         assert int(cnt.item()) == want_cnt == int(total.item())
     finally:
         dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("lg", [6, 16], ids=["short-segments", "long-segments"])
+@pytest.mark.parametrize("cuts", [[70001, 0, (1 << 22) + 9, 123], [(1 << 21) + 1, (1 << 21) + 1, 5]],
+                         ids=["uneven-with-empty", "two-long-one-short"])
+def test_pieces_segscanned_and_fixed_make_the_whole_segmented_scan(u, cuts, lg):
+    """Pieces scanned on their own, summed up, their carries combined and
+    the pieces fixed: the whole array's segmented scan and segment count
+    (long segments leave whole pieces without a head)."""
+    from u32_prefix_scan_gb300.shard import KernelSteps
+
+    n = sum(cuts)
+    a = inputs.splitmix_u32(69, 0, n)
+    f = inputs.segment_heads_geometric(n, 69, log2_mean=lg)
+    steps = KernelSteps()
+    bounds = np.cumsum([0] + cuts)
+    pieces = [dev32(a[bounds[r]:bounds[r + 1]]) for r in range(len(cuts))]
+    flags = [dev32(f[bounds[r]:bounds[r + 1]].view(np.uint32)) for r in range(len(cuts))]
+    summaries = []
+    for r, (p, fl) in enumerate(zip(pieces, flags)):
+        nseg = steps.segscan(p, fl)
+        summaries.append(steps.summary(p, fl, nseg, r == 0))
+    carries, total = steps.carries(torch.cat(summaries))  # the all-gather, emulated
+    for r, (p, fl) in enumerate(zip(pieces, flags)):
+        steps.fix(p, fl, carries[r:r + 1])
+    u.check()
+    got = np.concatenate([host_u32(p) for p in pieces])
+    assert np.array_equal(got, oracle.segscan_inclusive(a, f))
+    assert int(host_u32(total)[0]) == oracle.segreduce(a, f)[1]
+
+
+@pytest.mark.parametrize("first_head", [0, 5, 8191, 8192, 100000, None])
+def test_fix_adds_the_carry_before_the_first_head_only(u, first_head):
+    n = (1 << 20) + 3
+    a = inputs.splitmix_u32(70, 0, n)
+    f = np.zeros(n, np.int32)
+    if first_head is not None:
+        f[first_head] = 1
+        f[first_head + 1000::777] = -3
+    d, fl = dev32(a), dev32(f.view(np.uint32))
+    carry = torch.tensor([0x12345678], dtype=torch.int32, device="cuda")
+    u.segscan_fix_u32(d, fl, carry)
+    u.check()
+    want = a.copy()
+    stop = n if first_head is None else first_head
+    want[:stop] += np.uint32(0x12345678)
+    assert np.array_equal(host_u32(d), want)
+
+
+def test_sharded_segscan_on_a_one_rank_nccl_group(u):
+    import torch.distributed as dist
+
+    from u32_prefix_scan_gb300 import shard
+
+    if dist.is_initialized():
+        pytest.skip("a process group already exists")
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", rank=0, world_size=1)
+    try:
+        n = (1 << 22) + 77
+        a = inputs.splitmix_u32(71, 0, n)
+        f = inputs.segment_heads_geometric(n, 71, log2_mean=10)
+        d = dev32(a)
+        total = shard.sharded_segscan(d, dev32(f.view(np.uint32)))
+        u.check()
+        assert np.array_equal(host_u32(d), oracle.segscan_inclusive(a, f))
+        assert int(host_u32(total)[0]) == oracle.segreduce(a, f)[1]
+    finally:
+        dist.destroy_process_group()

@@ -50,6 +50,37 @@ class OracleSteps:
         shard.copy_(torch.from_numpy((out + c).astype(np.uint32).view(np.int32)))  # wraps mod 2^32
         return torch.from_numpy(np.array([total + c], np.uint64).astype(np.uint32).view(np.int32))
 
+    # the segmented scan's local steps, from their definitions
+    def segscan(self, shard, flags):
+        a, f = _u32(shard).copy(), flags.numpy()
+        shard.copy_(torch.from_numpy(oracle.segscan_inclusive(a, f).view(np.int32)))
+        return torch.tensor([oracle.segreduce(a, f)[1]], dtype=torch.int32)
+
+    def summary(self, shard, flags, nseg, first):
+        f = flags.numpy()
+        if f.size == 0:
+            return torch.zeros(3, dtype=torch.int32)
+        local = int(nseg[0])
+        has_head = int(local > 1 or f[0] != 0)
+        return torch.tensor([has_head, int(_u32(shard)[-1]), local if (first or f[0] != 0) else local - 1],
+                            dtype=torch.int64).to(torch.int32)
+
+    def carries(self, row):
+        r = _u32(row).reshape(-1, 3).astype(np.uint64)
+        c, out = 0, []
+        for has_head, tail, _ in r:
+            out.append(c)
+            c = int(tail) if has_head else (c + int(tail)) % (1 << 32)
+        return (torch.from_numpy(np.array(out, np.uint32).view(np.int32)),
+                torch.tensor([int(r[:, 2].sum())], dtype=torch.int32))
+
+    def fix(self, shard, flags, carry):
+        f = flags.numpy()
+        first = int(np.flatnonzero(f)[0]) if np.any(f) else f.size
+        a = _u32(shard).copy()
+        a[:first] += _u32(carry)[0]  # wraps mod 2^32
+        shard.copy_(torch.from_numpy(a.view(np.int32)))
+
     def count(self, flags):
         return torch.tensor([oracle.compact_indices(flags.numpy())[2]], dtype=torch.int32)
 
@@ -152,3 +183,47 @@ def test_two_gloo_ranks_compose_the_whole_compaction(tmp_path, case):
     for r in range(world):
         assert (np.load(tmp_path / f"tail{r}.npy") == -1).all()
         assert json.loads((tmp_path / f"c{r}.json").read_text())["total"] == want_count
+
+
+SEG_CASES = {
+    "geometric": (100003, [40000, 60003], 6),
+    "long_segments": (60001, [1000, 29000, 30001], 14),  # shards with no head at all
+    "empty_middle": (7001, [3000, 0, 4001], 4),
+}
+
+
+def _seg_rank_main(rank, world, port, out_dir, case):
+    import torch.distributed as dist
+
+    from u32_prefix_scan_gb300 import shard as sh
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        n, cuts, lg = SEG_CASES[case]
+        a = inputs.splitmix_u32(79, 0, n)
+        f = inputs.segment_heads_geometric(n, 79, log2_mean=lg)
+        lo = sum(cuts[:rank])
+        piece = torch.from_numpy(a[lo:lo + cuts[rank]].view(np.int32).copy())
+        flags = torch.from_numpy(f[lo:lo + cuts[rank]].copy())
+        total = sh.sharded_segscan(piece, flags, steps=OracleSteps())
+        np.save(os.path.join(out_dir, f"s{rank}.npy"), _u32(piece))
+        with open(os.path.join(out_dir, f"s{rank}.json"), "w") as fh:
+            json.dump({"nseg": int(total[0])}, fh)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("case", sorted(SEG_CASES))
+def test_gloo_ranks_compose_the_whole_segmented_scan(tmp_path, case):
+    import torch.multiprocessing as mp
+
+    n, cuts, lg = SEG_CASES[case]
+    world = len(cuts)
+    mp.spawn(_seg_rank_main, args=(world, free_port(), str(tmp_path), case), nprocs=world, join=True)
+    a = inputs.splitmix_u32(79, 0, n)
+    f = inputs.segment_heads_geometric(n, 79, log2_mean=lg)
+    got = np.concatenate([np.load(tmp_path / f"s{r}.npy") for r in range(world)])
+    assert np.array_equal(got, oracle.segscan_inclusive(a, f))
+    for r in range(world):
+        assert json.loads((tmp_path / f"s{r}.json").read_text())["nseg"] == oracle.segreduce(a, f)[1]

@@ -14,6 +14,9 @@ _API = {
     "scan_inclusive_u32_carry",
     "reduce_u32_op",
     "count_nonzero_u32",
+    "segscan_piece_summary_u32",
+    "segscan_piece_carries_u32",
+    "segscan_fix_u32",
     "compact_indices_u32_carry",
     "scan_exclusive_u32_host",
     "scan_inclusive_u32_host",

@@ -46,6 +46,9 @@ SIGNATURES = {
     "scan_inclusive_u32_carry": (_int, [_vp, _sz, _vp, _vp, _vp, _sz, _vp]),
     "reduce_u32_op": (_int, [_int, _vp, _sz, _vp, _vp, _sz, _vp]),
     "count_nonzero_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
+    "segscan_piece_summary_u32": (_int, [_vp, _vp, _sz, _vp, _int, _vp, _vp]),
+    "segscan_piece_carries_u32": (_int, [_vp, _sz, _vp, _vp, _vp]),
+    "segscan_fix_u32": (_int, [_vp, _vp, _sz, _vp, _vp, _sz, _vp]),
     "compact_indices_u32_carry": (_int, [_vp, _sz, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "scan_exclusive_u32_host": (_int, [_vp, _vp, _sz, _vp, _vp, _sz, _vp]),
     "scan_inclusive_u32_host": (_int, [_vp, _vp, _sz, _vp, _vp, _sz, _vp]),

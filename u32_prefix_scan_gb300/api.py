@@ -25,6 +25,9 @@ __all__ = [
     "scan_inclusive_u32_carry",
     "reduce_u32_op",
     "count_nonzero_u32",
+    "segscan_piece_summary_u32",
+    "segscan_piece_carries_u32",
+    "segscan_fix_u32",
     "compact_indices_u32_carry",
     "scan_exclusive_u32_host",
     "scan_inclusive_u32_host",
@@ -377,6 +380,61 @@ def compact_indices_u32_carry(flags: torch.Tensor, kept_before: torch.Tensor | N
         first_index.data_ptr() if first_index is not None else None, offsets.data_ptr(), indices.data_ptr(),
         count.data_ptr(), ws.ptr, ws.nbytes, sh), "compact_indices_u32_carry")
     return offsets, indices, count
+
+
+def segscan_piece_summary_u32(scanned: torch.Tensor, head_flags: torch.Tensor, nseg: torch.Tensor,
+                              first_opens: bool, summary: torch.Tensor | None = None, *,
+                              stream=None) -> torch.Tensor:
+    """A piece's summary after segscan_inclusive_u32: (has head, tail,
+    segments starting in it), three words in a device tensor."""
+    _require_cuda(scanned, "scanned")
+    _require_cuda(head_flags, "head_flags", (torch.int32,))
+    _require_cuda(nseg, "nseg")
+    if head_flags.numel() != scanned.numel():
+        raise ValueError("head_flags must have as many elements as scanned")
+    if summary is None:
+        summary = torch.empty(3, dtype=torch.int32, device=scanned.device)
+    _require_cuda(summary, "summary")
+    if summary.numel() < 3:
+        raise ValueError("summary must hold three elements")
+    _native.check(_native.lib().segscan_piece_summary_u32(
+        scanned.data_ptr(), head_flags.data_ptr(), scanned.numel(), nseg.data_ptr(), int(bool(first_opens)),
+        summary.data_ptr(), _stream_handle(stream)), "segscan_piece_summary_u32")
+    return summary
+
+
+def segscan_piece_carries_u32(summaries: torch.Tensor, carries: torch.Tensor | None = None,
+                              nseg_total: torch.Tensor | None = None, *, stream=None):
+    """From g pieces' summaries (3 g words, in piece order): each piece's
+    carry-in and the whole array's segment count (device tensors)."""
+    _require_cuda(summaries, "summaries")
+    if summaries.numel() % 3:
+        raise ValueError("summaries must hold three words a piece")
+    g = summaries.numel() // 3
+    if carries is None:
+        carries = torch.empty(g, dtype=torch.int32, device=summaries.device)
+    _require_cuda(carries, "carries")
+    nseg_total = _scalar_out(nseg_total, summaries, torch.int32)
+    _native.check(_native.lib().segscan_piece_carries_u32(summaries.data_ptr(), g, carries.data_ptr(),
+                                                          nseg_total.data_ptr(), _stream_handle(stream)),
+                  "segscan_piece_carries_u32")
+    return carries, nseg_total
+
+
+def segscan_fix_u32(data: torch.Tensor, head_flags: torch.Tensor, carry: torch.Tensor, *, stream=None,
+                    workspace: Workspace | None = None) -> torch.Tensor:
+    """Adds carry (one-element device tensor) to the elements of the scanned
+    piece before its first head. Returns data."""
+    _require_cuda(data, "data")
+    _require_cuda(head_flags, "head_flags", (torch.int32,))
+    _require_cuda(carry, "carry")
+    if head_flags.numel() != data.numel():
+        raise ValueError("head_flags must have as many elements as data")
+    sh = _stream_handle(stream)
+    ws = _ws(_native.OP_REDUCE, data.numel(), data.device, sh, workspace)
+    _native.check(_native.lib().segscan_fix_u32(data.data_ptr(), head_flags.data_ptr(), data.numel(),
+                                                carry.data_ptr(), ws.ptr, ws.nbytes, sh), "segscan_fix_u32")
+    return data
 
 
 def count_nonzero_u32(data: torch.Tensor, count: torch.Tensor | None = None, *, stream=None,

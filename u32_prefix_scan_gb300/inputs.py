@@ -103,11 +103,13 @@ def scan_values(n: int, seed: int, small: bool = False) -> np.ndarray:
     return v
 
 
-def segment_heads_geometric(n: int, seed: int, log2_mean: int = 10) -> np.ndarray:
-    """int32 head flags, Bernoulli(2^-log2_mean); index 0 always a head."""
-    draw = splitmix_u32(seed, 1, n)
+def segment_heads_geometric(n: int, seed: int, log2_mean: int = 10, start: int = 0) -> np.ndarray:
+    """int32 head flags, Bernoulli(2^-log2_mean); index 0 always a head.
+    Elements start .. start + n - 1 of that array (index 0 only when start
+    is 0)."""
+    draw = splitmix_u32(seed, 1, n, start=start)
     flags = (draw < np.uint32(1 << (32 - log2_mean))).astype(np.int32)
-    if n:
+    if n and start == 0:
         flags[0] = 1
     return flags
 

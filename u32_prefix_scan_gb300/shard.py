@@ -30,6 +30,15 @@ words (compact_indices_u32_carry: whole-array offsets and kept indices, 12
 bytes an element). The whole array's compacted indices are the ranks'
 kept fronts in rank order.
 
+The segmented scan of a sharded array ("Futhark.Pass.ExtractKernels.
+Segmented", regularSegmentedScan) scans first and fixes after: every rank
+scans its shard on its own (segscan_inclusive_u32, 12 bytes an element),
+sums it up as (holds a head, scanned value at its end, segments starting in
+it), one all-gather collects the G summaries, their segmented exclusive
+scan gives each rank its carry-in, and the fix adds the carry-in to the
+shard's elements before its first head (usually a short run; all of the
+shard when it holds no head).
+
 The composition takes its three local steps from a `steps` object (fold a
 shard, scan the gathered row in place, scan a shard from a carry-in): by
 default this library's kernels on CUDA tensors; the CPU tests pass other
@@ -61,6 +70,18 @@ class KernelSteps:
     def scan_from(self, shard: torch.Tensor, carry: torch.Tensor, inclusive: bool) -> torch.Tensor:
         fn = api.scan_inclusive_u32_carry if inclusive else api.scan_exclusive_u32_carry
         return fn(shard, carry, workspace=self.workspace)
+
+    def segscan(self, shard: torch.Tensor, flags: torch.Tensor) -> torch.Tensor:
+        return api.segscan_inclusive_u32(shard, flags, workspace=self.workspace)
+
+    def summary(self, shard: torch.Tensor, flags: torch.Tensor, nseg: torch.Tensor, first: bool) -> torch.Tensor:
+        return api.segscan_piece_summary_u32(shard, flags, nseg, first)
+
+    def carries(self, summaries: torch.Tensor):
+        return api.segscan_piece_carries_u32(summaries)
+
+    def fix(self, shard: torch.Tensor, flags: torch.Tensor, carry: torch.Tensor) -> None:
+        api.segscan_fix_u32(shard, flags, carry, workspace=self.workspace)
 
     def count(self, flags: torch.Tensor) -> torch.Tensor:
         return api.count_nonzero_u32(flags, workspace=self.workspace)
@@ -126,3 +147,25 @@ def sharded_compact(flags: torch.Tensor, group=None, steps=None, marks=None):
     if marks is not None:
         marks[1].record()
     return offsets, indices, count, total
+
+
+def sharded_segscan(shard: torch.Tensor, head_flags: torch.Tensor, group=None, steps=None,
+                    marks=None) -> torch.Tensor:
+    """Segmented inclusive scan of this rank's shard, in place, as its piece
+    of the whole array's (a non-zero flag opens a segment; the whole array's
+    element 0 opens one). Every rank of `group` calls it. Returns the whole
+    array's segment count (one-element tensor), the same on every rank.
+    `marks`: an optional pair of CUDA events recorded around the shard's own
+    segmented scan (for timing it)."""
+    steps = KernelSteps() if steps is None else steps
+    rank = dist.get_rank(group)
+    if marks is not None:
+        marks[0].record()
+    nseg = steps.segscan(shard, head_flags)
+    if marks is not None:
+        marks[1].record()
+    own = steps.summary(shard, head_flags, nseg, rank == 0).reshape(3)
+    row = _all_gather(own, group)  # the G summaries, in rank order
+    carries, total = steps.carries(row)
+    steps.fix(shard, head_flags, carries[rank:rank + 1])
+    return total

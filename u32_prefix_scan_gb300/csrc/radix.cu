@@ -27,16 +27,16 @@
 // for radix_sort_u32, the sorted keys into `keys_out`; a keys-only sort moves
 // no indices at all.
 //
-// Ranking. For the 32 keys of one warp round (one per lane), eight ballots,
-// one per digit bit, give each lane the mask of lanes holding its digit
-// value; the lowest lane of each value adds the value's count to the warp's
-// running counter for it (one shared atomic add, whose old value is
-// broadcast to the value's lanes), and a lane's rank is that old value plus
-// the lanes below it in the mask. So a round costs one shared-memory access
-// per distinct digit value; the shared tables a round reads and writes at
-// random digit values (and their bank conflicts) are what bound a pass
-// otherwise. Each block asks L2 for the keys and indices of the tile drawn
-// one resident grid later.
+// Ranking. For the 32 keys of one warp round (one per lane), a per-warp
+// table of lane masks, one word per digit value, gives each lane the mask of
+// lanes holding its digit value (each lane ORs its bit into its value's word
+// and reads the word back); the lowest lane of each value adds the value's
+// count to the warp's running counter for it (one shared atomic add, whose
+// old value is broadcast to the value's lanes) and clears the word, and a
+// lane's rank is that old value plus the lanes below it in the mask. A round
+// thus costs a few shared-memory accesses and little ALU work, which bounded
+// the pass when the masks came from ballots. Each block asks L2 for the keys
+// and indices of the tile drawn one resident grid later.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -63,6 +63,7 @@ constexpr unsigned int kRTile = kRThreads * kRKeys;
 constexpr int kRWarps = kRThreads / 32;
 constexpr unsigned int kRWarpKeys = 32 * kRKeys;  // a warp's run of the tile
 static_assert(kRThreads >= 256 && kRThreads % 32 == 0 && kRKeys <= 32, "a thread per digit value; key bits fit a word");
+static_assert(kRKeys >= 8, "the warps' match tables fit in the tile-ordered key buffer");
 #ifndef U32SCAN_R_LOOK
 #define U32SCAN_R_LOOK 8
 #endif
@@ -239,31 +240,24 @@ __device__ __forceinline__ PassBuffers pass_buffers(const RadixPlan &pl, const u
     return b;
 }
 
-// The lanes of this warp round whose key has digit value d (all lanes call
-// it; an invalid lane takes part in no mask and gets 0).
-// (Eight ballots measured faster than the match-any instruction.)
-template <bool FULL>
-__device__ __forceinline__ unsigned int radix_same_digit(unsigned int d, bool valid) {
-    unsigned int same = FULL ? 0xffffffffu : __ballot_sync(0xffffffffu, valid);
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-        const unsigned int bit = (d >> b) & 1u;
-        const unsigned int bb = __ballot_sync(0xffffffffu, bit != 0u);
-        same &= bb ^ (bit - 1u);  // the ballot where the bit is set, its complement where clear
-    }
-    return (FULL || valid) ? same : 0u;
-}
-
 // Load this thread's keys of tile t (warp-striped: round r of warp w covers
 // the 32 consecutive keys at t * kRTile + w * kRWarpKeys + 32 r) and rank
 // them stably within the warp: afterwards wrank[r] is the key's rank among
 // the warp's keys of its digit value (in tile order) and s_wcnt[v] the
 // warp's count of value v. FULL: every key of the tile lies in the array.
+//
+// A round finds the lanes holding each digit value through the warp's match
+// table s_wmatch[256] (zero between rounds): every lane ORs its lane bit
+// into the word of its value and reads the word back, so it holds the mask
+// of lanes sharing its value; the value's lowest lane then adds the count
+// to the warp's counter and clears the word. (Eight ballots, one per digit
+// bit, folded in every lane, measured slower: the fold costs about five ALU
+// instructions a bit, and the pass was bound by the ALU pipe.)
 template <bool FULL>
 __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restrict__ in_keys, unsigned int n32,
                                                         unsigned int wbase, int shift, uint32_t (&k)[kRKeys],
                                                         unsigned int (&wrank)[kRKeys], unsigned int *s_wcnt,
-                                                        int lane) {
+                                                        unsigned int *s_wmatch, int lane) {
     unsigned int valid_bits = FULL ? 0xffffffffu : 0u;
 #pragma unroll
     for (int r = 0; r < kRKeys; ++r) {
@@ -275,19 +269,29 @@ __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restri
             valid_bits |= (e < n32 ? 1u : 0u) << r;
         }
     }
-    for (int i = lane; i < 256; i += 32) s_wcnt[i] = 0;
+    for (int i = lane; i < 256; i += 32) {
+        s_wcnt[i] = 0;
+        s_wmatch[i] = 0;
+    }
     __syncwarp();
+    const unsigned int lanebit = 1u << lane;
 #pragma unroll
     for (int r = 0; r < kRKeys; ++r) {
         const bool valid = FULL || ((valid_bits >> r) & 1u);
         const unsigned int d = (k[r] >> shift) & 255u;
-        const unsigned int same = radix_same_digit<FULL>(d, valid);
+        if (valid) atomicOr(s_wmatch + d, lanebit);
+        __syncwarp();  // every lane's bit is in before any lane reads
+        const unsigned int same = valid ? s_wmatch[d] : 0u;
+        __syncwarp();  // every lane has read before a leader clears
         const unsigned int below = (unsigned int)__popc(same & lanemask_lt(lane));
         unsigned int old = 0;
-        if (valid && below == 0) old = atomicAdd(s_wcnt + d, (unsigned int)__popc(same));
+        if (valid && below == 0) {
+            old = atomicAdd(s_wcnt + d, (unsigned int)__popc(same));
+            s_wmatch[d] = 0u;
+        }
         const int leader = same ? __ffs(same) - 1 : 0;
         wrank[r] = __shfl_sync(0xffffffffu, old, leader) + below;
-        __syncwarp();  // orders this round's counter updates before the next round's
+        __syncwarp();  // this round's counter updates and clears before the next round
     }
     return valid_bits;
 }
@@ -355,8 +359,11 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     const unsigned int wbase = tile0 + (unsigned int)warp * kRWarpKeys;
     uint32_t k[kRKeys];
     unsigned int wrank[kRKeys];
-    const unsigned int valid_bits = full ? radix_rank_tile<true>(b.in_keys, n32, wbase, shift, k, wrank, s_cnt[warp], lane)
-                                         : radix_rank_tile<false>(b.in_keys, n32, wbase, shift, k, wrank, s_cnt[warp], lane);
+    // the warps' match tables live where the tile-ordered keys go later
+    unsigned int *s_wmatch = s_keys + 256 * warp;
+    const unsigned int valid_bits =
+        full ? radix_rank_tile<true>(b.in_keys, n32, wbase, shift, k, wrank, s_cnt[warp], s_wmatch, lane)
+             : radix_rank_tile<false>(b.in_keys, n32, wbase, shift, k, wrank, s_cnt[warp], s_wmatch, lane);
     __syncthreads();
     // Per digit value v (threads 0..255): warp offsets within the value's
     // run in this tile and the run's length, published at once.

@@ -56,7 +56,10 @@ def check_perm(u, keys):
     assert np.array_equal(d.cpu().numpy().view(np.uint32), keys)  # keys untouched
 
 
-SIZES = [1, 2, 3, 100, 8191, 8192, 8193, 3 * 8192 + 77, 100003, (1 << 20) + 5]
+# A digit pass takes tiles of 11264 keys (512 threads x 22); sizes around
+# one and several tiles, and around 8192 (the tile of the 16-key shape).
+TILE = 512 * 22
+SIZES = [1, 2, 3, 100, 8191, 8192, 8193, TILE - 1, TILE, TILE + 1, 3 * TILE + 77, 100003, (1 << 20) + 5]
 
 
 @pytest.mark.parametrize("kind", ["uniform", "ties256", "ties65536", "equal", "top_digit", "two_values",

@@ -52,7 +52,7 @@ namespace u32scan {
 #define U32SCAN_R_THREADS 512
 #endif
 #ifndef U32SCAN_R_KEYS
-#define U32SCAN_R_KEYS 16
+#define U32SCAN_R_KEYS 22
 #endif
 #ifndef U32SCAN_R_MINB
 #define U32SCAN_R_MINB 2
@@ -71,6 +71,12 @@ constexpr int kRLook = U32SCAN_R_LOOK;  // earlier tiles read per look-back roun
 // 1: each block asks L2 for the tile one resident grid ahead.
 #ifndef U32SCAN_R_PREFETCH
 #define U32SCAN_R_PREFETCH 1
+#endif
+// Digit bits resolved by the match table (the rest by ballots): 2^TBITS
+// words a warp; 7 measured 1 % faster than 8 (fewer bank conflicts on the
+// table for one ballot), 4 to 6 slower.
+#ifndef U32SCAN_R_TBITS
+#define U32SCAN_R_TBITS 7
 #endif
 // One pass's role, decided on the device from the histograms.
 struct RadixPlan {
@@ -240,9 +246,20 @@ __device__ __forceinline__ PassBuffers pass_buffers(const RadixPlan &pl, const u
     return b;
 }
 
+// A thread's ranks (later tile positions), two 16-bit halves a word: both
+// lie below the tile size. Halves are read and written by byte permutes.
+constexpr int kRWords = (kRKeys + 1) / 2;
+static_assert(kRTile <= 65536, "a tile position fits 16 bits");
+__device__ __forceinline__ unsigned int rank_get(const unsigned int (&w)[kRWords], int r) {
+    return (r & 1) ? (w[r >> 1] >> 16) : (w[r >> 1] & 0xffffu);
+}
+__device__ __forceinline__ void rank_set(unsigned int (&w)[kRWords], int r, unsigned int x) {
+    w[r >> 1] = (r & 1) ? __byte_perm(w[r >> 1], x, 0x5410) : __byte_perm(w[r >> 1], x, 0x3254);
+}
+
 // Load this thread's keys of tile t (warp-striped: round r of warp w covers
 // the 32 consecutive keys at t * kRTile + w * kRWarpKeys + 32 r) and rank
-// them stably within the warp: afterwards wrank[r] is the key's rank among
+// them stably within the warp: afterwards rank r of wrank is the key's rank among
 // the warp's keys of its digit value (in tile order) and s_wcnt[v] the
 // warp's count of value v. FULL: every key of the tile lies in the array.
 //
@@ -256,7 +273,7 @@ __device__ __forceinline__ PassBuffers pass_buffers(const RadixPlan &pl, const u
 template <bool FULL>
 __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restrict__ in_keys, unsigned int n32,
                                                         unsigned int wbase, int shift, uint32_t (&k)[kRKeys],
-                                                        unsigned int (&wrank)[kRKeys], unsigned int *s_wcnt,
+                                                        unsigned int (&wrank)[kRWords], unsigned int *s_wcnt,
                                                         unsigned int *s_wmatch, int lane) {
     unsigned int valid_bits = FULL ? 0xffffffffu : 0u;
 #pragma unroll
@@ -279,18 +296,29 @@ __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restri
     for (int r = 0; r < kRKeys; ++r) {
         const bool valid = FULL || ((valid_bits >> r) & 1u);
         const unsigned int d = (k[r] >> shift) & 255u;
-        if (valid) atomicOr(s_wmatch + d, lanebit);
+        const unsigned int te = d & ((1u << U32SCAN_R_TBITS) - 1u);
+        if (valid) atomicOr(s_wmatch + te, lanebit);
+        unsigned int hi = 0xffffffffu;
+#pragma unroll
+        for (int b = U32SCAN_R_TBITS; b < 8; ++b) {
+            const unsigned int bit = (d >> b) & 1u;
+            hi &= __ballot_sync(0xffffffffu, bit != 0u) ^ (bit - 1u);
+        }
         __syncwarp();  // every lane's bit is in before any lane reads
-        const unsigned int same = valid ? s_wmatch[d] : 0u;
+        const unsigned int same = valid ? (s_wmatch[te] & hi) : 0u;
         __syncwarp();  // every lane has read before a leader clears
         const unsigned int below = (unsigned int)__popc(same & lanemask_lt(lane));
         unsigned int old = 0;
         if (valid && below == 0) {
             old = atomicAdd(s_wcnt + d, (unsigned int)__popc(same));
-            s_wmatch[d] = 0u;
+            s_wmatch[te] = 0u;
         }
         const int leader = same ? __ffs(same) - 1 : 0;
-        wrank[r] = __shfl_sync(0xffffffffu, old, leader) + below;
+        const unsigned int rk = __shfl_sync(0xffffffffu, old, leader) + below;
+        if (r & 1)
+            rank_set(wrank, r, rk);
+        else
+            wrank[r >> 1] = rk;  // the odd half is written next round
         __syncwarp();  // this round's counter updates and clears before the next round
     }
     return valid_bits;
@@ -358,7 +386,7 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     const bool full = n32 - tile0 >= kRTile;
     const unsigned int wbase = tile0 + (unsigned int)warp * kRWarpKeys;
     uint32_t k[kRKeys];
-    unsigned int wrank[kRKeys];
+    unsigned int wrank[kRWords];
     // the warps' match tables live where the tile-ordered keys go later
     unsigned int *s_wmatch = s_keys + 256 * warp;
     const unsigned int valid_bits =
@@ -394,7 +422,7 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
         for (int w = 0; w < kRWarps; ++w) s_cnt[w][threadIdx.x] += start;
     }
     __syncthreads();
-    // Order the keys by digit value in shared memory; wrank becomes each
+    // Order the keys by digit value in shared memory; the ranks become each
     // key's position in the tile-ordered buffer. Then the indices: read from
     // the previous pass's buffer (all sixteen loads first, then the stores:
     // a load and its store taken in turn measured 16 % slower), or the
@@ -403,8 +431,9 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     for (int r = 0; r < kRKeys; ++r) {
         if (full || ((valid_bits >> r) & 1u)) {
             const unsigned int v = (k[r] >> shift) & 255u;
-            wrank[r] += s_cnt[warp][v];
-            s_keys[wrank[r]] = k[r];
+            const unsigned int pos = rank_get(wrank, r) + s_cnt[warp][v];
+            rank_set(wrank, r, pos);
+            s_keys[pos] = k[r];
         }
     }
     if (b.out_idx) {
@@ -416,7 +445,7 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
         }
 #pragma unroll
         for (int r = 0; r < kRKeys; ++r)
-            if (full || ((valid_bits >> r) & 1u)) s_idx[wrank[r]] = idx[r];
+            if (full || ((valid_bits >> r) & 1u)) s_idx[rank_get(wrank, r)] = idx[r];
     }
     // Look back (threads 0..255, value v): the count of v in all earlier
     // tiles. Window word j holds tile pos - j (a virtual inclusive zero

@@ -140,8 +140,8 @@ radix_histogram_kernel(const uint32_t *__restrict__ keys, unsigned long long n, 
         add(q.z);
         add(q.w);
     };
-    // scalar head up to 16-byte alignment, 16-byte body (four loads in
-    // flight a thread), scalar tail; n < 2^31 for a radix sort, so 32-bit
+    // scalar head up to 16-byte alignment, 16-byte body (four to eight loads
+    // in flight a thread), scalar tail; n < 2^31 for a radix sort, so 32-bit
     // indices suffice
     const unsigned int n32 = (unsigned int)n;
     const unsigned int head = (unsigned int)((16 - (reinterpret_cast<uintptr_t>(keys) & 15)) & 15) / 4;
@@ -152,9 +152,23 @@ radix_histogram_kernel(const uint32_t *__restrict__ keys, unsigned long long n, 
     if (gtid < h) add(keys[gtid]);
     const uint4 *kv = reinterpret_cast<const uint4 *>(keys + h);
     unsigned int i = gtid;
-    for (; i + 3 * gstride < nv; i += 4 * gstride) {
-        const uint4 q0 = __ldcs(kv + i), q1 = __ldcs(kv + i + gstride), q2 = __ldcs(kv + i + 2 * gstride),
-                    q3 = __ldcs(kv + i + 3 * gstride);
+    // software-pipelined: the next four loads are issued before the current
+    // four are counted, so loads stay in flight through the atomics
+    if (i + 3 * gstride < nv) {
+        uint4 q0 = __ldcs(kv + i), q1 = __ldcs(kv + i + gstride), q2 = __ldcs(kv + i + 2 * gstride),
+              q3 = __ldcs(kv + i + 3 * gstride);
+        for (i += 4 * gstride; i + 3 * gstride < nv; i += 4 * gstride) {
+            const uint4 n0 = __ldcs(kv + i), n1 = __ldcs(kv + i + gstride), n2 = __ldcs(kv + i + 2 * gstride),
+                        n3 = __ldcs(kv + i + 3 * gstride);
+            add4(q0);
+            add4(q1);
+            add4(q2);
+            add4(q3);
+            q0 = n0;
+            q1 = n1;
+            q2 = n2;
+            q3 = n3;
+        }
         add4(q0);
         add4(q1);
         add4(q2);

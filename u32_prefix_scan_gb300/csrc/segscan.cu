@@ -23,9 +23,11 @@
 // the next tile and publishes its aggregate, then walks the current tile's
 // look-back, adds the carry and stores. Per tile the look-back carries two
 // words (internal.cuh): the segmented value and the running head count; the
-// head count gives every segment end its index into the sums. The forms
-// without sums need no such index: they walk the value alone, and count
-// the segments with one atomic add a tile.
+// head count gives every segment end its index into the sums. Warp 0 walks
+// the value and warp 1 the head count, so the two walks overlap (one warp
+// walking both, the value first, measured 3 % slower for the scan with
+// sums). The forms without sums need no such index: they walk the value
+// alone, and count the segments with one atomic add a tile.
 //
 // Layout inside a tile (lane runs): lane l of warp w owns the E = 4R
 // consecutive elements at w * 32E + l * E of the tile (R u32x4, R odd: a
@@ -436,10 +438,12 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
     unsigned int tc = read_tile(0, Lc);
     unsigned int nh_c = 0, nh_n = 0;
     if (WANT_SUMS && threadIdx.x == 0 && tc < n_tiles) nh_c = head_after(tc);
-    // warp 0 keeps, per lane w < WARPS, what the look-back needs for the
-    // current tile: the tile aggregate and warp w's exclusive offsets
+    // The walking warps keep, per lane w < WARPS, what the look-back needs
+    // for the current tile: the tile aggregate and warp w's exclusive
+    // offsets (warp 0 the value's, the count's warp the head count's).
     unsigned int agg_val = 0, agg_cnt = 0, wex_val = 0, wex_cnt = 0;
     bool agg_head = false, head_before = false;
+    // Both aggregates in warp 0 (the forms counting segments by atomic add).
     auto block_aggregate = [&](int slot, unsigned int t, unsigned int &a_val, bool &a_head, unsigned int &a_cnt,
                                unsigned int &x_val, bool &h_before, unsigned int &x_cnt) {
         const unsigned int wv = lane < WARPS ? s_wval[slot][lane] : 0u;
@@ -455,11 +459,32 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
         if (lane == 0) x_val = 0;
         h_before = (hm & lanemask_lt(lane)) != 0;
         x_cnt = cw - wcn;
-        if (lane == 0 && t != skip_tile) {
-            // a tile holding a head knows its segmented carry at once
+        if (lane == 0 && t != skip_tile)  // a tile holding a head knows its segmented carry at once
             st_relaxed(desc2 + 2ull * t, tag | (a_head || t == 0 ? (kFlagH | kFlagP) : 0ull) | a_val);
-            if (!ATOM_COUNT) st_relaxed(desc2 + 2ull * t + 1, tag | (t == 0 ? kFlagP : 0ull) | a_cnt);
-        }
+    };
+    // With a walked head count (the forms with sums), warp 0 takes the
+    // segmented value and warp 1 the head count, each its own aggregate and
+    // look-back, so that the two walks overlap.
+    auto value_aggregate = [&](int slot, unsigned int t, unsigned int &a_val, bool &a_head, unsigned int &x_val,
+                               bool &h_before) {
+        const unsigned int wv = lane < WARPS ? s_wval[slot][lane] : 0u;
+        const bool wh = lane < WARPS ? s_whas[slot][lane] != 0 : false;
+        const unsigned int sw = warp_segmented_inclusive(wv, wh, 0u, lane);
+        const unsigned int hm = __ballot_sync(0xffffffffu, wh);
+        a_val = __shfl_sync(0xffffffffu, sw, 31);
+        a_head = hm != 0;
+        x_val = __shfl_up_sync(0xffffffffu, sw, 1);
+        if (lane == 0) x_val = 0;
+        h_before = (hm & lanemask_lt(lane)) != 0;
+        if (lane == 0 && t != skip_tile)
+            st_relaxed(desc2 + 2ull * t, tag | (a_head || t == 0 ? (kFlagH | kFlagP) : 0ull) | a_val);
+    };
+    auto count_aggregate = [&](int slot, unsigned int t, unsigned int &a_cnt, unsigned int &x_cnt) {
+        const unsigned int wcn = lane < WARPS ? s_wcnt[slot][lane] : 0u;
+        const unsigned int cw = warp_inclusive_sum(wcn, lane);
+        a_cnt = __shfl_sync(0xffffffffu, cw, 31);
+        x_cnt = cw - wcn;
+        if (lane == 0 && t != skip_tile) st_relaxed(desc2 + 2ull * t + 1, tag | (t == 0 ? kFlagP : 0ull) | a_cnt);
     };
 
     if (!__syncthreads_or(tc >= n_tiles)) {
@@ -468,7 +493,12 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
             issue(0);
             latest_parity ^= 1u;
         }
-        if (warp == 0) block_aggregate(0, tc, agg_val, agg_head, agg_cnt, wex_val, head_before, wex_cnt);
+        if constexpr (ATOM_COUNT) {
+            if (warp == 0) block_aggregate(0, tc, agg_val, agg_head, agg_cnt, wex_val, head_before, wex_cnt);
+        } else {
+            if (warp == 0) value_aggregate(0, tc, agg_val, agg_head, wex_val, head_before);
+            if (warp == 1) count_aggregate(0, tc, agg_cnt, wex_cnt);
+        }
         for (unsigned int u = 1;; ++u) {
             const unsigned int tn = read_tile(u, Ln);
             const bool more = !__syncthreads_or(tn >= n_tiles);  // barrier A
@@ -481,35 +511,49 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
                 issue(st);
                 latest_parity ^= 1u << st;
             }
-            if (warp == 0) {
+            if (!ATOM_COUNT && warp == 0) {
+                // the segmented value, walked while warp 1 walks the head count
+                if (more) value_aggregate((int)(u & 1u), tn, n_val, n_head, n_xval, n_before);
+                unsigned int seg = 0;
+                if (tc != 0) {
+                    unsigned long long wa[U32SCAN_S_LOOKA];
+                    lookback_window<U32SCAN_S_LOOKA, kAdd, 2>(desc2, (long long)tc - 1, tag, lane, wa);
+                    seg = lookback_prefix_wide<U32SCAN_S_LOOKA, kAdd, 2, kFlagP | kFlagH>(desc2, tc, tag, hdr,
+                                                                                        limit_ns, lane, wa);
+                }
+                if (lane == 0 && tc != 0 && tc != skip_tile && !agg_head)
+                    st_relaxed(desc2 + 2ull * tc, tag | kFlagP | (unsigned int)(seg + agg_val));
+                if (lane < WARPS) s_bval[lane] = head_before ? wex_val : seg + wex_val;
+                if (WANT_SUMS && lane == 0) s_nexthead = nh_c;
+            } else if (!ATOM_COUNT && warp == 1) {
+                if (more) count_aggregate((int)(u & 1u), tn, n_cnt, n_xcnt);
+                unsigned int cnt = 0;
+                if (tc != 0) {
+                    unsigned long long wb[U32SCAN_S_LOOKB];
+                    lookback_window<U32SCAN_S_LOOKB, kAdd, 2>(desc2 + 1, (long long)tc - 1, tag, lane, wb);
+                    cnt = lookback_prefix_wide<U32SCAN_S_LOOKB, kAdd, 2, kFlagP>(desc2 + 1, tc, tag, hdr, limit_ns,
+                                                                                 lane, wb);
+                }
+                if (lane == 0 && tc != 0 && tc != skip_tile)
+                    st_relaxed(desc2 + 2ull * tc + 1, tag | kFlagP | (unsigned int)(cnt + agg_cnt));
+                if (lane < WARPS) s_bcnt[lane] = cnt + wex_cnt;
+                if (lane == 0 && tc == n_tiles - 1u && nseg != nullptr) *nseg = cnt + agg_cnt;
+            } else if (ATOM_COUNT && warp == 0) {
+                // the value alone; the segments are counted by one atomic add
                 if (more) block_aggregate((int)(u & 1u), tn, n_val, n_head, n_cnt, n_xval, n_before, n_xcnt);
-                SegPrefix pre{0u, 0u};
-                if constexpr (ATOM_COUNT) {
-                    if (tc != 0) {
-                        unsigned long long wa[U32SCAN_S_LOOKA];
-                        lookback_window<U32SCAN_S_LOOKA, kAdd, 2>(desc2, (long long)tc - 1, tag, lane, wa);
-                        pre.seg = lookback_prefix_wide<U32SCAN_S_LOOKA, kAdd, 2, kFlagP | kFlagH>(desc2, tc, tag, hdr,
-                                                                                                limit_ns, lane, wa);
-                    }
-                } else {
-                    pre = lookback_seg_wide<U32SCAN_S_LOOKA, U32SCAN_S_LOOKB>(desc2, tc, tag, hdr, limit_ns, lane);
+                unsigned int seg = 0;
+                if (tc != 0) {
+                    unsigned long long wa[U32SCAN_S_LOOKA];
+                    lookback_window<U32SCAN_S_LOOKA, kAdd, 2>(desc2, (long long)tc - 1, tag, lane, wa);
+                    seg = lookback_prefix_wide<U32SCAN_S_LOOKA, kAdd, 2, kFlagP | kFlagH>(desc2, tc, tag, hdr,
+                                                                                        limit_ns, lane, wa);
                 }
-                if (lane == 0 && tc != 0 && tc != skip_tile) {
-                    if (!agg_head) st_relaxed(desc2 + 2ull * tc, tag | kFlagP | (unsigned int)(pre.seg + agg_val));
-                    if (!ATOM_COUNT)
-                        st_relaxed(desc2 + 2ull * tc + 1, tag | kFlagP | (unsigned int)(pre.cnt + agg_cnt));
-                }
-                if (lane < WARPS) {
-                    s_bval[lane] = head_before ? wex_val : pre.seg + wex_val;
-                    s_bcnt[lane] = pre.cnt + wex_cnt;
-                }
+                if (lane == 0 && tc != 0 && tc != skip_tile && !agg_head)
+                    st_relaxed(desc2 + 2ull * tc, tag | kFlagP | (unsigned int)(seg + agg_val));
+                if (lane < WARPS) s_bval[lane] = head_before ? wex_val : seg + wex_val;
                 if (lane == 0) {
                     unsigned int total;
-                    if (ATOM_COUNT) {
-                        if (nseg != nullptr && seg_count_add(hdr, n_tiles, agg_cnt, total)) *nseg = total;
-                    } else if (tc == n_tiles - 1u && nseg != nullptr) {
-                        *nseg = pre.cnt + agg_cnt;
-                    }
+                    if (nseg != nullptr && seg_count_add(hdr, n_tiles, agg_cnt, total)) *nseg = total;
                     if (WANT_SUMS) s_nexthead = nh_c;
                 }
             }

@@ -345,6 +345,19 @@ __device__ __forceinline__ void prefetch_l2_interior(const void *p, unsigned lon
     if (e > a) bulk_prefetch_l2(reinterpret_cast<const void *>(a), (unsigned int)(e - a));
 }
 
+// The identity permutation (and the keys unchanged) over this block's tile:
+// the result when every digit is constant. Kept out of line so that the
+// digit pass's own code is the same as without it.
+__device__ __noinline__ void radix_identity_tile(const uint32_t *keys, int32_t *perm, uint32_t *keys_out,
+                                                 unsigned long long n) {
+    const unsigned long long lo = (unsigned long long)blockIdx.x * kRTile;
+    const unsigned long long hi = lo + kRTile < n ? lo + kRTile : n;
+    for (unsigned long long i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+        if (perm) perm[i] = (int32_t)i;
+        if (keys_out) keys_out[i] = keys[i];
+    }
+}
+
 // One digit pass: tiles drawn in order; per tile: rank, carry each digit
 // value's count across tiles by decoupled look-back, order the tile by digit
 // value in shared memory, write each value's run of (key, index) pairs to
@@ -360,7 +373,12 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
                       const unsigned int *__restrict__ bases, WsHeader *hdr, unsigned long long *desc,
                       unsigned long long limit_ns, unsigned int ahead) {
     const RadixPlan pl = plan[p];
-    if (!pl.active) return;
+    if (!pl.active) {
+        // Every digit constant (every key equal): the permutation is the
+        // identity, written by the last digit's launch.
+        if (p == 3 && pl.m == 0) radix_identity_tile(keys, perm, keys_out, n);
+        return;
+    }
     // Shared memory (32-bit words): per-warp digit counters, later the warp
     // offsets in the tile-ordered buffer [kRWarps][256]; each value's run
     // start in the tile [256]; its first output slot minus that start [256];
@@ -524,17 +542,6 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
 
 constexpr size_t kRSmem = (size_t)(kRWarps * 256 + 512 + 2 * kRTile) * 4;
 
-// All digits constant (every key equal): the permutation is the identity.
-__global__ void radix_identity_kernel(const RadixPlan *__restrict__ plan, const uint32_t *keys, int32_t *perm,
-                                      uint32_t *keys_out, unsigned long long n) {
-    if (plan[0].m != 0) return;
-    for (unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (unsigned long long)gridDim.x * blockDim.x) {
-        if (perm) perm[i] = (int32_t)i;
-        if (keys_out) keys_out[i] = keys[i];
-    }
-}
-
 size_t radix_workspace_bytes(unsigned long long n) { return RadixLayout(n).total; }
 
 static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *perm, uint32_t *keys_out, void *ws,
@@ -593,7 +600,6 @@ static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *per
         radix_onesweep_kernel<<<L.n_tiles, kRThreads, kRSmem, stream>>>(plan, p, keys, k1, k2, i1, perm, keys_out, n,
                                                                          L.n_tiles, bases, hdr, desc, kDefaultLimitNs,
                                                                          (unsigned int)resident);
-    radix_identity_kernel<<<1024, 256, 0, stream>>>(plan, keys, perm, keys_out, n);
     if (cudaGetLastError() != cudaSuccess) return U32SCAN_ECUDA;
     // Leave no data where another operation's tile words may go: the
     // histograms, bases and ping-pong buffers hold small integers that could

@@ -193,3 +193,30 @@ def test_tag_period_end_clears_old_carry_words(u, which, big):
     assert ok, "a carry word from the previous tag period was taken as published"
     h = header(ws)
     assert h[H_EPOCH] == 2 * TAG_PERIOD - 1 and h[H_COUNTER] == 0 and h[H_DONE] == 0
+
+
+def test_tag_period_end_on_a_radix_pass_clears_other_operations_words(u):
+    """The launch that ends a tag period can be a radix digit pass. The
+    radix sort keeps no count of the blocks that finish; its end-of-call
+    clear must therefore reach every word another operation may have left,
+    not only the sort's own (smaller) part of the workspace. Here a scan of
+    2^26 elements leaves tile words out to 33 KB, a sort of 1000 keys (a
+    23 KB workspace part) ends the period with its first digit pass, and a
+    second scan carrying the first one's tag must still be exact."""
+    from u32_prefix_scan_gb300 import _native
+
+    big = (1 << 26) + 77
+    ws = u.Workspace(_native.lib().u32scan_workspace_bytes(1, big), torch.device("cuda"))
+    assert _native.lib().u32scan_workspace_bytes(4, 1000) < ws.nbytes
+    set_epoch(ws, TAG_PERIOD - 2)
+    ok, status = run_op(u, ws, "scan", big, 51)  # tag of launch 2^29 - 2
+    assert status == _native.OK and ok
+    assert header(ws)[H_EPOCH] == TAG_PERIOD - 1
+    k = inputs.radix_keys(1000, 52)  # four active digit passes; the first ends the period
+    perm = u.radix_sort_perm_u32(dev32(k), workspace=ws)
+    assert np.array_equal(perm.cpu().numpy(), oracle.sort_perm(k))
+    assert header(ws)[H_EPOCH] == TAG_PERIOD + 3
+    set_epoch(ws, 2 * TAG_PERIOD - 2)  # the first scan's tag again
+    ok, status = run_op(u, ws, "scan", big, 53)
+    assert status == _native.OK
+    assert ok, "a scan's carry word from the ended tag period was taken as published"

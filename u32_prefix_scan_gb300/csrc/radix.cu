@@ -604,9 +604,13 @@ static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *per
     // Leave no data where another operation's tile words may go: the
     // histograms, bases and ping-pong buffers hold small integers that could
     // pass for tagged words. Any other operation's tile words lie within the
-    // largest workspace it can need (n below 2^32), a few MiB at most.
+    // largest workspace it can need (n below 2^32), a few MiB at most. The
+    // whole of that span is zeroed, not only this call's part of it: the
+    // digit passes draw tiles, so one of them can be the launch that ends a
+    // tag period, and they keep no count of the blocks that finish; zeroing
+    // here leaves no other operation's word from the ending period behind.
     const size_t reach = tile_word_reach();
-    const size_t end = L.total < reach ? L.total : reach;
+    const size_t end = ws_bytes < reach ? ws_bytes : reach;
     return clear_tile_words(w + kHeaderBytes, end - kHeaderBytes, stream);
 }
 

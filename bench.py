@@ -1187,6 +1187,39 @@ def run_reference(args, rank):
     }
 
 
+def parse_cpulist(text: str) -> set:
+    """CPUs of a sysfs cpulist such as "0-15,32-47"."""
+    cpus = set()
+    for part in text.strip().split(","):
+        if part:
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+    return cpus
+
+
+def bind_to_gpu_numa_node(dev_index: int):
+    """Bind this process to the CPUs of the GPU's NUMA node, so that the
+    page-locked host buffers of the end-to-end leg are allocated next to the
+    GPU's host link. Returns the node, or None when sysfs does not name one
+    (the affinity is then left as it was)."""
+    import torch
+
+    try:
+        p = torch.cuda.get_device_properties(dev_index)
+        addr = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        node = int(pathlib.Path(f"/sys/bus/pci/devices/{addr}/numa_node").read_text())
+        if node < 0:
+            return None
+        cpus = parse_cpulist(pathlib.Path(f"/sys/devices/system/node/node{node}/cpulist").read_text())
+        mine = os.sched_getaffinity(0) & cpus
+        if mine:
+            os.sched_setaffinity(0, mine)
+            return node
+    except (AttributeError, OSError, ValueError):
+        pass
+    return None
+
+
 def run_ours(args, rank, local_rank, world):
     import torch
 
@@ -1195,6 +1228,7 @@ def run_ours(args, rank, local_rank, world):
     native_build.build()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+    numa_node = bind_to_gpu_numa_node(local_rank)  # before any host buffer is pinned
     stream = torch.cuda.current_stream()
     args.world, args.rank = world, rank
     op = make_op(args)
@@ -1323,7 +1357,7 @@ def run_ours(args, rank, local_rank, world):
                      "kernel_ms": kernel_ms, "copy_gbs_same_run": copy_now, "frac_of_same_run_copy": achieved / copy_now,
                      "nominal_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS},
         "e2e": {"value": world * op.n / (e2e_ms * 1e-3) / 1e9 if e2e_ms else None, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "host_numa_node": numa_node},
         "clocks": clocks,
         "gpu_launches": args.steps * op.launches_per_step,
     }

@@ -141,3 +141,11 @@ def test_segmented_scan_under_several_ranks_is_one_sharded_scan():
     args = bench.parse_args(["--op", "segscan_sums"])
     args.world, args.rank = 2, 0
     assert not bench.make_op(args).sharded  # only the plain segmented scan shards
+
+
+def test_parse_cpulist_reads_sysfs_ranges():
+    import bench
+
+    assert bench.parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench.parse_cpulist("5") == {5}
+    assert bench.parse_cpulist("") == set()

@@ -577,6 +577,23 @@ int u32scan_test_noalloc_skip_publish(uint32_t *data, size_t n, uint32_t *total,
  */
 int u32scan_test_noalloc_set_epoch(unsigned int epoch, u32scan_stream_t stream);
 
+/*
+ * Seeded synthetic input, drawn on the device (no counterpart on the pages,
+ * which measure on synthetic inputs only): out[i] = u32(seed, stream,
+ * start + i) for i < n, where u32 is counter-based SplitMix64 (S. Vigna's
+ * public-domain mixer): the high 32 bits of mix((seed << 40) | (stream << 32)
+ * | index), the same numbers as the host generator in
+ * u32_prefix_scan_gb300/inputs.py. Lets a caller draw a large input in
+ * device memory instead of copying it from the host.
+ *   out:    device, n words, 4-byte aligned; written, caller-owned.
+ *   seed:   below 2^24; stream: below 256; start + n at most 2^32.
+ * Asynchronous on `stream`. Errors: EINVAL for a null or misaligned `out`
+ * with n > 0 or an argument out of range; ECUDA if the launch fails. n = 0
+ * does nothing.
+ */
+int u32scan_fill_splitmix_u32(uint32_t *out, size_t n, uint32_t seed, uint32_t stream, size_t start,
+                              u32scan_stream_t cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

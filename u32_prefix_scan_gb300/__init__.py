@@ -14,6 +14,7 @@ _API = {
     "scan_inclusive_u32_carry",
     "reduce_u32_op",
     "count_nonzero_u32",
+    "fill_splitmix_u32",
     "segscan_piece_summary_u32",
     "segscan_piece_carries_u32",
     "segscan_fix_u32",

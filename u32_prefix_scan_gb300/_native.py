@@ -46,6 +46,7 @@ SIGNATURES = {
     "scan_inclusive_u32_carry": (_int, [_vp, _sz, _vp, _vp, _vp, _sz, _vp]),
     "reduce_u32_op": (_int, [_int, _vp, _sz, _vp, _vp, _sz, _vp]),
     "count_nonzero_u32": (_int, [_vp, _sz, _vp, _vp, _sz, _vp]),
+    "u32scan_fill_splitmix_u32": (_int, [_vp, _sz, ctypes.c_uint, ctypes.c_uint, _sz, _vp]),
     "segscan_piece_summary_u32": (_int, [_vp, _vp, _sz, _vp, _int, _vp, _vp]),
     "segscan_piece_carries_u32": (_int, [_vp, _sz, _vp, _vp, _vp]),
     "segscan_fix_u32": (_int, [_vp, _vp, _sz, _vp, _vp, _sz, _vp]),

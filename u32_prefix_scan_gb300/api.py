@@ -25,6 +25,7 @@ __all__ = [
     "scan_inclusive_u32_carry",
     "reduce_u32_op",
     "count_nonzero_u32",
+    "fill_splitmix_u32",
     "segscan_piece_summary_u32",
     "segscan_piece_carries_u32",
     "segscan_fix_u32",
@@ -449,6 +450,24 @@ def count_nonzero_u32(data: torch.Tensor, count: torch.Tensor | None = None, *, 
     _native.check(_native.lib().count_nonzero_u32(data.data_ptr(), n, count.data_ptr(), ws.ptr, ws.nbytes, sh),
                   "count_nonzero_u32")
     return count
+
+
+def fill_splitmix_u32(n: int, seed: int, stream_id: int = 0, start: int = 0, *, device=None,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The seeded input u32(seed, stream_id, start + i), i < n, drawn on the
+    device: the same numbers as inputs.splitmix_u32 (counter-based
+    SplitMix64), without a copy from the host. Returns an int32 tensor
+    holding the u32 bits (out, when given, is filled and returned)."""
+    if out is None:
+        dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        out = torch.empty(n, dtype=torch.int32, device=dev)
+    _require_cuda(out, "out")
+    if out.numel() != n:
+        raise ValueError("out must hold n elements")
+    sh = _stream_handle(stream)
+    _native.check(_native.lib().u32scan_fill_splitmix_u32(out.data_ptr(), n, seed, stream_id, start, sh),
+                  "u32scan_fill_splitmix_u32")
+    return out
 
 
 def compact_values_u32(values: torch.Tensor, flags: torch.Tensor | None = None, out: torch.Tensor | None = None,

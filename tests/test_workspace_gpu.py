@@ -220,3 +220,42 @@ def test_tag_period_end_on_a_radix_pass_clears_other_operations_words(u):
     ok, status = run_op(u, ws, "scan", big, 53)
     assert status == _native.OK
     assert ok, "a scan's carry word from the ended tag period was taken as published"
+
+
+def test_reduce_leaves_no_partials_that_pass_for_tile_words(u):
+    """count_nonzero_u32 and reduce_u32_op fold per-block partials in the
+    workspace, where a scan keeps its tile words. Left behind, two partials
+    side by side read as one 64-bit word whose tag field is a partial's bits:
+    at the launch count that tag names, a scan would take the word for a
+    published carry. The reduce must leave that region zero. End to end: the
+    word left at the scan's tile 0 (if any) sets the launch count its tag
+    names, tile 0 of a scan is made never to publish (the test hook), and
+    tile 1 must then wait for it and time out rather than take the word."""
+    from u32_prefix_scan_gb300 import _native
+
+    lib = _native.lib()
+    n = 1 << 20
+    ws = u.Workspace(max(lib.u32scan_workspace_bytes(_native.OP_SCAN, n),
+                         lib.u32scan_workspace_bytes(_native.OP_REDUCE, n)), torch.device("cuda"))
+    span = lib.u32scan_workspace_bytes(_native.OP_REDUCE, n)
+    ones = torch.ones(16384, dtype=torch.int32, device="cuda")
+    assert int(u.count_nonzero_u32(ones, workspace=ws).item()) == 16384
+    word = int(ws.buf[256:264].cpu().numpy().view(np.uint64)[0])
+    set_epoch(ws, (word >> 34) - 1 if word >> 34 else 1535)  # the launch count a left word's tag would name
+    a = inputs.scan_values(n, 61)
+    d, total = dev32(a), torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    assert lib.u32scan_test_scan_skip_publish(d.data_ptr(), n, total.data_ptr(), ws.ptr, ws.nbytes, 0,
+                                              20_000_000, stream) == _native.OK
+    assert lib.u32scan_check(ws.ptr, stream) == _native.ETIMEOUT, "a stale partial was taken as tile 0's carry"
+    # the workspace serves a normal call afterwards
+    d = dev32(a)
+    total = u.scan_exclusive_u32(d, workspace=ws)
+    assert lib.u32scan_check(ws.ptr, stream) == _native.OK
+    want, want_total = oracle.scan_exclusive(a)
+    assert np.array_equal(host_u32(d), want) and int(host_u32(total)[0]) == want_total
+    # and directly: after either fold on a zero-filled workspace, the span is zero again
+    for fold in (lambda: u.count_nonzero_u32(ones, workspace=ws), lambda: u.reduce_u32_op(ones, "add", workspace=ws)):
+        ws.buf.zero_()
+        assert int(fold().item()) == 16384
+        assert not ws.buf[256:span].any(), "a fold left its partials in the workspace"

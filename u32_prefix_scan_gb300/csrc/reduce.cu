@@ -13,8 +13,8 @@
 // Kernel: a grid of resident blocks strides over the array with four 16-byte
 // loads in flight a thread; each block folds its share (lanes, then warps)
 // into one partial in the workspace, and the last block to finish (counted
-// in the workspace header) folds the partials into the total. 4 bytes read
-// per element; nothing else but the partials moves.
+// in the workspace header) folds the partials into the total and zeroes
+// them. 4 bytes read per element; nothing else but the partials moves.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -76,9 +76,14 @@ reduce_u32_kernel(const uint32_t *__restrict__ data, unsigned long long n, uint3
     }
     __syncthreads();
     if (s_last == 0u) return;
-    // the last block folds every block's partial
+    // the last block folds every block's partial and zeroes it: the partials
+    // lie where other operations keep tagged tile words, and two of them
+    // side by side could pass for such a word of a later launch
     unsigned int f = M::identity();
-    for (unsigned int k = threadIdx.x; k < gridDim.x; k += kFThreads) f = M::apply(f, ld_relaxed_u32(partials + k));
+    for (unsigned int k = threadIdx.x; k < gridDim.x; k += kFThreads) {
+        f = M::apply(f, ld_relaxed_u32(partials + k));
+        st_relaxed_u32(partials + k, 0u);
+    }
     f = M::warp_fold(f);
     if (lane == 0) s_warp[warp] = f;
     __syncthreads();

@@ -259,3 +259,39 @@ def test_reduce_leaves_no_partials_that_pass_for_tile_words(u):
         ws.buf.zero_()
         assert int(fold().item()) == 16384
         assert not ws.buf[256:span].any(), "a fold left its partials in the workspace"
+
+
+def test_host_scan_leaves_nothing_that_passes_for_tile_words(u):
+    """scan_exclusive_u32_host stages its chunks in the workspace, past the
+    chunk scan's own tile words and inside the span where other operations
+    keep theirs; the scanned chunks (increasing integers here) read, two
+    side by side, as words whose tag field names some launch count. The
+    word left at tile t of a later scan sets that launch count, tile t is
+    made never to publish (the test hook), and tile t + 1 must then wait
+    for it and time out rather than take the staged data for its carry."""
+    from u32_prefix_scan_gb300 import _native
+
+    lib = _native.lib()
+    n_host, n = 1 << 22, 1 << 26
+    ws = u.Workspace(max(lib.u32scan_workspace_bytes(_native.OP_SCAN_HOST, n_host),
+                         lib.u32scan_workspace_bytes(_native.OP_SCAN, n)), torch.device("cuda"))
+    host_in = torch.ones(n_host, dtype=torch.int32).pin_memory()
+    out, total = u.scan_exclusive_u32_host(host_in, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(total[0]) == n_host and int(out[-1]) == n_host - 1
+    n_tiles = (lib.u32scan_workspace_bytes(_native.OP_SCAN, n) - 256) // 8  # at least the scan's tiles
+    t = 3000  # a tile word 24 KB in, among the host scan's staging slots
+    assert t + 2 < n_tiles - 32
+    word = int(ws.buf[256 + 8 * t: 264 + 8 * t].cpu().numpy().view(np.uint64)[0])
+    set_epoch(ws, (word >> 34) - 1 if word >> 34 else 1535)  # the launch count a left word's tag would name
+    a = inputs.scan_values(n, 62)
+    d, tot = dev32(a), torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    assert lib.u32scan_test_scan_skip_publish(d.data_ptr(), n, tot.data_ptr(), ws.ptr, ws.nbytes, t,
+                                              20_000_000, stream) == _native.OK
+    assert lib.u32scan_check(ws.ptr, stream) == _native.ETIMEOUT, "staged host data was taken as a carry"
+    d = dev32(a)
+    tot = u.scan_exclusive_u32(d, workspace=ws)
+    assert lib.u32scan_check(ws.ptr, stream) == _native.OK
+    want, want_total = oracle.scan_exclusive(a)
+    assert np.array_equal(host_u32(d), want) and int(host_u32(tot)[0]) == want_total

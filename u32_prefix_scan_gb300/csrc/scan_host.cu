@@ -200,7 +200,16 @@ static int scan_host(bool inclusive, const uint32_t *host_in, uint32_t *host_out
     // Whatever was queued, later work on `stream` comes after it.
     const bool joined = P.join(stream);
     if (rc != U32SCAN_OK) return rc;
-    return ok && joined ? U32SCAN_OK : U32SCAN_ECUDA;
+    if (!ok || !joined) return U32SCAN_ECUDA;
+    // The carry words and the staging slots hold plain data (the scanned
+    // chunks) where other operations keep tagged tile words; two values side
+    // by side could pass for such a word. Zero that part once the copies out
+    // are done (the slots past it no operation reads as tile words).
+    const size_t reach = tile_word_reach();
+    const size_t end = L.bytes < reach ? L.bytes : reach;
+    if (end > L.chain_off && cudaMemsetAsync(w + L.chain_off, 0, end - L.chain_off, stream) != cudaSuccess)
+        return U32SCAN_ECUDA;
+    return U32SCAN_OK;
 }
 
 }  // namespace u32scan

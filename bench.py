@@ -1187,6 +1187,57 @@ def run_reference(args, rank):
     }
 
 
+def measure_host_link(op, stream, reps: int = 3):
+    """The host link's copy rates in this run (GB/s): host to device, device
+    to host, and both at once on two streams, with the step's own page-locked
+    buffers (the largest input and output) and a device buffer of the same
+    size; the best of `reps` each. None when the step has no such buffers."""
+    import torch
+
+    ins = [t for t in getattr(op, "pinned_in", {}).values() if t.numel() > 1]
+    outs = [t for t in getattr(op, "pinned_out", {}).values() if t.numel() > 1]
+    if not ins or not outs:
+        return None
+    h_in = max(ins, key=lambda t: t.numel() * t.element_size()).view(torch.uint8)
+    h_out = max(outs, key=lambda t: t.numel() * t.element_size()).view(torch.uint8)
+    nbytes = min(h_in.numel(), h_out.numel())
+    h_in, h_out = h_in[:nbytes], h_out[:nbytes]
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device=stream.device)
+    d_b = torch.empty(nbytes, dtype=torch.uint8, device=stream.device)
+    s1, s2 = torch.cuda.Stream(stream.device), torch.cuda.Stream(stream.device)
+
+    def timed(fn):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None or ms < best else best
+        return best
+
+    def both():
+        s1.wait_stream(stream)
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s1):
+            d_a.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_b, non_blocking=True)
+        stream.wait_stream(s1)
+        stream.wait_stream(s2)
+
+    with torch.cuda.stream(stream):
+        h2d = timed(lambda: d_a.copy_(h_in, non_blocking=True))
+        d2h = timed(lambda: h_out.copy_(d_b, non_blocking=True))
+        two = timed(both)
+    del d_a, d_b
+    return {"h2d": nbytes / (h2d * 1e-3) / 1e9, "d2h": nbytes / (d2h * 1e-3) / 1e9,
+            "both": 2 * nbytes / (two * 1e-3) / 1e9, "bytes_each_way": nbytes}
+
+
 def parse_cpulist(text: str) -> set:
     """CPUs of a sysfs cpulist such as "0-15,32-47"."""
     cpus = set()
@@ -1304,6 +1355,7 @@ def run_ours(args, rank, local_rank, world):
     # end to end through the C ABI: pinned host inputs in, outputs back out
     h2d = d2h = 0
     e2e_ms = None
+    link = None
     if args.e2e_steps:
         for _ in range(2):
             op.e2e_step()
@@ -1320,6 +1372,7 @@ def run_ours(args, rank, local_rank, world):
         e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.e2e_steps, world)
         if not op.check_e2e(host):
             raise SystemExit("bench: e2e result fails its property check")
+        link = measure_host_link(op, stream)
 
     library = None
     if args.library_context:
@@ -1357,7 +1410,9 @@ def run_ours(args, rank, local_rank, world):
                      "kernel_ms": kernel_ms, "copy_gbs_same_run": copy_now, "frac_of_same_run_copy": achieved / copy_now,
                      "nominal_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS},
         "e2e": {"value": world * op.n / (e2e_ms * 1e-3) / 1e9 if e2e_ms else None, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "host_numa_node": numa_node},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "host_numa_node": numa_node,
+                "host_link_gbs": link,
+                "frac_of_host_link": ((h2d + d2h) / (e2e_ms * 1e-3) / 1e9 / link["both"]) if link and e2e_ms else None},
         "clocks": clocks,
         "gpu_launches": args.steps * op.launches_per_step,
     }

@@ -23,8 +23,9 @@
  *     zero-filled once before its first use (cudaMemset or
  *     u32scan_workspace_init); after that the library keeps it consistent
  *     itself, so it is reused across calls and shared between operations
- *     without clearing (the radix sort, which keeps data in it, clears what
- *     it leaves where other operations keep tile state). This holds for any
+ *     without clearing (the radix sort, the folds and the host-memory
+ *     scans, which keep other data in it, clear what they leave where other
+ *     operations keep tile state before they return). This holds for any
  *     number of calls: carry words are tagged with a per-workspace launch
  *     count whose tags repeat every 2^29 launches, and the launch that ends
  *     such a period zeroes the carry words (up to a few MiB of ws) before the

@@ -15,7 +15,7 @@
 // the keys, gives every pass its digit bases (keys with a smaller digit
 // value come first) and finds digits that are equal for every key, whose
 // passes are skipped (exact: such a pass moves nothing). Each digit pass is
-// then one kernel over tiles of 8192 keys drawn in order: a tile ranks its
+// then one kernel over tiles of 11264 keys drawn in order: a tile ranks its
 // keys stably within itself, publishes its 256 digit counts, and finds for
 // every digit value the count of that value in all earlier tiles by a
 // decoupled look-back (thread v walks back over the earlier tiles' words
@@ -28,9 +28,10 @@
 // no indices at all.
 //
 // Ranking. For the 32 keys of one warp round (one per lane), a per-warp
-// table of lane masks, one word per digit value, gives each lane the mask of
-// lanes holding its digit value (each lane ORs its bit into its value's word
-// and reads the word back); the lowest lane of each value adds the value's
+// table of lane masks, one word per value of the digit's low seven bits,
+// and one ballot on its eighth bit give each lane the mask of lanes holding
+// its digit value (each lane ORs its bit into its word of the table and
+// reads the word back); the lowest lane of each value adds the value's
 // count to the warp's running counter for it (one shared atomic add, whose
 // old value is broadcast to the value's lanes) and clears the word, and a
 // lane's rank is that old value plus the lanes below it in the mask. A round
@@ -278,12 +279,14 @@ __device__ __forceinline__ void rank_set(unsigned int (&w)[kRWords], int r, unsi
 // warp's count of value v. FULL: every key of the tile lies in the array.
 //
 // A round finds the lanes holding each digit value through the warp's match
-// table s_wmatch[256] (zero between rounds): every lane ORs its lane bit
-// into the word of its value and reads the word back, so it holds the mask
-// of lanes sharing its value; the value's lowest lane then adds the count
-// to the warp's counter and clears the word. (Eight ballots, one per digit
-// bit, folded in every lane, measured slower: the fold costs about five ALU
-// instructions a bit, and the pass was bound by the ALU pipe.)
+// table s_wmatch (2^U32SCAN_R_TBITS words, zero between rounds, indexed by
+// the digit's low TBITS bits): every lane ORs its lane bit into its word and
+// reads the word back, which, ANDed with ballots on the digit's other bits,
+// is the mask of lanes sharing its value; the value's lowest lane then adds
+// the count to the warp's counter and clears the word. (Eight ballots, one
+// per digit bit, folded in every lane, measured slower: the fold costs
+// about five ALU instructions a bit, and the pass was bound by the ALU
+// pipe.)
 template <bool FULL>
 __device__ __forceinline__ unsigned int radix_rank_tile(const uint32_t *__restrict__ in_keys, unsigned int n32,
                                                         unsigned int wbase, int shift, uint32_t (&k)[kRKeys],

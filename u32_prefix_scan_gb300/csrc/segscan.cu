@@ -512,12 +512,13 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
                 latest_parity ^= 1u << st;
             }
             if (!ATOM_COUNT && warp == 0) {
-                // the segmented value, walked while warp 1 walks the head count
+                // the segmented value, walked while warp 1 walks the head count;
+                // its first window is loaded before the next tile's aggregate
+                unsigned long long wa[U32SCAN_S_LOOKA];
+                if (tc != 0) lookback_window<U32SCAN_S_LOOKA, kAdd, 2>(desc2, (long long)tc - 1, tag, lane, wa);
                 if (more) value_aggregate((int)(u & 1u), tn, n_val, n_head, n_xval, n_before);
                 unsigned int seg = 0;
                 if (tc != 0) {
-                    unsigned long long wa[U32SCAN_S_LOOKA];
-                    lookback_window<U32SCAN_S_LOOKA, kAdd, 2>(desc2, (long long)tc - 1, tag, lane, wa);
                     seg = lookback_prefix_wide<U32SCAN_S_LOOKA, kAdd, 2, kFlagP | kFlagH>(desc2, tc, tag, hdr,
                                                                                         limit_ns, lane, wa);
                 }
@@ -526,11 +527,11 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
                 if (lane < WARPS) s_bval[lane] = head_before ? wex_val : seg + wex_val;
                 if (WANT_SUMS && lane == 0) s_nexthead = nh_c;
             } else if (!ATOM_COUNT && warp == 1) {
+                unsigned long long wb[U32SCAN_S_LOOKB];
+                if (tc != 0) lookback_window<U32SCAN_S_LOOKB, kAdd, 2>(desc2 + 1, (long long)tc - 1, tag, lane, wb);
                 if (more) count_aggregate((int)(u & 1u), tn, n_cnt, n_xcnt);
                 unsigned int cnt = 0;
                 if (tc != 0) {
-                    unsigned long long wb[U32SCAN_S_LOOKB];
-                    lookback_window<U32SCAN_S_LOOKB, kAdd, 2>(desc2 + 1, (long long)tc - 1, tag, lane, wb);
                     cnt = lookback_prefix_wide<U32SCAN_S_LOOKB, kAdd, 2, kFlagP>(desc2 + 1, tc, tag, hdr, limit_ns,
                                                                                  lane, wb);
                 }
@@ -540,11 +541,11 @@ segscan_lanes_persistent(uint32_t *__restrict__ data, const F *__restrict__ flag
                 if (lane == 0 && tc == n_tiles - 1u && nseg != nullptr) *nseg = cnt + agg_cnt;
             } else if (ATOM_COUNT && warp == 0) {
                 // the value alone; the segments are counted by one atomic add
+                unsigned long long wa[U32SCAN_S_LOOKA];
+                if (tc != 0) lookback_window<U32SCAN_S_LOOKA, kAdd, 2>(desc2, (long long)tc - 1, tag, lane, wa);
                 if (more) block_aggregate((int)(u & 1u), tn, n_val, n_head, n_cnt, n_xval, n_before, n_xcnt);
                 unsigned int seg = 0;
                 if (tc != 0) {
-                    unsigned long long wa[U32SCAN_S_LOOKA];
-                    lookback_window<U32SCAN_S_LOOKA, kAdd, 2>(desc2, (long long)tc - 1, tag, lane, wa);
                     seg = lookback_prefix_wide<U32SCAN_S_LOOKA, kAdd, 2, kFlagP | kFlagH>(desc2, tc, tag, hdr,
                                                                                         limit_ns, lane, wa);
                 }

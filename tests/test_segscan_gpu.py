@@ -114,6 +114,37 @@ def test_segreduce_parity(u, kind, n):
     assert np.array_equal(host(d), a)  # the reduce leaves data as it was
 
 
+@pytest.mark.parametrize("kind", ["regular4", "regular7", "half", "geometric16"])
+@pytest.mark.parametrize("word_offset", [0, 1])
+@pytest.mark.parametrize("cut", [False, True])
+def test_segreduce_sums_at_any_word_and_capacity(u, kind, word_offset, cut):
+    """The reduce writes a lane's consecutive segment sums two to a store
+    where the index allows: sums rows at an even and an odd word (8-byte
+    alignment or not), with the capacity at the count or cut to an odd
+    number inside a lane's run of ends; nothing before the row or past the
+    capacity is written."""
+    from u32_prefix_scan_gb300 import _native
+
+    lib = _native.lib()
+    n = 3 * 14336 + 77
+    a, f = inputs.scan_values(n, 9), heads(kind, n, 9)
+    want_sums, want_nseg = oracle.segreduce(a, f)
+    cap = (want_nseg // 2) | 1 if cut else want_nseg
+    buf = torch.full((cap + word_offset + 4,), -1, dtype=torch.int32, device="cuda")
+    sums = buf[word_offset: word_offset + cap]
+    d, fl = dev(a), dev(f)
+    nseg = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = u.Workspace(lib.u32scan_workspace_bytes(_native.OP_SEGSCAN, n), torch.device("cuda"))
+    st = torch.cuda.current_stream().cuda_stream
+    assert lib.segreduce_u32(d.data_ptr(), fl.data_ptr(), n, sums.data_ptr(), cap, nseg.data_ptr(), ws.ptr,
+                             ws.nbytes, st) == _native.OK
+    assert lib.u32scan_check(ws.ptr, st) == _native.OK
+    assert int(nseg.item()) == want_nseg
+    got = host(buf)
+    assert np.array_equal(got[word_offset: word_offset + cap], want_sums[:cap])
+    assert np.all(got[:word_offset] == 0xFFFFFFFF) and np.all(got[word_offset + cap:] == 0xFFFFFFFF)
+
+
 def test_segreduce_count_only_and_empty(u):
     from u32_prefix_scan_gb300 import _native
 

@@ -66,7 +66,7 @@ constexpr unsigned int kRWarpKeys = 32 * kRKeys;  // a warp's run of the tile
 static_assert(kRThreads >= 256 && kRThreads % 32 == 0 && kRKeys <= 32, "a thread per digit value; key bits fit a word");
 static_assert(kRKeys >= 8, "the warps' match tables fit in the tile-ordered key buffer");
 #ifndef U32SCAN_R_LOOK
-#define U32SCAN_R_LOOK 8
+#define U32SCAN_R_LOOK 4
 #endif
 constexpr int kRLook = U32SCAN_R_LOOK;  // earlier tiles read per look-back round trip
 // 1: each block asks L2 for the tile one resident grid ahead.
@@ -471,6 +471,19 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
             s_keys[pos] = k[r];
         }
     }
+    // The look-back's first window (threads 0..255, value v), loaded before
+    // the indices are placed so that its round trip overlaps that work (4
+    // words: 8 measured slower loaded here, and before the keys are placed
+    // they spill).
+    unsigned long long wd[kRLook];
+    if (threadIdx.x < 256) {
+        const unsigned long long *col = desc + threadIdx.x;
+#pragma unroll
+        for (int j = 0; j < kRLook; ++j) {
+            const long long q = (long long)t - 1 - j;
+            wd[j] = q >= 0 ? ld_relaxed(col + 256ull * (unsigned long long)q) : (tag | kFlagP);
+        }
+    }
     if (b.out_idx) {
         int32_t idx[kRKeys];
 #pragma unroll
@@ -489,12 +502,6 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     if (threadIdx.x < 256) {
         const int v = threadIdx.x;
         const unsigned long long *col = desc + v;  // value v's word of tile q at col[256 q]
-        unsigned long long wd[kRLook];
-#pragma unroll
-        for (int j = 0; j < kRLook; ++j) {
-            const long long q = (long long)t - 1 - j;
-            wd[j] = q >= 0 ? ld_relaxed(col + 256ull * (unsigned long long)q) : (tag | kFlagP);
-        }
         unsigned int before = 0;
         long long pos = (long long)t - 1;
         unsigned long long t0 = 0;

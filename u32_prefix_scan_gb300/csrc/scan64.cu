@@ -77,24 +77,31 @@ __device__ __forceinline__ void publish64(unsigned long long *desc2, unsigned in
 // Fold (under OP) of tiles 0 .. t-1, by a warp: 32 tiles a round trip,
 // lane l reading the tile l + 1 places back; stops at the nearest tile
 // whose carry is an inclusive prefix.
+// Lane l's word pair of the tile l + 1 places before tile t (a virtual
+// inclusive prefix before tile 0): the walk's first window, which a caller
+// may load early so that its round trip overlaps other work.
+template <int OP>
+__device__ __forceinline__ void window64(const unsigned long long *desc2, long long idx, unsigned long long tag,
+                                         unsigned long long &lo, unsigned long long &hi) {
+    using M = Monoid64<OP>;
+    if (idx >= 0) {
+        lo = ld_relaxed(desc2 + 2 * idx);
+        hi = ld_relaxed(desc2 + 2 * idx + 1);
+    } else {
+        lo = tag | kFlagP | (M::identity() & 0xffffffffull);
+        hi = tag | kFlagP | (M::identity() >> 32);
+    }
+}
+
 template <int OP>
 __device__ unsigned long long lookback64(const unsigned long long *desc2, unsigned int t, unsigned long long tag,
-                                         WsHeader *hdr, unsigned long long limit_ns, int lane) {
+                                         WsHeader *hdr, unsigned long long limit_ns, int lane,
+                                         unsigned long long lo, unsigned long long hi) {
     using M = Monoid64<OP>;
     if (t == 0) return M::identity();
     unsigned long long prefix = M::identity();
     long long pos = (long long)t - 1;
-    auto load = [&](long long idx, unsigned long long &lo, unsigned long long &hi) {
-        if (idx >= 0) {
-            lo = ld_relaxed(desc2 + 2 * idx);
-            hi = ld_relaxed(desc2 + 2 * idx + 1);
-        } else {  // a virtual inclusive prefix before tile 0
-            lo = tag | kFlagP | (M::identity() & 0xffffffffull);
-            hi = tag | kFlagP | (M::identity() >> 32);
-        }
-    };
-    unsigned long long lo, hi;
-    load(pos - lane, lo, hi);
+    auto load = [&](long long idx, unsigned long long &l, unsigned long long &h) { window64<OP>(desc2, idx, tag, l, h); };
     while (true) {
         unsigned long long t0 = 0;
         for (unsigned int iter = 0;; ++iter) {
@@ -200,7 +207,9 @@ scan_u64_kernel(unsigned long long *__restrict__ data, unsigned long long n, uns
         const unsigned long long agg = __shfl_sync(0xffffffffu, winc, 31);
         const unsigned long long wex = M::warp_exclusive(winc, wt, lane);
         if (lane == 0) publish64(desc2, t, agg, t == 0, tag);
-        const unsigned long long prefix = lookback64<OP>(desc2, t, tag, hdr, limit_ns, lane);
+        unsigned long long wlo, whi;
+        window64<OP>(desc2, (long long)t - 1 - lane, tag, wlo, whi);
+        const unsigned long long prefix = lookback64<OP>(desc2, t, tag, hdr, limit_ns, lane, wlo, whi);
         if (lane == 0 && t != 0) publish64(desc2, t, M::apply(prefix, agg), true, tag);
         if (lane < WARPS) s_warp[lane] = M::apply(prefix, wex);
         if (t == n_tiles - 1u && lane == 0 && total != nullptr) *total = M::apply(prefix, agg);
@@ -405,11 +414,15 @@ scan_u64_persistent(unsigned long long *__restrict__ data, unsigned long long n,
                 latest_parity ^= 1u << st;
             }
             if (warp == 0) {
+                // the current tile's first window, loaded before the next
+                // tile's aggregate so that its round trip overlaps that work
+                unsigned long long wlo, whi;
+                window64<OP>(desc2, (long long)tc - 1 - lane, tag, wlo, whi);
                 if (more) {
                     agg_n = block_aggregate((int)(u & 1), wex_n);
                     if (lane == 0) publish64(desc2, tn, agg_n, tn == 0, tag);
                 }
-                const unsigned long long prefix = lookback64<OP>(desc2, tc, tag, hdr, limit_ns, lane);
+                const unsigned long long prefix = lookback64<OP>(desc2, tc, tag, hdr, limit_ns, lane, wlo, whi);
                 if (lane == 0 && tc != 0) publish64(desc2, tc, M::apply(prefix, agg_c), true, tag);
                 if (lane < WARPS) s_base[lane] = M::apply(prefix, wex_c);
                 if (tc == n_tiles - 1u && lane == 0 && total != nullptr) *total = M::apply(prefix, agg_c);

@@ -82,7 +82,8 @@ extern "C" const char *u32scan_strerror(int status) {
     case U32SCAN_ECUDA:
         return "CUDA runtime error";
     case U32SCAN_ETIMEOUT:
-        return "a tile timed out waiting for its predecessor's carry; results are invalid";
+        return "a wait timed out (a predecessor's carry or a tile's bulk copy): the results of the calls "
+               "since the last check are invalid; zero-fill the workspace before reusing it";
     default:
         return "unknown status";
     }

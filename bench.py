@@ -972,6 +972,8 @@ def parse_args(argv=None):
                    help="after the timed region, repeat timed windows of the same steps this long (clock record)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-rows", action="store_true",
+                   help="default scan line: skip timing the other primitives on their workloads")
     p.add_argument("--log2n", type=int, default=None,
                    help="array size 2^log2n instead of the workload's (for profiler captures)")
     a = p.parse_args(argv)
@@ -1271,6 +1273,69 @@ def bind_to_gpu_numa_node(dev_index: int):
     return None
 
 
+ROW_WORKLOADS = [
+    ["--op", "segscan"],
+    ["--op", "segscan_sums"],
+    ["--op", "segscan_sums", "--heads", "regular4"],
+    ["--op", "segreduce"],
+    ["--op", "segreduce", "--heads", "regular4"],
+    ["--op", "compact"],
+    ["--op", "compact", "--p", "0.9"],
+    ["--op", "radix"],
+    ["--op", "radix", "--ties"],
+]
+
+
+def measure_rows(dev, stream, peak: float, seconds: float = 0.3):
+    """The other primitives on their own workloads, each timed on the device
+    like the headline (warm-up, then a timed run of about `seconds`, events
+    on the launching stream), so that one bench line carries every
+    primitive's fraction of the copy peak."""
+    import torch
+
+    rows = []
+    sampler = ClockSampler(torch.cuda.current_device()).start()
+    t_start = time.time()
+    for argv in ROW_WORKLOADS:
+        a = parse_args(argv)
+        a.world, a.rank = 1, 0
+        op = make_op(a)
+        op.setup(dev, op.host_inputs())
+        marked = op.is_marked()
+        for _ in range(5):
+            op.step()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        for _ in range(5):
+            op.step()
+        torch.cuda.synchronize()
+        steps = max(50, int(seconds / max((time.time() - t0) / 5, 1e-6)))
+        marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(steps if marked else 0)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for k in range(steps):
+            if marked:
+                op.step_marked(*marks[k])
+            else:
+                op.step()
+        end.record(stream)
+        torch.cuda.synchronize()
+        op.u.check(workspace=op.ws)
+        ms = start.elapsed_time(end) / steps
+        kernel_ms = sum(x.elapsed_time(y) for x, y in marks) / steps if marked else ms
+        achieved = op.algorithmic_bytes() / (kernel_ms * 1e-3) / 1e9
+        rows.append({"op": " ".join(argv[1:]), "workload": op.workload(), "value": op.n / (ms * 1e-3) / 1e9,
+                     "unit": UNIT, "steps": steps, "ms_per_step": ms, "hbm_gbs": achieved, "frac": achieved / peak,
+                     "algorithmic_bytes_per_step": op.algorithmic_bytes(), "traffic": load_traffic(op)})
+        del op, marks
+        torch.cuda.empty_cache()
+    sampler.stop()
+    return {"note": "each primitive timed on the device in this run, L2 not flushed (inputs above 129 MB); "
+                    "frac is of the measured copy peak",
+            "clocks": sampler.summary(t_start, time.time()), "rows": rows}
+
+
 def run_ours(args, rank, local_rank, world):
     import torch
 
@@ -1435,6 +1500,8 @@ def run_ours(args, rank, local_rank, world):
         if "hbm_gbs" in library:
             library["frac"] = library["hbm_gbs"] / peak
         result["library_context"] = library
+    if world == 1 and args.op == "scan_exclusive" and args.log2n is None and not args.no_rows:
+        result["other_rows"] = measure_rows(dev, stream, peak)
     if rank == 0 and not args.no_cpu_baseline:
         v, reps, el = time_oracle(op, host, args.cpu_seconds, op.n)
         result["cpu_baseline"] = {"value": v / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",

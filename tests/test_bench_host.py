@@ -149,3 +149,20 @@ def test_parse_cpulist_reads_sysfs_ranges():
     assert bench.parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
     assert bench.parse_cpulist("5") == {5}
     assert bench.parse_cpulist("") == set()
+
+
+def test_other_rows_cover_every_primitive_workload():
+    """The default line's other rows: the segmented forms at both segment
+    mixes, compaction at both keep rates, the radix permutation on both key
+    sets, each at its workload's full size with its own byte count."""
+    seen = set()
+    for argv in bench.ROW_WORKLOADS:
+        a = bench.parse_args(argv)
+        a.world, a.rank = 1, 0
+        op = bench.make_op(a)
+        assert op.n == 1 << op.log2n and not getattr(op, "sharded", False)
+        seen.add(op.name)
+    assert seen == {"segscan_geometric", "segscan_sums_geometric", "segscan_sums_regular4", "segreduce_geometric",
+                    "segreduce_regular4", "compact_p0.1", "compact_p0.9", "radix_sort_perm_u32",
+                    "radix_sort_perm_u32_ties"}
+    assert not bench.parse_args([]).no_rows and bench.parse_args(["--no-rows"]).no_rows

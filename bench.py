@@ -683,7 +683,7 @@ class CompactValuesOp(Op):
 
 class RadixOp(Op):
     log2n = 25
-    launches_per_step = 6  # histogram, plan, 4 digit passes (inactive ones return at once)
+    launches_per_step = 5  # histogram (its last block plans the passes), 4 digit passes (inactive ones return at once)
     kernel_sources = ["u32_prefix_scan_gb300/csrc/radix.cu", "u32_prefix_scan_gb300/csrc/scan.cu",
                       "u32_prefix_scan_gb300/csrc/internal.cuh"]
 

@@ -23,9 +23,10 @@
  *     zero-filled once before its first use (cudaMemset or
  *     u32scan_workspace_init); after that the library keeps it consistent
  *     itself, so it is reused across calls and shared between operations
- *     without clearing (the radix sort, the folds and the host-memory
- *     scans, which keep other data in it, clear what they leave where other
- *     operations keep tile state before they return). This holds for any
+ *     without clearing (the folds, the host-memory scans and small radix
+ *     sorts, which keep other data in it, clear what they leave where other
+ *     operations keep tile state before they return; a large radix sort
+ *     keeps its buffers past that span). This holds for any
  *     number of calls: carry words are tagged with a per-workspace launch
  *     count whose tags repeat every 2^29 launches, and the launch that ends
  *     such a period zeroes the carry words (up to a few MiB of ws) before the
@@ -428,7 +429,10 @@ int compact_indices_u32_carry(const int32_t *flags, size_t n, const int32_t *kep
  *   perm   device, int32_t[n]: keys[perm[0]] <= keys[perm[1]] <= ..., equal
  *          keys in increasing index order (the unique stable permutation).
  *   ws, ws_bytes  u32scan_workspace_bytes(U32SCAN_OP_RADIX, n) bytes (about
- *          12 * n bytes: two key buffers and one index buffer).
+ *          12 * n bytes: two key buffers and one index buffer; from n of
+ *          about 700,000 on, plus about 8.4 MB before them, the span other
+ *          operations' carry words can take, which the sort then need not
+ *          clear).
  * Digits that are equal for every key are skipped; which passes run is
  * decided on the device, so the call is asynchronous like the others.
  * Errors: EINVAL (null keys or perm with n > 0, misaligned pointers,

@@ -96,8 +96,11 @@ def test_radix_leaves_nothing_that_passes_for_tile_words(u):
     lib = _native.lib()
     big = 1 << 25
     need = max([lib.u32scan_workspace_bytes(op, big) for op in (1, 2, 3, 6)] +
-               [lib.u32scan_workspace_bytes(4, 70001)])
-    for n_r in (1000, 70001):
+               [lib.u32scan_workspace_bytes(4, n_r) for n_r in (70001, 1 << 20)])
+    # 1000 and 70001 keys: the small-sort layout (everything after the
+    # header, cleared at the end); 2^20: the large-sort one (buffers past
+    # the span other operations' words take, nothing cleared)
+    for n_r in (1000, 70001, 1 << 20):
         for which in ("scan", "segscan", "compact", "values", "scan64"):
             ws = u.Workspace(need, torch.device("cuda"))
             k = inputs.radix_keys(n_r, 3, ties=True)
@@ -196,10 +199,11 @@ def test_tag_period_end_clears_old_carry_words(u, which, big):
 
 
 def test_tag_period_end_on_a_radix_pass_clears_other_operations_words(u):
-    """The launch that ends a tag period can be a radix digit pass. The
-    radix sort keeps no count of the blocks that finish; its end-of-call
-    clear must therefore reach every word another operation may have left,
-    not only the sort's own (smaller) part of the workspace. Here a scan of
+    """The launch that ends a tag period can be a radix digit pass. A small
+    sort (its buffers packed after the header) clears at the end of the
+    call instead of counting its blocks out; that clear must therefore reach
+    every word another operation may have left, not only the sort's own
+    (smaller) part of the workspace. Here a scan of
     2^26 elements leaves tile words out to 33 KB, a sort of 1000 keys (a
     23 KB workspace part) ends the period with its first digit pass, and a
     second scan carrying the first one's tag must still be exact."""
@@ -220,6 +224,61 @@ def test_tag_period_end_on_a_radix_pass_clears_other_operations_words(u):
     ok, status = run_op(u, ws, "scan", big, 53)
     assert status == _native.OK
     assert ok, "a scan's carry word from the ended tag period was taken as published"
+
+
+def test_tag_period_end_on_a_large_radix_pass(u):
+    """A large sort keeps its buffers past the span other operations' carry
+    words can take and clears nothing at its end. When its first digit pass
+    ends a tag period, that pass's blocks count themselves out and the last
+    one zeroes the span: a later scan carrying an earlier scan's tag must
+    still be exact, and so must the sort's own later passes (new period)."""
+    from u32_prefix_scan_gb300 import _native
+
+    lib = _native.lib()
+    big, n_r = (1 << 26) + 77, 1 << 20
+    ws = u.Workspace(max(lib.u32scan_workspace_bytes(1, big), lib.u32scan_workspace_bytes(4, n_r)),
+                     torch.device("cuda"))
+    set_epoch(ws, TAG_PERIOD - 2)
+    ok, status = run_op(u, ws, "scan", big, 61)  # tag of launch 2^29 - 2
+    assert status == _native.OK and ok
+    assert header(ws)[H_EPOCH] == TAG_PERIOD - 1
+    k = inputs.radix_keys(n_r, 62)  # four active digit passes; the first ends the period
+    perm = u.radix_sort_perm_u32(dev32(k), workspace=ws)
+    assert lib.u32scan_check(ws.ptr, torch.cuda.current_stream().cuda_stream) == _native.OK
+    assert np.array_equal(perm.cpu().numpy(), oracle.sort_perm(k))
+    h = header(ws)
+    assert h[H_EPOCH] == TAG_PERIOD + 3 and h[H_COUNTER] == 0 and h[H_DONE] == 0
+    set_epoch(ws, 2 * TAG_PERIOD - 2)  # the first scan's tag again
+    ok, status = run_op(u, ws, "scan", big, 63)
+    assert status == _native.OK
+    assert ok, "a scan's carry word from the ended tag period was taken as published"
+
+
+def test_large_radix_clears_its_carry_words_past_the_shared_span(u):
+    """A sort of more than 4096 tiles (here 3 x 2^24 keys) has carry words
+    past the span other operations' words can take, where another call's
+    histograms or buffers may lie. Words planted there that read as
+    published inclusive zeros carrying the sort's first tag (every slot
+    computed from them would stay in bounds, only wrong) must be cleared
+    before the passes run."""
+    from u32_prefix_scan_gb300 import _native
+
+    lib = _native.lib()
+    n = 3 << 24
+    reach = max(lib.u32scan_workspace_bytes(op, (1 << 32) - 1) for op in (1, 2, 3, 6))
+    reach = (reach + 255) // 256 * 256
+    n_tiles = (n + 11263) // 11264
+    desc_end = 256 + (8 * 256 * n_tiles + 255) // 256 * 256
+    assert desc_end > reach
+    ws = u.Workspace(lib.u32scan_workspace_bytes(4, n), torch.device("cuda"))
+    e = int(header(ws)[H_EPOCH])
+    word = (((e & (TAG_PERIOD - 1)) + 1) << 34) | (1 << 32)  # tag of the first pass, inclusive, count 0
+    planted = torch.full(((desc_end - reach) // 8,), word, dtype=torch.int64, device="cuda")
+    ws.buf[reach:desc_end].copy_(planted.view(torch.uint8))
+    k = inputs.radix_keys(n, 72)
+    perm = u.radix_sort_perm_u32(dev32(k), workspace=ws)
+    assert lib.u32scan_check(ws.ptr, torch.cuda.current_stream().cuda_stream) == _native.OK
+    assert np.array_equal(perm.cpu().numpy(), oracle.sort_perm(k))
 
 
 def test_reduce_leaves_no_partials_that_pass_for_tile_words(u):

@@ -21,10 +21,11 @@
 // ("epoch"), so words left by earlier launches read as "not ready" and the
 // workspace needs zeroing only once, before its first use. That holds as
 // long as the workspace holds nothing but tile words at those offsets: the
-// radix sort, which also keeps histograms and its ping-pong buffers in the
-// workspace (stale small integers there could pass for tagged words), clears
-// its own tile words before its passes and, before it returns, the part of
-// the workspace any other operation's tile words can occupy.
+// radix sort also keeps histograms and ping-pong buffers in the workspace
+// (stale small integers there could pass for tagged words). A large sort
+// keeps them past the span any other operation's tile words can occupy
+// (tile_word_reach) and leaves only tagged words inside it; a small sort
+// packs them after the header and clears that span before it returns.
 //
 // Re-arming. Every block reads the epoch before its first draw; the block
 // that draws the launch's last index resets the tile counter and advances

@@ -14,7 +14,8 @@
 // instead of 32. A histogram of all four digits, taken first in one read of
 // the keys, gives every pass its digit bases (keys with a smaller digit
 // value come first) and finds digits that are equal for every key, whose
-// passes are skipped (exact: such a pass moves nothing). Each digit pass is
+// passes are skipped (exact: such a pass moves nothing); the histogram
+// kernel's last block to finish derives both. Each digit pass is
 // then one kernel over tiles of 11264 keys drawn in order: a tile ranks its
 // keys stably within itself, publishes its 256 digit counts, and finds for
 // every digit value the count of that value in all earlier tiles by a
@@ -91,20 +92,43 @@ struct RadixPlan {
 // header every operation keeps at offset 0 (tile counter, call epoch,
 // device status), the histograms, the digit bases, the plan, one carry word
 // per (tile, digit value), and the ping-pong buffers.
+// Workspace of a sort of n keys. The histograms, digit bases, plan and
+// ping-pong buffers hold small integers that could pass for another
+// operation's tagged tile words, which lie in [header, reach). Far layout
+// (the buffers at least as large as that span): the carry words first, then
+// everything else from `reach` on, so the call leaves nothing but tagged
+// words where other operations look and needs no clear at its end. Near
+// layout (small sorts): everything packed after the header, and the call
+// clears [header, reach) before it returns.
 struct RadixLayout {
-    size_t hist, bases, plan, desc, k1, k2, i1, total;
+    size_t hist, done, bases, plan, desc, desc_end, k1, k2, i1, total, reach;
     unsigned int n_tiles;
+    bool far;
     explicit RadixLayout(unsigned long long n) {
         n_tiles = (unsigned int)((n + kRTile - 1) / kRTile);
+        reach = round_up(tile_word_reach(), 256);
+        far = 12ull * n >= reach;
+        const size_t desc_bytes = round_up(8ull * 256 * n_tiles, 256);
         size_t o = kHeaderBytes;
-        hist = o;
-        o += round_up(4 * 256 * 4, 256);
+        if (far) {
+            desc = o;
+            o += desc_bytes;
+            desc_end = o;
+            o = o > reach ? o : reach;
+        }
+        hist = o;  // then the histogram kernel's count of finished blocks
+        o += 4 * 256 * 4;
+        done = o;
+        o += 256;
         bases = o;
         o += round_up(4 * 256 * 4, 256);
         plan = o;
         o += round_up(4 * sizeof(RadixPlan), 256);
-        desc = o;
-        o += round_up(8ull * 256 * n_tiles, 256);
+        if (!far) {
+            desc = o;
+            o += desc_bytes;
+            desc_end = o;
+        }
         k1 = o;
         o += round_up(4 * n, 256);
         k2 = o;
@@ -122,8 +146,51 @@ struct RadixLayout {
 constexpr int kHThreads = 1024;
 constexpr size_t kHSmem = (size_t)4 * 256 * 32 * 4;  // 128 KiB
 
+// The plan from the four complete histograms (called by every thread of
+// one block; warp p < 4 takes digit p): a digit is constant when one value
+// holds all n keys; each pass's base for digit value v is the number of
+// keys whose digit is below v (an exclusive scan of that digit's
+// histogram).
+__device__ __forceinline__ void radix_plan_block(const unsigned int *hist, unsigned long long n, RadixPlan *plan,
+                                                 unsigned int *bases) {
+    __shared__ int s_active[4];
+    const int lane = threadIdx.x & 31, p = threadIdx.x >> 5;
+    if (p < 4) {
+        // lane l holds digit values 8l .. 8l+7
+        unsigned int c[8], sum = 0;
+        bool whole = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            c[i] = ld_relaxed_u32(hist + 256 * p + 8 * lane + i);
+            sum += c[i];
+            whole = whole || c[i] == n;
+        }
+        const bool active = !__any_sync(0xffffffffu, whole);
+        unsigned int run = warp_inclusive_sum(sum, lane) - sum;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            bases[256 * p + 8 * lane + i] = run;
+            run += c[i];
+        }
+        if (lane == 0) s_active[p] = active ? 1 : 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int j = 0, m = s_active[0] + s_active[1] + s_active[2] + s_active[3];
+        for (int q = 0; q < 4; ++q) {
+            plan[q].active = s_active[q];
+            plan[q].j = j;
+            plan[q].m = m;
+            j += s_active[q];
+        }
+    }
+}
+
+// `done` counts the blocks that have added their counts (zero at launch);
+// the last one computes the plan.
 __global__ void __launch_bounds__(kHThreads, 1)
-radix_histogram_kernel(const uint32_t *__restrict__ keys, unsigned long long n, unsigned int *__restrict__ hist) {
+radix_histogram_kernel(const uint32_t *__restrict__ keys, unsigned long long n, unsigned int *hist,
+                       unsigned int *done, RadixPlan *plan, unsigned int *bases) {
     extern __shared__ __align__(16) unsigned int h_cols[];  // [4 * 256][32]
     for (int i = threadIdx.x; i < 4 * 256 * 32; i += kHThreads) h_cols[i] = 0;
     __syncthreads();
@@ -186,43 +253,16 @@ radix_histogram_kernel(const uint32_t *__restrict__ keys, unsigned long long n, 
         for (int c = 0; c < 32; ++c) sum += h_cols[32 * r + ((c + (int)lane) & 31)];
         if (sum) atomicAdd(hist + r, sum);
     }
-}
-
-// Four warps, one per digit: a digit is constant when one value holds all
-// n keys; each pass's base for digit value v is the number of keys whose
-// digit is below v (an exclusive scan of that digit's histogram).
-__global__ void __launch_bounds__(128) radix_plan_kernel(const unsigned int *__restrict__ hist,
-                                                         unsigned long long n, RadixPlan *plan,
-                                                         unsigned int *__restrict__ bases) {
-    __shared__ int s_active[4];
-    const int lane = threadIdx.x & 31, p = threadIdx.x >> 5;
-    // lane l holds digit values 8l .. 8l+7
-    unsigned int c[8], sum = 0;
-    bool whole = false;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        c[i] = hist[256 * p + 8 * lane + i];
-        sum += c[i];
-        whole = whole || c[i] == n;
-    }
-    const bool active = !__any_sync(0xffffffffu, whole);
-    unsigned int run = warp_inclusive_sum(sum, lane) - sum;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        bases[256 * p + 8 * lane + i] = run;
-        run += c[i];
-    }
-    if (lane == 0) s_active[p] = active ? 1 : 0;
+    __shared__ unsigned int s_last;
+    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-        int j = 0, m = s_active[0] + s_active[1] + s_active[2] + s_active[3];
-        for (int q = 0; q < 4; ++q) {
-            plan[q].active = s_active[q];
-            plan[q].j = j;
-            plan[q].m = m;
-            j += s_active[q];
-        }
+        const bool last = atom_add_acq_rel(done, 1u) == gridDim.x - 1u;
+        if (last) st_relaxed_u32(done, 0u);
+        s_last = last ? 1u : 0u;
     }
+    __syncthreads();
+    if (s_last) radix_plan_block(hist, n, plan, bases);
 }
 
 // Buffers of one pass. Pass j of m active ones reads what pass j - 1 wrote
@@ -374,7 +414,7 @@ __global__ void __launch_bounds__(kRThreads, U32SCAN_R_MINB)
 radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
                       int32_t *i1, int32_t *perm, uint32_t *keys_out, unsigned long long n, unsigned int n_tiles,
                       const unsigned int *__restrict__ bases, WsHeader *hdr, unsigned long long *desc,
-                      unsigned long long limit_ns, unsigned int ahead) {
+                      unsigned long long limit_ns, unsigned int ahead, unsigned long long clear_words) {
     const RadixPlan pl = plan[p];
     if (!pl.active) {
         // Every digit constant (every key equal): the permutation is the
@@ -548,6 +588,11 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
             if (b.out_idx) b.out_idx[slot] = s_idx[i];
         }
     }
+    // A launch that ends a tag period zeroes the first clear_words tile
+    // words (far layout: every word another operation may read; the sort's
+    // own buffers lie past them). Near layout: 0, the call clears at its end.
+    finish_period(hdr, s_epoch, reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(hdr) + kHeaderBytes),
+                  clear_words);
 }
 
 constexpr size_t kRSmem = (size_t)(kRWarps * 256 + 512 + 2 * kRTile) * 4;
@@ -571,6 +616,7 @@ static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *per
     char *w = static_cast<char *>(ws);
     WsHeader *hdr = reinterpret_cast<WsHeader *>(w);
     unsigned int *hist = reinterpret_cast<unsigned int *>(w + L.hist);
+    unsigned int *done = reinterpret_cast<unsigned int *>(w + L.done);
     unsigned int *bases = reinterpret_cast<unsigned int *>(w + L.bases);
     RadixPlan *plan = reinterpret_cast<RadixPlan *>(w + L.plan);
     unsigned long long *desc = reinterpret_cast<unsigned long long *>(w + L.desc);
@@ -601,26 +647,29 @@ static int radix_launch(const uint32_t *keys, unsigned long long n, int32_t *per
         sms = dev_sms[dev];
         resident = dev_resident[dev];
     }
-    if (cudaMemsetAsync(hist, 0, 4 * 256 * 4, stream) != cudaSuccess) return U32SCAN_ECUDA;
-    // the digit passes' carry words (each pass's launch has its own tag)
-    if (const int rc = clear_tile_words(desc, 8ull * 256 * L.n_tiles, stream); rc != U32SCAN_OK) return rc;
-    radix_histogram_kernel<<<sms, kHThreads, kHSmem, stream>>>(keys, n, hist);
-    radix_plan_kernel<<<1, 128, 0, stream>>>(hist, n, plan, bases);
+    // the histograms and the finished-block count (one memset: they are adjacent)
+    if (cudaMemsetAsync(hist, 0, L.bases - L.hist, stream) != cudaSuccess) return U32SCAN_ECUDA;
+    // The digit passes' carry words (each pass's launch has its own tag).
+    // Where other operations keep tile words, the words can only be tagged
+    // or zero; past that span another call's histograms or buffers may lie.
+    {
+        const size_t from = L.far ? (L.desc > L.reach ? L.desc : L.reach) : L.desc;
+        if (L.desc_end > from)
+            if (const int rc = clear_tile_words(w + from, L.desc_end - from, stream); rc != U32SCAN_OK) return rc;
+    }
+    radix_histogram_kernel<<<sms, kHThreads, kHSmem, stream>>>(keys, n, hist, done, plan, bases);
+    const unsigned long long clear_words = L.far ? tile_words_to_clear(ws_bytes) : 0ull;
     for (int p = 0; p < 4; ++p)
         radix_onesweep_kernel<<<L.n_tiles, kRThreads, kRSmem, stream>>>(plan, p, keys, k1, k2, i1, perm, keys_out, n,
                                                                          L.n_tiles, bases, hdr, desc, kDefaultLimitNs,
-                                                                         (unsigned int)resident);
+                                                                         (unsigned int)resident, clear_words);
     if (cudaGetLastError() != cudaSuccess) return U32SCAN_ECUDA;
-    // Leave no data where another operation's tile words may go: the
-    // histograms, bases and ping-pong buffers hold small integers that could
-    // pass for tagged words. Any other operation's tile words lie within the
-    // largest workspace it can need (n below 2^32), a few MiB at most. The
-    // whole of that span is zeroed, not only this call's part of it: the
-    // digit passes draw tiles, so one of them can be the launch that ends a
-    // tag period, and they keep no count of the blocks that finish; zeroing
-    // here leaves no other operation's word from the ending period behind.
-    const size_t reach = tile_word_reach();
-    const size_t end = ws_bytes < reach ? ws_bytes : reach;
+    if (L.far) return U32SCAN_OK;
+    // Near layout: leave no data where another operation's tile words may
+    // go (the histograms, bases and ping-pong buffers lie there). The whole
+    // of that span is zeroed, not only this call's part of it, which also
+    // serves as the end of a tag period if one of the passes ended one.
+    const size_t end = ws_bytes < L.reach ? ws_bytes : L.reach;
     return clear_tile_words(w + kHeaderBytes, end - kHeaderBytes, stream);
 }
 

@@ -37,6 +37,8 @@ def keys_for(kind: str, n: int, seed: int = 5) -> np.ndarray:
         return np.full(n, 0xDEADBEEF, dtype=np.uint32)
     if kind == "top_digit":  # only the most significant digit varies
         return (inputs.radix_keys(n, seed) & np.uint32(0xFF000000)) | np.uint32(0x00ABCDEF)
+    if kind == "mid_digit":  # only the second digit varies, set bits on both sides of it
+        return (inputs.radix_keys(n, seed) & np.uint32(0x0000FF00)) | np.uint32(0x12340056)
     if kind == "two_values":
         return np.where(inputs.radix_keys(n, seed) & np.uint32(1), np.uint32(7), np.uint32(0xFFFFFFFF))
     if kind == "sorted":
@@ -62,7 +64,7 @@ TILE = 512 * 22
 SIZES = [1, 2, 3, 100, 8191, 8192, 8193, TILE - 1, TILE, TILE + 1, 3 * TILE + 77, 100003, (1 << 20) + 5]
 
 
-@pytest.mark.parametrize("kind", ["uniform", "ties256", "ties65536", "equal", "top_digit", "two_values",
+@pytest.mark.parametrize("kind", ["uniform", "ties256", "ties65536", "equal", "top_digit", "mid_digit", "two_values",
                                   "sorted", "reversed"])
 @pytest.mark.parametrize("n", SIZES)
 def test_radix_parity(u, kind, n):
@@ -103,7 +105,7 @@ def test_workload_2_25_full_parity(u, kind):
     check_perm(u, keys_for(kind, 1 << 25))
 
 
-@pytest.mark.parametrize("kind", ["uniform", "ties256", "equal", "top_digit", "two_values", "reversed"])
+@pytest.mark.parametrize("kind", ["uniform", "ties256", "equal", "top_digit", "mid_digit", "two_values", "reversed"])
 @pytest.mark.parametrize("n", [1, 8193, 100003, (1 << 20) + 5])
 def test_sort_keys_and_permutation(u, kind, n):
     keys = keys_for(kind, n)
@@ -116,7 +118,7 @@ def test_sort_keys_and_permutation(u, kind, n):
     assert np.array_equal(d.cpu().numpy().view(np.uint32), keys)
 
 
-@pytest.mark.parametrize("kind", ["uniform", "ties256", "equal"])
+@pytest.mark.parametrize("kind", ["uniform", "ties256", "equal", "top_digit", "mid_digit"])
 def test_sort_keys_only(u, kind):
     keys = keys_for(kind, 300007)
     d = torch.from_numpy(keys.view(np.int32).copy()).cuda()

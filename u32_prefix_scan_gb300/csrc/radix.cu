@@ -26,7 +26,9 @@
 // and which buffers they read and write, is decided on the device, so the
 // call stays asynchronous. The last pass writes the indices into `perm` and,
 // for radix_sort_u32, the sorted keys into `keys_out`; a keys-only sort moves
-// no indices at all.
+// no indices at all. When only one digit varies, its pass orders one word a
+// key (the key's place in the tile and its digit) and rebuilds the index and
+// the key from it.
 //
 // Ranking. For the 32 keys of one warp round (one per lane), a per-warp
 // table of lane masks, one word per value of the digit's low seven bits,
@@ -410,18 +412,16 @@ __device__ __noinline__ void radix_identity_tile(const uint32_t *keys, int32_t *
 // (aggregate) or the count of v in tiles 0..t (inclusive, P bit).
 // One tile per block; `ahead`: tiles between a block's tile and the one it
 // asks L2 for (the resident grid).
-__global__ void __launch_bounds__(kRThreads, U32SCAN_R_MINB)
-radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
-                      int32_t *i1, int32_t *perm, uint32_t *keys_out, unsigned long long n, unsigned int n_tiles,
-                      const unsigned int *__restrict__ bases, WsHeader *hdr, unsigned long long *desc,
-                      unsigned long long limit_ns, unsigned int ahead, unsigned long long clear_words) {
-    const RadixPlan pl = plan[p];
-    if (!pl.active) {
-        // Every digit constant (every key equal): the permutation is the
-        // identity, written by the last digit's launch.
-        if (p == 3 && pl.m == 0) radix_identity_tile(keys, perm, keys_out, n);
-        return;
-    }
+// One tile of a digit pass (the block's whole work). SINGLE: the only active
+// pass (every other digit is equal for all keys): its indices are the
+// identity, so a key is placed in shared memory as one word holding its
+// place in the tile and its digit, and its index and key are rebuilt from
+// that word when the tile is written (no second array of indices).
+template <bool SINGLE>
+__device__ __forceinline__ void radix_pass_tile(const PassBuffers &b, int p, unsigned long long n, unsigned int n_tiles,
+                                                const unsigned int *__restrict__ bases, WsHeader *hdr,
+                                                unsigned long long *desc, unsigned long long limit_ns,
+                                                unsigned int ahead, unsigned long long clear_words) {
     // Shared memory (32-bit words): per-warp digit counters, later the warp
     // offsets in the tile-ordered buffer [kRWarps][256]; each value's run
     // start in the tile [256]; its first output slot minus that start [256];
@@ -434,9 +434,8 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     unsigned int *s_keys = s_delta + 256;
     int32_t *s_idx = reinterpret_cast<int32_t *>(s_keys + kRTile);
     __shared__ unsigned int s_part[kRWarps];
-    __shared__ unsigned int s_t, s_epoch;
+    __shared__ unsigned int s_t, s_epoch, s_kbase;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm, keys_out);
     const int shift = 8 * p;
     // n < 2^31 for a radix sort: 32-bit element indices
     const unsigned int n32 = (unsigned int)n;
@@ -507,10 +506,17 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
         if (full || ((valid_bits >> r) & 1u)) {
             const unsigned int v = (k[r] >> shift) & 255u;
             const unsigned int pos = rank_get(wrank, r) + s_cnt[warp][v];
-            rank_set(wrank, r, pos);
-            s_keys[pos] = k[r];
+            if (SINGLE) {
+                // the key's place in the tile (below 2^16) and its digit
+                s_keys[pos] = ((unsigned int)warp * kRWarpKeys + 32u * r + (unsigned int)lane) | (v << 16);
+            } else {
+                rank_set(wrank, r, pos);
+                s_keys[pos] = k[r];
+            }
         }
     }
+    // the digits every key shares (thread 0's first key is always in the array)
+    if (SINGLE && threadIdx.x == 0) s_kbase = k[0] & ~(255u << shift);
     // The look-back's first window (threads 0..255, value v), loaded before
     // the indices are placed so that its round trip overlaps that work (4
     // words: 8 measured slower loaded here, and before the keys are placed
@@ -524,7 +530,7 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
             wd[j] = q >= 0 ? ld_relaxed(col + 256ull * (unsigned long long)q) : (tag | kFlagP);
         }
     }
-    if (b.out_idx) {
+    if (!SINGLE && b.out_idx) {
         int32_t idx[kRKeys];
 #pragma unroll
         for (int r = 0; r < kRKeys; ++r) {
@@ -579,7 +585,19 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
         s_delta[v] = bases[256 * p + v] + before - s_tileoff[v];
     }
     __syncthreads();
-    {
+    if (SINGLE) {
+        // the index is the key's place (the identity before the only pass);
+        // the key, the shared digits with its own
+        const unsigned int count = full ? kRTile : n32 - tile0;
+        const unsigned int kbase = s_kbase;
+        for (unsigned int i = threadIdx.x; i < count; i += kRThreads) {
+            const unsigned int w = s_keys[i];
+            const unsigned int v = w >> 16;
+            const unsigned int slot = s_delta[v] + i;
+            if (b.out_keys) b.out_keys[slot] = kbase | (v << shift);
+            if (b.out_idx) b.out_idx[slot] = (int32_t)(tile0 + (w & 0xffffu));
+        }
+    } else {
         const unsigned int count = full ? kRTile : n32 - tile0;
         for (unsigned int i = threadIdx.x; i < count; i += kRThreads) {
             const unsigned int key = s_keys[i];
@@ -593,6 +611,38 @@ radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t 
     // own buffers lie past them). Near layout: 0, the call clears at its end.
     finish_period(hdr, s_epoch, reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(hdr) + kHeaderBytes),
                   clear_words);
+}
+
+// The single-pass tile. (Kept out of line, the call cost the other passes'
+// code a spill and 5 % of their time.)
+__device__ __forceinline__ void radix_pass_tile_single(int p, const uint32_t *keys, int32_t *perm, uint32_t *keys_out,
+                                                    unsigned long long n, unsigned int n_tiles,
+                                                    const unsigned int *__restrict__ bases, WsHeader *hdr,
+                                                    unsigned long long *desc, unsigned long long limit_ns,
+                                                    unsigned int ahead, unsigned long long clear_words) {
+    // the only pass reads the caller's keys and writes the results
+    const PassBuffers b{keys, nullptr, keys_out, perm};
+    radix_pass_tile<true>(b, p, n, n_tiles, bases, hdr, desc, limit_ns, ahead, clear_words);
+}
+
+__global__ void __launch_bounds__(kRThreads, U32SCAN_R_MINB)
+radix_onesweep_kernel(const RadixPlan *__restrict__ plan, int p, const uint32_t *keys, uint32_t *k1, uint32_t *k2,
+                      int32_t *i1, int32_t *perm, uint32_t *keys_out, unsigned long long n, unsigned int n_tiles,
+                      const unsigned int *__restrict__ bases, WsHeader *hdr, unsigned long long *desc,
+                      unsigned long long limit_ns, unsigned int ahead, unsigned long long clear_words) {
+    const RadixPlan pl = plan[p];
+    if (!pl.active) {
+        // Every digit constant (every key equal): the permutation is the
+        // identity, written by the last digit's launch.
+        if (p == 3 && pl.m == 0) radix_identity_tile(keys, perm, keys_out, n);
+        return;
+    }
+    if (pl.m == 1) {
+        radix_pass_tile_single(p, keys, perm, keys_out, n, n_tiles, bases, hdr, desc, limit_ns, ahead, clear_words);
+    } else {
+        const PassBuffers b = pass_buffers(pl, keys, k1, k2, i1, perm, keys_out);
+        radix_pass_tile<false>(b, p, n, n_tiles, bases, hdr, desc, limit_ns, ahead, clear_words);
+    }
 }
 
 constexpr size_t kRSmem = (size_t)(kRWarps * 256 + 512 + 2 * kRTile) * 4;

@@ -425,9 +425,8 @@ __device__ __forceinline__ void radix_pass_tile(const PassBuffers &b, int p, uns
     // Shared memory (32-bit words): per-warp digit counters, later the warp
     // offsets in the tile-ordered buffer [kRWarps][256]; each value's run
     // start in the tile [256]; its first output slot minus that start [256];
-    // the tile's keys in digit order [kRTile] (the single pass: a key's place
-    // in the tile | its digit << 16); its indices in digit order [kRTile]
-    // (unused by the single pass).
+    // the tile's keys in digit order [kRTile]; its indices in digit order
+    // [kRTile].
     extern __shared__ __align__(128) unsigned int r_smem[];
     unsigned int(*s_cnt)[256] = reinterpret_cast<unsigned int(*)[256]>(r_smem);
     unsigned int *s_tileoff = r_smem + kRWarps * 256;

@@ -80,6 +80,31 @@ def test_scan_rejects_bad_arguments_on_host(lib, name):
     assert fn(None, 0, None, None, 0, None) == _native.OK
 
 
+def test_radix_workspace_layouts(lib):
+    """A radix sort's workspace: small sorts pack their histograms, carry
+    words and buffers after the header; from 12 n bytes of buffers at least
+    the span other operations' carry words can take (the largest of their
+    workspaces for n below 2^32), the carry words come first and everything
+    else starts past that span, so a large sort leaves only tagged carry
+    words where other operations look."""
+    wb = lib.u32scan_workspace_bytes
+    reach = max(wb(op, (1 << 32) - 1) for op in (_native.OP_SCAN, _native.OP_SEGSCAN, _native.OP_COMPACT,
+                                                  _native.OP_SCAN64))
+
+    def r256(x):
+        return -(-x // 256) * 256
+
+    small = 4096 + 256 + 4096 + 256  # histograms, finished-block count, bases, plan
+    n0 = -(-reach // 12)  # the first large sort
+    for n in (1, 1000, 70001, n0 - 1, n0, (1 << 20) + 5, 1 << 25, 3 << 24):
+        carry = r256(8 * 256 * -(-n // 11264))
+        bufs = 3 * r256(4 * n)
+        if n < n0:
+            assert wb(_native.OP_RADIX, n) == 256 + small + carry + bufs, n
+        else:
+            assert wb(_native.OP_RADIX, n) == max(256 + carry, reach) + small + bufs, n
+
+
 def test_workspace_init_rejects_null(lib):
     assert lib.u32scan_workspace_init(None, 4096, None) == _native.EWORKSPACE
     assert lib.u32scan_check(None, None) == _native.EWORKSPACE
